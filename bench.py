@@ -1,0 +1,482 @@
+#!/usr/bin/env python
+"""Benchmark: MoE-layer tokens/s of the Q4_K sparse-MoE layer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload qwen_decode] [--tokens T]
+
+One step = one pass of the whole layer (route, bucket, gate/up + SiLU*mul,
+down + weighted combine) over every distinct layer of the workload, each
+with a T-token window: the qwen_decode workload has 48 distinct layers of
+512 Q4_K experts (~34 GB resident, far larger than L2), so consecutive calls
+never find their weights in L2.  The step is captured once as a CUDA graph
+and replayed; `value` = T * layers * K / time (tokens per second per layer).
+
+Also reported: the dominant kernel's achieved bandwidth (or throughput)
+against the measured peak, timed with CUDA events on the launching stream in
+a separate eager pass; an end-to-end figure through the C ABI with host
+buffers (pinned H2D of x and D2H of y inside the timed region); the CPU
+oracle on a bounded sample of the same workload; SM clocks during the run.
+
+Multi-GPU (torchrun): the layer does not shard here -- every rank runs an
+independent replica ("replicas only"); value sums all ranks' tokens over the
+slowest rank's time.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_moe_expert_04_b300 import moe, synth  # noqa: E402
+from quantized_moe_expert_04_b300.layer import pack_layer, routing_views, workspace  # noqa: E402
+
+DEFAULT_TOKENS = {"tiny": 4, "qwen_decode": 3, "deepseek_decode": 4, "qwen_prefill": 4096,
+                  "deepseek_prefill_skewed": 4096}
+METRIC = "MoE-layer tokens/s"
+UNIT = "tokens/s"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ dist
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def all_max(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [c.strip() for c in line.split(",")]
+                if len(f) >= 9 and f[1].replace(".", "").isdigit():
+                    rows.append(f)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()) if rows else None}
+
+
+# ------------------------------------------------------------------ oracle leg
+
+def oracle_sample(wl, T, layers, x_layers, time_budget_s=12.0, max_tokens=None, gen_device="cuda"):
+    """Time the CPU oracle on a bounded sample: the first layers (and, for
+    large T, the first max_tokens tokens) of the same workload.  Packing the
+    oracle's blobs is untimed set-up; routing, bucketing, dequantisation and
+    the FFNs are timed.  Returns (tokens/s per layer, threads, description)."""
+    import oracle
+    threads = oracle.set_threads(0)
+    done_tok, spent, used_layers = 0, 0.0, 0
+    for l in layers:
+        x = x_layers[l].cpu()
+        if max_tokens is not None:
+            x = x[:max_tokens]
+        xb = synth.bf16_bits(x)
+        wr = synth.router_weight(wl, 0, l, device=gen_device).cpu().numpy()
+        b = synth.router_bias(wl, 0, l, device=gen_device)
+        b = None if b is None else b.cpu().numpy()
+        ids, _, _, _ = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
+        blobs = [None] * wl.n_experts
+        for e in sorted(set(ids.reshape(-1).tolist())):
+            blobs[e] = oracle.pack_expert_q4k(synth.expert_weight(wl, e, 0, l, device=gen_device).cpu().numpy())
+        sblob = None
+        if wl.has_shared:
+            sblob = oracle.pack_shared_q8_0(synth.shared_weight(wl, 0, l, device=gen_device).cpu().numpy())
+        t0 = time.perf_counter()
+        oracle.moe_forward(wl.hidden, wl.n_experts, wl.ff, wl.top_k, wl.score_fn, xb, wr, b, blobs,
+                           wl.shared_ff, sblob)
+        spent += time.perf_counter() - t0
+        done_tok += xb.shape[0]
+        used_layers += 1
+        if spent >= time_budget_s:
+            break
+    desc = "%d layer(s) x %d token(s) of %s (oracle: fp64 route+bucket+dequant+FFN; packing untimed)" % (
+        used_layers, done_tok // max(used_layers, 1), wl.name)
+    return done_tok / spent, threads, desc
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def algorithmic(wl, T, ids_per_layer):
+    """Bytes and flops one layer call must move / compute, from its routing.
+
+    Bytes: each selected expert's blob once per window (+ shared blob), the
+    fp32 router matrix, bias, x in, y out, ids and weights.  Flops: router
+    2*T*E*H + 2*T*k*3*H*FF (+ 2*T*3*H*FF_s shared); padding not counted."""
+    E, H, FF, k = wl.n_experts, wl.hidden, wl.ff, wl.top_k
+    total_bytes, gateup_bytes = [], []
+    for ids in ids_per_layer:
+        U = len(np.unique(ids))
+        b = U * wl.blob_bytes + wl.shared_blob_bytes + E * H * 4 + (E * 4 if wl.bias != "none" else 0)
+        b += 2 * T * H * 2 + T * k * 8
+        total_bytes.append(b)
+        gateup_bytes.append(U * 2 * FF * (H // 256) * 144 + T * H * 2)
+    flops = 2 * T * E * H + 2 * T * k * 3 * H * FF + (2 * T * 3 * H * wl.shared_ff if wl.has_shared else 0)
+    gemm_gateup_flops = 2 * T * k * 2 * H * FF
+    return np.mean(total_bytes), np.mean(gateup_bytes), flops, gemm_gateup_flops
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(os.path.join(ROOT, "quantized_moe_expert_04_b300", "csrc"))):
+        with open(os.path.join(ROOT, "quantized_moe_expert_04_b300", "csrc", fn), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload, T):
+    """DRAM bytes per launch from a committed ncu summary, if it still matches the source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        rec = d.get("%s:%s:T%d" % (kernel, workload, T))
+        if rec and rec.get("source_hash") == kernel_source_hash():
+            return rec["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ arms
+
+def run_ours(args, world, rank, local):
+    wl = synth.WORKLOADS[args.workload]
+    T = args.tokens or DEFAULT_TOKENS[args.workload]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    nL = wl.layers if args.layers is None else args.layers
+    cfg = moe.config_for(wl)
+    t_setup = time.time()
+    layers = [pack_layer(wl, 0, l, gen_device="cuda") for l in range(nL)]
+    xs = [synth.hidden_states(wl, T, 0, l, device="cuda").contiguous() for l in range(nL)]
+    ys = [torch.empty(T, wl.hidden, dtype=torch.bfloat16, device=dev) for _ in range(nL)]
+    ws = workspace(cfg, T)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    setup_s = time.time() - t_setup
+
+    def step():
+        for l in range(nL):
+            pl = layers[l]
+            moe.moe_forward(cfg, xs[l], pl.router_w, pl.router_bias, pl.table, pl.shared, T, ys[l], None, ws,
+                            stream)
+
+    # routing of each layer (for the algorithmic byte counts) + correctness status
+    ids_per_layer = []
+    with torch.cuda.stream(stream):
+        for l in range(nL):
+            pl = layers[l]
+            moe.moe_forward(cfg, xs[l], pl.router_w, pl.router_bias, pl.table, pl.shared, T, ys[l], None, ws,
+                            stream)
+            ids, _, _, _ = routing_views(cfg, T, ws)
+            ids_per_layer.append(ids.cpu().numpy().copy())
+    st = moe.moe_last_device_status(ws, stream)
+    if st != moe.MOE_OK:
+        raise moe.MoeError(st, "device status after the first pass")
+
+    # launches per layer call + per-kernel durations (eager, profiled pass)
+    moe.moe_profile_enable(True)
+    prof_steps = max(3, min(args.steps or 20, 20))
+    with torch.cuda.stream(stream):
+        for _ in range(prof_steps):
+            step()
+    stream.synchronize()
+    prof = moe.moe_profile_read()
+    moe.moe_profile_enable(False)
+    launches_per_call = sum(v[0] for v in prof.values()) / (prof_steps * nL)
+
+    # CUDA graph of one step
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        step()                                   # warm
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    # steps: fixed by the caller, else enough for ~3 s of timed work
+    K = args.steps
+    if K is None:
+        t0 = time.perf_counter()
+        for _ in range(5):
+            graph.replay()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 5
+        K = int(max(10, min(5000, 3.0 / max(per, 1e-6))))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(K):
+                graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    ms = all_max(ms, world)
+    clocks = clk.summary()
+    step_ms = ms / K
+    tokens = T * nL * K * world
+    value = tokens / (ms / 1e3)
+
+    # end to end through the C ABI with host buffers
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = [torch.empty(T, wl.hidden, dtype=torch.bfloat16).pin_memory() for _ in range(nL)]
+    xd = [torch.empty_like(x) for x in xs]
+    Ke = max(3, min(K, 50))
+
+    def e2e_step():
+        for l in range(nL):
+            pl = layers[l]
+            xd[l].copy_(xh[l], non_blocking=True)
+            moe.moe_forward(cfg, xd[l], pl.router_w, pl.router_bias, pl.table, pl.shared, T, ys[l], None, ws,
+                            stream)
+            yh[l].copy_(ys[l], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = all_max(e0.elapsed_time(e1), world)
+    e2e_value = T * nL * Ke * world / (e2e_ms / 1e3)
+
+    # roofline of the dominant kernel
+    pk = peaks()
+    step_bytes, gateup_bytes, flops, gemm_flops = algorithmic(wl, T, ids_per_layer)
+    kernel_ms = {name: (v[2] / v[1] if v[1] else float("nan")) for name, v in prof.items()}
+    share = {name: v[2] for name, v in prof.items()}
+    top = max(share, key=share.get)
+    decode = "gemv_gateup" in prof
+    if decode:
+        dom = "gemv_gateup"
+        achieved = gateup_bytes / (kernel_ms[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": profiled_traffic(dom, wl.name, T), "peak_source": pk["source"],
+                "avg_launch_us": round(kernel_ms[dom] * 1e3, 3),
+                "algorithmic_bytes_per_launch": int(gateup_bytes)}
+    else:
+        dom = "gemm_gateup" if "gemm_gateup" in prof else top
+        achieved = gemm_flops / (kernel_ms[dom] / 1e3) / 1e12
+        peak = pk["bf16_tflops"]
+        roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(dom, wl.name, T),
+                "peak_source": pk["source"] + " (fp16 operands; same nominal rate as bf16)",
+                "avg_launch_us": round(kernel_ms[dom] * 1e3, 3), "algorithmic_flops_per_launch": int(gemm_flops)}
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if decode else "f16",
+        "data": "synthetic (seeded; x~N(0,1) bf16, router W~N(0,1/H), experts N(0,0.02^2) packed to Q4_K)",
+        "config": {"workload": wl.name, "tokens_per_window": T, "hidden": wl.hidden, "experts": wl.n_experts,
+                   "top_k": wl.top_k, "ff": wl.ff, "shared_ff": wl.shared_ff, "distinct_layers": nL,
+                   "resident_expert_gb": round(nL * (wl.n_experts * wl.blob_bytes + wl.shared_blob_bytes) / 1e9, 2),
+                   "l2": "inputs larger than L2 (distinct layers rotated)", "graph": "one CUDA graph per step",
+                   "parallelism": "replicas x%d" % world},
+        "hbm": {"algorithmic_bytes_per_call": int(step_bytes),
+                "gbs": round(step_bytes * nL * K / (ms / 1e3) / 1e9 * 1, 1),
+                "frac": round(step_bytes * nL * K / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)},
+        "tflops": round(flops * nL * K / (ms / 1e3) / 1e12, 3),
+        "roofline": roof,
+        "kernels_ms_per_launch": {k: round(v, 5) for k, v in kernel_ms.items()},
+        "gpu_launches": int(round(launches_per_call * nL * K)),
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(nL * T * wl.hidden * 2), "d2h_bytes_per_step": int(nL * T * wl.hidden * 2),
+                "path": "pinned H2D x -> moe_forward -> D2H y, per layer, eager"},
+        "clocks": clocks,
+        "setup_s": round(setup_s, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, threads, desc = oracle_sample(wl, T, list(range(nL)), xs, time_budget_s=args.cpu_budget,
+                                         max_tokens=args.cpu_tokens if T > 64 else None)
+        out["cpu_baseline"] = {"value": round(v, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+                               "sample": desc}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm, on this arm's workload and metric."""
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    T = args.tokens or DEFAULT_TOKENS[args.workload]
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    nL = min(wl.layers if args.layers is None else args.layers, 8)
+    Ts = T if T <= 64 else args.cpu_tokens
+    xs = [synth.hidden_states(wl, T, 0, l, device=gen)[:Ts] for l in range(nL)]
+    import oracle
+    threads = oracle.set_threads(0)
+    prepared = []
+    for l in range(nL):
+        xb = synth.bf16_bits(xs[l])
+        wr = synth.router_weight(wl, 0, l, device=gen).cpu().numpy()
+        b = synth.router_bias(wl, 0, l, device=gen)
+        b = None if b is None else b.cpu().numpy()
+        ids, _, _, _ = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
+        blobs = [None] * wl.n_experts
+        for e in sorted(set(ids.reshape(-1).tolist())):
+            blobs[e] = oracle.pack_expert_q4k(synth.expert_weight(wl, e, 0, l, device=gen).cpu().numpy())
+        sblob = oracle.pack_shared_q8_0(synth.shared_weight(wl, 0, l, device=gen).cpu().numpy()) \
+            if wl.has_shared else None
+        prepared.append((xb, wr, b, blobs, sblob))
+
+    def step(i):
+        xb, wr, b, blobs, sblob = prepared[i % nL]
+        oracle.moe_forward(wl.hidden, wl.n_experts, wl.ff, wl.top_k, wl.score_fn, xb, wr, b, blobs,
+                           wl.shared_ff, sblob)
+
+    for i in range(args.warmup):
+        step(i)
+    K = args.steps if args.steps is not None else 10
+    t0 = time.perf_counter()
+    for i in range(K):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = Ts * K / dt
+    desc = "%d token(s) of a %d-token window, layers rotated over %d" % (Ts, T, nL)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(dt / K * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "tokens_per_window": T, "hidden": wl.hidden, "experts": wl.n_experts,
+                   "top_k": wl.top_k, "ff": wl.ff, "shared_ff": wl.shared_ff},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="qwen_decode")
+    ap.add_argument("--tokens", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--cpu-tokens", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py: the CUDA path needs a GPU (no CPU fallback)")
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

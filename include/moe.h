@@ -1,0 +1,252 @@
+/*
+ * moe.h -- C ABI of the single-GPU (B300, sm_103a) sparse mixture-of-experts
+ * layer over Q4_K block-quantised experts.
+ *
+ * The layer (pages cited by title and section):
+ *   "Strata 改源码去跑 DeepSeek V4 Flash？要不就试试！" (lcz.me/post/23082),
+ *     section 二 (GGUF anatomy table): routed experts are the fused tensors
+ *     ffn_{gate,up,down}_exps in Q4_K; the always-on shared expert is Q8_0;
+ *     256 routed experts, 6 active, "router bias" on most layers.
+ *     section 三 item 4: one expert is a 1,382,400-byte blob at width 2560.
+ *   "Strata 引擎深度拆解：125B MoE 跑进 2×3090 + EPYC" (lcz.me/topic/2098/5),
+ *     section 二: 48 layers x 512 experts, ~10 active per token, MTP verify
+ *     windows of 3-5 tokens run as one forward; section 一 (CPU ledger): the
+ *     multi-token expert kernel reads an expert's bytes once per window.
+ *   "Qwen3.8-Flash-Next UD-Q4_K_XL 引擎对比：llama.cpp 与 Strata"
+ *     (lcz.me/user/wml-ai/posts), section 一 (部署): Q4_K expert prompt
+ *     (prefill) kernels.
+ *
+ * For each token t with hidden state x_t (bf16, length H):
+ *   1. router logits l_e = sum_h x_t[h] * Wr[e][h]                 (Wr fp32 [E][H])
+ *   2. scores: softmax p = softmax(l), or sigmoid s_e = 1/(1+exp(-l_e));
+ *      the k experts with the largest p (softmax) or s_e + b_e (sigmoid with
+ *      per-expert bias b) are selected, largest first, equal scores to the
+ *      lower id; weights w_r = p_{e_r} / sum_sel p  or  s_{e_r} / sum_sel s.
+ *   3. bucketing: stable counting sort of the T*k assignments a = t*k + r by
+ *      expert id -> expert_offsets[E+1], assign[T*k] (ascending t in an expert).
+ *   4. per assignment: g = Wg x_t, u = Wu x_t, a = SiLU(g) * u   (Wg, Wu [FF][H])
+ *   5. o = sum_f a_f * Wd[f][:]   (Wd stored [FF][H], super-blocks along H)
+ *   6. y_t = sum_r w_r * o_{t,r} (+ the shared expert's FFN of x_t, weight 1).
+ *
+ * Data formats (the pages name Q4_K and Q8_0 but print no layout; the GGUF
+ * layouts are used):
+ *   Q4_K  144 bytes per 256 weights along a row: fp16 d, fp16 dmin,
+ *         12 bytes of packed 6-bit sub-block scales/mins, 128 bytes of 4-bit
+ *         quants; weight = (d*sc_j)*q - dmin*m_j.
+ *   Q8_0  34 bytes per 32 weights: fp16 d then 32 int8; weight = d*q.
+ *   Expert blob  [gate FF x H][up FF x H][down FF x H], each row-major with
+ *         its blocks along H: 3*FF*(H/256)*144 bytes (1,382,400 at H=2560,
+ *         FF=320).  The shared blob has the same order in Q8_0.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise; the
+ *     caller owns every buffer.  The library never allocates device memory
+ *     and never synchronises the stream, except moe_last_device_status().
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Arguments are checked on the host before anything is launched; a
+ *     failing check returns its status and enqueues nothing.
+ *   - Faults found on the device (non-finite pack input, router id out of
+ *     range, a bounded wait that gave up) are recorded in a status word
+ *     and read with moe_last_device_status() (pack calls take their own
+ *     status word).  Nothing traps and nothing throws.
+ *   - Calls sharing one workspace must not overlap on the device (same
+ *     stream, or ordered by events); distinct workspaces are independent.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* == cudaStream_t */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,         /* null pointer, negative size, bad enum value      */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,   /* a shape the kernels do not handle (see moe_config) */
+    MOE_ERR_MISALIGNED = 3,          /* a pointer that must be 16-byte aligned is not    */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes < moe_workspace_bytes(cfg, T)           */
+    MOE_ERR_CUDA = 5,                /* a CUDA runtime call or launch failed             */
+    MOE_ERR_TIMEOUT = 6,             /* a device-side bounded wait gave up               */
+    MOE_ERR_DEVICE_FAULT = 7         /* the device found invalid data (non-finite input,
+                                        an expert id out of range, a null expert blob)   */
+} moe_status;
+
+typedef enum {
+    MOE_SCORE_SOFTMAX = 0,           /* softmax over all E logits, renormalised over k   */
+    MOE_SCORE_SIGMOID_BIAS = 1       /* sigmoid scores; selection by score + bias        */
+} moe_score_fn;
+
+enum {
+    MOE_FLAG_DETERMINISTIC = 1,      /* combine through per-assignment slots in a fixed
+                                        order on every path (bit-identical reruns)        */
+    MOE_FLAG_FORCE_GEMV = 2,         /* use the decode (grouped GEMV) path at any T      */
+    MOE_FLAG_FORCE_GEMM = 4          /* use the prefill (tensor-core GEMM) path at any T */
+};
+
+/*
+ * Layer shape.  Limits: hidden % 256 == 0 and 256 <= hidden <= 8192;
+ * 1 <= n_experts <= 1024; ff % 64 == 0 and 64 <= ff <= 8192;
+ * 1 <= top_k <= min(n_experts, 32); shared_ff == 0 (no shared expert) or
+ * shared_ff % 64 == 0 and <= 8192.
+ */
+typedef struct {
+    int32_t hidden;      /* H                                   */
+    int32_t n_experts;   /* E routed experts                    */
+    int32_t ff;          /* expert intermediate width FF        */
+    int32_t top_k;       /* k experts per token                 */
+    int32_t score_fn;    /* moe_score_fn                        */
+    int32_t shared_ff;   /* shared expert width, 0 = none       */
+    int32_t flags;       /* MOE_FLAG_*                          */
+    int32_t reserved;    /* must be 0                           */
+} moe_config;
+
+/* ---------------------------------------------------------------- sizes */
+
+/* Bytes of a [rows][cols] matrix in Q4_K (cols % 256 == 0): rows*cols/256*144.
+ * Returns 0 for an invalid shape. */
+MOE_API size_t moe_q4k_bytes(int64_t rows, int64_t cols);
+/* Bytes of a [rows][cols] matrix in Q8_0 (cols % 32 == 0): rows*cols/32*34. */
+MOE_API size_t moe_q8_0_bytes(int64_t rows, int64_t cols);
+/* Bytes of one routed-expert blob, 3*moe_q4k_bytes(ff, hidden); 0 if cfg invalid. */
+MOE_API size_t moe_expert_bytes(const moe_config *cfg);
+/* Bytes of the shared-expert blob, 3*moe_q8_0_bytes(shared_ff, hidden); 0 if none. */
+MOE_API size_t moe_shared_bytes(const moe_config *cfg);
+
+/* ---------------------------------------------------------------- packing */
+
+/*
+ * Quantise a row-major fp32 matrix w[rows][cols] (device) to Q4_K, written
+ * to out (device, moe_q4k_bytes(rows, cols) bytes, 16-byte aligned).  The
+ * quantiser is deterministic (fp32 IEEE, round half to even) and gives the
+ * same bytes as its definition everywhere:
+ *   per 32-weight sub-block: mn = min(0, min x), mx = max x,
+ *     scale_j = (mx - mn)/15, nmin_j = -mn;
+ *   d = fp16(max_j scale_j / 63), dmin = fp16(max_j nmin_j / 63);
+ *   sc_j = d > 0 ? min(63, rint(scale_j / d)) : 0  (m_j alike with dmin);
+ *   q = d*sc_j > 0 ? clamp(rint((x + dmin*m_j) / (d*sc_j)), 0, 15) : 0.
+ * Non-finite input, or a d / dmin that overflows fp16, sets *dev_status
+ * (device uint32, may be NULL) to MOE_ERR_DEVICE_FAULT; the block is still
+ * written.  Errors: INVALID_ARG (null, rows < 0), UNSUPPORTED_SHAPE
+ * (cols % 256), MISALIGNED (out or w not 16-byte aligned), CUDA.
+ */
+MOE_API moe_status moe_pack_q4k(const float *w, int64_t rows, int64_t cols, uint8_t *out,
+                        uint32_t *dev_status, moe_stream_t stream);
+
+/*
+ * Quantise w[rows][cols] (device fp32) to Q8_0: d = fp16(max|x|/127),
+ * q = d > 0 ? clamp(rint(x/d), -127, 127) : 0.  cols % 32 == 0; out gets
+ * moe_q8_0_bytes(rows, cols) bytes.  cols*34/32 must be a multiple of 16 for
+ * rows to stay 16-byte aligned (cols % 256 == 0 always satisfies it); errors
+ * as moe_pack_q4k.
+ */
+MOE_API moe_status moe_pack_q8_0(const float *w, int64_t rows, int64_t cols, uint8_t *out,
+                         uint32_t *dev_status, moe_stream_t stream);
+
+/* Test hooks: dequantise a Q4_K / Q8_0 matrix to fp32 out[rows][cols]
+ * (device).  Bit-exact with the format definition (each product and the
+ * difference rounded to fp32 separately). */
+MOE_API moe_status moe_dequant_q4k(const uint8_t *blocks, int64_t rows, int64_t cols, float *out,
+                           moe_stream_t stream);
+MOE_API moe_status moe_dequant_q8_0(const uint8_t *blocks, int64_t rows, int64_t cols, float *out,
+                            moe_stream_t stream);
+
+/* ---------------------------------------------------------------- workspace */
+
+/*
+ * Device workspace bytes for calls with up to max_tokens tokens (0 if cfg is
+ * invalid).  The workspace holds routing results, intermediate activations,
+ * accumulators and the device status word.  Before its first use, a
+ * workspace must be initialised with moe_workspace_init (it zeroes the
+ * 256-byte header that holds the status word and the completion counters).
+ */
+MOE_API size_t moe_workspace_bytes(const moe_config *cfg, int32_t max_tokens);
+MOE_API moe_status moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- the layer */
+
+/*
+ * Steps 1-3 only.  x: bf16 [T][H] (16-byte aligned); router_w: fp32 [E][H];
+ * router_bias: fp32 [E] (required for MOE_SCORE_SIGMOID_BIAS, may be NULL
+ * there to mean zero; ignored for softmax).  Outputs (device): topk_ids
+ * int32 [T][k], topk_w fp32 [T][k], expert_offsets int32 [E+1],
+ * assign int32 [T*k].  T may be 0 (offsets become all zero).
+ */
+MOE_API moe_status moe_route(const moe_config *cfg, const uint16_t *x, const float *router_w,
+                     const float *router_bias, int32_t T, int32_t *topk_ids, float *topk_w,
+                     int32_t *expert_offsets, int32_t *assign, void *ws, size_t ws_bytes,
+                     moe_stream_t stream);
+
+/*
+ * The whole layer.  expert_blobs: DEVICE array of E device pointers, each to
+ * a 16-byte aligned expert blob (moe_expert_bytes); an expert that no token
+ * selects may be NULL.  shared_blob: the shared expert's blob
+ * (moe_shared_bytes) when cfg->shared_ff > 0, else ignored.  Output y:
+ * bf16 [T][H]; y_f32: optional fp32 [T][H] copy before rounding (may be NULL).
+ * The routing of the call stays readable in the workspace
+ * (moe_workspace_routing) until the next call.
+ * Path: T <= 8 (or MOE_FLAG_FORCE_GEMV) streams the selected experts with a
+ * grouped GEMV in fp32; larger T runs the tensor-core grouped GEMM with fp16
+ * operands and fp32 accumulation.
+ */
+MOE_API moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *router_w,
+                       const float *router_bias, const uint8_t *const *expert_blobs,
+                       const uint8_t *shared_blob, int32_t T, uint16_t *y, float *y_f32,
+                       void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Device pointers, inside ws, to the routing of the last moe_forward with
+ * this workspace and T tokens: ids [T][k], w [T][k], offsets [E+1],
+ * assign [T*k].  Any out pointer may be NULL.  No device work.
+ */
+MOE_API moe_status moe_workspace_routing(const moe_config *cfg, int32_t T, const void *ws, size_t ws_bytes,
+                                 const int32_t **ids, const float **w, const int32_t **offsets,
+                                 const int32_t **assign);
+
+/*
+ * Synchronises `stream`, then returns the first device-side fault recorded
+ * in the workspace's status word since the last call of this function
+ * (MOE_OK if none) and clears it.
+ */
+MOE_API moe_status moe_last_device_status(void *ws, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- diagnostics */
+
+/*
+ * Per-kernel timing for benchmarks.  While enabled, every kernel launch made
+ * by moe_forward / moe_route is bracketed by two CUDA events recorded on the
+ * call's stream (not while the stream is being captured into a graph), and
+ * the launches are counted per kernel.  Enabling (on != 0) or disabling
+ * resets the counters.  Host-global state: use from one host thread.
+ */
+typedef struct {
+    const char *name;     /* kernel name (static string)                    */
+    int64_t launches;     /* launches counted since the last reset          */
+    int64_t timed;        /* launches with an event pair (<= launches)      */
+    double total_ms;      /* sum of event-measured durations of those       */
+} moe_profile_entry;
+
+MOE_API moe_status moe_profile_enable(int32_t on);
+/* Waits for the recorded events, fills up to max_entries entries (kernels
+ * with at least one launch) and returns how many it filled. */
+MOE_API int32_t moe_profile_read(moe_profile_entry *out, int32_t max_entries);
+
+/* Static string for a status code. */
+MOE_API const char *moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

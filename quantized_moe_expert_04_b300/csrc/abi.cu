@@ -1,0 +1,307 @@
+// abi.cu -- the extern "C" entry points of libmoe.so: host-side argument
+// checks, workspace layout, and the sequence of kernel launches of a call.
+// The ABI itself (argument meaning, layouts, ownership, errors) is specified
+// in include/moe.h.
+#include <algorithm>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static bool cfg_valid(const moe_config *c)
+{
+    if (!c) return false;
+    if (c->hidden < 256 || c->hidden > 8192 || c->hidden % 256) return false;
+    if (c->n_experts < 1 || c->n_experts > 1024) return false;
+    if (c->ff < 64 || c->ff > 8192 || c->ff % 64) return false;
+    if (c->top_k < 1 || c->top_k > 32 || c->top_k > c->n_experts) return false;
+    if (c->score_fn != MOE_SCORE_SOFTMAX && c->score_fn != MOE_SCORE_SIGMOID_BIAS) return false;
+    if (c->shared_ff != 0 && (c->shared_ff < 64 || c->shared_ff > 8192 || c->shared_ff % 64)) return false;
+    if (c->reserved != 0) return false;
+    return true;
+}
+
+bool use_gemv(const moe_config &c, int32_t T)
+{
+    if (c.flags & MOE_FLAG_FORCE_GEMV) return true;
+    if (c.flags & MOE_FLAG_FORCE_GEMM) return false;
+    return T <= kGemvMaxTokens;
+}
+
+WsLayout ws_layout(const moe_config &c, int32_t T)
+{
+    WsLayout L{};
+    const size_t TK = (size_t)T * c.top_k, E = c.n_experts, H = c.hidden;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    L.header = take(kHeaderBytes);
+    L.logits = take((size_t)T * E * 4);
+    L.ids = take(TK * 4);
+    L.w = take(TK * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.assign = take(TK * 4);
+    L.active = take((E + 1) * 4);
+    L.act = take(TK * c.ff * 4);
+    L.slots = take(TK * H * 4);
+    L.yacc = take((size_t)T * H * 4);
+    L.x16 = take((size_t)T * H * 2);
+    L.sh_act = take(c.shared_ff ? (size_t)T * c.shared_ff * 4 : 0);
+    L.sh_out = take(c.shared_ff ? (size_t)T * H * 4 : 0);
+    L.tiles = take(0);
+    L.total = off;
+    return L;
+}
+
+static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_q4k_bytes(int64_t rows, int64_t cols)
+{
+    if (rows < 0 || cols <= 0 || cols % kQK) return 0;
+    return (size_t)rows * (size_t)(cols / kQK) * kQ4KBytes;
+}
+
+size_t moe_q8_0_bytes(int64_t rows, int64_t cols)
+{
+    if (rows < 0 || cols <= 0 || cols % kQK8) return 0;
+    return (size_t)rows * (size_t)(cols / kQK8) * kQ8Bytes;
+}
+
+size_t moe_expert_bytes(const moe_config *cfg)
+{
+    if (!cfg_valid(cfg)) return 0;
+    return 3 * moe_q4k_bytes(cfg->ff, cfg->hidden);
+}
+
+size_t moe_shared_bytes(const moe_config *cfg)
+{
+    if (!cfg_valid(cfg) || cfg->shared_ff == 0) return 0;
+    return 3 * moe_q8_0_bytes(cfg->shared_ff, cfg->hidden);
+}
+
+moe_status moe_pack_q4k(const float *w, int64_t rows, int64_t cols, uint8_t *out, uint32_t *dev_status,
+                        moe_stream_t stream)
+{
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % kQK) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!w || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(out)) return MOE_ERR_MISALIGNED;
+    return cuda_status(launch_pack_q4k(w, rows * (cols / kQK), out, dev_status, (cudaStream_t)stream));
+}
+
+moe_status moe_pack_q8_0(const float *w, int64_t rows, int64_t cols, uint8_t *out, uint32_t *dev_status,
+                         moe_stream_t stream)
+{
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % kQK8) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!w || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(out)) return MOE_ERR_MISALIGNED;
+    return cuda_status(launch_pack_q8_0(w, rows * (cols / kQK8), out, dev_status, (cudaStream_t)stream));
+}
+
+moe_status moe_dequant_q4k(const uint8_t *blocks, int64_t rows, int64_t cols, float *out, moe_stream_t stream)
+{
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % kQK) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(blocks) || !aligned16(out)) return MOE_ERR_MISALIGNED;
+    return cuda_status(launch_dequant_q4k(blocks, rows * (cols / kQK), out, (cudaStream_t)stream));
+}
+
+moe_status moe_dequant_q8_0(const uint8_t *blocks, int64_t rows, int64_t cols, float *out, moe_stream_t stream)
+{
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % kQK8) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !out) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_dequant_q8_0(blocks, rows * (cols / kQK8), out, (cudaStream_t)stream));
+}
+
+size_t moe_workspace_bytes(const moe_config *cfg, int32_t max_tokens)
+{
+    if (!cfg_valid(cfg) || max_tokens < 0) return 0;
+    return ws_layout(*cfg, max_tokens).total;
+}
+
+moe_status moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!ws || ws_bytes < (size_t)kHeaderBytes) return MOE_ERR_INVALID_ARG;
+    return cuda_status(cudaMemsetAsync(ws, 0, kHeaderBytes, (cudaStream_t)stream));
+}
+
+static moe_status check_call(const moe_config *cfg, const uint16_t *x, const float *router_w,
+                             const float *router_bias, int32_t T, void *ws, size_t ws_bytes)
+{
+    if (!cfg_valid(cfg)) {
+        if (!cfg) return MOE_ERR_INVALID_ARG;
+        if (cfg->score_fn != MOE_SCORE_SOFTMAX && cfg->score_fn != MOE_SCORE_SIGMOID_BIAS)
+            return MOE_ERR_INVALID_ARG;
+        if (cfg->reserved != 0 || cfg->top_k < 1 || cfg->top_k > cfg->n_experts) return MOE_ERR_INVALID_ARG;
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !router_w)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ws) || (x && !aligned16(x)) || (router_w && !aligned16(router_w)))
+        return MOE_ERR_MISALIGNED;
+    (void)router_bias;
+    if (ws_bytes < ws_layout(*cfg, T).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return MOE_OK;
+}
+
+static RouteArgs route_args(const moe_config *cfg, const uint16_t *x, const float *router_w,
+                            const float *router_bias, int32_t T, void *ws)
+{
+    const WsLayout L = ws_layout(*cfg, T);
+    char *base = (char *)ws;
+    RouteArgs r{};
+    r.H = cfg->hidden;
+    r.E = cfg->n_experts;
+    r.k = cfg->top_k;
+    r.T = T;
+    r.score_fn = cfg->score_fn;
+    r.x = x;
+    r.wr = router_w;
+    r.bias = router_bias;
+    r.logits = (float *)(base + L.logits);
+    r.ids = (int32_t *)(base + L.ids);
+    r.w = (float *)(base + L.w);
+    r.counts = (int32_t *)(base + L.counts);
+    r.offsets = (int32_t *)(base + L.offsets);
+    r.assign = (int32_t *)(base + L.assign);
+    r.active = (int32_t *)(base + L.active);
+    r.header = (uint32_t *)(base + L.header);
+    return r;
+}
+
+moe_status moe_route(const moe_config *cfg, const uint16_t *x, const float *router_w,
+                     const float *router_bias, int32_t T, int32_t *topk_ids, float *topk_w,
+                     int32_t *expert_offsets, int32_t *assign, void *ws, size_t ws_bytes,
+                     moe_stream_t stream)
+{
+    moe_status st = check_call(cfg, x, router_w, router_bias, T, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (!expert_offsets || (T > 0 && (!topk_ids || !topk_w || !assign))) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    RouteArgs r = route_args(cfg, x, router_w, router_bias, T, ws);
+    cudaError_t e = launch_route(r, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    const size_t TK = (size_t)T * cfg->top_k;
+    if (TK) {
+        e = cudaMemcpyAsync(topk_ids, r.ids, TK * 4, cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(topk_w, r.w, TK * 4, cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(assign, r.assign, TK * 4, cudaMemcpyDeviceToDevice, s);
+    }
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(expert_offsets, r.offsets, (cfg->n_experts + 1) * 4, cudaMemcpyDeviceToDevice, s);
+    return cuda_status(e);
+}
+
+moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *router_w,
+                       const float *router_bias, const uint8_t *const *expert_blobs,
+                       const uint8_t *shared_blob, int32_t T, uint16_t *y, float *y_f32, void *ws,
+                       size_t ws_bytes, moe_stream_t stream)
+{
+    moe_status st = check_call(cfg, x, router_w, router_bias, T, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (T > 0 && (!y || !expert_blobs)) return MOE_ERR_INVALID_ARG;
+    if (cfg->shared_ff > 0 && T > 0 && !shared_blob) return MOE_ERR_INVALID_ARG;
+    if ((y && !aligned16(y)) || (y_f32 && !aligned16(y_f32)) || (shared_blob && !aligned16(shared_blob)))
+        return MOE_ERR_MISALIGNED;
+    if (T == 0) return MOE_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    RouteArgs r = route_args(cfg, x, router_w, router_bias, T, ws);
+    cudaError_t e = launch_route(r, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    const WsLayout L = ws_layout(*cfg, T);
+    char *base = (char *)ws;
+    ExpertArgs a{};
+    a.H = cfg->hidden;
+    a.E = cfg->n_experts;
+    a.FF = cfg->ff;
+    a.k = cfg->top_k;
+    a.T = T;
+    a.SFF = cfg->shared_ff;
+    a.x = x;
+    a.blobs = expert_blobs;
+    a.shared_blob = cfg->shared_ff > 0 ? shared_blob : nullptr;
+    a.offsets = r.offsets;
+    a.assign = r.assign;
+    a.active = r.active;
+    a.w = r.w;
+    a.act = (float *)(base + L.act);
+    a.slots = (float *)(base + L.slots);
+    a.sh_act = cfg->shared_ff ? (float *)(base + L.sh_act) : nullptr;
+    a.sh_out = cfg->shared_ff ? (float *)(base + L.sh_out) : nullptr;
+    a.y = y;
+    a.y_f32 = y_f32;
+    a.header = r.header;
+    e = launch_experts_gemv(a, s);
+    return cuda_status(e);
+}
+
+moe_status moe_workspace_routing(const moe_config *cfg, int32_t T, const void *ws, size_t ws_bytes,
+                                 const int32_t **ids, const float **w, const int32_t **offsets,
+                                 const int32_t **assign)
+{
+    if (!cfg_valid(cfg) || !ws || T < 0) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*cfg, T);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    const char *base = (const char *)ws;
+    if (ids) *ids = (const int32_t *)(base + L.ids);
+    if (w) *w = (const float *)(base + L.w);
+    if (offsets) *offsets = (const int32_t *)(base + L.offsets);
+    if (assign) *assign = (const int32_t *)(base + L.assign);
+    return MOE_OK;
+}
+
+moe_status moe_last_device_status(void *ws, moe_stream_t stream)
+{
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (v != 0) {
+        e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return (moe_status)v;
+}
+
+const char *moe_status_string(moe_status status)
+{
+    switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_FAULT: return "device found invalid data";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,113 @@
+// moe_internal.cuh -- internal declarations shared by the CUDA translation
+// units of libmoe.so (kernels + C ABI).  Nothing here is part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---- block formats (GGUF layouts; the pages name Q4_K / Q8_0 for the expert
+// ---- tensors in the DeepSeek-V4-Flash GGUF anatomy table, section 二)
+constexpr int kQK = 256;          // weights per Q4_K super-block
+constexpr int kQ4KBytes = 144;    // fp16 d, fp16 dmin, scales[12], qs[128]
+constexpr int kQK8 = 32;          // weights per Q8_0 block
+constexpr int kQ8Bytes = 34;      // fp16 d, int8 qs[32]
+
+constexpr int kHeaderBytes = 256; // workspace header (status word, counters)
+constexpr int kGemvMaxTokens = 8; // decode windows: MTP verify windows of 1-8 tokens
+
+// Header words of the workspace.
+enum HeaderWord : int {
+    kHdrStatus = 0,       // first device-side fault (moe_status), sticky until read
+    kHdrNActive = 1,      // number of experts with at least one token
+    kHdrTileCount = 2,    // prefill: number of GEMM work tiles
+    kHdrCounter0 = 8,     // completion counters, reset by their last user
+};
+
+__device__ __forceinline__ void set_status(uint32_t *status, uint32_t code)
+{
+    if (status) atomicCAS(status, 0u, code);
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t h)
+{
+    return __half2float(__ushort_as_half((unsigned short)h));
+}
+
+// 6-bit scale / min of sub-block j from the 12 packed bytes.
+__device__ __forceinline__ void q4k_scale_min(const uint8_t *scales, int j, int &sc, int &m)
+{
+    if (j < 4) {
+        sc = scales[j] & 63;
+        m = scales[j + 4] & 63;
+    } else {
+        sc = (scales[j + 4] & 15) | ((scales[j - 4] >> 6) << 4);
+        m = (scales[j + 4] >> 4) | ((scales[j] >> 6) << 4);
+    }
+}
+
+// Kernels counted / timed by the diagnostics API (moe_profile_*).
+enum Phase : int {
+    kPhRouterLogits = 0, kPhTopk, kPhBucket, kPhGateUp, kPhGateUpShared, kPhDown, kPhDownShared,
+    kPhCombine, kPhGemmPrep, kPhGemmGateUp, kPhGemmDown, kPhGemmFinish, kNumPhases
+};
+void prof_begin(int phase, cudaStream_t s);   // no-ops unless profiling is enabled
+void prof_end(int phase, cudaStream_t s);
+
+// Workspace regions (byte offsets from the workspace base) for one call shape.
+struct WsLayout {
+    size_t header, logits, ids, w, counts, offsets, assign, active;
+    size_t act, slots, yacc, x16, sh_act, sh_out, tiles;
+    size_t total;
+};
+
+// Routing path choice for T tokens under cfg flags.
+bool use_gemv(const moe_config &c, int32_t T);
+WsLayout ws_layout(const moe_config &c, int32_t T);
+
+// ---- launchers (each returns cudaGetLastError() of its launches) ----------
+cudaError_t launch_pack_q4k(const float *w, int64_t nblocks, uint8_t *out, uint32_t *status,
+                            cudaStream_t s);
+cudaError_t launch_pack_q8_0(const float *w, int64_t nblocks, uint8_t *out, uint32_t *status,
+                             cudaStream_t s);
+cudaError_t launch_dequant_q4k(const uint8_t *blk, int64_t nblocks, float *out, cudaStream_t s);
+cudaError_t launch_dequant_q8_0(const uint8_t *blk, int64_t nblocks, float *out, cudaStream_t s);
+
+struct RouteArgs {
+    int H, E, k, T, score_fn;
+    const uint16_t *x;
+    const float *wr, *bias;
+    float *logits;
+    int32_t *ids;
+    float *w;
+    int32_t *counts, *offsets, *assign, *active;
+    uint32_t *header;
+};
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t s);
+
+struct ExpertArgs {
+    int H, E, FF, k, T, SFF;
+    const uint16_t *x;                  // bf16 [T][H]
+    const uint8_t *const *blobs;        // device table [E]
+    const uint8_t *shared_blob;         // Q8_0 or null
+    const int32_t *offsets, *assign, *active;
+    const float *w;                     // routing weights [T*k]
+    float *act;                         // [T*k][FF] by bucket position
+    float *slots;                       // [T*k][H]
+    float *sh_act;                      // [T][SFF]
+    float *sh_out;                      // [T][H]
+    uint16_t *y;                        // bf16 [T][H]
+    float *y_f32;                       // optional
+    uint32_t *header;
+};
+cudaError_t launch_experts_gemv(const ExpertArgs &a, cudaStream_t s);
+
+}  // namespace moe

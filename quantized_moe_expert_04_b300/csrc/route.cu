@@ -1,0 +1,316 @@
+// route.cu -- router scoring, top-k selection and token-to-expert bucketing.
+//
+// The router picks ~10 of 512 experts per token in the Qwen-shaped model
+// ("Strata 引擎深度拆解", lcz.me/topic/2098/5, section 二) and 6 of 256
+// with a per-expert router bias in the DeepSeek-shaped one ("Strata 改源码去跑
+// DeepSeek V4 Flash？", lcz.me/post/23082, section 二, anatomy table).  The
+// multi-token expert kernel of the teardown page (section 一, CPU ledger)
+// computes each expert once for all tokens of a window; the bucketing below
+// groups a window's (token, slot) assignments by expert for exactly that.
+//
+// Kernels:
+//   k_router_logits  fp32 logits [T][E]: warps own experts, a CTA owns up to
+//                    8 tokens whose bf16 rows sit in shared memory, so each
+//                    router row is read once per 8 tokens.
+//   k_topk           one warp per token, E/32 logits per lane in registers,
+//                    k rounds of a warp arg-max (equal keys: lower id).
+//   k_bucket         one CTA: stable counting sort of the T*k assignments.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+constexpr int kRouterTokens = 8;     // tokens per CTA in the logits kernel
+constexpr int kRouterWarps = 4;      // warps per CTA (one expert row at a time each)
+constexpr int kMaxPerLane = 32;      // E <= 1024 logits per warp
+
+__global__ void __launch_bounds__(kRouterWarps * 32)
+k_router_logits(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H, int E,
+                int experts_per_cta, float *__restrict__ logits)
+{
+    extern __shared__ __align__(16) uint16_t xs[];     // [kRouterTokens][H] bf16
+    const int t0 = blockIdx.y * kRouterTokens;
+    const int nt = min(kRouterTokens, T - t0);
+    // stage the token rows (16-byte vectors)
+    {
+        const int vec_per_row = H / 8;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)t0 * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(xs);
+        for (int i = threadIdx.x; i < nt * vec_per_row; i += blockDim.x) dst[i] = src[i];
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int e_begin = blockIdx.x * experts_per_cta;
+    const int e_end = min(E, e_begin + experts_per_cta);
+    for (int e = e_begin + warp; e < e_end; e += kRouterWarps) {
+        const float4 *row = reinterpret_cast<const float4 *>(wr + (int64_t)e * H);
+        float acc[kRouterTokens];
+#pragma unroll
+        for (int t = 0; t < kRouterTokens; ++t) acc[t] = 0.0f;
+        for (int h4 = lane; h4 < H / 4; h4 += 32) {
+            const float4 wv = row[h4];
+#pragma unroll
+            for (int t = 0; t < kRouterTokens; ++t) {
+                if (t < nt) {
+                    const uint2 xv = *reinterpret_cast<const uint2 *>(xs + t * H + 4 * h4);
+                    acc[t] = fmaf(wv.x, bf16_bits_to_f32(xv.x & 0xffff), acc[t]);
+                    acc[t] = fmaf(wv.y, bf16_bits_to_f32(xv.x >> 16), acc[t]);
+                    acc[t] = fmaf(wv.z, bf16_bits_to_f32(xv.y & 0xffff), acc[t]);
+                    acc[t] = fmaf(wv.w, bf16_bits_to_f32(xv.y >> 16), acc[t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kRouterTokens; ++t) {
+            float v = acc[t];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == t && t < nt) logits[(int64_t)(t0 + t) * E + e] = v;
+        }
+    }
+}
+
+// One warp per token.  Keys: the logit (softmax: the order of p equals the
+// order of the logits) or s_e + b_e (sigmoid).  Weights: softmax over the k
+// selected logits (= the full softmax renormalised over the k), or
+// s_e / sum of the selected s.
+__global__ void __launch_bounds__(256)
+k_topk(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k,
+       int score_fn, int32_t *__restrict__ ids, float *__restrict__ wout, uint32_t *status)
+{
+    const int lane = threadIdx.x & 31;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const float *lrow = logits + (int64_t)t * E;
+    float key[kMaxPerLane], val[kMaxPerLane];
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = -INFINITY;
+        val[i] = 0.0f;
+        if (e < E) {
+            const float l = lrow[e];
+            if (score_fn == MOE_SCORE_SOFTMAX) {
+                key[i] = l;
+                val[i] = l;
+            } else {
+                const float sg = 1.0f / (1.0f + expf(-l));
+                val[i] = sg;
+                key[i] = sg + (bias ? bias[e] : 0.0f);
+            }
+        }
+    }
+    uint32_t taken = 0;
+    int my_id = 0;
+    float my_val = 0.0f;
+    bool fault = false;
+    for (int r = 0; r < k; ++r) {
+        // this lane's best untaken key (ascending ids: '>' keeps the lower id)
+        float bv = -INFINITY, bval = 0.0f;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && (be == 0x7fffffff || key[i] > bv)) {
+                bv = key[i];
+                be = e;
+                bval = val[i];
+            }
+        }
+        // warp arg-max; equal keys -> lower id; NaN loses to any number
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            const float oval = __shfl_xor_sync(0xffffffffu, bval, off);
+            bool take = false;
+            if (oe != 0x7fffffff) {
+                if (be == 0x7fffffff) take = true;
+                else if (isnan(bv)) take = !isnan(ov) || oe < be;
+                else if (!isnan(ov)) take = ov > bv || (ov == bv && oe < be);
+            }
+            if (take) {
+                bv = ov;
+                be = oe;
+                bval = oval;
+            }
+        }
+        if (be == 0x7fffffff || isnan(bv)) {  // nothing selectable: non-finite router input
+            fault = true;
+            be = r;
+            bval = 0.0f;
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == r) {
+            my_id = be;
+            my_val = bval;
+        }
+    }
+    // weights over the k selected (lane r holds selection r)
+    float num;
+    if (score_fn == MOE_SCORE_SOFTMAX) {
+        const float lmax = __shfl_sync(0xffffffffu, my_val, 0);   // the first pick is the largest
+        num = lane < k ? expf(my_val - lmax) : 0.0f;
+    } else {
+        num = lane < k ? my_val : 0.0f;
+    }
+    float den = num;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    if (lane < k) {
+        ids[(int64_t)t * k + lane] = my_id;
+        wout[(int64_t)t * k + lane] = num / den;
+    }
+    if (fault && lane == 0) set_status(status, MOE_ERR_DEVICE_FAULT);
+}
+
+// Stable counting sort of the T*k assignments by expert, one CTA of 1024
+// threads.  Warp w owns the contiguous assignment range [w*S, (w+1)*S):
+//   1. per-warp histograms hist[w][e] (shared memory);
+//   2. for each expert, the warps' counts are prefix-summed in warp order and
+//      the expert totals scanned -> offsets; base[w][e] = where warp w's
+//      first assignment to e goes;
+//   3. each warp walks its range in order, 32 at a time; lanes with the same
+//      expert are ranked by lane index (__match_any_sync) so the order of
+//      equal keys is the input order -- the sort is stable.
+// Also writes the ascending list of experts that received tokens.
+constexpr int kBucketThreads = 1024;
+constexpr int kBucketWarps = kBucketThreads / 32;
+
+__global__ void __launch_bounds__(kBucketThreads)
+k_bucket(const int32_t *__restrict__ ids, int TK, int E, int32_t *__restrict__ counts,
+         int32_t *__restrict__ offsets, int32_t *__restrict__ assign, int32_t *__restrict__ active,
+         uint32_t *header)
+{
+    extern __shared__ int32_t sh[];              // hist[kBucketWarps][E], then scan scratch
+    int32_t *hist = sh;
+    int32_t *scan = sh + kBucketWarps * E;       // [kBucketThreads]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kBucketWarps * E; i += kBucketThreads) hist[i] = 0;
+    __syncthreads();
+    const int S = (TK + kBucketWarps - 1) / kBucketWarps;
+    const int a0 = warp * S, a1 = min(TK, a0 + S);
+    bool bad = false;
+    for (int a = a0 + lane; a < a1; a += 32) {
+        const int e = ids[a];
+        if (e >= 0 && e < E) atomicAdd(&hist[warp * E + e], 1);
+        else bad = true;
+    }
+    __syncthreads();
+    // per expert: prefix over warps (in place), expert total
+    const int per_thread = (E + kBucketThreads - 1) / kBucketThreads;
+    int local_total = 0;
+    for (int j = 0; j < per_thread; ++j) {
+        const int e = threadIdx.x * per_thread + j;
+        if (e < E) {
+            int run = 0;
+            for (int w = 0; w < kBucketWarps; ++w) {
+                const int c = hist[w * E + e];
+                hist[w * E + e] = run;
+                run += c;
+            }
+            counts[e] = run;
+            local_total += run;
+        }
+    }
+    // block exclusive scan of the per-thread totals (contiguous expert ranges)
+    scan[threadIdx.x] = local_total;
+    __syncthreads();
+    for (int off = 1; off < kBucketThreads; off <<= 1) {
+        const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
+        __syncthreads();
+        scan[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int base = scan[threadIdx.x] - local_total;
+    int n_active_before = 0;
+    // count actives in earlier threads: second scan on (count > 0)
+    int local_active = 0;
+    for (int j = 0; j < per_thread; ++j) {
+        const int e = threadIdx.x * per_thread + j;
+        if (e < E && counts[e] > 0) ++local_active;
+    }
+    __syncthreads();
+    scan[threadIdx.x] = local_active;
+    __syncthreads();
+    for (int off = 1; off < kBucketThreads; off <<= 1) {
+        const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
+        __syncthreads();
+        scan[threadIdx.x] += v;
+        __syncthreads();
+    }
+    n_active_before = scan[threadIdx.x] - local_active;
+    for (int j = 0; j < per_thread; ++j) {
+        const int e = threadIdx.x * per_thread + j;
+        if (e < E) {
+            const int c = counts[e];
+            offsets[e] = base;
+            for (int w = 0; w < kBucketWarps; ++w) hist[w * E + e] += base;
+            base += c;
+            if (c > 0) active[n_active_before++] = e;
+        }
+    }
+    if (threadIdx.x == kBucketThreads - 1) {
+        offsets[E] = base;                        // = number of valid assignments
+        header[kHdrNActive] = (uint32_t)n_active_before;
+    }
+    __syncthreads();
+    // stable scatter
+    for (int c0 = a0; c0 < a1; c0 += 32) {
+        const int a = c0 + lane;
+        const bool valid = a < a1;
+        int e = valid ? ids[a] : -1;
+        if (e < 0 || e >= E) e = -1 - lane;      // unique non-matching key for invalid lanes
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        int pos = 0;
+        if (valid && e >= 0) pos = hist[warp * E + e] + rank;
+        __syncwarp();
+        if (valid && e >= 0) {
+            assign[pos] = a;
+            if (rank == 0) hist[warp * E + e] += __popc(peers);
+        }
+        __syncwarp();
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(header + kHdrStatus, MOE_ERR_DEVICE_FAULT);
+}
+
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
+{
+    if (a.T <= 0) {
+        // offsets all zero, no active experts
+        cudaMemsetAsync(a.offsets, 0, sizeof(int32_t) * (a.E + 1), s);
+        cudaMemsetAsync(a.counts, 0, sizeof(int32_t) * a.E, s);
+        cudaMemsetAsync(a.header + kHdrNActive, 0, sizeof(uint32_t), s);
+        return cudaGetLastError();
+    }
+    // opt-in shared memory limits, set once per process (the kernels run on one device per process)
+    static bool attrs_set = false;
+    if (!attrs_set) {
+        cudaFuncSetAttribute(k_router_logits, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kRouterTokens * 8192 * sizeof(uint16_t)));
+        cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)((kBucketWarps * 1024 + kBucketThreads) * sizeof(int32_t)));
+        attrs_set = true;
+    }
+    const size_t xs_bytes = (size_t)kRouterTokens * a.H * sizeof(uint16_t);
+    const int experts_per_cta = a.T > kRouterTokens ? 16 * kRouterWarps : kRouterWarps;
+    dim3 grid((a.E + experts_per_cta - 1) / experts_per_cta, (a.T + kRouterTokens - 1) / kRouterTokens);
+    prof_begin(kPhRouterLogits, s);
+    k_router_logits<<<grid, kRouterWarps * 32, xs_bytes, s>>>(a.x, a.wr, a.T, a.H, a.E, experts_per_cta,
+                                                              a.logits);
+    prof_end(kPhRouterLogits, s);
+    const int warps_per_block = 8;
+    prof_begin(kPhTopk, s);
+    k_topk<<<(a.T + warps_per_block - 1) / warps_per_block, warps_per_block * 32, 0, s>>>(
+        a.logits, a.score_fn == MOE_SCORE_SIGMOID_BIAS ? a.bias : nullptr, a.T, a.E, a.k, a.score_fn,
+        a.ids, a.w, a.header + kHdrStatus);
+    prof_end(kPhTopk, s);
+    const size_t sh = (size_t)(kBucketWarps * a.E + kBucketThreads) * sizeof(int32_t);
+    prof_begin(kPhBucket, s);
+    k_bucket<<<1, kBucketThreads, sh, s>>>(a.ids, a.T * a.k, a.E, a.counts, a.offsets, a.assign, a.active,
+                                           a.header);
+    prof_end(kPhBucket, s);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

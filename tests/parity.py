@@ -1,0 +1,74 @@
+"""Shared helpers of the parity tests: tolerances, id comparison, oracle runs.
+
+Tolerances (the layer's stated bar): expert ids bit-exact except where the
+oracle's k-th and (k+1)-th selection keys lie within 1e-6 of each other
+(reported); outputs within relative L2 <= 5e-3 and max-abs <= 2e-2 * max|ref|.
+"""
+import numpy as np
+import torch
+
+import oracle
+from quantized_moe_expert_04_b300 import synth
+
+REL_L2 = 5e-3
+MAX_ABS_FRAC = 2e-2
+NEAR_TIE = 1e-6
+
+
+def check_close(got, ref, rel_l2=REL_L2, max_abs_frac=MAX_ABS_FRAC, what="y"):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    if ref.size == 0:
+        return 0.0, 0.0
+    assert np.isfinite(got).all(), "%s: non-finite output" % what
+    den = np.linalg.norm(ref)
+    rl = np.linalg.norm(got - ref) / den if den > 0 else np.linalg.norm(got)
+    scale = np.abs(ref).max()
+    ma = np.abs(got - ref).max() / scale if scale > 0 else np.abs(got).max()
+    assert rl <= rel_l2, "%s: rel-L2 %.3e > %.1e" % (what, rl, rel_l2)
+    assert ma <= max_abs_frac, "%s: max-abs %.3e * max|ref| > %.1e" % (what, ma, max_abs_frac)
+    return rl, ma
+
+
+def compare_ids(gpu_ids, orc_ids, kth_key, next_key):
+    """Tokens whose selected id sets differ; every one must be an oracle near-tie.
+
+    Returns the list of differing tokens (reported by the caller)."""
+    gpu_ids = np.asarray(gpu_ids)
+    orc_ids = np.asarray(orc_ids)
+    diff = [t for t in range(orc_ids.shape[0]) if not np.array_equal(gpu_ids[t], orc_ids[t])]
+    for t in diff:
+        gap = kth_key[t] - next_key[t]
+        assert gap <= NEAR_TIE, "token %d: ids differ (gpu %s, oracle %s) with key gap %.3e > %.0e" % (
+            t, gpu_ids[t].tolist(), orc_ids[t].tolist(), gap, NEAR_TIE)
+        # a near-tie may only swap the last place(s): the sets differ in the tied ids
+    return diff
+
+
+def oracle_inputs(wl, T, seed=0, layer=0, gen_device="cpu", experts=None, x=None):
+    """Oracle-side inputs drawn from the same generators as the GPU side."""
+    if x is None:
+        x = synth.hidden_states(wl, T, seed, layer)
+    xb = synth.bf16_bits(x)
+    wr = synth.router_weight(wl, seed, layer, device=gen_device).cpu().numpy()
+    b = synth.router_bias(wl, seed, layer, device=gen_device)
+    b = None if b is None else b.cpu().numpy()
+    return xb, wr, b
+
+
+def oracle_blobs(wl, expert_ids, seed=0, layer=0, gen_device="cpu"):
+    """The oracle's own Q4_K blobs (its quantiser) for the listed experts; None elsewhere."""
+    blobs = [None] * wl.n_experts
+    for e in sorted(set(int(i) for i in expert_ids)):
+        w = synth.expert_weight(wl, e, seed, layer, device=gen_device).cpu().numpy()
+        blobs[e] = oracle.pack_expert_q4k(w)
+    sblob = None
+    if wl.has_shared:
+        sblob = oracle.pack_shared_q8_0(synth.shared_weight(wl, seed, layer, device=gen_device).cpu().numpy())
+    return blobs, sblob
+
+
+def oracle_forward(wl, xb, wr, b, blobs, sblob, forced=None):
+    return oracle.moe_forward(wl.hidden, wl.n_experts, wl.ff, wl.top_k, wl.score_fn, xb, wr, b, blobs,
+                              wl.shared_ff, sblob, forced_ids=forced)

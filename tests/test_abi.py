@@ -1,0 +1,82 @@
+"""The C-ABI library loads, exports every entry point include/moe.h declares,
+and rejects bad arguments on the host (no GPU needed: these checks run before
+any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from quantized_moe_expert_04_b300 import moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^MOE_API\s+[\w\s\*]*?\b(moe_\w+)\s*\(", text, re.M))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    declared = _declared()
+    assert len(declared) >= 15
+    L = moe.lib()
+    for name in sorted(declared):
+        assert hasattr(L, name), name
+    assert declared == set(moe.EXPORTS)
+
+
+def test_sizes():
+    assert moe.moe_q4k_bytes(320, 2560) == 460800
+    assert moe.moe_q4k_bytes(1, 255) == 0
+    assert moe.moe_q8_0_bytes(2048, 4096) == 2048 * 128 * 34
+    qwen = moe.make_config(2560, 512, 320, 10)
+    assert moe.moe_expert_bytes(qwen) == 1382400          # the pages' per-expert blob
+    ds = moe.make_config(4096, 256, 2048, 6, moe.MOE_SCORE_SIGMOID_BIAS, 2048)
+    assert moe.moe_expert_bytes(ds) == 3 * 2048 * 16 * 144
+    assert moe.moe_shared_bytes(ds) == 3 * 2048 * 128 * 34
+    assert moe.moe_shared_bytes(qwen) == 0
+    assert moe.moe_workspace_bytes(qwen, 5) > 0
+    assert moe.moe_workspace_bytes(moe.make_config(2560, 512, 320, 10, 7), 5) == 0   # bad score_fn
+    assert moe.moe_workspace_bytes(moe.make_config(2500, 512, 320, 10), 5) == 0     # H % 256
+    assert moe.moe_workspace_bytes(moe.make_config(2560, 512, 300, 10), 5) == 0     # FF % 64
+    assert moe.moe_workspace_bytes(moe.make_config(256, 4, 64, 5), 5) == 0          # k > E
+
+
+def test_host_checks_reject_before_launch():
+    L = moe.lib()
+    p = ctypes.c_void_p(4096)           # never dereferenced: checks fail first
+    assert L.moe_pack_q4k(p, 4, 100, p, None, None) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_pack_q4k(p, -1, 256, p, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pack_q4k(None, 4, 256, p, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pack_q4k(ctypes.c_void_p(4100), 4, 256, p, None, None) == moe.MOE_ERR_MISALIGNED
+    assert L.moe_pack_q8_0(p, 4, 48, p, None, None) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    cfg = moe.make_config(256, 16, 128, 2)
+    need = moe.moe_workspace_bytes(cfg, 4)
+    args = (ctypes.byref(cfg), p, p, None, 4, p, p, p, p, p)
+    assert L.moe_route(*args, need - 1, None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert L.moe_route(ctypes.byref(cfg), p, p, None, -1, p, p, p, p, p, need, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_forward(ctypes.byref(cfg), ctypes.c_void_p(4098), p, None, p, None, 4, p, None, p, need,
+                         None) == moe.MOE_ERR_MISALIGNED
+    assert L.moe_forward(ctypes.byref(cfg), p, p, None, None, None, 4, p, None, p, need,
+                         None) == moe.MOE_ERR_INVALID_ARG
+    bad = moe.make_config(256, 16, 128, 2, 5)
+    assert L.moe_forward(ctypes.byref(bad), p, p, None, p, None, 4, p, None, p, need, None) == moe.MOE_ERR_INVALID_ARG
+    odd = moe.make_config(320, 16, 128, 2)
+    assert L.moe_forward(ctypes.byref(odd), p, p, None, p, None, 4, p, None, p, need,
+                         None) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    ds = moe.make_config(256, 16, 128, 2, moe.MOE_SCORE_SIGMOID_BIAS, 64)
+    need_ds = moe.moe_workspace_bytes(ds, 4)
+    assert L.moe_forward(ctypes.byref(ds), p, p, None, p, None, 4, p, None, p, need_ds,
+                         None) == moe.MOE_ERR_INVALID_ARG     # shared expert without its blob
+    # T = 0 is a no-op success
+    assert L.moe_forward(ctypes.byref(cfg), None, None, None, None, None, 0, None, None, p, need, None) == 0
+
+
+def test_status_strings():
+    for code in range(8):
+        assert moe.status_string(code) and moe.status_string(code) != "unknown status"
