@@ -221,6 +221,40 @@ MOE_API moe_status moe_workspace_routing(const moe_config *cfg, int32_t T, const
  */
 MOE_API moe_status moe_last_device_status(void *ws, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- no-allocation variant */
+
+/*
+ * moe_forward for callers that cannot allocate device memory where they run
+ * the layer (a runtime that only hands out pre-registered buffers, a plugin
+ * inside another framework's allocator, a hot path that must not call
+ * cudaMalloc).  There is no counterpart on the source pages: it is a
+ * convenience of this library.
+ *
+ * Same arguments and results as moe_forward, without the workspace: the
+ * scratch is a file-scope device array of MOE_STATIC_WS_BYTES bytes inside
+ * the library, which every GPU that loads the library holds until the
+ * process exits.  Calls whose moe_workspace_bytes(cfg, T) exceeds it return
+ * MOE_ERR_WORKSPACE_TOO_SMALL (4 MiB fits decode windows of up to 8 tokens of
+ * both the 2560x512x320 and the 4096x256x2048 + shared layer shapes).
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *
+ * dev_status (device uint32, may be NULL) receives the call's device-side
+ * status (0 = MOE_OK, else a moe_status), as moe_last_device_status reports
+ * it for an ordinary workspace.
+ *
+ * Every call on a device shares the one array, which keeps the previous
+ * call's contents (the call clears its header itself).  Calls that overlap on
+ * the GPU -- different streams without ordering, or several host threads --
+ * race on it: order them.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.
+ */
+#define MOE_STATIC_WS_BYTES (4u << 20)
+MOE_API moe_status moe_forward_static_ws(const moe_config *cfg, const uint16_t *x, const float *router_w,
+                                         const float *router_bias, const uint8_t *const *expert_blobs,
+                                         const uint8_t *shared_blob, int32_t T, uint16_t *y, float *y_f32,
+                                         uint32_t *dev_status, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- diagnostics */
 
 /*

@@ -36,8 +36,10 @@ EXPORTS = (
     "moe_pack_q4k", "moe_pack_q8_0", "moe_dequant_q4k", "moe_dequant_q8_0",
     "moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_forward",
     "moe_workspace_routing", "moe_last_device_status", "moe_status_string",
-    "moe_profile_enable", "moe_profile_read",
+    "moe_profile_enable", "moe_profile_read", "moe_forward_static_ws",
 )
+
+MOE_STATIC_WS_BYTES = 4 << 20
 
 
 class moe_profile_entry(ctypes.Structure):
@@ -100,6 +102,7 @@ def lib() -> ctypes.CDLL:
             "moe_last_device_status": (ctypes.c_int, [_P, _P]),
             "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "moe_profile_enable": (ctypes.c_int, [_I32]),
+            "moe_forward_static_ws": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P]),
             "moe_profile_read": (_I32, [ctypes.POINTER(moe_profile_entry), _I32]),
         }
         for name, (res, args) in sig.items():
@@ -221,6 +224,20 @@ def moe_forward(cfg: moe_config, x: torch.Tensor, router_w: torch.Tensor, router
     _check(lib().moe_forward(ctypes.byref(cfg), _ptr(x), _ptr(router_w), _ptr(router_bias), _ptr(expert_blobs),
                              _ptr(shared_blob), T, _ptr(y), _ptr(y_f32), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(stream)), "moe_forward")
+
+
+def moe_forward_static_ws(cfg: moe_config, x: torch.Tensor, router_w: torch.Tensor,
+                          router_bias: Optional[torch.Tensor], expert_blobs: torch.Tensor,
+                          shared_blob: Optional[torch.Tensor], T: int, y: torch.Tensor,
+                          y_f32: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+                          stream=None):
+    """moe_forward without a workspace, for callers that cannot allocate device
+    memory: the scratch is the library's own fixed array (MOE_STATIC_WS_BYTES).
+    Calls sharing a device must not overlap on the GPU."""
+    x = _bf16_bits(x)
+    _check(lib().moe_forward_static_ws(ctypes.byref(cfg), _ptr(x), _ptr(router_w), _ptr(router_bias),
+                                       _ptr(expert_blobs), _ptr(shared_blob), T, _ptr(y), _ptr(y_f32),
+                                       _ptr(dev_status), _stream(stream)), "moe_forward_static_ws")
 
 
 def moe_workspace_routing(cfg: moe_config, T: int, ws: torch.Tensor):
