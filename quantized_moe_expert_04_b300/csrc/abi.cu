@@ -48,13 +48,20 @@ WsLayout ws_layout(const moe_config &c, int32_t T)
     L.offsets = take((E + 1) * 4);
     L.assign = take(TK * 4);
     L.active = take((E + 1) * 4);
-    L.act = take(TK * c.ff * 4);
-    L.slots = take(TK * H * 4);
-    L.yacc = take((size_t)T * H * 4);
-    L.x16 = take((size_t)T * H * 2);
-    L.sh_act = take(c.shared_ff ? (size_t)T * c.shared_ff * 4 : 0);
-    L.sh_out = take(c.shared_ff ? (size_t)T * H * 4 : 0);
-    L.tiles = take(0);
+    const bool gemv = use_gemv(c, T), det = (c.flags & MOE_FLAG_DETERMINISTIC) != 0;
+    L.act = take(gemv ? TK * c.ff * 4 : 0);
+    L.slots = take(gemv || det ? TK * H * 4 : 0);
+    L.yacc = take(gemv ? 0 : (size_t)T * H * 4);
+    L.x16 = take(gemv ? 0 : (size_t)T * H * 2);
+    L.sh_act = take(gemv && c.shared_ff ? (size_t)T * c.shared_ff * 4 : 0);
+    L.sh_out = take(c.shared_ff && (gemv || det) ? (size_t)T * H * 4 : 0);
+    L.act16 = take(gemv ? 0 : TK * c.ff * 2);
+    L.sh_act16 = take(!gemv && c.shared_ff ? (size_t)T * c.shared_ff * 2 : 0);
+    const size_t sh_tiles = (size_t)((T + 15) / 16 + 1);
+    L.tiles_gu = take(gemv ? 0 : gemm_tile_capacity(c.ff / 64, (int64_t)TK, c.n_experts) * 16);
+    L.tiles_dn = take(gemv ? 0 : gemm_tile_capacity(c.hidden / 128, (int64_t)TK, c.n_experts) * 16);
+    L.tiles_gus = take(!gemv && c.shared_ff ? sh_tiles * (c.shared_ff / 64) * 16 : 0);
+    L.tiles_dns = take(!gemv && c.shared_ff ? sh_tiles * (c.hidden / 128) * 16 : 0);
     L.total = off;
     return L;
 }
@@ -254,7 +261,21 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
     a.y = y;
     a.y_f32 = y_f32;
     a.header = r.header;
-    e = launch_experts_gemv(a, s);
+    if (use_gemv(*cfg, T)) {
+        e = launch_experts_gemv(a, s);
+    } else {
+        GemmWs gw{};
+        gw.x16 = (__half *)(base + L.x16);
+        gw.act16 = (__half *)(base + L.act16);
+        gw.sh_act16 = (__half *)(base + L.sh_act16);
+        gw.yacc = (float *)(base + L.yacc);
+        gw.tiles_gu = (int4 *)(base + L.tiles_gu);
+        gw.tiles_dn = (int4 *)(base + L.tiles_dn);
+        gw.tiles_gus = (int4 *)(base + L.tiles_gus);
+        gw.tiles_dns = (int4 *)(base + L.tiles_dns);
+        gw.det = (cfg->flags & MOE_FLAG_DETERMINISTIC) != 0;
+        e = launch_experts_gemm(a, gw, s);
+    }
     return cuda_status(e);
 }
 

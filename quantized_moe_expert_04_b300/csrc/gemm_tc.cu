@@ -1,0 +1,777 @@
+// gemm_tc.cu -- grouped expert GEMM on the 5th-generation tensor cores
+// (tcgen05 MMA, fp32 accumulators in tensor memory), with the Q4_K / Q8_0
+// dequantisation fused into the operand pipeline.
+//
+// The pages' engine has dedicated Q4_K expert "prompt" (prefill) kernels on
+// NVIDIA GPUs ("Qwen3.8-Flash-Next UD-Q4_K_XL 引擎对比", lcz.me/user/wml-ai/posts,
+// section 一); its kernels target sm_86/sm_120 (mma.sync generation).  Here a
+// persistent CTA per SM walks a device-built list of work tiles; each tile is
+// one expert's 128 weight rows x up to 256 of its tokens:
+//
+//   gate/up  A = 64 gate rows and the 64 up rows of the same ff indices,
+//              interleaved (row 2i = gate f0+i, row 2i+1 = up f0+i), K = H;
+//            B = the tile's token rows of x (fp16);
+//            epilogue: lanes 2i / 2i+1 hold g / u of one ff index ->
+//              a = SiLU(g) * u, stored fp16 at the assignment's bucket position.
+//   down     A = Wd^T tile (128 hidden rows, K = FF; Wd is stored [FF][H], so the
+//              dequantiser writes it transposed), B = the tile's rows of a;
+//            epilogue: * routing weight, atomically added into y (fp32), or
+//              stored to the assignment's slot when the call is deterministic.
+//
+// Warp roles (12 warps): 0-3 epilogue (tensor-memory lane quarters 0-3),
+// 4 MMA issue + tensor-memory allocation, 5 raw weight bytes (1-D bulk copies
+// into a ring), 6-7 token rows (16-byte cp.async gathers, 128-byte swizzle),
+// 8-11 dequantisation (raw ring -> fp16 A ring).  All hand-offs are mbarriers;
+// every wait is bounded and sets MOE_ERR_TIMEOUT instead of hanging.
+//
+// Operand precision: fp16 A and B (sub-block scale and min rounded to fp16,
+// one fused multiply-add per weight), fp32 accumulation.
+#include <algorithm>
+
+#include "moe_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+using namespace ptx;
+
+enum GemmOp { kOpGateUp = 0, kOpDown = 1 };
+enum WFmt { kWQ4K = 0, kWQ80 = 1 };
+
+constexpr int kGemmThreads = 384;
+constexpr int kABytes = 128 * 128;          // 128 rows x 64 fp16
+constexpr int kRawBytes = 18432;            // 128 rows x 144 B (largest raw stage)
+constexpr long long kWaitCycles = 1ll << 32; // ~2 s at 2 GHz
+
+struct GemmArgs {
+    int H, FF, SFF, k, T, det;
+    const uint8_t *const *blobs;
+    const uint8_t *shared_blob;
+    const int32_t *offsets, *assign;
+    const float *w;
+    const __half *x16;       // [T][H]
+    __half *act16;           // [T*k][FF] by bucket position
+    __half *sh_act16;        // [T][SFF]
+    float *yacc;             // [T][H]
+    float *slots, *sh_out;   // deterministic combine
+    const int4 *tiles;       // {expert (-1 shared), m tile, n0, n}
+    const uint32_t *n_tiles; // device count
+    uint32_t *status;
+};
+
+struct TileInfo {
+    int e, m, n0, n, nmma, bb, ksteps;
+    const uint8_t *blob;
+};
+
+template <int OP, int FMT>
+__device__ __forceinline__ TileInfo tile_info(const GemmArgs &g, int idx)
+{
+    const int4 t = g.tiles[idx];
+    TileInfo ti;
+    ti.e = t.x;
+    ti.m = t.y;
+    ti.n0 = t.z;
+    ti.n = t.w;
+    ti.nmma = (t.w + 15) & ~15;
+    ti.bb = t.x >= 0 ? g.offsets[t.x] : 0;
+    ti.blob = t.x >= 0 ? g.blobs[t.x] : g.shared_blob;
+    ti.ksteps = (OP == kOpGateUp ? g.H : (FMT == kWQ4K ? g.FF : g.SFF)) / 64;
+    return ti;
+}
+
+// Bounded wait on an mbarrier phase; false on abort (another role gave up) or
+// on timeout (this call records MOE_ERR_TIMEOUT and raises the abort flag).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort, uint32_t *status)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            *abort = 1;
+            set_status(status, MOE_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ __half2 u2h2(uint32_t u)
+{
+    __half2 h;
+    memcpy(&h, &u, 4);
+    return h;
+}
+
+__device__ __forceinline__ uint32_t h22u(__half2 h)
+{
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+}
+
+// ---------------------------------------------------------------- dequant
+
+// 4-bit quants of 4 consecutive bytes -> fp16 pairs (exact integers), low and
+// high nibbles: 1024 + q via the fp16 exponent trick, then remove the offset.
+__device__ __forceinline__ void nibbles_to_q(uint32_t w, __half2 &lo01, __half2 &lo23, __half2 &hi01, __half2 &hi23)
+{
+    const uint32_t p01 = __byte_perm(w, 0, 0x4140);   // bytes b0, b1 into the two halves
+    const uint32_t p23 = __byte_perm(w, 0, 0x4342);   // b2, b3
+    const __half2 k1024 = __float2half2_rn(1024.0f);
+    const __half2 k16th = __float2half2_rn(0.0625f);
+    const __half2 km64 = __float2half2_rn(-64.0f);
+    lo01 = __hsub2(u2h2((p01 & 0x000F000Fu) | 0x64006400u), k1024);          // q
+    lo23 = __hsub2(u2h2((p23 & 0x000F000Fu) | 0x64006400u), k1024);
+    hi01 = __hfma2(u2h2((p01 & 0x00F000F0u) | 0x64006400u), k16th, km64);    // (1024 + 16q)/16 - 64 = q
+    hi23 = __hfma2(u2h2((p23 & 0x00F000F0u) | 0x64006400u), k16th, km64);
+}
+
+__device__ __forceinline__ void q4k_subblock_scales(uint4 hdr, int j, __half &s, __half &nz)
+{
+    const float d = f16_bits_to_f32(hdr.x & 0xffff), dmin = f16_bits_to_f32(hdr.x >> 16);
+    uint8_t scales[12];
+    memcpy(scales, &hdr.y, 4);
+    memcpy(scales + 4, &hdr.z, 4);
+    memcpy(scales + 8, &hdr.w, 4);
+    int sc, m;
+    q4k_scale_min(scales, j, sc, m);
+    s = __float2half_rn(__fmul_rn(d, (float)sc));
+    nz = __float2half_rn(-__fmul_rn(dmin, (float)m));
+}
+
+// gate/up, Q4_K: thread t dequantises row t (64 weights of K-step `sub` of the
+// raw block) into the swizzled fp16 A tile.
+__device__ __forceinline__ void dequant_gu_q4k(const uint8_t *raw, uint32_t a_tile, int row, int sub)
+{
+    const uint8_t *rr = raw + row * 144;
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(rr);
+    __half s_lo, nz_lo, s_hi, nz_hi;
+    q4k_subblock_scales(hdr, 2 * sub, s_lo, nz_lo);
+    q4k_subblock_scales(hdr, 2 * sub + 1, s_hi, nz_hi);
+    const __half2 S_lo = __half2half2(s_lo), NZ_lo = __half2half2(nz_lo);
+    const __half2 S_hi = __half2half2(s_hi), NZ_hi = __half2half2(nz_hi);
+    const uint4 qa = *reinterpret_cast<const uint4 *>(rr + 16 + 32 * sub);
+    const uint4 qb = *reinterpret_cast<const uint4 *>(rr + 16 + 32 * sub + 16);
+    const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        __half2 l0, l1, h0, h1, l2, l3, h2, h3;
+        nibbles_to_q(words[2 * p], l0, l1, h0, h1);
+        nibbles_to_q(words[2 * p + 1], l2, l3, h2, h3);
+        st_shared_v4(a_tile + sw128_off(row, p), h22u(__hfma2(l0, S_lo, NZ_lo)), h22u(__hfma2(l1, S_lo, NZ_lo)),
+                     h22u(__hfma2(l2, S_lo, NZ_lo)), h22u(__hfma2(l3, S_lo, NZ_lo)));
+        st_shared_v4(a_tile + sw128_off(row, p + 4), h22u(__hfma2(h0, S_hi, NZ_hi)),
+                     h22u(__hfma2(h1, S_hi, NZ_hi)), h22u(__hfma2(h2, S_hi, NZ_hi)),
+                     h22u(__hfma2(h3, S_hi, NZ_hi)));
+    }
+}
+
+// int8 pair (two bytes of a 16-bit word) -> exact fp16 pair
+__device__ __forceinline__ __half2 i8pair_to_h2(uint32_t pair16)
+{
+    const uint32_t p = (__byte_perm(pair16, 0, 0x4140) ^ 0x00800080u) & 0x00FF00FFu;   // q + 128
+    return __hsub2(u2h2(p | 0x64006400u), __float2half2_rn(1152.0f));                  // 1024 + q + 128 - 1152
+}
+
+// gate/up, Q8_0: row t, K-step s: two 34-byte blocks at offset (68 s) mod 16
+// of the 80-byte raw row.
+__device__ __forceinline__ void dequant_gu_q80(const uint8_t *raw, uint32_t a_tile, int row, int s)
+{
+    const uint8_t *rr = raw + row * 80 + ((68 * s) & 15);
+    const uint16_t *r16 = reinterpret_cast<const uint16_t *>(rr);   // offset is a multiple of 4
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        const __half2 D = __half2half2(__ushort_as_half(r16[17 * blk]));
+#pragma unroll
+        for (int cq = 0; cq < 4; ++cq) {          // 4 chunks of 8 weights per block
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = h22u(__hmul2(i8pair_to_h2(r16[17 * blk + 1 + 4 * cq + i]), D));
+            st_shared_v4(a_tile + sw128_off(row, 4 * blk + cq), o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+// down, Q4_K: A[h][f] = Wd[f][h0 + h] for the tile's 128 hidden columns and
+// the K-step's 64 ff rows.  Raw row i (f = 64 s + i) holds the block header
+// and the 64 quant bytes of this half block (80 bytes).  Item = (row, group of
+// 8 quant bytes): 8 low-nibble weights at h = 64 c + l .. +7 and 8 high-nibble
+// weights at h + 32, stored as 16-bit values into their transposed places.
+__device__ __forceinline__ void dequant_dn_q4k(const uint8_t *raw, uint32_t a_tile, int dt, int half)
+{
+#pragma unroll
+    for (int it4 = 0; it4 < 4; ++it4) {
+        const int it = dt + 128 * it4;
+        const int row = it & 63, bg = it >> 6;           // bg 0..7
+        const uint8_t *rr = raw + row * 80;
+        const uint4 hdr = *reinterpret_cast<const uint4 *>(rr);
+        const int c_loc = bg >> 2, l0 = (8 * bg) & 31;
+        const int jsb = 2 * (2 * half + c_loc);
+        __half s_lo, nz_lo, s_hi, nz_hi;
+        q4k_subblock_scales(hdr, jsb, s_lo, nz_lo);
+        q4k_subblock_scales(hdr, jsb + 1, s_hi, nz_hi);
+        const __half2 S_lo = __half2half2(s_lo), NZ_lo = __half2half2(nz_lo);
+        const __half2 S_hi = __half2half2(s_hi), NZ_hi = __half2half2(nz_hi);
+        const uint2 q8 = *reinterpret_cast<const uint2 *>(rr + 16 + 8 * bg);
+        const int h_lo = 64 * c_loc + l0;
+        const uint32_t kchunk = (uint32_t)row >> 3, kbyte = ((uint32_t)row & 7) * 2;
+#pragma unroll
+        for (int wsel = 0; wsel < 2; ++wsel) {
+            __half2 l01, l23, h01, h23;
+            nibbles_to_q(wsel ? q8.y : q8.x, l01, l23, h01, h23);
+            const __half2 vl01 = __hfma2(l01, S_lo, NZ_lo), vl23 = __hfma2(l23, S_lo, NZ_lo);
+            const __half2 vh01 = __hfma2(h01, S_hi, NZ_hi), vh23 = __hfma2(h23, S_hi, NZ_hi);
+            const int hb = h_lo + 4 * wsel;
+            st_shared_u16(a_tile + sw128_off(hb + 0, kchunk) + kbyte, __half_as_ushort(__low2half(vl01)));
+            st_shared_u16(a_tile + sw128_off(hb + 1, kchunk) + kbyte, __half_as_ushort(__high2half(vl01)));
+            st_shared_u16(a_tile + sw128_off(hb + 2, kchunk) + kbyte, __half_as_ushort(__low2half(vl23)));
+            st_shared_u16(a_tile + sw128_off(hb + 3, kchunk) + kbyte, __half_as_ushort(__high2half(vl23)));
+            st_shared_u16(a_tile + sw128_off(hb + 32, kchunk) + kbyte, __half_as_ushort(__low2half(vh01)));
+            st_shared_u16(a_tile + sw128_off(hb + 33, kchunk) + kbyte, __half_as_ushort(__high2half(vh01)));
+            st_shared_u16(a_tile + sw128_off(hb + 34, kchunk) + kbyte, __half_as_ushort(__low2half(vh23)));
+            st_shared_u16(a_tile + sw128_off(hb + 35, kchunk) + kbyte, __half_as_ushort(__high2half(vh23)));
+        }
+    }
+}
+
+// down, Q8_0: raw row i (f = 64 s + i) is a 144-byte window holding the 4
+// blocks of this tile's 128 hidden columns at offset o8 (0 or 8).
+__device__ __forceinline__ void dequant_dn_q80(const uint8_t *raw, uint32_t a_tile, int dt, int o8)
+{
+#pragma unroll
+    for (int it8 = 0; it8 < 8; ++it8) {
+        const int it = dt + 128 * it8;
+        const int row = it & 63, g = it >> 6;            // g 0..15: 8 columns each
+        const int b = g >> 2, hh0 = 8 * (g & 3);
+        const uint16_t *blk = reinterpret_cast<const uint16_t *>(raw + row * 144 + o8 + 34 * b);
+        const __half2 D = __half2half2(__ushort_as_half(blk[0]));
+        const uint32_t kchunk = (uint32_t)row >> 3, kbyte = ((uint32_t)row & 7) * 2;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 v = __hmul2(i8pair_to_h2(blk[1 + hh0 / 2 + i]), D);
+            const int h = 32 * b + hh0 + 2 * i;
+            st_shared_u16(a_tile + sw128_off(h, kchunk) + kbyte, __half_as_ushort(__low2half(v)));
+            st_shared_u16(a_tile + sw128_off(h + 1, kchunk) + kbyte, __half_as_ushort(__high2half(v)));
+        }
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int OP, int FMT, int NMAX, int S, int RS>
+struct GemmSmem {
+    static constexpr int kBBytes = NMAX * 128;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + S * kABytes;
+    static constexpr int kOffRaw = kOffB + S * kBBytes;
+    static constexpr int kOffBar = kOffRaw + RS * kRawBytes;
+    static constexpr int kNumBars = 2 * RS + 3 * S + 5;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr int kBytes = kOffMisc + 16 + 1024;   // + alignment slack
+};
+
+template <int OP, int FMT>
+__device__ __forceinline__ int raw_stage_bytes()
+{
+    if (OP == kOpGateUp) return FMT == kWQ4K ? 128 * 144 : 128 * 80;
+    return FMT == kWQ4K ? 64 * 80 : 64 * 144;
+}
+
+template <int OP, int FMT, int NMAX, int S, int RS>
+__global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
+{
+    using L = GemmSmem<OP, FMT, NMAX, S, RS>;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_dyn + 1023) & ~(uintptr_t)1023);
+    const uint32_t sA = smem_addr(smem + L::kOffA), sB = smem_addr(smem + L::kOffB);
+    uint8_t *raw_base = smem + L::kOffRaw;
+    const uint32_t bar0 = smem_addr(smem + L::kOffBar);
+    // barrier addresses
+    auto full_raw = [&](int i) { return bar0 + 8 * i; };
+    auto empty_raw = [&](int i) { return bar0 + 8 * (RS + i); };
+    auto full_a = [&](int i) { return bar0 + 8 * (2 * RS + i); };
+    auto full_b = [&](int i) { return bar0 + 8 * (2 * RS + S + i); };
+    auto empty_ab = [&](int i) { return bar0 + 8 * (2 * RS + 2 * S + i); };
+    auto acc_full = [&](int i) { return bar0 + 8 * (2 * RS + 3 * S + i); };
+    auto acc_empty = [&](int i) { return bar0 + 8 * (2 * RS + 3 * S + 2 + i); };
+    const uint32_t final_bar = bar0 + 8 * (2 * RS + 3 * S + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RS; ++i) {
+            mbar_init(full_raw(i), 1);
+            mbar_init(empty_raw(i), 128);
+        }
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full_a(i), 128);
+            mbar_init(full_b(i), 64);
+            mbar_init(empty_ab(i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(acc_full(i), 1);
+            mbar_init(acc_empty(i), 128);
+        }
+        mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(smem_addr(tmem_slot), 2 * NMAX);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int n_tiles = (int)*g.n_tiles;
+
+    if (warp < 4) {
+        // ------------------------------------------------------------ epilogue
+        uint32_t t_it = 0;
+        const int row = 32 * warp + lane;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            const TileInfo ti = tile_info<OP, FMT>(g, tile);
+            if (!ti.blob) {
+                if (threadIdx.x == 0) set_status(g.status, MOE_ERR_DEVICE_FAULT);
+                continue;
+            }
+            const int acc = t_it & 1;
+            if (!wait_bar(acc_full(acc), (t_it >> 1) & 1, abort_flag, g.status)) break;
+            tc_fence_after();
+            for (int cc = 0; cc < ti.nmma / 16; ++cc) {
+                uint32_t v[16];
+                tmem_ld16(tmem_base + ((uint32_t)(32 * warp) << 16) + acc * NMAX + cc * 16, v);
+                tmem_wait_ld();
+                if (OP == kOpGateUp) {
+                    const int ffop = FMT == kWQ4K ? g.FF : g.SFF;
+                    const int f = ti.m * 64 + (row >> 1);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float val = __uint_as_float(v[i]);
+                        const float other = __shfl_xor_sync(0xffffffffu, val, 1);
+                        const int j = cc * 16 + i;
+                        if (!(lane & 1) && j < ti.n) {
+                            const float a = val / (1.0f + expf(-val)) * other;
+                            __half *dst = FMT == kWQ4K ? g.act16 + (int64_t)(ti.bb + ti.n0 + j) * ffop + f
+                                                       : g.sh_act16 + (int64_t)(ti.n0 + j) * ffop + f;
+                            *dst = __float2half_rn(a);
+                        }
+                    }
+                } else {
+                    const int h = ti.m * 128 + row;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int j = cc * 16 + i;
+                        if (j < ti.n) {
+                            const float val = __uint_as_float(v[i]);
+                            if (FMT == kWQ4K) {
+                                const int asg = g.assign[ti.bb + ti.n0 + j];
+                                const float wt = g.w[asg];
+                                if (g.det) g.slots[(int64_t)asg * g.H + h] = wt * val;
+                                else red_add_f32(g.yacc + (int64_t)(asg / g.k) * g.H + h, wt * val);
+                            } else {
+                                const int t = ti.n0 + j;
+                                if (g.det) g.sh_out[(int64_t)t * g.H + h] = val;
+                                else red_add_f32(g.yacc + (int64_t)t * g.H + h, val);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(acc_empty(acc));
+            ++t_it;
+        }
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            uint32_t s_it = 0, t_it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+                const TileInfo ti = tile_info<OP, FMT>(g, tile);
+                if (!ti.blob) continue;
+                const int acc = t_it & 1;
+                if (!(ok = wait_bar(acc_empty(acc), ((t_it >> 1) & 1) ^ 1, abort_flag, g.status))) break;
+                tc_fence_after();
+                const uint32_t idesc = idesc_f16_f32(128, ti.nmma);
+                const uint32_t d_tmem = tmem_base + acc * NMAX;
+                for (int s = 0; s < ti.ksteps; ++s, ++s_it) {
+                    const int slot = s_it % S;
+                    const uint32_t ph = (s_it / S) & 1;
+                    if (!(ok = wait_bar(full_a(slot), ph, abort_flag, g.status))) break;
+                    if (!(ok = wait_bar(full_b(slot), ph, abort_flag, g.status))) break;
+                    tc_fence_after();
+                    const uint32_t a0 = sA + slot * kABytes, b0 = sB + slot * L::kBBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16(d_tmem, sdesc_kmajor_sw128(a0 + 32 * kk), sdesc_kmajor_sw128(b0 + 32 * kk), idesc,
+                                (s | kk) != 0);
+                    mma_commit(empty_ab(slot));
+                }
+                if (!ok) break;
+                mma_commit(acc_full(acc));
+                ++t_it;
+            }
+            // every issued MMA must be complete before the tensor memory is freed
+            mma_commit(final_bar);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(final_bar, 0) && clock64() - t0 < kWaitCycles) {
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ raw weight bytes
+        uint32_t rs_it = 0;
+        const int H = g.H;
+        const int64_t rb = FMT == kWQ4K ? (int64_t)(H / 256) * 144 : (int64_t)(H / 32) * 34;   // row bytes
+        const int ffop = FMT == kWQ4K ? g.FF : g.SFF;
+        const uint32_t tx = (uint32_t)raw_stage_bytes<OP, FMT>();
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+            const TileInfo ti = tile_info<OP, FMT>(g, tile);
+            if (!ti.blob) continue;
+            const int nraw = (OP == kOpGateUp && FMT == kWQ4K) ? ti.ksteps / 4 : ti.ksteps;
+            for (int r = 0; r < nraw; ++r, ++rs_it) {
+                const int slot = rs_it % RS;
+                if (!(ok = wait_bar(empty_raw(slot), ((rs_it / RS) & 1) ^ 1, abort_flag, g.status))) break;
+                if (lane == 0) mbar_arrive_expect_tx(full_raw(slot), tx);
+                __syncwarp();
+                const uint32_t dst0 = smem_addr(raw_base + slot * kRawBytes);
+                if (OP == kOpGateUp) {
+                    // 128 rows: row 2i = gate f0+i, row 2i+1 = up f0+i
+                    for (int i = lane; i < 128; i += 32) {
+                        const int64_t mrow = (int64_t)((i & 1) ? ffop : 0) + ti.m * 64 + (i >> 1);
+                        const uint8_t *rowp = ti.blob + mrow * rb;
+                        if (FMT == kWQ4K) {
+                            bulk_g2s(dst0 + i * 144, rowp + (int64_t)r * 144, 144, full_raw(slot));
+                        } else {
+                            const int off = 68 * r;
+                            bulk_g2s(dst0 + i * 80, rowp + (off & ~15), 80, full_raw(slot));
+                        }
+                    }
+                } else {
+                    // 64 ff rows of Wd for this K-step, this tile's 128 hidden columns
+                    const int h0 = ti.m * 128;
+                    for (int i = lane; i < 64; i += 32) {
+                        const uint8_t *rowp = ti.blob + ((int64_t)2 * ffop + 64 * r + i) * rb;
+                        if (FMT == kWQ4K) {
+                            const uint8_t *blk = rowp + (int64_t)(h0 / 256) * 144;
+                            bulk_g2s(dst0 + i * 80, blk, 16, full_raw(slot));
+                            bulk_g2s(dst0 + i * 80 + 16, blk + 16 + 64 * ((h0 / 128) & 1), 64, full_raw(slot));
+                        } else {
+                            const int off = 34 * (h0 / 32);
+                            bulk_g2s(dst0 + i * 144, rowp + (off & ~15), 144, full_raw(slot));
+                        }
+                    }
+                }
+            }
+        }
+        // copies still in flight (an early exit) must land before the CTA ends
+        for (uint32_t i = rs_it > (uint32_t)RS ? rs_it - RS : 0; i < rs_it; ++i) {
+            const long long t0 = clock64();
+            while (!mbar_try_wait(full_raw(i % RS), (i / RS) & 1) && clock64() - t0 < kWaitCycles) {
+            }
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ token rows (B)
+        // thread bt copies 16-byte chunk (bt & 7) of rows j = (bt >> 3) + 8 i
+        const int bt = threadIdx.x - 192;   // 0..63
+        const int c = bt & 7, r0 = bt >> 3;
+        const __half *srcbase = OP == kOpGateUp ? g.x16 : (FMT == kWQ4K ? g.act16 : g.sh_act16);
+        const int ld = OP == kOpGateUp ? g.H : (FMT == kWQ4K ? g.FF : g.SFF);
+        uint32_t s_it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+            const TileInfo ti = tile_info<OP, FMT>(g, tile);
+            if (!ti.blob) continue;
+            int src[NMAX / 8];
+#pragma unroll
+            for (int i = 0; i < NMAX / 8; ++i) {
+                const int j = r0 + 8 * i;
+                src[i] = 0;
+                if (j < ti.n) {
+                    if (OP == kOpGateUp) src[i] = FMT == kWQ4K ? g.assign[ti.bb + ti.n0 + j] / g.k : ti.n0 + j;
+                    else src[i] = FMT == kWQ4K ? ti.bb + ti.n0 + j : ti.n0 + j;
+                }
+            }
+            int prev = -1;
+            for (int s = 0; s < ti.ksteps; ++s, ++s_it) {
+                const int slot = s_it % S;
+                if (!(ok = wait_bar(empty_ab(slot), ((s_it / S) & 1) ^ 1, abort_flag, g.status))) break;
+                const uint32_t b_tile = sB + slot * L::kBBytes;
+#pragma unroll
+                for (int i = 0; i < NMAX / 8; ++i) {
+                    const int j = r0 + 8 * i;
+                    if (j < ti.n)
+                        cp_async16(b_tile + sw128_off(j, c), srcbase + (int64_t)src[i] * ld + s * 64 + c * 8);
+                }
+                cp_async_commit();
+                if (prev >= 0) {
+                    cp_async_wait<1>();
+                    fence_proxy_async();
+                    mbar_arrive(full_b(prev));
+                }
+                prev = slot;
+            }
+            cp_async_wait<0>();
+            if (ok && prev >= 0) {
+                fence_proxy_async();
+                mbar_arrive(full_b(prev));
+            }
+        }
+        cp_async_wait<0>();
+    } else {
+        // ------------------------------------------------------------ dequantisation (A)
+        const int dt = threadIdx.x - 256;   // 0..127
+        uint32_t s_it = 0, rs_it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+            const TileInfo ti = tile_info<OP, FMT>(g, tile);
+            if (!ti.blob) continue;
+            for (int s = 0; s < ti.ksteps; ++s, ++s_it) {
+                const bool per_block = OP == kOpGateUp && FMT == kWQ4K;
+                const int sub = per_block ? (s & 3) : 0;
+                const bool first = sub == 0, last = per_block ? sub == 3 : true;
+                const int rslot = rs_it % RS;
+                if (first && !(ok = wait_bar(full_raw(rslot), (rs_it / RS) & 1, abort_flag, g.status))) break;
+                const int slot = s_it % S;
+                if (!(ok = wait_bar(empty_ab(slot), ((s_it / S) & 1) ^ 1, abort_flag, g.status))) break;
+                const uint8_t *raw = raw_base + rslot * kRawBytes;
+                const uint32_t a_tile = sA + slot * kABytes;
+                if (OP == kOpGateUp) {
+                    if (FMT == kWQ4K) dequant_gu_q4k(raw, a_tile, dt, sub);
+                    else dequant_gu_q80(raw, a_tile, dt, s);
+                } else {
+                    if (FMT == kWQ4K) dequant_dn_q4k(raw, a_tile, dt, ti.m & 1);
+                    else dequant_dn_q80(raw, a_tile, dt, (34 * (ti.m * 128 / 32)) & 15);
+                }
+                fence_proxy_async();
+                mbar_arrive(full_a(slot));
+                if (last) {
+                    mbar_arrive(empty_raw(rslot));
+                    ++rs_it;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 2 * NMAX);
+    }
+}
+
+// ---------------------------------------------------------------- helpers
+
+// x -> fp16 operand copy; zero the fp32 output accumulator.
+__global__ void __launch_bounds__(256) k_gemm_prep(const uint16_t *__restrict__ x, __half *__restrict__ x16,
+                                                   float *__restrict__ yacc, int64_t n, uint32_t *status)
+{
+    bool bad = false;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = bf16_bits_to_f32(x[i]);
+        const __half hv = __float2half_rn(v);
+        bad |= isfinite(v) && !isfinite(__half2float(hv));    // beyond the fp16 range
+        x16[i] = hv;
+        if (yacc) yacc[i] = 0.0f;
+    }
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, MOE_ERR_DEVICE_FAULT);
+}
+
+struct PlanArgs {
+    int H, FF, SFF, T;
+    const int32_t *offsets, *active;
+    uint32_t *header;
+    int4 *gu, *dn, *gus, *dns;
+};
+
+__device__ __forceinline__ void split_tokens(int n_e, int &tn, int &nt)
+{
+    const int nt0 = (n_e + 255) / 256;
+    tn = (((n_e + nt0 - 1) / nt0) + 15) & ~15;
+    nt = (n_e + tn - 1) / tn;
+}
+
+// Work tiles of the routed experts (both projections) and of the shared
+// expert; one CTA, one thread per active expert, block-wide prefix sums.
+__global__ void __launch_bounds__(1024) k_gemm_plan(PlanArgs p)
+{
+    __shared__ int scan_gu[1024], scan_dn[1024];
+    const int u = threadIdx.x;
+    const int n_active = (int)p.header[kHdrNActive];
+    const int mt_gu = p.FF / 64, mt_dn = p.H / 128;
+    int e = -1, n_e = 0, tn = 0, nt = 0;
+    if (u < n_active) {
+        e = p.active[u];
+        n_e = p.offsets[e + 1] - p.offsets[e];
+        split_tokens(n_e, tn, nt);
+    }
+    scan_gu[u] = nt * mt_gu;
+    scan_dn[u] = nt * mt_dn;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+        const int a = u >= off ? scan_gu[u - off] : 0, b = u >= off ? scan_dn[u - off] : 0;
+        __syncthreads();
+        scan_gu[u] += a;
+        scan_dn[u] += b;
+        __syncthreads();
+    }
+    const int base_gu = scan_gu[u] - nt * mt_gu, base_dn = scan_dn[u] - nt * mt_dn;
+    for (int j = 0; j < nt; ++j) {
+        const int n0 = j * tn, n = min(tn, n_e - n0);
+        for (int m = 0; m < mt_gu; ++m) p.gu[base_gu + j * mt_gu + m] = make_int4(e, m, n0, n);
+        for (int m = 0; m < mt_dn; ++m) p.dn[base_dn + j * mt_dn + m] = make_int4(e, m, n0, n);
+    }
+    if (u == 1023) {
+        p.header[kHdrTilesGU] = (uint32_t)scan_gu[1023];
+        p.header[kHdrTilesDN] = (uint32_t)scan_dn[1023];
+    }
+    if (p.SFF > 0) {
+        int stn, snt;
+        split_tokens(p.T, stn, snt);
+        const int smt_gu = p.SFF / 64;
+        for (int i = u; i < snt * smt_gu; i += 1024) {
+            const int j = i / smt_gu, m = i % smt_gu;
+            p.gus[i] = make_int4(-1, m, j * stn, min(stn, p.T - j * stn));
+        }
+        for (int i = u; i < snt * mt_dn; i += 1024) {
+            const int j = i / mt_dn, m = i % mt_dn;
+            p.dns[i] = make_int4(-1, m, j * stn, min(stn, p.T - j * stn));
+        }
+        if (u == 0) {
+            p.header[kHdrTilesGUS] = (uint32_t)(snt * smt_gu);
+            p.header[kHdrTilesDNS] = (uint32_t)(snt * mt_dn);
+        }
+    } else if (u == 0) {
+        p.header[kHdrTilesGUS] = 0;
+        p.header[kHdrTilesDNS] = 0;
+    }
+}
+
+// y = bf16(accumulated y) (atomic path) or the fixed-order sum of the slots.
+__global__ void __launch_bounds__(256) k_gemm_finish(const float *__restrict__ yacc, const float *__restrict__ slots,
+                                                     const float *__restrict__ sh_out, int T, int H, int k,
+                                                     uint16_t *__restrict__ y, float *__restrict__ y_f32)
+{
+    const int64_t n = (int64_t)T * H;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float acc;
+        if (slots) {
+            const int64_t t = i / H, h = i % H;
+            acc = 0.0f;
+            for (int r = 0; r < k; ++r) acc += slots[(t * k + r) * H + h];
+            if (sh_out) acc += sh_out[i];
+        } else {
+            acc = yacc[i];
+        }
+        y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+        if (y_f32) y_f32[i] = acc;
+    }
+}
+
+// ---------------------------------------------------------------- launch
+
+template <int OP, int FMT, int NMAX, int S, int RS>
+static cudaError_t launch_gemm(const GemmArgs &g, int grid, cudaStream_t s)
+{
+    using L = GemmSmem<OP, FMT, NMAX, S, RS>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<OP, FMT, NMAX, S, RS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    k_moe_gemm<OP, FMT, NMAX, S, RS><<<grid, kGemmThreads, L::kBytes, s>>>(g);
+    return cudaGetLastError();
+}
+
+static int num_sms()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+size_t gemm_tile_capacity(int mt, int64_t TK, int E)
+{
+    return (size_t)mt * (size_t)(TK / 256 + 1 + std::min<int64_t>(E, TK));
+}
+
+cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream_t s)
+{
+    const int64_t n = (int64_t)a.T * a.H;
+    const int det = w.det;
+    prof_begin(kPhGemmPrep, s);
+    k_gemm_prep<<<(unsigned)std::min<int64_t>((n + 255) / 256, 148 * 8), 256, 0, s>>>(
+        a.x, w.x16, det ? nullptr : w.yacc, n, a.header + kHdrStatus);
+    PlanArgs p{a.H, a.FF, a.SFF, a.T, a.offsets, a.active, a.header, w.tiles_gu, w.tiles_dn, w.tiles_gus,
+               w.tiles_dns};
+    k_gemm_plan<<<1, 1024, 0, s>>>(p);
+    prof_end(kPhGemmPrep, s);
+
+    GemmArgs g{};
+    g.H = a.H;
+    g.FF = a.FF;
+    g.SFF = a.SFF;
+    g.k = a.k;
+    g.T = a.T;
+    g.det = det;
+    g.blobs = a.blobs;
+    g.shared_blob = a.shared_blob;
+    g.offsets = a.offsets;
+    g.assign = a.assign;
+    g.w = a.w;
+    g.x16 = w.x16;
+    g.act16 = w.act16;
+    g.sh_act16 = w.sh_act16;
+    g.yacc = w.yacc;
+    g.slots = a.slots;
+    g.sh_out = a.sh_out;
+    g.status = a.header + kHdrStatus;
+    const int grid = num_sms();
+    cudaError_t e;
+
+    prof_begin(kPhGemmGateUp, s);
+    g.tiles = w.tiles_gu;
+    g.n_tiles = a.header + kHdrTilesGU;
+    e = launch_gemm<kOpGateUp, kWQ4K, 256, 3, 3>(g, grid, s);
+    if (e == cudaSuccess && a.shared_blob) {
+        g.tiles = w.tiles_gus;
+        g.n_tiles = a.header + kHdrTilesGUS;
+        e = launch_gemm<kOpGateUp, kWQ80, 256, 3, 3>(g, grid, s);
+    }
+    prof_end(kPhGemmGateUp, s);
+    if (e != cudaSuccess) return e;
+
+    prof_begin(kPhGemmDown, s);
+    g.tiles = w.tiles_dn;
+    g.n_tiles = a.header + kHdrTilesDN;
+    e = launch_gemm<kOpDown, kWQ4K, 256, 3, 3>(g, grid, s);
+    if (e == cudaSuccess && a.shared_blob) {
+        g.tiles = w.tiles_dns;
+        g.n_tiles = a.header + kHdrTilesDNS;
+        e = launch_gemm<kOpDown, kWQ80, 256, 3, 3>(g, grid, s);
+    }
+    prof_end(kPhGemmDown, s);
+    if (e != cudaSuccess) return e;
+
+    prof_begin(kPhGemmFinish, s);
+    k_gemm_finish<<<(unsigned)std::min<int64_t>((n + 255) / 256, 148 * 8), 256, 0, s>>>(
+        w.yacc, det ? a.slots : nullptr, det ? a.sh_out : nullptr, a.T, a.H, a.k, a.y, a.y_f32);
+    prof_end(kPhGemmFinish, s);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -26,7 +26,10 @@ constexpr int kGemvMaxTokens = 8; // decode windows: MTP verify windows of 1-8 t
 enum HeaderWord : int {
     kHdrStatus = 0,       // first device-side fault (moe_status), sticky until read
     kHdrNActive = 1,      // number of experts with at least one token
-    kHdrTileCount = 2,    // prefill: number of GEMM work tiles
+    kHdrTilesGU = 2,      // GEMM path: work tiles of the routed gate/up projection
+    kHdrTilesDN = 3,      //            routed down projection
+    kHdrTilesGUS = 4,     //            shared expert gate/up
+    kHdrTilesDNS = 5,     //            shared expert down
     kHdrCounter0 = 8,     // completion counters, reset by their last user
 };
 
@@ -65,7 +68,8 @@ void prof_end(int phase, cudaStream_t s);
 // Workspace regions (byte offsets from the workspace base) for one call shape.
 struct WsLayout {
     size_t header, logits, ids, w, counts, offsets, assign, active;
-    size_t act, slots, yacc, x16, sh_act, sh_out, tiles;
+    size_t act, slots, yacc, x16, sh_act, sh_out;
+    size_t act16, sh_act16, tiles_gu, tiles_dn, tiles_gus, tiles_dns;
     size_t total;
 };
 
@@ -109,5 +113,15 @@ struct ExpertArgs {
     uint32_t *header;
 };
 cudaError_t launch_experts_gemv(const ExpertArgs &a, cudaStream_t s);
+
+// Tensor-core (tcgen05) grouped GEMM path: its workspace regions.
+struct GemmWs {
+    __half *x16, *act16, *sh_act16;
+    float *yacc;
+    int4 *tiles_gu, *tiles_dn, *tiles_gus, *tiles_dns;
+    int det;
+};
+size_t gemm_tile_capacity(int mt, int64_t TK, int E);
+cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream_t s);
 
 }  // namespace moe

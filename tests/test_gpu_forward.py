@@ -116,3 +116,31 @@ def test_device_faults_are_reported():
     y = torch.empty(4, wl.hidden, dtype=torch.bfloat16, device="cuda")
     moe.moe_forward(cfg, x, pl.router_w, pl.router_bias, table, pl.shared, 4, y, None, ws)
     assert moe.moe_last_device_status(ws) == moe.MOE_ERR_DEVICE_FAULT
+
+
+GEMM_SMALL = [
+    (W["tiny"], 4),
+    (W["tiny"], 1),
+    (sv(W["qwen_decode"], name="qwen_e64", n_experts=64), 5),
+    (sv(W["deepseek_decode"], name="ds_small", hidden=1024, n_experts=32, ff=512, shared_ff=512), 8),
+    (sv(W["qwen_decode"], name="qwen_e8_skew", n_experts=8, top_k=2), 700),   # buckets > 256: several N tiles
+]
+
+
+@pytest.mark.parametrize("wl,T", GEMM_SMALL, ids=lambda c: getattr(c, "name", str(c)))
+def test_forced_gemm_path_matches_oracle(wl, T):
+    """The tensor-core path at decode-sized and ragged buckets."""
+    _run(wl, T, gen_device="cpu", flags=moe.MOE_FLAG_FORCE_GEMM)
+
+
+@pytest.mark.parametrize("wl,T", [(sv(W["qwen_decode"], name="qwen_e64", n_experts=64), 37),
+                                  (sv(W["deepseek_prefill_skewed"], name="ds_skew_small", hidden=1024,
+                                      n_experts=32, ff=256, shared_ff=256), 77)],
+                         ids=["qwen_e64", "ds_skew_small"])
+def test_gemm_deterministic_mode(wl, T):
+    flags = moe.MOE_FLAG_FORCE_GEMM | moe.MOE_FLAG_DETERMINISTIC
+    y, y32, ws, pl = _run(wl, T, gen_device="cpu", flags=flags)
+    cfg = moe.config_for(wl, flags)
+    x = synth.hidden_states(wl, T).cuda()
+    y2 = forward(pl, x, ws, cfg=cfg)
+    assert torch.equal(y, y2)
