@@ -236,7 +236,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     nL = wl.layers if args.layers is None else args.layers
-    cfg = moe.config_for(wl)
+    flags = {"auto": 0, "gemv": moe.MOE_FLAG_FORCE_GEMV, "gemm": moe.MOE_FLAG_FORCE_GEMM}[args.path]
+    cfg = moe.config_for(wl, flags)
     t_setup = time.time()
     layers = [pack_layer(wl, 0, l, gen_device="cuda") for l in range(nL)]
     xs = [synth.hidden_states(wl, T, 0, l, device="cuda").contiguous() for l in range(nL)]
@@ -377,6 +378,7 @@ def run_ours(args, world, rank, local):
                    "top_k": wl.top_k, "ff": wl.ff, "shared_ff": wl.shared_ff, "distinct_layers": nL,
                    "resident_expert_gb": round(nL * (wl.n_experts * wl.blob_bytes + wl.shared_blob_bytes) / 1e9, 2),
                    "l2": "inputs larger than L2 (distinct layers rotated)", "graph": "one CUDA graph per step",
+                   "path": args.path,
                    "parallelism": "replicas x%d" % world},
         "hbm": {"algorithmic_bytes_per_call": int(step_bytes),
                 "gbs": round(step_bytes * nL * K / (ms / 1e3) / 1e9 * 1, 1),
@@ -463,6 +465,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--cpu-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["auto", "gemv", "gemm"], default="auto",
+                    help="expert kernels: auto (GEMV for T <= 8, tensor-core GEMM above), or force one")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

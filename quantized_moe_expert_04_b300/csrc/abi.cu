@@ -57,11 +57,19 @@ WsLayout ws_layout(const moe_config &c, int32_t T)
     L.sh_out = take(c.shared_ff && (gemv || det) ? (size_t)T * H * 4 : 0);
     L.act16 = take(gemv ? 0 : TK * c.ff * 2);
     L.sh_act16 = take(!gemv && c.shared_ff ? (size_t)T * c.shared_ff * 2 : 0);
-    const size_t sh_tiles = (size_t)((T + 15) / 16 + 1);
-    L.tiles_gu = take(gemv ? 0 : gemm_tile_capacity(c.ff / 64, (int64_t)TK, c.n_experts) * 16);
-    L.tiles_dn = take(gemv ? 0 : gemm_tile_capacity(c.hidden / 128, (int64_t)TK, c.n_experts) * 16);
-    L.tiles_gus = take(!gemv && c.shared_ff ? sh_tiles * (c.shared_ff / 64) * 16 : 0);
-    L.tiles_dns = take(!gemv && c.shared_ff ? sh_tiles * (c.hidden / 128) * 16 : 0);
+    const size_t sh_tiles = (size_t)((T + 255) / 256 + 1);
+    const GemmSplits sp = gemv ? GemmSplits{1, 1, 1, 1} : gemm_splits(c, T);
+    const size_t cap_gu = gemv ? 0 : gemm_tile_capacity(c.ff / 64, (int64_t)TK, c.n_experts);
+    const size_t cap_dn = gemv ? 0 : gemm_tile_capacity(c.hidden / 128, (int64_t)TK, c.n_experts);
+    const size_t cap_gus = !gemv && c.shared_ff ? sh_tiles * (c.shared_ff / 64) : 0;
+    const size_t cap_dns = !gemv && c.shared_ff ? sh_tiles * (c.hidden / 128) : 0;
+    L.tiles_gu = take(cap_gu * sp.gu * 16);
+    L.tiles_dn = take(cap_dn * sp.dn * 16);
+    L.tiles_gus = take(cap_gus * sp.gus * 16);
+    L.tiles_dns = take(cap_dns * sp.dns * 16);
+    L.gu = take(sp.gu > 1 ? TK * 2 * c.ff * 4 : 0);
+    L.sh_gu = take(sp.gus > 1 ? (size_t)T * 2 * c.shared_ff * 4 : 0);
+    L.split_cnt = take(((sp.gu > 1 ? cap_gu : 0) + (sp.gus > 1 ? cap_gus : 0)) * 4);
     L.total = off;
     return L;
 }
@@ -273,6 +281,15 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
         gw.tiles_dn = (int4 *)(base + L.tiles_dn);
         gw.tiles_gus = (int4 *)(base + L.tiles_gus);
         gw.tiles_dns = (int4 *)(base + L.tiles_dns);
+        gw.splits = gemm_splits(*cfg, T);
+        gw.gu = (float *)(base + L.gu);
+        gw.sh_gu = (float *)(base + L.sh_gu);
+        gw.n_gu = gw.splits.gu > 1 || gw.splits.gus > 1 ? (int64_t)((L.split_cnt - L.gu) / 4) : 0;
+        gw.split_cnt = (uint32_t *)(base + L.split_cnt);
+        gw.n_cnt_routed = gw.splits.gu > 1 ? (int64_t)gemm_tile_capacity(cfg->ff / 64, (int64_t)T * cfg->top_k,
+                                                                             cfg->n_experts)
+                                           : 0;
+        gw.n_cnt = (int64_t)((L.total - L.split_cnt) / 4);
         gw.det = (cfg->flags & MOE_FLAG_DETERMINISTIC) != 0;
         e = launch_experts_gemm(a, gw, s);
     }

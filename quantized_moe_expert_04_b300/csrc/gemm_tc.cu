@@ -27,6 +27,7 @@
 // Operand precision: fp16 A and B (sub-block scale and min rounded to fp16,
 // one fused multiply-add per weight), fp32 accumulation.
 #include <algorithm>
+#include <cmath>
 
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
@@ -40,11 +41,10 @@ enum WFmt { kWQ4K = 0, kWQ80 = 1 };
 
 constexpr int kGemmThreads = 384;
 constexpr int kABytes = 128 * 128;          // 128 rows x 64 fp16
-constexpr int kRawBytes = 18432;            // 128 rows x 144 B (largest raw stage)
 constexpr long long kWaitCycles = 1ll << 32; // ~2 s at 2 GHz
 
 struct GemmArgs {
-    int H, FF, SFF, k, T, det;
+    int H, FF, SFF, k, T, det, splits;
     const uint8_t *const *blobs;
     const uint8_t *shared_blob;
     const int32_t *offsets, *assign;
@@ -54,13 +54,15 @@ struct GemmArgs {
     __half *sh_act16;        // [T][SFF]
     float *yacc;             // [T][H]
     float *slots, *sh_out;   // deterministic combine
-    const int4 *tiles;       // {expert (-1 shared), m tile, n0, n}
+    const int4 *tiles;       // {expert (-1 shared), m tile | k split << 16, n0, n}
     const uint32_t *n_tiles; // device count
+    float *gu;               // split-K gate/up partial sums [rows][2 FF] (splits > 1)
+    uint32_t *split_cnt;     // split-K arrival counters, one per (expert, m, n) group
     uint32_t *status;
 };
 
 struct TileInfo {
-    int e, m, n0, n, nmma, bb, ksteps;
+    int e, m, ks, n0, n, nmma, bb, ksteps, k0;   // k0: first K-step of this split
     const uint8_t *blob;
 };
 
@@ -70,13 +72,15 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs &g, int idx)
     const int4 t = g.tiles[idx];
     TileInfo ti;
     ti.e = t.x;
-    ti.m = t.y;
+    ti.m = t.y & 0xffff;
+    ti.ks = t.y >> 16;
     ti.n0 = t.z;
     ti.n = t.w;
     ti.nmma = (t.w + 15) & ~15;
     ti.bb = t.x >= 0 ? g.offsets[t.x] : 0;
     ti.blob = t.x >= 0 ? g.blobs[t.x] : g.shared_blob;
-    ti.ksteps = (OP == kOpGateUp ? g.H : (FMT == kWQ4K ? g.FF : g.SFF)) / 64;
+    ti.ksteps = (OP == kOpGateUp ? g.H : (FMT == kWQ4K ? g.FF : g.SFF)) / 64 / g.splits;
+    ti.k0 = ti.ks * ti.ksteps;
     return ti;
 }
 
@@ -260,45 +264,64 @@ __device__ __forceinline__ void dequant_dn_q80(const uint8_t *raw, uint32_t a_ti
 
 // ---------------------------------------------------------------- the kernel
 
-template <int OP, int FMT, int NMAX, int S, int RS>
-struct GemmSmem {
-    static constexpr int kBBytes = NMAX * 128;
-    static constexpr int kOffA = 0;
-    static constexpr int kOffB = kOffA + S * kABytes;
-    static constexpr int kOffRaw = kOffB + S * kBBytes;
-    static constexpr int kOffBar = kOffRaw + RS * kRawBytes;
-    static constexpr int kNumBars = 2 * RS + 3 * S + 5;
-    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-    static constexpr int kBytes = kOffMisc + 16 + 1024;   // + alignment slack
-};
-
 template <int OP, int FMT>
-__device__ __forceinline__ int raw_stage_bytes()
+__host__ __device__ constexpr int raw_stage_bytes()
 {
-    if (OP == kOpGateUp) return FMT == kWQ4K ? 128 * 144 : 128 * 80;
-    return FMT == kWQ4K ? 64 * 80 : 64 * 144;
+    return OP == kOpGateUp ? (FMT == kWQ4K ? 128 * 144 : 128 * 80) : (FMT == kWQ4K ? 64 * 80 : 64 * 144);
 }
 
-template <int OP, int FMT, int NMAX, int S, int RS>
+// K-steps covered by one raw stage: a whole Q4_K block column (4 K-steps) for
+// gate/up, one K-step otherwise.
+template <int OP, int FMT>
+__host__ __device__ constexpr int ksteps_per_raw()
+{
+    return (OP == kOpGateUp && FMT == kWQ4K) ? 4 : 1;
+}
+
+template <int OP, int FMT, int NMAX, int SA, int SB, int RAW>
+struct GemmCfg {
+    static constexpr int kRawStage = raw_stage_bytes<OP, FMT>();
+    static constexpr int RS = RAW / kRawStage;           // raw ring depth
+    static constexpr int kBBytes = NMAX * 128;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + SA * kABytes;
+    static constexpr int kOffRaw = kOffB + SB * kBBytes;
+    static constexpr int kOffBar = kOffRaw + ((RS * kRawStage + 1023) & ~1023);
+    static constexpr int kNumBars = 2 * RS + 2 * SA + 2 * SB + 6;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr int kOffMeta = kOffMisc + 16;              // [2][NMAX] token, weight, slot
+    static constexpr int kBytes = kOffMeta + 2 * NMAX * 12 + 1024;
+    static_assert(RS >= 2, "raw ring too shallow");
+    static_assert(kBytes <= 232448, "shared memory budget");
+};
+
+template <int OP, int FMT, int NMAX, int SA, int SB, int RAW>
 __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
 {
-    using L = GemmSmem<OP, FMT, NMAX, S, RS>;
+    using C = GemmCfg<OP, FMT, NMAX, SA, SB, RAW>;
+    constexpr int RS = C::RS;
+    constexpr int KPR = ksteps_per_raw<OP, FMT>();
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_dyn + 1023) & ~(uintptr_t)1023);
-    const uint32_t sA = smem_addr(smem + L::kOffA), sB = smem_addr(smem + L::kOffB);
-    uint8_t *raw_base = smem + L::kOffRaw;
-    const uint32_t bar0 = smem_addr(smem + L::kOffBar);
-    // barrier addresses
+    const uint32_t sA = smem_addr(smem + C::kOffA), sB = smem_addr(smem + C::kOffB);
+    uint8_t *raw_base = smem + C::kOffRaw;
+    const uint32_t bar0 = smem_addr(smem + C::kOffBar);
     auto full_raw = [&](int i) { return bar0 + 8 * i; };
     auto empty_raw = [&](int i) { return bar0 + 8 * (RS + i); };
     auto full_a = [&](int i) { return bar0 + 8 * (2 * RS + i); };
-    auto full_b = [&](int i) { return bar0 + 8 * (2 * RS + S + i); };
-    auto empty_ab = [&](int i) { return bar0 + 8 * (2 * RS + 2 * S + i); };
-    auto acc_full = [&](int i) { return bar0 + 8 * (2 * RS + 3 * S + i); };
-    auto acc_empty = [&](int i) { return bar0 + 8 * (2 * RS + 3 * S + 2 + i); };
-    const uint32_t final_bar = bar0 + 8 * (2 * RS + 3 * S + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
+    auto empty_a = [&](int i) { return bar0 + 8 * (2 * RS + SA + i); };
+    auto full_b = [&](int i) { return bar0 + 8 * (2 * RS + 2 * SA + i); };
+    auto empty_b = [&](int i) { return bar0 + 8 * (2 * RS + 2 * SA + SB + i); };
+    const uint32_t bx = bar0 + 8 * (2 * RS + 2 * SA + 2 * SB);
+    auto acc_full = [&](int i) { return bx + 8 * i; };
+    auto acc_empty = [&](int i) { return bx + 8 * (2 + i); };
+    const uint32_t final_bar = bx + 8 * 4, epi_bar = bx + 8 * 5;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 8);
+    int32_t *meta_tok = reinterpret_cast<int32_t *>(smem + C::kOffMeta);           // [2][NMAX]
+    float *meta_w = reinterpret_cast<float *>(smem + C::kOffMeta + 2 * NMAX * 4);   // [2][NMAX]
+    int32_t *meta_slot = reinterpret_cast<int32_t *>(smem + C::kOffMeta + 2 * NMAX * 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -306,17 +329,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
             mbar_init(full_raw(i), 1);
             mbar_init(empty_raw(i), 128);
         }
-        for (int i = 0; i < S; ++i) {
+        for (int i = 0; i < SA; ++i) {
             mbar_init(full_a(i), 128);
+            mbar_init(empty_a(i), 1);
+        }
+        for (int i = 0; i < SB; ++i) {
             mbar_init(full_b(i), 64);
-            mbar_init(empty_ab(i), 1);
+            mbar_init(empty_b(i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full(i), 1);
             mbar_init(acc_empty(i), 128);
         }
         mbar_init(final_bar, 1);
+        mbar_init(epi_bar, 128);
         *abort_flag = 0;
+        *last_flag = 0;
         fence_mbar_init();
     }
     if (warp == 4) {
@@ -331,52 +359,96 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
 
     if (warp < 4) {
         // ------------------------------------------------------------ epilogue
-        uint32_t t_it = 0;
-        const int row = 32 * warp + lane;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        uint32_t t_it = 0, epi_it = 0;
+        const int et = threadIdx.x;          // 0..127 = tensor-memory lane
+        auto epi_sync = [&]() -> bool {      // the 4 epilogue warps only, bounded
+            mbar_arrive(epi_bar);
+            return wait_bar(epi_bar, (epi_it++) & 1, abort_flag, g.status);
+        };
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<OP, FMT>(g, tile);
             if (!ti.blob) {
-                if (threadIdx.x == 0) set_status(g.status, MOE_ERR_DEVICE_FAULT);
+                if (et == 0) set_status(g.status, MOE_ERR_DEVICE_FAULT);
                 continue;
             }
             const int acc = t_it & 1;
-            if (!wait_bar(acc_full(acc), (t_it >> 1) & 1, abort_flag, g.status)) break;
+            if (OP == kOpDown) {
+                // column metadata: token, routing weight and slot of each column
+                for (int j = et; j < ti.n; j += 128) {
+                    int tok, slot;
+                    float wt;
+                    if (FMT == kWQ4K) {
+                        slot = g.assign[ti.bb + ti.n0 + j];
+                        tok = slot / g.k;
+                        wt = g.w[slot];
+                    } else {
+                        tok = slot = ti.n0 + j;
+                        wt = 1.0f;
+                    }
+                    meta_tok[acc * NMAX + j] = tok;
+                    meta_w[acc * NMAX + j] = wt;
+                    meta_slot[acc * NMAX + j] = slot;
+                }
+                if (!(ok = epi_sync())) break;
+            }
+            if (!(ok = wait_bar(acc_full(acc), (t_it >> 1) & 1, abort_flag, g.status))) break;
             tc_fence_after();
+            const int ffop = FMT == kWQ4K ? g.FF : g.SFF;
             for (int cc = 0; cc < ti.nmma / 16; ++cc) {
                 uint32_t v[16];
                 tmem_ld16(tmem_base + ((uint32_t)(32 * warp) << 16) + acc * NMAX + cc * 16, v);
                 tmem_wait_ld();
                 if (OP == kOpGateUp) {
-                    const int ffop = FMT == kWQ4K ? g.FF : g.SFF;
-                    const int f = ti.m * 64 + (row >> 1);
+                    const int f = ti.m * 64 + (et >> 1);
+                    if (g.splits == 1) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float val = __uint_as_float(v[i]);
-                        const float other = __shfl_xor_sync(0xffffffffu, val, 1);
-                        const int j = cc * 16 + i;
-                        if (!(lane & 1) && j < ti.n) {
-                            const float a = val / (1.0f + expf(-val)) * other;
-                            __half *dst = FMT == kWQ4K ? g.act16 + (int64_t)(ti.bb + ti.n0 + j) * ffop + f
-                                                       : g.sh_act16 + (int64_t)(ti.n0 + j) * ffop + f;
-                            *dst = __float2half_rn(a);
+                        for (int i = 0; i < 16; ++i) {
+                            const float val = __uint_as_float(v[i]);
+                            const float other = __shfl_xor_sync(0xffffffffu, val, 1);
+                            const int j = cc * 16 + i;
+                            if (!(lane & 1) && j < ti.n) {
+                                const float a = val / (1.0f + expf(-val)) * other;
+                                __half *dst = FMT == kWQ4K ? g.act16 + (int64_t)(ti.bb + ti.n0 + j) * ffop + f
+                                                           : g.sh_act16 + (int64_t)(ti.n0 + j) * ffop + f;
+                                *dst = __float2half_rn(a);
+                            }
+                        }
+                    } else {
+                        // partial sums of this K split: g into [row][f], u into [row][FF + f]
+                        const int col = (et & 1) ? ffop + f : f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int j = cc * 16 + i;
+                            const int rowi = FMT == kWQ4K ? ti.bb + ti.n0 + j : ti.n0 + j;
+                            if (j < ti.n) red_add_f32(g.gu + (int64_t)rowi * 2 * ffop + col, __uint_as_float(v[i]));
                         }
                     }
                 } else {
-                    const int h = ti.m * 128 + row;
+                    // 4x4 transposes within lane quads: lane (q, r) ends with the
+                    // values of hidden rows 4q..4q+3 for column 4b + r
+                    const int hq = ti.m * 128 + 32 * warp + (lane & ~3);
+                    const int r = lane & 3;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int j = cc * 16 + i;
+                    for (int b = 0; b < 4; ++b) {
+                        float a0 = __uint_as_float(v[4 * b]), a1 = __uint_as_float(v[4 * b + 1]);
+                        float a2 = __uint_as_float(v[4 * b + 2]), a3 = __uint_as_float(v[4 * b + 3]);
+                        float t0 = __shfl_xor_sync(0xffffffffu, (r & 2) ? a0 : a2, 2);
+                        float t1 = __shfl_xor_sync(0xffffffffu, (r & 2) ? a1 : a3, 2);
+                        if (r & 2) { a0 = t0; a1 = t1; } else { a2 = t0; a3 = t1; }
+                        t0 = __shfl_xor_sync(0xffffffffu, (r & 1) ? a0 : a1, 1);
+                        t1 = __shfl_xor_sync(0xffffffffu, (r & 1) ? a2 : a3, 1);
+                        if (r & 1) { a0 = t0; a2 = t1; } else { a1 = t0; a3 = t1; }
+                        const int j = cc * 16 + 4 * b + r;
                         if (j < ti.n) {
-                            const float val = __uint_as_float(v[i]);
-                            if (FMT == kWQ4K) {
-                                const int asg = g.assign[ti.bb + ti.n0 + j];
-                                const float wt = g.w[asg];
-                                if (g.det) g.slots[(int64_t)asg * g.H + h] = wt * val;
-                                else red_add_f32(g.yacc + (int64_t)(asg / g.k) * g.H + h, wt * val);
+                            const float wt = meta_w[acc * NMAX + j];
+                            if (g.det) {
+                                float *dst = FMT == kWQ4K ? g.slots + (int64_t)meta_slot[acc * NMAX + j] * g.H + hq
+                                                          : g.sh_out + (int64_t)meta_tok[acc * NMAX + j] * g.H + hq;
+                                *reinterpret_cast<float4 *>(dst) = make_float4(wt * a0, wt * a1, wt * a2, wt * a3);
                             } else {
-                                const int t = ti.n0 + j;
-                                if (g.det) g.sh_out[(int64_t)t * g.H + h] = val;
-                                else red_add_f32(g.yacc + (int64_t)t * g.H + h, val);
+                                red_add_v4_f32(g.yacc + (int64_t)meta_tok[acc * NMAX + j] * g.H + hq, wt * a0,
+                                               wt * a1, wt * a2, wt * a3);
                             }
                         }
                     }
@@ -385,11 +457,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
             tc_fence_before();
             mbar_arrive(acc_empty(acc));
             ++t_it;
+            if (OP == kOpGateUp && g.splits > 1) {
+                // the last split of this (expert, m, n) group turns g, u into a
+                __threadfence();
+                if (!(ok = epi_sync())) break;
+                if (et == 0) {
+                    const uint32_t old = atomicAdd(g.split_cnt + tile / g.splits, 1u);
+                    *last_flag = old == (uint32_t)(g.splits - 1);
+                }
+                if (!(ok = epi_sync())) break;
+                if (*last_flag) {
+                    __threadfence();
+                    const int f = ti.m * 64 + (et >> 1);
+                    if (!(et & 1)) {
+                        for (int j = 0; j < ti.n; ++j) {
+                            const int rowi = FMT == kWQ4K ? ti.bb + ti.n0 + j : ti.n0 + j;
+                            const float gg = ld_cg_f32(g.gu + (int64_t)rowi * 2 * ffop + f);
+                            const float uu = ld_cg_f32(g.gu + (int64_t)rowi * 2 * ffop + ffop + f);
+                            __half *dst = FMT == kWQ4K ? g.act16 + (int64_t)rowi * ffop + f
+                                                       : g.sh_act16 + (int64_t)rowi * ffop + f;
+                            *dst = __float2half_rn(gg / (1.0f + expf(-gg)) * uu);
+                        }
+                    }
+                    if (et == 0) g.split_cnt[tile / g.splits] = 0;
+                }
+                if (!(ok = epi_sync())) break;     // last_flag is rewritten by the next group
+            }
         }
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            uint32_t s_it = 0, t_it = 0;
+            uint32_t sa_it = 0, sb_it = 0, t_it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
                 const TileInfo ti = tile_info<OP, FMT>(g, tile);
@@ -399,18 +497,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
                 tc_fence_after();
                 const uint32_t idesc = idesc_f16_f32(128, ti.nmma);
                 const uint32_t d_tmem = tmem_base + acc * NMAX;
-                for (int s = 0; s < ti.ksteps; ++s, ++s_it) {
-                    const int slot = s_it % S;
-                    const uint32_t ph = (s_it / S) & 1;
-                    if (!(ok = wait_bar(full_a(slot), ph, abort_flag, g.status))) break;
-                    if (!(ok = wait_bar(full_b(slot), ph, abort_flag, g.status))) break;
+                for (int s = 0; s < ti.ksteps; ++s, ++sa_it, ++sb_it) {
+                    const int slot_a = sa_it % SA, slot_b = sb_it % SB;
+                    if (!(ok = wait_bar(full_a(slot_a), (sa_it / SA) & 1, abort_flag, g.status))) break;
+                    if (!(ok = wait_bar(full_b(slot_b), (sb_it / SB) & 1, abort_flag, g.status))) break;
                     tc_fence_after();
-                    const uint32_t a0 = sA + slot * kABytes, b0 = sB + slot * L::kBBytes;
+                    const uint32_t a0 = sA + slot_a * kABytes, b0 = sB + slot_b * C::kBBytes;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_f16(d_tmem, sdesc_kmajor_sw128(a0 + 32 * kk), sdesc_kmajor_sw128(b0 + 32 * kk), idesc,
                                 (s | kk) != 0);
-                    mma_commit(empty_ab(slot));
+                    mma_commit(empty_a(slot_a));
+                    mma_commit(empty_b(slot_b));
                 }
                 if (!ok) break;
                 mma_commit(acc_full(acc));
@@ -429,18 +527,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
         const int H = g.H;
         const int64_t rb = FMT == kWQ4K ? (int64_t)(H / 256) * 144 : (int64_t)(H / 32) * 34;   // row bytes
         const int ffop = FMT == kWQ4K ? g.FF : g.SFF;
-        const uint32_t tx = (uint32_t)raw_stage_bytes<OP, FMT>();
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<OP, FMT>(g, tile);
             if (!ti.blob) continue;
-            const int nraw = (OP == kOpGateUp && FMT == kWQ4K) ? ti.ksteps / 4 : ti.ksteps;
-            for (int r = 0; r < nraw; ++r, ++rs_it) {
+            const int nraw = ti.ksteps / KPR, r0 = ti.k0 / KPR;
+            for (int rr = 0; rr < nraw; ++rr, ++rs_it) {
+                const int r = r0 + rr;                    // raw stage (block column / K-step) index
                 const int slot = rs_it % RS;
                 if (!(ok = wait_bar(empty_raw(slot), ((rs_it / RS) & 1) ^ 1, abort_flag, g.status))) break;
-                if (lane == 0) mbar_arrive_expect_tx(full_raw(slot), tx);
+                if (lane == 0) mbar_arrive_expect_tx(full_raw(slot), (uint32_t)C::kRawStage);
                 __syncwarp();
-                const uint32_t dst0 = smem_addr(raw_base + slot * kRawBytes);
+                const uint32_t dst0 = smem_addr(raw_base + slot * C::kRawStage);
                 if (OP == kOpGateUp) {
                     // 128 rows: row 2i = gate f0+i, row 2i+1 = up f0+i
                     for (int i = lane; i < 128; i += 32) {
@@ -478,12 +576,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------ token rows (B)
-        // thread bt copies 16-byte chunk (bt & 7) of rows j = (bt >> 3) + 8 i
+        // thread bt copies 16-byte chunk (bt & 7) of rows j = (bt >> 3) + 8 i;
+        // a stage is announced full once its copies have landed, SB-1 stages
+        // behind the newest one (the lag runs across tiles)
+        constexpr int LAG = SB - 1;
         const int bt = threadIdx.x - 192;   // 0..63
         const int c = bt & 7, r0 = bt >> 3;
         const __half *srcbase = OP == kOpGateUp ? g.x16 : (FMT == kWQ4K ? g.act16 : g.sh_act16);
         const int ld = OP == kOpGateUp ? g.H : (FMT == kWQ4K ? g.FF : g.SFF);
-        uint32_t s_it = 0;
+        uint32_t sb_it = 0, pending = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<OP, FMT>(g, tile);
@@ -498,53 +599,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
                     else src[i] = FMT == kWQ4K ? ti.bb + ti.n0 + j : ti.n0 + j;
                 }
             }
-            int prev = -1;
-            for (int s = 0; s < ti.ksteps; ++s, ++s_it) {
-                const int slot = s_it % S;
-                if (!(ok = wait_bar(empty_ab(slot), ((s_it / S) & 1) ^ 1, abort_flag, g.status))) break;
-                const uint32_t b_tile = sB + slot * L::kBBytes;
+            for (int s = 0; s < ti.ksteps; ++s, ++sb_it) {
+                const int slot = sb_it % SB;
+                if (!(ok = wait_bar(empty_b(slot), ((sb_it / SB) & 1) ^ 1, abort_flag, g.status))) break;
+                const uint32_t b_tile = sB + slot * C::kBBytes;
+                const int kcol = (ti.k0 + s) * 64 + c * 8;
 #pragma unroll
                 for (int i = 0; i < NMAX / 8; ++i) {
                     const int j = r0 + 8 * i;
-                    if (j < ti.n)
-                        cp_async16(b_tile + sw128_off(j, c), srcbase + (int64_t)src[i] * ld + s * 64 + c * 8);
+                    if (j < ti.n) cp_async16(b_tile + sw128_off(j, c), srcbase + (int64_t)src[i] * ld + kcol);
                 }
                 cp_async_commit();
-                if (prev >= 0) {
-                    cp_async_wait<1>();
+                if (++pending > (uint32_t)LAG) {
+                    cp_async_wait<LAG>();
                     fence_proxy_async();
-                    mbar_arrive(full_b(prev));
+                    mbar_arrive(full_b((sb_it - LAG) % SB));
+                    --pending;
                 }
-                prev = slot;
-            }
-            cp_async_wait<0>();
-            if (ok && prev >= 0) {
-                fence_proxy_async();
-                mbar_arrive(full_b(prev));
             }
         }
         cp_async_wait<0>();
+        fence_proxy_async();
+        if (ok)
+            for (; pending > 0; --pending) mbar_arrive(full_b((sb_it - pending) % SB));
     } else {
         // ------------------------------------------------------------ dequantisation (A)
         const int dt = threadIdx.x - 256;   // 0..127
-        uint32_t s_it = 0, rs_it = 0;
+        uint32_t sa_it = 0, rs_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<OP, FMT>(g, tile);
             if (!ti.blob) continue;
-            for (int s = 0; s < ti.ksteps; ++s, ++s_it) {
-                const bool per_block = OP == kOpGateUp && FMT == kWQ4K;
-                const int sub = per_block ? (s & 3) : 0;
-                const bool first = sub == 0, last = per_block ? sub == 3 : true;
+            for (int s = 0; s < ti.ksteps; ++s, ++sa_it) {
+                const int sg = ti.k0 + s;                 // global K-step
+                const int sub = sg % KPR;
+                const bool first = s == 0 || sub == 0, last = s == ti.ksteps - 1 || sub == KPR - 1;
                 const int rslot = rs_it % RS;
                 if (first && !(ok = wait_bar(full_raw(rslot), (rs_it / RS) & 1, abort_flag, g.status))) break;
-                const int slot = s_it % S;
-                if (!(ok = wait_bar(empty_ab(slot), ((s_it / S) & 1) ^ 1, abort_flag, g.status))) break;
-                const uint8_t *raw = raw_base + rslot * kRawBytes;
+                const int slot = sa_it % SA;
+                if (!(ok = wait_bar(empty_a(slot), ((sa_it / SA) & 1) ^ 1, abort_flag, g.status))) break;
+                const uint8_t *raw = raw_base + rslot * C::kRawStage;
                 const uint32_t a_tile = sA + slot * kABytes;
                 if (OP == kOpGateUp) {
                     if (FMT == kWQ4K) dequant_gu_q4k(raw, a_tile, dt, sub);
-                    else dequant_gu_q80(raw, a_tile, dt, s);
+                    else dequant_gu_q80(raw, a_tile, dt, sg);
                 } else {
                     if (FMT == kWQ4K) dequant_dn_q4k(raw, a_tile, dt, ti.m & 1);
                     else dequant_dn_q80(raw, a_tile, dt, (34 * (ti.m * 128 / 32)) & 15);
@@ -569,23 +667,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
 
 // ---------------------------------------------------------------- helpers
 
-// x -> fp16 operand copy; zero the fp32 output accumulator.
+// x -> fp16 operand copy; zero the fp32 output accumulator, the split-K
+// partial sums and their counters.
 __global__ void __launch_bounds__(256) k_gemm_prep(const uint16_t *__restrict__ x, __half *__restrict__ x16,
-                                                   float *__restrict__ yacc, int64_t n, uint32_t *status)
+                                                   float *__restrict__ yacc, int64_t n, float *__restrict__ gu,
+                                                   int64_t n_gu, uint32_t *__restrict__ cnt, int64_t n_cnt,
+                                                   uint32_t *status)
 {
     bool bad = false;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
         const float v = bf16_bits_to_f32(x[i]);
         const __half hv = __float2half_rn(v);
         bad |= isfinite(v) && !isfinite(__half2float(hv));    // beyond the fp16 range
         x16[i] = hv;
         if (yacc) yacc[i] = 0.0f;
     }
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_gu; i += stride) gu[i] = 0.0f;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_cnt; i += stride) cnt[i] = 0u;
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, MOE_ERR_DEVICE_FAULT);
 }
 
 struct PlanArgs {
-    int H, FF, SFF, T;
+    int H, FF, SFF, T, split_gu, split_dn, split_gus, split_dns;
     const int32_t *offsets, *active;
     uint32_t *header;
     int4 *gu, *dn, *gus, *dns;
@@ -600,6 +704,9 @@ __device__ __forceinline__ void split_tokens(int n_e, int &tn, int &nt)
 
 // Work tiles of the routed experts (both projections) and of the shared
 // expert; one CTA, one thread per active expert, block-wide prefix sums.
+// Tile (e, m | ks << 16, n0, n): expert e (-1 = shared), weight tile m, K
+// split ks, tokens n0 .. n0+n-1 of the expert's bucket.  The splits of one
+// (e, m, n0) group are consecutive.
 __global__ void __launch_bounds__(1024) k_gemm_plan(PlanArgs p)
 {
     __shared__ int scan_gu[1024], scan_dn[1024];
@@ -612,8 +719,8 @@ __global__ void __launch_bounds__(1024) k_gemm_plan(PlanArgs p)
         n_e = p.offsets[e + 1] - p.offsets[e];
         split_tokens(n_e, tn, nt);
     }
-    scan_gu[u] = nt * mt_gu;
-    scan_dn[u] = nt * mt_dn;
+    scan_gu[u] = nt * mt_gu * p.split_gu;
+    scan_dn[u] = nt * mt_dn * p.split_dn;
     __syncthreads();
     for (int off = 1; off < 1024; off <<= 1) {
         const int a = u >= off ? scan_gu[u - off] : 0, b = u >= off ? scan_dn[u - off] : 0;
@@ -622,11 +729,13 @@ __global__ void __launch_bounds__(1024) k_gemm_plan(PlanArgs p)
         scan_dn[u] += b;
         __syncthreads();
     }
-    const int base_gu = scan_gu[u] - nt * mt_gu, base_dn = scan_dn[u] - nt * mt_dn;
+    int at_gu = scan_gu[u] - nt * mt_gu * p.split_gu, at_dn = scan_dn[u] - nt * mt_dn * p.split_dn;
     for (int j = 0; j < nt; ++j) {
         const int n0 = j * tn, n = min(tn, n_e - n0);
-        for (int m = 0; m < mt_gu; ++m) p.gu[base_gu + j * mt_gu + m] = make_int4(e, m, n0, n);
-        for (int m = 0; m < mt_dn; ++m) p.dn[base_dn + j * mt_dn + m] = make_int4(e, m, n0, n);
+        for (int m = 0; m < mt_gu; ++m)
+            for (int ks = 0; ks < p.split_gu; ++ks) p.gu[at_gu++] = make_int4(e, m | (ks << 16), n0, n);
+        for (int m = 0; m < mt_dn; ++m)
+            for (int ks = 0; ks < p.split_dn; ++ks) p.dn[at_dn++] = make_int4(e, m | (ks << 16), n0, n);
     }
     if (u == 1023) {
         p.header[kHdrTilesGU] = (uint32_t)scan_gu[1023];
@@ -636,17 +745,18 @@ __global__ void __launch_bounds__(1024) k_gemm_plan(PlanArgs p)
         int stn, snt;
         split_tokens(p.T, stn, snt);
         const int smt_gu = p.SFF / 64;
-        for (int i = u; i < snt * smt_gu; i += 1024) {
-            const int j = i / smt_gu, m = i % smt_gu;
-            p.gus[i] = make_int4(-1, m, j * stn, min(stn, p.T - j * stn));
+        const int n_gus = snt * smt_gu * p.split_gus, n_dns = snt * mt_dn * p.split_dns;
+        for (int i = u; i < n_gus; i += 1024) {
+            const int ks = i % p.split_gus, grp = i / p.split_gus, j = grp / smt_gu, m = grp % smt_gu;
+            p.gus[i] = make_int4(-1, m | (ks << 16), j * stn, min(stn, p.T - j * stn));
         }
-        for (int i = u; i < snt * mt_dn; i += 1024) {
-            const int j = i / mt_dn, m = i % mt_dn;
-            p.dns[i] = make_int4(-1, m, j * stn, min(stn, p.T - j * stn));
+        for (int i = u; i < n_dns; i += 1024) {
+            const int ks = i % p.split_dns, grp = i / p.split_dns, j = grp / mt_dn, m = grp % mt_dn;
+            p.dns[i] = make_int4(-1, m | (ks << 16), j * stn, min(stn, p.T - j * stn));
         }
         if (u == 0) {
-            p.header[kHdrTilesGUS] = (uint32_t)(snt * smt_gu);
-            p.header[kHdrTilesDNS] = (uint32_t)(snt * mt_dn);
+            p.header[kHdrTilesGUS] = (uint32_t)n_gus;
+            p.header[kHdrTilesDNS] = (uint32_t)n_dns;
         }
     } else if (u == 0) {
         p.header[kHdrTilesGUS] = 0;
@@ -677,19 +787,28 @@ __global__ void __launch_bounds__(256) k_gemm_finish(const float *__restrict__ y
 
 // ---------------------------------------------------------------- launch
 
-template <int OP, int FMT, int NMAX, int S, int RS>
+template <int OP, int FMT, int NMAX, int SA, int SB, int RAW>
 static cudaError_t launch_gemm(const GemmArgs &g, int grid, cudaStream_t s)
 {
-    using L = GemmSmem<OP, FMT, NMAX, S, RS>;
+    using C = GemmCfg<OP, FMT, NMAX, SA, SB, RAW>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<OP, FMT, NMAX, S, RS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+        cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<OP, FMT, NMAX, SA, SB, RAW>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    k_moe_gemm<OP, FMT, NMAX, S, RS><<<grid, kGemmThreads, L::kBytes, s>>>(g);
+    k_moe_gemm<OP, FMT, NMAX, SA, SB, RAW><<<grid, kGemmThreads, C::kBytes, s>>>(g);
     return cudaGetLastError();
+}
+
+// Configurations: small buckets (every token tile <= 16 wide: decode windows)
+// keep deep A and raw rings; large buckets (prefill) keep a deep B ring.
+template <int OP, int FMT>
+static cudaError_t launch_gemm_cfg(const GemmArgs &g, int grid, bool small, cudaStream_t s)
+{
+    if (small) return launch_gemm<OP, FMT, 16, 6, 8, 92160>(g, grid, s);
+    return launch_gemm<OP, FMT, 256, 2, 4, 55296>(g, grid, s);
 }
 
 static int num_sms()
@@ -709,15 +828,53 @@ size_t gemm_tile_capacity(int mt, int64_t TK, int E)
     return (size_t)mt * (size_t)(TK / 256 + 1 + std::min<int64_t>(E, TK));
 }
 
+// K split for `tiles` work tiles of `ksteps` K-steps: the smallest divisor d
+// of `units` (K-steps come in units: Q4_K blocks or 64-row groups) whose waves
+// over the SMs are at least 85% full, keeping >= 4 K-steps per tile; the best
+// wave fill among the allowed divisors otherwise.
+static int pick_split(int64_t tiles, int units, int ksteps, int sms)
+{
+    int best = 1;
+    double best_eff = 0.0;
+    for (int d = 1; d <= units; ++d) {
+        if (units % d || (d > 1 && ksteps / d < 4)) continue;
+        const double waves = (double)(tiles * d) / sms;
+        const double eff = waves / std::ceil(waves);
+        if (eff >= 0.85) return d;
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = d;
+        }
+    }
+    return best;
+}
+
+GemmSplits gemm_splits(const moe_config &c, int32_t T)
+{
+    GemmSplits sp{1, 1, 1, 1};
+    if (T > kGemmSmallTokens) return sp;                  // prefill: enough tiles without splitting K
+    const int sms = num_sms();
+    const int64_t active = std::min<int64_t>(c.n_experts, (int64_t)T * c.top_k);
+    sp.gu = pick_split(active * (c.ff / 64), c.hidden / 256, c.hidden / 64, sms);
+    sp.dn = pick_split(active * (c.hidden / 128), c.ff / 64, c.ff / 64, sms);
+    if (c.shared_ff) {
+        sp.gus = pick_split(c.shared_ff / 64, c.hidden / 256, c.hidden / 64, sms);
+        sp.dns = pick_split(c.hidden / 128, c.shared_ff / 64, c.shared_ff / 64, sms);
+    }
+    return sp;
+}
+
 cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream_t s)
 {
     const int64_t n = (int64_t)a.T * a.H;
     const int det = w.det;
+    const bool small = a.T <= kGemmSmallTokens;
+    const GemmSplits sp = w.splits;
     prof_begin(kPhGemmPrep, s);
-    k_gemm_prep<<<(unsigned)std::min<int64_t>((n + 255) / 256, 148 * 8), 256, 0, s>>>(
-        a.x, w.x16, det ? nullptr : w.yacc, n, a.header + kHdrStatus);
-    PlanArgs p{a.H, a.FF, a.SFF, a.T, a.offsets, a.active, a.header, w.tiles_gu, w.tiles_dn, w.tiles_gus,
-               w.tiles_dns};
+    k_gemm_prep<<<(unsigned)std::min<int64_t>((std::max<int64_t>(n, w.n_gu) + 255) / 256, 148 * 8), 256, 0, s>>>(
+        a.x, w.x16, det ? nullptr : w.yacc, n, w.gu, w.n_gu, w.split_cnt, w.n_cnt, a.header + kHdrStatus);
+    PlanArgs p{a.H, a.FF, a.SFF, a.T, sp.gu, sp.dn, sp.gus, sp.dns, a.offsets, a.active, a.header,
+               w.tiles_gu, w.tiles_dn, w.tiles_gus, w.tiles_dns};
     k_gemm_plan<<<1, 1024, 0, s>>>(p);
     prof_end(kPhGemmPrep, s);
 
@@ -746,11 +903,17 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     prof_begin(kPhGemmGateUp, s);
     g.tiles = w.tiles_gu;
     g.n_tiles = a.header + kHdrTilesGU;
-    e = launch_gemm<kOpGateUp, kWQ4K, 256, 3, 3>(g, grid, s);
+    g.splits = sp.gu;
+    g.gu = w.gu;
+    g.split_cnt = w.split_cnt;
+    e = launch_gemm_cfg<kOpGateUp, kWQ4K>(g, grid, small, s);
     if (e == cudaSuccess && a.shared_blob) {
         g.tiles = w.tiles_gus;
         g.n_tiles = a.header + kHdrTilesGUS;
-        e = launch_gemm<kOpGateUp, kWQ80, 256, 3, 3>(g, grid, s);
+        g.splits = sp.gus;
+        g.gu = w.sh_gu;
+        g.split_cnt = w.split_cnt + w.n_cnt_routed;
+        e = launch_gemm_cfg<kOpGateUp, kWQ80>(g, grid, small, s);
     }
     prof_end(kPhGemmGateUp, s);
     if (e != cudaSuccess) return e;
@@ -758,11 +921,13 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     prof_begin(kPhGemmDown, s);
     g.tiles = w.tiles_dn;
     g.n_tiles = a.header + kHdrTilesDN;
-    e = launch_gemm<kOpDown, kWQ4K, 256, 3, 3>(g, grid, s);
+    g.splits = sp.dn;
+    e = launch_gemm_cfg<kOpDown, kWQ4K>(g, grid, small, s);
     if (e == cudaSuccess && a.shared_blob) {
         g.tiles = w.tiles_dns;
         g.n_tiles = a.header + kHdrTilesDNS;
-        e = launch_gemm<kOpDown, kWQ80, 256, 3, 3>(g, grid, s);
+        g.splits = sp.dns;
+        e = launch_gemm_cfg<kOpDown, kWQ80>(g, grid, small, s);
     }
     prof_end(kPhGemmDown, s);
     if (e != cudaSuccess) return e;

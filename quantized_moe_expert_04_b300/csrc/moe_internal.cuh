@@ -69,7 +69,7 @@ void prof_end(int phase, cudaStream_t s);
 struct WsLayout {
     size_t header, logits, ids, w, counts, offsets, assign, active;
     size_t act, slots, yacc, x16, sh_act, sh_out;
-    size_t act16, sh_act16, tiles_gu, tiles_dn, tiles_gus, tiles_dns;
+    size_t act16, sh_act16, tiles_gu, tiles_dn, tiles_gus, tiles_dns, gu, sh_gu, split_cnt;
     size_t total;
 };
 
@@ -115,13 +115,23 @@ struct ExpertArgs {
 cudaError_t launch_experts_gemv(const ExpertArgs &a, cudaStream_t s);
 
 // Tensor-core (tcgen05) grouped GEMM path: its workspace regions.
+constexpr int kGemmSmallTokens = 16;   // calls with T <= 16 use the small-bucket GEMM configuration
+struct GemmSplits {
+    int gu, dn, gus, dns;                // K splits: routed gate/up, down; shared gate/up, down
+};
 struct GemmWs {
     __half *x16, *act16, *sh_act16;
     float *yacc;
+    float *gu, *sh_gu;                   // split-K partial sums of g and u
+    int64_t n_gu;                        // floats to zero in gu and sh_gu (contiguous)
+    uint32_t *split_cnt;                 // split-K counters (routed groups, then shared groups)
+    int64_t n_cnt, n_cnt_routed;
     int4 *tiles_gu, *tiles_dn, *tiles_gus, *tiles_dns;
+    GemmSplits splits;
     int det;
 };
 size_t gemm_tile_capacity(int mt, int64_t TK, int E);
+GemmSplits gemm_splits(const moe_config &c, int32_t T);
 cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream_t s);
 
 }  // namespace moe

@@ -166,5 +166,19 @@ __device__ __forceinline__ void red_add_f32(float *p, float v)
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+// four consecutive fp32 (16-byte aligned) added atomically as one vector
+__device__ __forceinline__ void red_add_v4_f32(float *p, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ float ld_cg_f32(const float *p)
+{
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+
 }  // namespace ptx
 }  // namespace moe

@@ -144,3 +144,12 @@ def test_gemm_deterministic_mode(wl, T):
     x = synth.hidden_states(wl, T).cuda()
     y2 = forward(pl, x, ws, cfg=cfg)
     assert torch.equal(y, y2)
+
+
+FULL_GEMM = [(W["qwen_decode"], 1), (W["qwen_decode"], 3), (W["deepseek_decode"], 1), (W["deepseek_decode"], 8)]
+
+
+@pytest.mark.parametrize("wl,T", FULL_GEMM, ids=lambda c: getattr(c, "name", str(c)))
+def test_full_size_decode_on_tensor_cores(wl, T):
+    """Decode windows through the tensor-core path (K split across CTAs)."""
+    _run(wl, T, gen_device="cuda", flags=moe.MOE_FLAG_FORCE_GEMM)
