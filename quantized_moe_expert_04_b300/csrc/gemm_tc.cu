@@ -861,6 +861,11 @@ GemmSplits gemm_splits(const moe_config &c, int32_t T)
         sp.gus = pick_split(c.shared_ff / 64, c.hidden / 256, c.hidden / 64, sms);
         sp.dns = pick_split(c.hidden / 128, c.shared_ff / 64, c.shared_ff / 64, sms);
     }
+    if (c.flags & MOE_FLAG_DETERMINISTIC) {
+        // the deterministic down epilogue stores each slot once: no K split there
+        sp.dn = 1;
+        sp.dns = 1;
+    }
     return sp;
 }
 
