@@ -190,19 +190,25 @@ def algorithmic(wl, T, ids_per_layer):
     """Bytes and flops one layer call must move / compute, from its routing.
 
     Bytes: each selected expert's blob once per window (+ shared blob), the
-    fp32 router matrix, bias, x in, y out, ids and weights.  Flops: router
-    2*T*E*H + 2*T*k*3*H*FF (+ 2*T*3*H*FF_s shared); padding not counted."""
+    fp32 router matrix, bias, x in, y out, ids and weights.  Per kernel of the
+    decode path: router E*H*4 + T*H*2; gate/up U*2*FF*(H/256)*144; down
+    U*FF*(H/256)*144 (U = distinct experts the window selected).  Flops:
+    router 2*T*E*H + 2*T*k*3*H*FF (+ 2*T*3*H*FF_s shared); padding not
+    counted."""
     E, H, FF, k = wl.n_experts, wl.hidden, wl.ff, wl.top_k
-    total_bytes, gateup_bytes = [], []
+    rb = (H // 256) * 144
+    total_bytes, per_kernel = [], {"dec_route": [], "dec_gateup": [], "dec_down": []}
     for ids in ids_per_layer:
         U = len(np.unique(ids))
         b = U * wl.blob_bytes + wl.shared_blob_bytes + E * H * 4 + (E * 4 if wl.bias != "none" else 0)
         b += 2 * T * H * 2 + T * k * 8
         total_bytes.append(b)
-        gateup_bytes.append(U * 2 * FF * (H // 256) * 144 + T * H * 2)
+        per_kernel["dec_route"].append(E * H * 4 + T * H * 2)
+        per_kernel["dec_gateup"].append(U * 2 * FF * rb)
+        per_kernel["dec_down"].append(U * FF * rb)
     flops = 2 * T * E * H + 2 * T * k * 3 * H * FF + (2 * T * 3 * H * wl.shared_ff if wl.has_shared else 0)
     gemm_gateup_flops = 2 * T * k * 2 * H * FF
-    return np.mean(total_bytes), np.mean(gateup_bytes), flops, gemm_gateup_flops
+    return np.mean(total_bytes), {n: float(np.mean(v)) for n, v in per_kernel.items()}, flops, gemm_gateup_flops
 
 
 def kernel_source_hash():
@@ -237,6 +243,7 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     nL = wl.layers if args.layers is None else args.layers
     flags = {"auto": 0, "gemv": moe.MOE_FLAG_FORCE_GEMV, "gemm": moe.MOE_FLAG_FORCE_GEMM}[args.path]
+    flags |= moe.MOE_FLAG_STATIC_WEIGHTS     # the layers' weights are never rewritten
     cfg = moe.config_for(wl, flags)
     t_setup = time.time()
     layers = [pack_layer(wl, 0, l, gen_device="cuda") for l in range(nL)]
@@ -346,19 +353,21 @@ def run_ours(args, world, rank, local):
 
     # roofline of the dominant kernel
     pk = peaks()
-    step_bytes, gateup_bytes, flops, gemm_flops = algorithmic(wl, T, ids_per_layer)
+    step_bytes, kernel_bytes, flops, gemm_flops = algorithmic(wl, T, ids_per_layer)
     kernel_ms = {name: (v[2] / v[1] if v[1] else float("nan")) for name, v in prof.items()}
     share = {name: v[2] for name, v in prof.items()}
     top = max(share, key=share.get)
-    decode = "gemv_gateup" in prof
+    decode = "dec_gateup" in prof
     if decode:
-        dom = "gemv_gateup"
-        achieved = gateup_bytes / (kernel_ms[dom] / 1e3) / 1e9
+        dom = max((n for n in kernel_bytes if n in share), key=lambda n: share[n])
+        achieved = kernel_bytes[dom] / (kernel_ms[dom] / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": profiled_traffic(dom, wl.name, T), "peak_source": pk["source"],
+                "traffic": profiled_traffic(dom, wl.name, T), "peak_source": pk["source"] + " (burst copy)",
                 "avg_launch_us": round(kernel_ms[dom] * 1e3, 3),
-                "algorithmic_bytes_per_launch": int(gateup_bytes)}
+                "algorithmic_bytes_per_launch": int(kernel_bytes[dom]),
+                "per_kernel_gbs": {n: round(kernel_bytes[n] / (kernel_ms[n] / 1e3) / 1e9, 1)
+                                   for n in kernel_bytes if n in kernel_ms}}
     else:
         dom = "gemm_gateup" if "gemm_gateup" in prof else top
         achieved = gemm_flops / (kernel_ms[dom] / 1e3) / 1e12
@@ -372,12 +381,12 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if decode else "f16",
+        "dtype": "f16xf16->f32 (gate/up), f32 (down)" if decode else "f16xf16->f32",
         "data": "synthetic (seeded; x~N(0,1) bf16, router W~N(0,1/H), experts N(0,0.02^2) packed to Q4_K)",
         "config": {"workload": wl.name, "tokens_per_window": T, "hidden": wl.hidden, "experts": wl.n_experts,
                    "top_k": wl.top_k, "ff": wl.ff, "shared_ff": wl.shared_ff, "distinct_layers": nL,
                    "resident_expert_gb": round(nL * (wl.n_experts * wl.blob_bytes + wl.shared_blob_bytes) / 1e9, 2),
-                   "l2": "inputs larger than L2 (distinct layers rotated)", "graph": "one CUDA graph per step",
+                   "l2": "inputs larger than L2 (distinct layers rotated)", "graph": "one CUDA graph per step", "static_weights": True,
                    "path": args.path,
                    "parallelism": "replicas x%d" % world},
         "hbm": {"algorithmic_bytes_per_call": int(step_bytes),

@@ -91,8 +91,14 @@ typedef enum {
 enum {
     MOE_FLAG_DETERMINISTIC = 1,      /* combine through per-assignment slots in a fixed
                                         order on every path (bit-identical reruns)        */
-    MOE_FLAG_FORCE_GEMV = 2,         /* use the decode (grouped GEMV) path at any T      */
-    MOE_FLAG_FORCE_GEMM = 4          /* use the prefill (tensor-core GEMM) path at any T */
+    MOE_FLAG_FORCE_GEMV = 2,         /* use the decode (grouped GEMV) path; T <= 8 only  */
+    MOE_FLAG_FORCE_GEMM = 4,         /* use the prefill (tensor-core GEMM) path at any T */
+    MOE_FLAG_STATIC_WEIGHTS = 8      /* the caller guarantees that router_w, router_bias
+                                        and the expert blobs are not written by the work
+                                        enqueued just before this call on the stream: a
+                                        decode call may then start reading the router
+                                        rows while that work is still running (its other
+                                        inputs are read only after it has finished)     */
 };
 
 /*
@@ -196,9 +202,12 @@ MOE_API moe_status moe_route(const moe_config *cfg, const uint16_t *x, const flo
  * bf16 [T][H]; y_f32: optional fp32 [T][H] copy before rounding (may be NULL).
  * The routing of the call stays readable in the workspace
  * (moe_workspace_routing) until the next call.
- * Path: T <= 8 (or MOE_FLAG_FORCE_GEMV) streams the selected experts with a
- * grouped GEMV in fp32; larger T runs the tensor-core grouped GEMM with fp16
- * operands and fp32 accumulation.
+ * Path: T <= 8 (or MOE_FLAG_FORCE_GEMV) runs the decode path: each selected
+ * expert's bytes are streamed once per window; gate/up multiply fp16
+ * dequantised weights by the fp16 hidden states with fp32 accumulation (warp
+ * MMAs), the down projection runs in fp32.  Larger T runs the tensor-core
+ * grouped GEMM with fp16 operands and fp32 accumulation.  Both paths need
+ * |x| < 65504 (fp16 range; larger values set MOE_ERR_DEVICE_FAULT).
  */
 MOE_API moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *router_w,
                        const float *router_bias, const uint8_t *const *expert_blobs,

@@ -23,10 +23,13 @@ static bool cfg_valid(const moe_config *c)
     return true;
 }
 
+// Decode path (windows of up to kDecTok tokens) unless the tensor-core GEMM
+// is forced or the hidden width has no router split.
 bool use_gemv(const moe_config &c, int32_t T)
 {
-    if (c.flags & MOE_FLAG_FORCE_GEMV) return true;
     if (c.flags & MOE_FLAG_FORCE_GEMM) return false;
+    if (T > kDecTok || dec_route_parts(c.hidden) == 0) return false;
+    if (c.flags & MOE_FLAG_FORCE_GEMV) return true;
     return T <= kGemvMaxTokens;
 }
 
@@ -49,12 +52,16 @@ WsLayout ws_layout(const moe_config &c, int32_t T)
     L.assign = take(TK * 4);
     L.active = take((E + 1) * 4);
     const bool gemv = use_gemv(c, T), det = (c.flags & MOE_FLAG_DETERMINISTIC) != 0;
+    const size_t maxu = std::min<size_t>(E, TK);
+    L.plan = take(gemv ? maxu * sizeof(DecPlan) : 0);
+    L.xfrag = take(gemv ? (size_t)H * 16 : 0);
     L.act = take(gemv ? TK * c.ff * 4 : 0);
-    L.slots = take(gemv || det ? TK * H * 4 : 0);
-    L.yacc = take(gemv ? 0 : (size_t)T * H * 4);
+    L.slots = take(det ? TK * H * 4 * (gemv ? dec_down_splits(c, T) : 1) : 0);
+    L.yacc = take((size_t)T * H * 4);
     L.x16 = take(gemv ? 0 : (size_t)T * H * 2);
     L.sh_act = take(gemv && c.shared_ff ? (size_t)T * c.shared_ff * 4 : 0);
     L.sh_out = take(c.shared_ff && (gemv || det) ? (size_t)T * H * 4 : 0);
+    (void)maxu;
     L.act16 = take(gemv ? 0 : TK * c.ff * 2);
     L.sh_act16 = take(!gemv && c.shared_ff ? (size_t)T * c.shared_ff * 2 : 0);
     const size_t sh_tiles = (size_t)((T + 255) / 256 + 1);
@@ -241,13 +248,53 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
     if ((y && !aligned16(y)) || (y_f32 && !aligned16(y_f32)) || (shared_blob && !aligned16(shared_blob)))
         return MOE_ERR_MISALIGNED;
     if (T == 0) return MOE_OK;
+    if ((cfg->flags & MOE_FLAG_FORCE_GEMV) && !use_gemv(*cfg, T)) return MOE_ERR_UNSUPPORTED_SHAPE;
     cudaStream_t s = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(*cfg, T);
+    char *base = (char *)ws;
     RouteArgs r = route_args(cfg, x, router_w, router_bias, T, ws);
+    if (use_gemv(*cfg, T)) {
+        DecArgs d{};
+        d.H = cfg->hidden;
+        d.E = cfg->n_experts;
+        d.FF = cfg->ff;
+        d.k = cfg->top_k;
+        d.T = T;
+        d.SFF = cfg->shared_ff;
+        d.score_fn = cfg->score_fn;
+        d.det = (cfg->flags & MOE_FLAG_DETERMINISTIC) != 0;
+        d.route_parts = dec_route_parts(cfg->hidden);
+        d.fs_dn = dec_down_splits(*cfg, T);
+        d.overlap_prev = (cfg->flags & MOE_FLAG_STATIC_WEIGHTS) != 0;
+        d.prefetch_down = 1;
+        d.prefetch_budget = kDecPrefetchBudget;
+        d.x = x;
+        d.wr = router_w;
+        d.bias = cfg->score_fn == MOE_SCORE_SIGMOID_BIAS ? router_bias : nullptr;
+        d.blobs = expert_blobs;
+        d.shared_blob = cfg->shared_ff > 0 ? shared_blob : nullptr;
+        d.logits = r.logits;
+        d.ids = r.ids;
+        d.w = r.w;
+        d.counts = r.counts;
+        d.offsets = r.offsets;
+        d.assign = r.assign;
+        d.active = r.active;
+        d.plan = (DecPlan *)(base + L.plan);
+        d.xfrag = (uint4 *)(base + L.xfrag);
+        d.act = (float *)(base + L.act);
+        d.sh_act = cfg->shared_ff ? (float *)(base + L.sh_act) : nullptr;
+        d.sh_out = cfg->shared_ff ? (float *)(base + L.sh_out) : nullptr;
+        d.yacc = (float *)(base + L.yacc);
+        d.slots = d.det ? (float *)(base + L.slots) : nullptr;
+        d.y = y;
+        d.y_f32 = y_f32;
+        d.header = r.header;
+        return cuda_status(launch_decode(d, s));
+    }
     cudaError_t e = launch_route(r, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-    const WsLayout L = ws_layout(*cfg, T);
-    char *base = (char *)ws;
     ExpertArgs a{};
     a.H = cfg->hidden;
     a.E = cfg->n_experts;
@@ -269,9 +316,7 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
     a.y = y;
     a.y_f32 = y_f32;
     a.header = r.header;
-    if (use_gemv(*cfg, T)) {
-        e = launch_experts_gemv(a, s);
-    } else {
+    {
         GemmWs gw{};
         gw.x16 = (__half *)(base + L.x16);
         gw.act16 = (__half *)(base + L.act16);

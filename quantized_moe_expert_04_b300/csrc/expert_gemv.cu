@@ -11,7 +11,6 @@
 //             the expert's tokens; act is indexed by bucket position.
 //   k_down    warp per (expert, 256 hidden columns): o = sum_f a_f Wd[f][:],
 //             scaled by the routing weight into the assignment's slot.
-//   k_combine y_t = sum_r slot[t*k + r] (+ shared expert), fixed order.
 // The shared expert (Q8_0) runs through the same kernels as an expert whose
 // bucket is every token with weight 1.
 #include <algorithm>
@@ -220,47 +219,30 @@ __global__ void __launch_bounds__(256) k_down(ExpertArgs a)
     }
 }
 
-// y_t = sum_r slot[t*k + r] in r order (+ shared), rounded to bf16.
-__global__ void __launch_bounds__(256) k_combine(ExpertArgs a)
-{
-    const int64_t n = (int64_t)a.T * a.H;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = i / a.H, h = i % a.H;
-        float acc = 0.0f;
-        for (int r = 0; r < a.k; ++r) acc += a.slots[(t * a.k + r) * a.H + h];
-        if (a.sh_out) acc += a.sh_out[i];
-        a.y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
-        if (a.y_f32) a.y_f32[i] = acc;
-    }
-}
-
 static unsigned blocks_for_warps(int64_t warps) { return (unsigned)((warps + 7) / 8); }
 
-cudaError_t launch_experts_gemv(const ExpertArgs &a, cudaStream_t s)
+// The shared expert of a decode window (every token, weight 1): gate/up into
+// sh_act, down into sh_out; the decode path's last down CTA adds sh_out to y.
+cudaError_t launch_shared_gemv(const DecArgs &d, cudaStream_t s)
 {
-    if (a.T <= 0) return cudaGetLastError();
-    const int64_t max_active = std::min<int64_t>(a.E, (int64_t)a.T * a.k);
-    prof_begin(kPhGateUp, s);
-    k_gateup<kFmtQ4K, false><<<blocks_for_warps(max_active * a.FF), 256, 0, s>>>(a);
-    prof_end(kPhGateUp, s);
-    if (a.shared_blob) {
-        prof_begin(kPhGateUpShared, s);
-        k_gateup<kFmtQ80, true><<<blocks_for_warps(a.SFF), 256, 0, s>>>(a);
-        prof_end(kPhGateUpShared, s);
-    }
-    prof_begin(kPhDown, s);
-    k_down<kFmtQ4K, false><<<blocks_for_warps(max_active * (a.H / 256)), 256, 0, s>>>(a);
-    prof_end(kPhDown, s);
-    if (a.shared_blob) {
-        prof_begin(kPhDownShared, s);
-        k_down<kFmtQ80, true><<<blocks_for_warps(a.H / 256), 256, 0, s>>>(a);
-        prof_end(kPhDownShared, s);
-    }
-    const int64_t n = (int64_t)a.T * a.H;
-    prof_begin(kPhCombine, s);
-    k_combine<<<(unsigned)std::min<int64_t>((n + 255) / 256, 148 * 16), 256, 0, s>>>(a);
-    prof_end(kPhCombine, s);
+    ExpertArgs a{};
+    a.H = d.H;
+    a.E = d.E;
+    a.FF = d.FF;
+    a.k = d.k;
+    a.T = d.T;
+    a.SFF = d.SFF;
+    a.x = d.x;
+    a.shared_blob = d.shared_blob;
+    a.sh_act = d.sh_act;
+    a.sh_out = d.sh_out;
+    a.header = d.header;
+    prof_begin(kPhGateUpShared, s);
+    k_gateup<kFmtQ80, true><<<blocks_for_warps(a.SFF), 256, 0, s>>>(a);
+    prof_end(kPhGateUpShared, s);
+    prof_begin(kPhDownShared, s);
+    k_down<kFmtQ80, true><<<blocks_for_warps(a.H / 256), 256, 0, s>>>(a);
+    prof_end(kPhDownShared, s);
     return cudaGetLastError();
 }
 

@@ -30,6 +30,8 @@ enum HeaderWord : int {
     kHdrTilesDN = 3,      //            routed down projection
     kHdrTilesGUS = 4,     //            shared expert gate/up
     kHdrTilesDNS = 5,     //            shared expert down
+    kHdrTicketRoute = 6,  // decode path: CTAs done with the router logits (last one routes)
+    kHdrTicketDown = 7,   // decode path: CTAs done with the down projection (last one writes y)
     kHdrCounter0 = 8,     // completion counters, reset by their last user
 };
 
@@ -60,14 +62,15 @@ __device__ __forceinline__ void q4k_scale_min(const uint8_t *scales, int j, int 
 // Kernels counted / timed by the diagnostics API (moe_profile_*).
 enum Phase : int {
     kPhRouterLogits = 0, kPhTopk, kPhBucket, kPhGateUp, kPhGateUpShared, kPhDown, kPhDownShared,
-    kPhCombine, kPhGemmPrep, kPhGemmGateUp, kPhGemmDown, kPhGemmFinish, kNumPhases
+    kPhCombine, kPhGemmPrep, kPhGemmGateUp, kPhGemmDown, kPhGemmFinish, kPhDecRoute, kPhDecGateUp,
+    kPhDecDown, kPhDecFinish, kNumPhases
 };
 void prof_begin(int phase, cudaStream_t s);   // no-ops unless profiling is enabled
 void prof_end(int phase, cudaStream_t s);
 
 // Workspace regions (byte offsets from the workspace base) for one call shape.
 struct WsLayout {
-    size_t header, logits, ids, w, counts, offsets, assign, active;
+    size_t header, logits, ids, w, counts, offsets, assign, active, plan, xfrag;
     size_t act, slots, yacc, x16, sh_act, sh_out;
     size_t act16, sh_act16, tiles_gu, tiles_dn, tiles_gus, tiles_dns, gu, sh_gu, split_cnt;
     size_t total;
@@ -112,7 +115,46 @@ struct ExpertArgs {
     float *y_f32;                       // optional
     uint32_t *header;
 };
-cudaError_t launch_experts_gemv(const ExpertArgs &a, cudaStream_t s);
+
+// ---- decode path (T <= kDecTok): route + grouped gate/up (mma) + down, chained with PDL
+constexpr int kDecTok = 8;                         // window tokens = MMA N columns
+constexpr int kDecMaxAssign = kDecTok * 32;        // T * k
+constexpr int kRouteMaxVec = 10;                   // router float4 per lane and warp
+constexpr int64_t kDecPrefetchBudget = 64ll << 20; // down bytes asked of L2 ahead of use
+
+struct DecPlan {                 // one active expert of the window
+    int32_t e, count;
+    int32_t tok_assign[kDecTok]; // assignment t*k + r of token t to this expert, -1 if none
+};
+
+struct DecArgs {
+    int H, E, FF, k, T, SFF, score_fn, det;
+    int route_parts;             // router row split per CTA (1, 2, 4 or 8)
+    int fs_dn;                   // ff segments per down unit
+    int overlap_prev;            // router rows may be read before the previous kernel ends
+    int prefetch_down;           // ask L2 for the down matrices during gate/up
+    int64_t prefetch_budget;     // at most this many bytes of them
+    const uint16_t *x;
+    const float *wr, *bias;
+    const uint8_t *const *blobs;
+    const uint8_t *shared_blob;
+    float *logits;
+    int32_t *ids;
+    float *w;
+    int32_t *counts, *offsets, *assign, *active;
+    DecPlan *plan;
+    uint4 *xfrag;                // fp16 MMA B fragments of x: [H/256][8][32 lanes] x 16 B
+    float *act;                  // [T*k][FF] by assignment
+    float *sh_act, *sh_out;      // shared expert [T][SFF], [T][H]
+    float *yacc, *slots;         // [T][H] fp32 accumulator; [T*k][fs_dn][H] (deterministic)
+    uint16_t *y;
+    float *y_f32;
+    uint32_t *header;
+};
+int dec_route_parts(int H);
+int dec_down_splits(const moe_config &c, int32_t T);
+cudaError_t launch_decode(const DecArgs &a, cudaStream_t s);
+cudaError_t launch_shared_gemv(const DecArgs &a, cudaStream_t s);
 
 // Tensor-core (tcgen05) grouped GEMM path: its workspace regions.
 constexpr int kGemmSmallTokens = 16;   // calls with T <= 16 use the small-bucket GEMM configuration

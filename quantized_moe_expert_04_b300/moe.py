@@ -30,6 +30,7 @@ MOE_SCORE_SIGMOID_BIAS = 1
 MOE_FLAG_DETERMINISTIC = 1
 MOE_FLAG_FORCE_GEMV = 2
 MOE_FLAG_FORCE_GEMM = 4
+MOE_FLAG_STATIC_WEIGHTS = 8
 
 EXPORTS = (
     "moe_q4k_bytes", "moe_q8_0_bytes", "moe_expert_bytes", "moe_shared_bytes",

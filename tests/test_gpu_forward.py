@@ -66,10 +66,48 @@ def test_small_shapes_match_oracle(wl, T):
     _run(wl, T, gen_device="cpu")
 
 
-@pytest.mark.parametrize("wl,T", [(W["tiny"], 4), (sv(W["qwen_decode"], name="qwen_e64", n_experts=64), 37)],
-                         ids=["tiny", "qwen_e64"])
-def test_forced_gemv_path_any_T(wl, T):
+@pytest.mark.parametrize("wl,T", [(W["tiny"], 4), (sv(W["qwen_decode"], name="qwen_e64", n_experts=64), 8),
+                                  (sv(W["qwen_decode"], name="qwen_e8_k4", n_experts=8, top_k=4), 8)],
+                         ids=["tiny", "qwen_e64", "qwen_e8_k4"])
+def test_forced_gemv_path(wl, T):
+    """The decode path at its largest window; with 8 experts every expert
+    serves several tokens (token pairs in the down projection)."""
     _run(wl, T, gen_device="cpu", flags=moe.MOE_FLAG_FORCE_GEMV)
+
+
+def test_forced_gemv_rejects_windows_above_8():
+    wl = sv(W["qwen_decode"], name="qwen_e64", n_experts=64)
+    pl = pack_layer(wl, gen_device="cpu", experts=[])
+    cfg = moe.config_for(wl, moe.MOE_FLAG_FORCE_GEMV)
+    ws = workspace(cfg, 9)
+    x = synth.hidden_states(wl, 9).cuda()
+    y = torch.empty(9, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoeError) as err:
+        moe.moe_forward(cfg, x, pl.router_w, pl.router_bias, pl.table, pl.shared, 9, y, None, ws)
+    assert err.value.status == moe.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_decode_deterministic_mode_matches_oracle(T):
+    wl = sv(W["deepseek_decode"], name="ds_small", hidden=1024, n_experts=32, ff=512, shared_ff=512)
+    y, y32, ws, pl = _run(wl, T, gen_device="cpu", flags=moe.MOE_FLAG_DETERMINISTIC)
+    cfg = moe.config_for(wl, moe.MOE_FLAG_DETERMINISTIC)
+    x = synth.hidden_states(wl, T).cuda()
+    assert torch.equal(forward(pl, x, ws, cfg=cfg), y)
+
+
+def test_static_weights_flag_matches():
+    """Calls that may start reading the router early give the same result."""
+    wl = sv(W["qwen_decode"], name="qwen_e64", n_experts=64)
+    pl = pack_layer(wl, gen_device="cpu")
+    x = synth.hidden_states(wl, 5).cuda()
+    cfg0 = moe.config_for(wl, moe.MOE_FLAG_DETERMINISTIC)
+    cfg1 = moe.config_for(wl, moe.MOE_FLAG_DETERMINISTIC | moe.MOE_FLAG_STATIC_WEIGHTS)
+    ws = workspace(cfg0, 5)
+    a = forward(pl, x, ws, cfg=cfg0).clone()
+    outs = [forward(pl, x, ws, cfg=cfg1).clone() for _ in range(3)]
+    for b in outs:
+        assert torch.equal(a, b)
 
 
 FULL = [
