@@ -266,7 +266,7 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
         d.route_parts = dec_route_parts(cfg->hidden);
         d.fs_dn = dec_down_splits(*cfg, T);
         d.overlap_prev = (cfg->flags & MOE_FLAG_STATIC_WEIGHTS) != 0;
-        d.prefetch_down = 1;
+        d.prefetch_down = 0;   // measured: the bulk L2 prefetch slows both projections
         d.prefetch_budget = kDecPrefetchBudget;
         d.x = x;
         d.wr = router_w;

@@ -128,64 +128,63 @@ __device__ __forceinline__ uint32_t key_bits(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Top-k of one token by one warp from its E logits in shared memory.  Lane l
-// holds the experts l, l + 32, ... (NPER per lane) as 64-bit keys (score key,
-// then the complement of the id, so that equal scores order the lower id
-// first), sorted once in descending order; each round takes the warp maximum
-// of the lanes' heads (two redux steps) and the winning lane shifts its list.
-// Keys: the logit (softmax: p is monotone in it) or sigmoid + bias.  Weights:
-// softmax over the k selected logits (= the full softmax renormalised over
-// the k), or s / sum of the selected s.  Lane r < k receives selection r.
+// Top-k of one token by one warp.  key[e] (shared memory) holds the
+// order-preserving integer of expert e's selection score (0 = not
+// selectable).  Lane l keeps the keys of experts l, l + 32, ... (NPER) in
+// registers and its best one (a reduction tree, equal keys to the lower id);
+// each round takes the warp maximum (redux), the lowest expert id among equal
+// keys, and only the winning lane clears that key and recomputes its best.
+// Weights: softmax over the k selected logits (= the full softmax
+// renormalised over the k) or s / sum of the selected s, from the logits in
+// global memory.  Lane r < k receives selection r.
 template <int NPER>
-__device__ void warp_topk(const float *lrow, const float *bias, int E, int k, int score_fn, int lane, int &out_id,
-                          float &out_w, bool &fault)
+__device__ void warp_topk(const uint32_t *keys, const float *logit_row, int E, int k, int score_fn, int lane,
+                          int &out_id, float &out_w, bool &fault)
 {
-    uint64_t c[NPER];
+    uint32_t key[NPER];
 #pragma unroll
     for (int i = 0; i < NPER; ++i) {
         const int e = lane + 32 * i;
-        c[i] = 0ull;
-        if (e < E) {
-            const float l = lrow[e];
-            float key;
-            if (score_fn == MOE_SCORE_SOFTMAX) key = l;
-            else key = 1.0f / (1.0f + expf(-l)) + (bias ? __ldg(bias + e) : 0.0f);
-            c[i] = ((uint64_t)key_bits(key) << 32) | (uint32_t)~(uint32_t)e;
-        }
+        key[i] = e < E ? keys[e] : 0u;
     }
-    // bitonic sort, descending
+    auto best = [&](uint32_t &bk, int &bi) {
+        uint32_t kk[NPER];
+        int ii[NPER];
 #pragma unroll
-    for (int size = 2; size <= NPER; size <<= 1)
+        for (int i = 0; i < NPER; ++i) {
+            kk[i] = key[i];
+            ii[i] = i;
+        }
 #pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1)
+        for (int w = 1; w < NPER; w <<= 1)
 #pragma unroll
-            for (int i = 0; i < NPER; ++i) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const bool desc = (i & size) == 0;
-                    const uint64_t x = c[i], y = c[j];
-                    const bool sw = desc ? (x < y) : (x > y);
-                    c[i] = sw ? y : x;
-                    c[j] = sw ? x : y;
+            for (int i = 0; i + w < NPER; i += 2 * w)
+                if (kk[i + w] > kk[i]) {        // strict: equal keys keep the lower index
+                    kk[i] = kk[i + w];
+                    ii[i] = ii[i + w];
                 }
-            }
+        bk = kk[0];
+        bi = ii[0];
+    };
+    uint32_t bk;
+    int bi;
+    best(bk, bi);
     int my_id = 0;
     fault = false;
     for (int r = 0; r < k; ++r) {
-        const uint32_t hk = (uint32_t)(c[0] >> 32);
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, hk);
-        const uint32_t lo = __reduce_max_sync(0xffffffffu, hk == mk ? (uint32_t)c[0] : 0u);
-        const int e = (int)~lo;
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const int e = (int)__reduce_min_sync(0xffffffffu, bk == mk ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
         if (mk == 0u) fault = true;          // nothing selectable (non-finite scores)
         if (lane == r) my_id = mk == 0u ? r : e;
         if (mk != 0u && lane == (e & 31)) {
 #pragma unroll
-            for (int i = 0; i + 1 < NPER; ++i) c[i] = c[i + 1];
-            c[NPER - 1] = 0ull;
+            for (int i = 0; i < NPER; ++i)
+                if (i == (e >> 5)) key[i] = 0u;
+            best(bk, bi);
         }
     }
     const bool sel = lane < k;
-    const float lv = sel ? lrow[my_id] : 0.0f;
+    const float lv = sel ? __ldcg(logit_row + my_id) : 0.0f;
     float num;
     if (score_fn == MOE_SCORE_SOFTMAX) {
         const float lmax = __shfl_sync(0xffffffffu, lv, 0);   // the first pick is the largest
@@ -247,7 +246,10 @@ __global__ void __launch_bounds__(kRouteThreads) k_dec_route(DecArgs a)
     // k-step s of block column cb, lane (g, t): elements e = 256 cb + 64 t + 4 s + j
     // as b0 = (x[e+0], x[e+2]), b1 = (x[e+1], x[e+3])
     const int gtid = blockIdx.x * kRouteThreads + threadIdx.x, gthreads = gridDim.x * kRouteThreads;
-    for (int i = gtid; i < T * H; i += gthreads) a.yacc[i] = 0.0f;
+    for (int i = gtid; i < T * H; i += gthreads) {
+        a.yacc[i] = 0.0f;
+        if (a.sh_out) a.sh_out[i] = 0.0f;
+    }
     bool bad = false;
     const int n_frag = (H / 256) * 16 * 32;
     for (int i = gtid; i < n_frag; i += gthreads) {
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_dec_route(DecArgs a)
 // result; CTA 0 publishes it).  Shared scratch `scr` holds the logits and the
 // sort; the plan (active experts and their tokens) stays in `pe` / `ptok`.
 struct RouteScratch {
-    float *logit;        // [T][E]
+    uint32_t *key;       // [T][E] selection keys
     int32_t *ids;        // [T*k]
     float *w;            // [T*k]
     int32_t *rank;       // [T*k]
@@ -325,13 +327,21 @@ __device__ void route_window(const DecArgs &a, const RouteScratch &sc, int16_t *
 {
     const int T = a.T, E = a.E, k = a.k, TK = T * k;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x;
-    for (int i0 = threadIdx.x; i0 < T * E; i0 += 4 * nthr) {      // 4 loads in flight per thread
-        float v[4];
+    // selection keys of every (token, expert): 4 loads in flight per thread
+    for (int i0 = threadIdx.x; i0 < T * E; i0 += 4 * nthr) {
+        float v[4], b[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = i0 + j * nthr < T * E ? __ldcg(a.logits + i0 + j * nthr) : 0.0f;
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * nthr;
+            v[j] = i < T * E ? __ldcg(a.logits + i) : 0.0f;
+            b[j] = (i < T * E && a.bias && a.score_fn != MOE_SCORE_SOFTMAX) ? __ldg(a.bias + i % E) : 0.0f;
+        }
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (i0 + j * nthr < T * E) sc.logit[i0 + j * nthr] = v[j];
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * nthr;
+            if (i < T * E)
+                sc.key[i] = key_bits(a.score_fn == MOE_SCORE_SOFTMAX ? v[j] : 1.0f / (1.0f + expf(-v[j])) + b[j]);
+        }
     }
     if (threadIdx.x < 32) sc.bits[threadIdx.x] = 0u;
     __syncthreads();
@@ -339,10 +349,11 @@ __device__ void route_window(const DecArgs &a, const RouteScratch &sc, int16_t *
         int id;
         float wt;
         bool f;
-        const float *lrow = sc.logit + warp * E;
-        if (E <= 256) warp_topk<8>(lrow, a.bias, E, k, a.score_fn, lane, id, wt, f);
-        else if (E <= 512) warp_topk<16>(lrow, a.bias, E, k, a.score_fn, lane, id, wt, f);
-        else warp_topk<32>(lrow, a.bias, E, k, a.score_fn, lane, id, wt, f);
+        const uint32_t *kr = sc.key + warp * E;
+        const float *lr = a.logits + (int64_t)warp * E;
+        if (E <= 256) warp_topk<8>(kr, lr, E, k, a.score_fn, lane, id, wt, f);
+        else if (E <= 512) warp_topk<16>(kr, lr, E, k, a.score_fn, lane, id, wt, f);
+        else warp_topk<32>(kr, lr, E, k, a.score_fn, lane, id, wt, f);
         if (lane < k) {
             sc.ids[warp * k + lane] = id;
             sc.w[warp * k + lane] = wt;
@@ -514,7 +525,7 @@ __global__ void __launch_bounds__(kGuWarps * 32, 1) k_dec_gateup(DecArgs a)
     {
         RouteScratch sc;
         uint8_t *p = ring;
-        sc.logit = reinterpret_cast<float *>(p);
+        sc.key = reinterpret_cast<uint32_t *>(p);
         p += (size_t)T * E * 4;
         sc.ids = reinterpret_cast<int32_t *>(p);
         p += kDecMaxAssign * 4;

@@ -221,8 +221,59 @@ __global__ void __launch_bounds__(256) k_down(ExpertArgs a)
 
 static unsigned blocks_for_warps(int64_t warps) { return (unsigned)((warps + 7) / 8); }
 
+// Shared-expert down projection: warp (256-column block hb, ff segment fs)
+// accumulates sum_f sh_act[t][f] * Wd[f][h] over its FR rows for every token,
+// lane l owning columns 256 hb + 8 l .. + 7 (a quarter of one Q8_0 block), and
+// adds the result into sh_out (zeroed by the routing kernel); with one
+// segment (deterministic mode) it stores instead.
+__global__ void __launch_bounds__(256) k_shared_down(ExpertArgs a, int nfs)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nhb = a.H / 256;
+    if (task >= (int64_t)nhb * nfs) return;
+    const int hb = (int)(task % nhb), fs = (int)(task / nhb);
+    const int FR = a.SFF / nfs, T = a.T;
+    const int64_t rb = RowFmt<kFmtQ80>::row_bytes(a.H);
+    const uint8_t *dbase = a.shared_blob + 2 * (int64_t)a.SFF * rb;
+    const int h0 = hb * 256 + lane * 8;
+    float acc[kChunk][8];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[j][i] = 0.0f;
+    for (int r = 0; r < FR; ++r) {
+        const int f = fs * FR + r;
+        float wv[8];
+        RowFmt<kFmtQ80>::load8(dbase + (int64_t)f * rb, h0, wv);
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+            if (j < T) {
+                const float av = __ldg(a.sh_act + (int64_t)j * a.SFF + f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[j][i] = fmaf(av, wv[i], acc[j][i]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+        if (j < T) {
+            float *dst = a.sh_out + (int64_t)j * a.H + h0;
+            if (nfs == 1) {
+                reinterpret_cast<float4 *>(dst)[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+                reinterpret_cast<float4 *>(dst)[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+            } else {
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc[j][0]), "f"(acc[j][1]),
+                             "f"(acc[j][2]), "f"(acc[j][3]) : "memory");
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4), "f"(acc[j][4]),
+                             "f"(acc[j][5]), "f"(acc[j][6]), "f"(acc[j][7]) : "memory");
+            }
+        }
+    }
+}
+
 // The shared expert of a decode window (every token, weight 1): gate/up into
-// sh_act, down into sh_out; the decode path's last down CTA adds sh_out to y.
+// sh_act, down into sh_out; the finish kernel adds sh_out to y.
 cudaError_t launch_shared_gemv(const DecArgs &d, cudaStream_t s)
 {
     ExpertArgs a{};
@@ -240,8 +291,11 @@ cudaError_t launch_shared_gemv(const DecArgs &d, cudaStream_t s)
     prof_begin(kPhGateUpShared, s);
     k_gateup<kFmtQ80, true><<<blocks_for_warps(a.SFF), 256, 0, s>>>(a);
     prof_end(kPhGateUpShared, s);
+    int nfs = 1;
+    if (!d.det)
+        while (nfs < 64 && a.SFF % (2 * nfs) == 0 && a.SFF / (2 * nfs) >= 32) nfs *= 2;
     prof_begin(kPhDownShared, s);
-    k_down<kFmtQ80, true><<<blocks_for_warps(a.H / 256), 256, 0, s>>>(a);
+    k_shared_down<<<blocks_for_warps((int64_t)(a.H / 256) * nfs), 256, 0, s>>>(a, nfs);
     prof_end(kPhDownShared, s);
     return cudaGetLastError();
 }

@@ -19,8 +19,9 @@
 //              stored to the assignment's slot when the call is deterministic.
 //
 // Warp roles (12 warps): 0-3 epilogue (tensor-memory lane quarters 0-3),
-// 4 MMA issue + tensor-memory allocation, 5 raw weight bytes (1-D bulk copies
-// into a ring), 6-7 token rows (16-byte cp.async gathers, 128-byte swizzle),
+// 4 MMA issue + tensor-memory allocation, 5 raw weight bytes (16-byte cp.async
+// pieces into a ring, completion counted on its mbarrier), 6-7 token rows
+// (16-byte cp.async gathers, 128-byte swizzle),
 // 8-11 dequantisation (raw ring -> fp16 A ring).  All hand-offs are mbarriers;
 // every wait is bounded and sets MOE_ERR_TIMEOUT instead of hanging.
 //
@@ -326,7 +327,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
-            mbar_init(full_raw(i), 1);
+            mbar_init(full_raw(i), 32);          // the 32 lanes of the raw-byte warp
             mbar_init(empty_raw(i), 128);
         }
         for (int i = 0; i < SA; ++i) {
@@ -536,36 +537,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
                 const int r = r0 + rr;                    // raw stage (block column / K-step) index
                 const int slot = rs_it % RS;
                 if (!(ok = wait_bar(empty_raw(slot), ((rs_it / RS) & 1) ^ 1, abort_flag, g.status))) break;
-                if (lane == 0) mbar_arrive_expect_tx(full_raw(slot), (uint32_t)C::kRawStage);
-                __syncwarp();
-                const uint32_t dst0 = smem_addr(raw_base + slot * C::kRawStage);
+                uint8_t *dst0 = raw_base + slot * C::kRawStage;
+                // 16-byte asynchronous copies; each lane's completion arrives on full_raw
                 if (OP == kOpGateUp) {
                     // 128 rows: row 2i = gate f0+i, row 2i+1 = up f0+i
-                    for (int i = lane; i < 128; i += 32) {
+                    constexpr int kPieces = FMT == kWQ4K ? 9 : 5;           // 144 or 80 bytes per row
+                    for (int p = lane; p < 128 * kPieces; p += 32) {
+                        const int i = p / kPieces, pc = p % kPieces;
                         const int64_t mrow = (int64_t)((i & 1) ? ffop : 0) + ti.m * 64 + (i >> 1);
                         const uint8_t *rowp = ti.blob + mrow * rb;
-                        if (FMT == kWQ4K) {
-                            bulk_g2s(dst0 + i * 144, rowp + (int64_t)r * 144, 144, full_raw(slot));
-                        } else {
-                            const int off = 68 * r;
-                            bulk_g2s(dst0 + i * 80, rowp + (off & ~15), 80, full_raw(slot));
-                        }
+                        const uint8_t *src = FMT == kWQ4K ? rowp + (int64_t)r * 144 : rowp + ((68 * r) & ~15);
+                        cp_async16(smem_addr(dst0 + i * (16 * kPieces) + pc * 16), src + pc * 16);
                     }
                 } else {
                     // 64 ff rows of Wd for this K-step, this tile's 128 hidden columns
                     const int h0 = ti.m * 128;
-                    for (int i = lane; i < 64; i += 32) {
+                    constexpr int kPieces = FMT == kWQ4K ? 5 : 9;           // 16 + 64 or 144 bytes per row
+                    for (int p = lane; p < 64 * kPieces; p += 32) {
+                        const int i = p / kPieces, pc = p % kPieces;
                         const uint8_t *rowp = ti.blob + ((int64_t)2 * ffop + 64 * r + i) * rb;
+                        const uint8_t *src;
                         if (FMT == kWQ4K) {
                             const uint8_t *blk = rowp + (int64_t)(h0 / 256) * 144;
-                            bulk_g2s(dst0 + i * 80, blk, 16, full_raw(slot));
-                            bulk_g2s(dst0 + i * 80 + 16, blk + 16 + 64 * ((h0 / 128) & 1), 64, full_raw(slot));
+                            src = pc == 0 ? blk : blk + 16 + 64 * ((h0 / 128) & 1) + (pc - 1) * 16;
                         } else {
-                            const int off = 34 * (h0 / 32);
-                            bulk_g2s(dst0 + i * 144, rowp + (off & ~15), 144, full_raw(slot));
+                            src = rowp + ((34 * (h0 / 32)) & ~15) + pc * 16;
                         }
+                        cp_async16(smem_addr(dst0 + i * (16 * kPieces) + pc * 16), src);
                     }
                 }
+                cp_async_arrive_noinc(full_raw(slot));
             }
         }
         // copies still in flight (an early exit) must land before the CTA ends

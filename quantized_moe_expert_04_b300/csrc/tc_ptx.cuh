@@ -63,6 +63,13 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
+// arrive (once per calling thread) on `bar` when all cp.async of this thread
+// issued so far have completed; the barrier counts these arrivals
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // generic-proxy writes to shared memory -> visible to async-proxy readers (MMA)
