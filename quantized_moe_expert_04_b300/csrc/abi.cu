@@ -64,7 +64,7 @@ WsLayout ws_layout(const moe_config &c, int32_t T)
     (void)maxu;
     L.act16 = take(gemv ? 0 : TK * c.ff * 2);
     L.sh_act16 = take(!gemv && c.shared_ff ? (size_t)T * c.shared_ff * 2 : 0);
-    const size_t sh_tiles = (size_t)((T + 255) / 256 + 1);
+    const size_t sh_tiles = (size_t)((T + kGemmMaxN - 1) / kGemmMaxN + 1);
     const GemmSplits sp = gemv ? GemmSplits{1, 1, 1, 1} : gemm_splits(c, T);
     const size_t cap_gu = gemv ? 0 : gemm_tile_capacity(c.ff / 64, (int64_t)TK, c.n_experts);
     const size_t cap_dn = gemv ? 0 : gemm_tile_capacity(c.hidden / 128, (int64_t)TK, c.n_experts);

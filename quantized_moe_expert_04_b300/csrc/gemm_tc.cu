@@ -6,7 +6,7 @@
 // NVIDIA GPUs ("Qwen3.8-Flash-Next UD-Q4_K_XL 引擎对比", lcz.me/user/wml-ai/posts,
 // section 一); its kernels target sm_86/sm_120 (mma.sync generation).  Here a
 // persistent CTA per SM walks a device-built list of work tiles; each tile is
-// one expert's 128 weight rows x up to 256 of its tokens:
+// one expert's 128 weight rows x up to kGemmMaxN of its tokens:
 //
 //   gate/up  A = 64 gate rows and the 64 up rows of the same ff indices,
 //              interleaved (row 2i = gate f0+i, row 2i+1 = up f0+i), K = H;
@@ -698,7 +698,7 @@ struct PlanArgs {
 
 __device__ __forceinline__ void split_tokens(int n_e, int &tn, int &nt)
 {
-    const int nt0 = (n_e + 255) / 256;
+    const int nt0 = (n_e + kGemmMaxN - 1) / kGemmMaxN;
     tn = (((n_e + nt0 - 1) / nt0) + 15) & ~15;
     nt = (n_e + tn - 1) / tn;
 }
@@ -804,12 +804,14 @@ static cudaError_t launch_gemm(const GemmArgs &g, int grid, cudaStream_t s)
 }
 
 // Configurations: small buckets (every token tile <= 16 wide: decode windows)
-// keep deep A and raw rings; large buckets (prefill) keep a deep B ring.
+// keep deep A and raw rings; large buckets (prefill) use token tiles of
+// kGemmMaxN with a 5-deep A ring, so that the dequantisation runs ahead of the
+// MMAs.
 template <int OP, int FMT>
 static cudaError_t launch_gemm_cfg(const GemmArgs &g, int grid, bool small, cudaStream_t s)
 {
     if (small) return launch_gemm<OP, FMT, 16, 6, 8, 92160>(g, grid, s);
-    return launch_gemm<OP, FMT, 256, 2, 4, 55296>(g, grid, s);
+    return launch_gemm<OP, FMT, kGemmMaxN, 5, 4, 55296>(g, grid, s);
 }
 
 static int num_sms()
@@ -826,7 +828,7 @@ static int num_sms()
 
 size_t gemm_tile_capacity(int mt, int64_t TK, int E)
 {
-    return (size_t)mt * (size_t)(TK / 256 + 1 + std::min<int64_t>(E, TK));
+    return (size_t)mt * (size_t)(TK / kGemmMaxN + 1 + std::min<int64_t>(E, TK));
 }
 
 // K split for `tiles` work tiles of `ksteps` K-steps: the smallest divisor d

@@ -158,6 +158,7 @@ cudaError_t launch_shared_gemv(const DecArgs &a, cudaStream_t s);
 
 // Tensor-core (tcgen05) grouped GEMM path: its workspace regions.
 constexpr int kGemmSmallTokens = 16;   // calls with T <= 16 use the small-bucket GEMM configuration
+constexpr int kGemmMaxN = 128;         // tokens per work tile of the large-bucket configuration
 struct GemmSplits {
     int gu, dn, gus, dns;                // K splits: routed gate/up, down; shared gate/up, down
 };

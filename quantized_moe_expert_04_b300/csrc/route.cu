@@ -69,6 +69,185 @@ k_router_logits(const uint16_t *__restrict__ x, const float *__restrict__ wr, in
     }
 }
 
+// Router logits for larger T on the warp-level tensor cores: C[T][E] =
+// X[T][H] * Wr[E][H]^T.  Each fp32 router weight is split exactly into three
+// bf16 parts (w = w1 + w2 + w3: 8 significant bits each), so with bf16 x the
+// three bf16 x bf16 products are exact and the MMAs accumulate them in fp32 --
+// the logits of an fp32 dot product, in another summation order.  Each
+// 32-wide K stage is summed by the MMAs into a fresh accumulator and the
+// stage sums are added with fp32 adds, so no long chain runs inside the MMA
+// accumulator.
+// CTA tile 128 tokens x RN experts, K stages of 32, double-buffered in
+// padded shared memory (rows of 40 bf16: ldmatrix without bank conflicts);
+// 8 warps as 4 (tokens) x 2 (experts), each 32 x RN/2.
+constexpr int kRmM = 128, kRmK = 32, kRmLd = 40;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+
+// w -> (w1, w2, w3) bf16 with w1 + w2 + w3 == w
+__device__ __forceinline__ void split3(float w, uint16_t &a, uint16_t &b, uint16_t &c)
+{
+    const __nv_bfloat16 h1 = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(h1);
+    const __nv_bfloat16 h2 = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(h2);
+    const __nv_bfloat16 h3 = __float2bfloat16_rn(r2);
+    a = __bfloat16_as_ushort(h1);
+    b = __bfloat16_as_ushort(h2);
+    c = __bfloat16_as_ushort(h3);
+}
+
+template <int RN>
+__global__ void __launch_bounds__(256) k_router_mma(const uint16_t *__restrict__ x, const float *__restrict__ wr,
+                                                    int T, int H, int E, float *__restrict__ logits)
+{
+    constexpr int NT = RN / 16;                       // n8 tiles per warp (warp covers RN/2 experts)
+    extern __shared__ __align__(16) uint16_t rsm[];
+    uint16_t *sX = rsm;                               // [2][128][40]
+    uint16_t *sW = rsm + 2 * kRmM * kRmLd;            // [2][3][RN][40]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wm = warp & 3, wn = warp >> 2;
+    const int t0 = blockIdx.x * kRmM, e0 = blockIdx.y * RN;
+    const int nstage = H / kRmK;
+
+    float acc[2][NT][4], sacc[2][NT][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.0f;
+
+    // X: 128 rows x 4 pieces of 16 bytes; Wr: RN rows x 8 float4
+    auto load_x = [&](int st, int buf) {
+        for (int p = tid; p < kRmM * 4; p += 256) {
+            const int r = p >> 2, pc = p & 3;
+            const int t = t0 + r;
+            const uint16_t *src = x + (int64_t)min(t, T - 1) * H + st * kRmK + pc * 8;
+            cp_async16_zfill((uint32_t)__cvta_generic_to_shared(sX + (buf * kRmM + r) * kRmLd + pc * 8), src, t < T);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    constexpr int WV = RN * 8 / 256;                  // float4 of Wr per thread per stage
+    float4 wreg[WV];
+    auto load_w = [&](int st) {
+#pragma unroll
+        for (int i = 0; i < WV; ++i) {
+            const int p = tid + i * 256, r = p >> 3, c4 = p & 7;
+            const int e = min(e0 + r, E - 1);
+            wreg[i] = __ldg(reinterpret_cast<const float4 *>(wr + (int64_t)e * H + st * kRmK) + c4);
+        }
+    };
+    auto store_w = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < WV; ++i) {
+            const int p = tid + i * 256, r = p >> 3, c4 = p & 7;
+            uint16_t h[3][4];
+            split3(wreg[i].x, h[0][0], h[1][0], h[2][0]);
+            split3(wreg[i].y, h[0][1], h[1][1], h[2][1]);
+            split3(wreg[i].z, h[0][2], h[1][2], h[2][2]);
+            split3(wreg[i].w, h[0][3], h[1][3], h[2][3]);
+#pragma unroll
+            for (int sp = 0; sp < 3; ++sp) {
+                uint2 v;
+                v.x = (uint32_t)h[sp][0] | ((uint32_t)h[sp][1] << 16);
+                v.y = (uint32_t)h[sp][2] | ((uint32_t)h[sp][3] << 16);
+                *reinterpret_cast<uint2 *>(sW + ((buf * 3 + sp) * RN + r) * kRmLd + c4 * 4) = v;
+            }
+        }
+    };
+
+    load_x(0, 0);
+    load_w(0);
+    store_w(0);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    for (int st = 0; st < nstage; ++st) {
+        const int buf = st & 1;
+        if (st + 1 < nstage) {
+            load_x(st + 1, buf ^ 1);
+            load_w(st + 1);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) sacc[i][j][q] = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < kRmK; kk += 16) {
+            uint32_t af[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int r = wm * 32 + i * 16 + (lane & 15);
+                const int c = kk + (lane >> 4) * 8;
+                ldsm_x4((uint32_t)__cvta_generic_to_shared(sX + (buf * kRmM + r) * kRmLd + c), af[i][0], af[i][1],
+                        af[i][2], af[i][3]);
+            }
+#pragma unroll
+            for (int sp = 0; sp < 3; ++sp) {
+#pragma unroll
+                for (int j = 0; j < NT; j += 2) {
+                    // two n8 tiles: lanes 0-7 / 8-15 rows of tile j at k, k+8; 16-23 / 24-31 tile j+1
+                    const int n = wn * (RN / 2) + (j + (lane >> 4)) * 8 + (lane & 7);
+                    const int c = kk + ((lane >> 3) & 1) * 8;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4((uint32_t)__cvta_generic_to_shared(sW + ((buf * 3 + sp) * RN + n) * kRmLd + c), b0, b1,
+                            b2, b3);
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        mma_bf16(sacc[i][j], af[i][0], af[i][1], af[i][2], af[i][3], b0, b1);
+                        mma_bf16(sacc[i][j + 1], af[i][0], af[i][1], af[i][2], af[i][3], b2, b3);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[i][j][q] += sacc[i][j][q];
+        if (st + 1 < nstage) store_w(buf ^ 1);
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+    }
+    // C fragment: c0,c1 = (row g, cols 2t, 2t+1), c2,c3 = (row g+8, ...)
+    const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int t = t0 + wm * 32 + i * 16 + g + 8 * hh;
+                const int e = e0 + wn * (RN / 2) + j * 8 + 2 * tq;
+                if (t < T) {
+                    if (e < E) logits[(int64_t)t * E + e] = acc[i][j][2 * hh];
+                    if (e + 1 < E) logits[(int64_t)t * E + e + 1] = acc[i][j][2 * hh + 1];
+                }
+            }
+}
+
 // One warp per token.  Keys: the logit (softmax: the order of p equals the
 // order of the logits) or s_e + b_e (sigmoid).  Weights: softmax over the k
 // selected logits (= the full softmax renormalised over the k), or
@@ -296,8 +475,23 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
     const int experts_per_cta = a.T > kRouterTokens ? 16 * kRouterWarps : kRouterWarps;
     dim3 grid((a.E + experts_per_cta - 1) / experts_per_cta, (a.T + kRouterTokens - 1) / kRouterTokens);
     prof_begin(kPhRouterLogits, s);
-    k_router_logits<<<grid, kRouterWarps * 32, xs_bytes, s>>>(a.x, a.wr, a.T, a.H, a.E, experts_per_cta,
-                                                              a.logits);
+    if (a.T > kRouterTokens && a.H % kRmK == 0) {
+        // tensor-core logits: 128-token x 64-expert tiles
+        const bool wide = false;
+        const size_t smem = (size_t)(2 * kRmM * kRmLd + 2 * 3 * (wide ? 128 : 64) * kRmLd) * sizeof(uint16_t);
+        static bool mattr = false;
+        if (!mattr) {
+            cudaFuncSetAttribute(k_router_mma<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
+            cudaFuncSetAttribute(k_router_mma<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
+            mattr = true;
+        }
+        const dim3 g2((a.T + kRmM - 1) / kRmM, (a.E + (wide ? 127 : 63)) / (wide ? 128 : 64));
+        if (wide) k_router_mma<128><<<g2, 256, smem, s>>>(a.x, a.wr, a.T, a.H, a.E, a.logits);
+        else k_router_mma<64><<<g2, 256, smem, s>>>(a.x, a.wr, a.T, a.H, a.E, a.logits);
+    } else {
+        k_router_logits<<<grid, kRouterWarps * 32, xs_bytes, s>>>(a.x, a.wr, a.T, a.H, a.E, experts_per_cta,
+                                                                  a.logits);
+    }
     prof_end(kPhRouterLogits, s);
     const int warps_per_block = 8;
     prof_begin(kPhTopk, s);

@@ -13,7 +13,7 @@ import torch
 import oracle
 from quantized_moe_expert_04_b300 import moe, synth
 from quantized_moe_expert_04_b300.layer import forward, pack_layer, routing_views, workspace
-from parity import check_close, compare_ids, oracle_blobs, oracle_forward, oracle_inputs
+from parity import check_close, compare_ids, oracle_blobs, oracle_forward, oracle_inputs, selection_keys
 
 pytestmark = pytest.mark.gpu
 W = synth.WORKLOADS
@@ -47,7 +47,7 @@ def _run(wl, T, gen_device, sample=None, flags=0, seed=0, layer=0):
     xb, wr, b = oracle_inputs(wl, T, seed, layer, gen_device=gen_device, x=x)
     xs = xb[toks]
     oids, ow, kth, nxt = oracle.route(xs, wr, b, wl.top_k, wl.score_fn)
-    diff = compare_ids(gids, oids, kth, nxt)
+    diff = compare_ids(gids, oids, kth, nxt, keys_of=lambda t: selection_keys(xs[t], wr, b, wl.score_fn))
     used = set(oids.reshape(-1).tolist()) | set(gids.reshape(-1).tolist())
     blobs, sblob = oracle_blobs(wl, used, seed, layer, gen_device=gen_device)
     forced = gids if diff else None

@@ -7,7 +7,7 @@ import torch
 import oracle
 from quantized_moe_expert_04_b300 import moe, synth
 from quantized_moe_expert_04_b300.layer import workspace
-from parity import compare_ids, oracle_inputs
+from parity import compare_ids, oracle_inputs, selection_keys
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +44,7 @@ def test_route_matches_oracle(wl, T):
         assert (offs == 0).all()
         return
     oids, ow, kth, nxt = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
-    diff = compare_ids(ids, oids, kth, nxt)
+    diff = compare_ids(ids, oids, kth, nxt, keys_of=lambda t: selection_keys(xb[t], wr, b, wl.score_fn))
     if diff:
         print("near-ties (reported): %d token(s): %s" % (len(diff), diff[:10]))
     same = [t for t in range(T) if t not in set(diff)]
