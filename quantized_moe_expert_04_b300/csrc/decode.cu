@@ -701,48 +701,73 @@ __global__ void __launch_bounds__(kGuWarps * 32, 1) k_dec_gateup(DecArgs a)
 
 // ---------------------------------------------------------------- down
 
-// Unit (active expert u, hidden block cb, ff segment fs): the segment's FR
-// rows of block column cb (144 bytes each) are staged in shared memory with
-// cp.async, one unit ahead.  Thread (q = tid & 7, r = tid >> 3) takes the 16
-// quant bytes q of rows r, r + 16, ...: 32 weights, 16 of sub-block 2c and 16
-// of sub-block 2c + 1 (c = q / 2).  With v = 0.5 + q/256 (the nibble placed in
-// the fp32 mantissa) a weight is s*q - z = 256 s v - (128 s + z), so
-// sum_f a_f w_f = sum_f (256 a_f s_f) v_f - sum_f a_f (128 s_f + z_f): one FMA
-// per weight and token; the second sum once per row and sub-block.
-constexpr int kDnThreads = 128;
-constexpr int kDnMaxRows = 320;
-constexpr int kDnRowStride = 160;     // 144 + 16 padding
-constexpr int kDnRowBatch = 4;
+// Unit (active expert u, hidden block cb, ff segment fs): the segment's FR <=
+// kDnMaxRows rows of block column cb (144 bytes each).  One warp per unit:
+// the warp stages its units in its own two shared-memory buffers with
+// cp.async, one unit ahead, and the activations of the unit's tokens next to
+// them.  Lane (q = lane & 7, rl = lane >> 3) takes the 16 quant bytes q of
+// rows rl, rl + 4, ...: 32 weights, 16 of sub-block 2c and 16 of sub-block
+// 2c + 1 (c = q / 2).  With v = 0.5 + q/256 (the nibble placed in the fp32
+// mantissa) a weight is s*q - z = 256 s v - (128 s + z), so
+// sum_f a_f w_f = sum_f (256 a_f s_f) v_f - sum_f a_f (128 s_f + z_f): one
+// FMA per weight and token; the second sum once per row and sub-block.
+constexpr int kDnWarps = 4;                 // warps (independent units) per CTA
+constexpr int kDnThreads = kDnWarps * 32;
+constexpr int kDnMaxRows = 80;
+constexpr int kDnRowStride = 160;           // 144 + 16 padding
+constexpr int kDnBuf = kDnMaxRows * kDnRowStride + 2 * kDnMaxRows * 4;   // rows + activations of 2 tokens
+
+// fp32 scale and min of the sub-block pair (2c, 2c + 1) of a Q4_K header:
+// d * sc and dmin * m, each one rounding (exact integer conversions).
+__device__ __forceinline__ void q4k_pair_scales_f(uint4 hdr, int c, float &s0, float &z0, float &s1, float &z1)
+{
+    const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, m_lo = hdr.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    const uint32_t scw = c >= 2 ? sc_hi : sc_lo, mw = c >= 2 ? m_hi : m_lo;
+    const uint32_t sel0 = (c & 1) ? 0x4442u : 0x4440u, sel1 = (c & 1) ? 0x4443u : 0x4441u;   // byte -> low byte
+    const float k23 = 8388608.0f;
+    const float sc0 = __uint_as_float(__byte_perm(scw, 0x4B000000u, sel0 | 0x7000u)) - k23;
+    const float sc1 = __uint_as_float(__byte_perm(scw, 0x4B000000u, sel1 | 0x7000u)) - k23;
+    const float m0 = __uint_as_float(__byte_perm(mw, 0x4B000000u, sel0 | 0x7000u)) - k23;
+    const float m1 = __uint_as_float(__byte_perm(mw, 0x4B000000u, sel1 | 0x7000u)) - k23;
+    const float d = f16_bits_to_f32(hdr.x & 0xffff), dmin = f16_bits_to_f32(hdr.x >> 16);
+    s0 = __fmul_rn(d, sc0);
+    s1 = __fmul_rn(d, sc1);
+    z0 = __fmul_rn(dmin, m0);
+    z1 = __fmul_rn(dmin, m1);
+}
 
 __global__ void __launch_bounds__(kDnThreads) k_dec_down(DecArgs a)
 {
-    extern __shared__ __align__(16) uint8_t smem[];                  // 2 x [kDnMaxRows][160]
-    __shared__ float s_acc[kDnThreads / 32][2][256];                 // per warp partials: [warp][token][h]
+    extern __shared__ __align__(16) uint8_t smem[];     // [warp][2][kDnBuf]
     griddep_wait();
     const int U = (int)a.header[kHdrNActive];
     const int H = a.H, FF = a.FF, nb = H / 256, FS = a.fs_dn;
     const int64_t rb = (int64_t)nb * 144;
     const int units = U * nb * FS;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int q = tid & 7, r = tid >> 3;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int q = lane & 7, rl = lane >> 3;
     const int c = q >> 1, l0 = 16 * (q & 1);
     const int FR = FF / FS;
+    uint8_t *wbuf = smem + warp * 2 * kDnBuf;
+    const int gw = blockIdx.x * kDnWarps + warp, nw = gridDim.x * kDnWarps;
 
-    auto unit_src = [&](int unit, int &u, int &cb, int &fs) -> const uint8_t * {
+    auto unit_of = [&](int unit, int &u, int &cb, int &fs) {
         u = unit / (nb * FS);
         const int rem = unit % (nb * FS);
         cb = rem / FS;
         fs = rem % FS;
-        const uint8_t *blob = a.blobs[a.plan[u].e];
-        return blob ? blob + (2 * (int64_t)FF + (int64_t)fs * FR) * rb + (int64_t)cb * 144 : nullptr;
     };
     auto issue = [&](int unit, int buf) {
         if (unit < units) {
             int u, cb, fs;
-            const uint8_t *src = unit_src(unit, u, cb, fs);
-            if (src) {
-                uint8_t *dst = smem + buf * kDnMaxRows * kDnRowStride;
-                for (int p = tid; p < FR * 9; p += kDnThreads) {
+            unit_of(unit, u, cb, fs);
+            const uint8_t *blob = a.blobs[a.plan[u].e];
+            if (blob) {
+                const uint8_t *src = blob + (2 * (int64_t)FF + (int64_t)fs * FR) * rb + (int64_t)cb * 144;
+                uint8_t *dst = wbuf + buf * kDnBuf;
+                for (int p = lane; p < FR * 9; p += 32) {
                     const int row = p / 9, pc = p % 9;
                     cp_async16(dst + row * kDnRowStride + pc * 16, src + row * rb + pc * 16);
                 }
@@ -751,19 +776,16 @@ __global__ void __launch_bounds__(kDnThreads) k_dec_down(DecArgs a)
         cp_async_commit();
     };
 
-    issue(blockIdx.x, 0);
+    issue(gw, 0);
     int buf = 0;
-    for (int unit = blockIdx.x; unit < units; unit += gridDim.x, buf ^= 1) {
-        issue(unit + gridDim.x, buf ^ 1);
+    for (int unit = gw; unit < units; unit += nw, buf ^= 1) {
+        issue(unit + nw, buf ^ 1);
         int u, cb, fs;
-        const uint8_t *src = unit_src(unit, u, cb, fs);
-        if (!src) {
-            if (tid == 0) set_status(a.header + kHdrStatus, MOE_ERR_DEVICE_FAULT);
+        unit_of(unit, u, cb, fs);
+        if (!a.blobs[a.plan[u].e]) {
+            if (lane == 0) set_status(a.header + kHdrStatus, MOE_ERR_DEVICE_FAULT);
             continue;
         }
-        cp_async_wait<1>();
-        __syncthreads();
-        const uint8_t *tile = smem + buf * kDnMaxRows * kDnRowStride;
         int tok_a[kDecTok];
         int n = 0;
 #pragma unroll
@@ -772,51 +794,50 @@ __global__ void __launch_bounds__(kDnThreads) k_dec_down(DecArgs a)
             tok_a[tt] = -1;
             if (as >= 0) tok_a[n++] = as;
         }
+        uint8_t *tile = wbuf + buf * kDnBuf;
+        float *s_act = reinterpret_cast<float *>(tile + kDnMaxRows * kDnRowStride);   // [2][kDnMaxRows]
         for (int p0 = 0; p0 < n; p0 += 2) {
             const int np = min(2, n - p0);
             const int as0 = tok_a[p0], as1 = np > 1 ? tok_a[p0 + 1] : -1;
+            // activations of the pass's tokens for the segment's rows (written by the previous kernel)
+            __syncwarp();
+            for (int i = lane; i < 2 * FR; i += 32) {
+                const int tk = i / FR, row = i % FR;
+                const int as = tk ? as1 : as0;
+                s_act[tk * kDnMaxRows + row] = as >= 0 ? __ldg(a.act + (int64_t)as * FF + fs * FR + row) : 0.0f;
+            }
+            cp_async_wait<1>();
+            __syncwarp();
             float acc[2][32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc[0][j] = acc[1][j] = 0.0f;
             float zl0 = 0.0f, zh0 = 0.0f, zl1 = 0.0f, zh1 = 0.0f;
-            for (int rr = r; rr < FR; rr += 16 * kDnRowBatch) {
-                float av0[kDnRowBatch], av1[kDnRowBatch];
+#pragma unroll 2
+            for (int row = rl; row < FR; row += 4) {
+                const uint4 hv = *reinterpret_cast<const uint4 *>(tile + row * kDnRowStride);
+                const uint4 qv = *reinterpret_cast<const uint4 *>(tile + row * kDnRowStride + 16 + 16 * q);
+                const float av0 = s_act[row], av1 = s_act[kDnMaxRows + row];
+                float sl, zl, sh, zh;
+                q4k_pair_scales_f(hv, c, sl, zl, sh, zh);
+                const float A0l = 256.0f * av0 * sl, A0h = 256.0f * av0 * sh;
+                const float A1l = 256.0f * av1 * sl, A1h = 256.0f * av1 * sh;
+                zl0 = fmaf(av0, fmaf(128.0f, sl, zl), zl0);
+                zh0 = fmaf(av0, fmaf(128.0f, sh, zh), zh0);
+                zl1 = fmaf(av1, fmaf(128.0f, sl, zl), zl1);
+                zh1 = fmaf(av1, fmaf(128.0f, sh, zh), zh1);
+                const uint32_t wds[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-                for (int b = 0; b < kDnRowBatch; ++b) {
-                    const int f = fs * FR + min(rr + 16 * b, FR - 1);
-                    av0[b] = __ldg(a.act + (int64_t)as0 * FF + f);          // written by the previous kernel
-                    av1[b] = as1 >= 0 ? __ldg(a.act + (int64_t)as1 * FF + f) : 0.0f;
-                }
+                for (int wi = 0; wi < 4; ++wi) {
+                    const uint32_t lo = wds[wi] & 0x0F0F0F0Fu, hi = (wds[wi] >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
-                for (int b = 0; b < kDnRowBatch; ++b) {
-                    const int row = rr + 16 * b;
-                    if (row < FR) {
-                        const uint4 hv = *reinterpret_cast<const uint4 *>(tile + row * kDnRowStride);
-                        const uint4 qv = *reinterpret_cast<const uint4 *>(tile + row * kDnRowStride + 16 + 16 * q);
-                        float sl, zl, sh, zh;
-                        q4k_scales_f(hv, 2 * c, sl, zl);
-                        q4k_scales_f(hv, 2 * c + 1, sh, zh);
-                        const float A0l = 256.0f * av0[b] * sl, A0h = 256.0f * av0[b] * sh;
-                        const float A1l = 256.0f * av1[b] * sl, A1h = 256.0f * av1[b] * sh;
-                        zl0 = fmaf(av0[b], fmaf(128.0f, sl, zl), zl0);
-                        zh0 = fmaf(av0[b], fmaf(128.0f, sh, zh), zh0);
-                        zl1 = fmaf(av1[b], fmaf(128.0f, sl, zl), zl1);
-                        zh1 = fmaf(av1[b], fmaf(128.0f, sh, zh), zh1);
-                        const uint32_t wds[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-                        for (int wi = 0; wi < 4; ++wi) {
-                            const uint32_t lo = wds[wi] & 0x0F0F0F0Fu, hi = (wds[wi] >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-                            for (int bb = 0; bb < 4; ++bb) {
-                                const float vl = __uint_as_float(__byte_perm(lo, 0x3F000000u, 0x7044 | (bb << 8)));
-                                const float vh = __uint_as_float(__byte_perm(hi, 0x3F000000u, 0x7044 | (bb << 8)));
-                                acc[0][4 * wi + bb] = fmaf(A0l, vl, acc[0][4 * wi + bb]);
-                                acc[0][16 + 4 * wi + bb] = fmaf(A0h, vh, acc[0][16 + 4 * wi + bb]);
-                                if (np > 1) {
-                                    acc[1][4 * wi + bb] = fmaf(A1l, vl, acc[1][4 * wi + bb]);
-                                    acc[1][16 + 4 * wi + bb] = fmaf(A1h, vh, acc[1][16 + 4 * wi + bb]);
-                                }
-                            }
+                    for (int bb = 0; bb < 4; ++bb) {
+                        const float vl = __uint_as_float(__byte_perm(lo, 0x3F000000u, 0x7044 | (bb << 8)));
+                        const float vh = __uint_as_float(__byte_perm(hi, 0x3F000000u, 0x7044 | (bb << 8)));
+                        acc[0][4 * wi + bb] = fmaf(A0l, vl, acc[0][4 * wi + bb]);
+                        acc[0][16 + 4 * wi + bb] = fmaf(A0h, vh, acc[0][16 + 4 * wi + bb]);
+                        if (np > 1) {
+                            acc[1][4 * wi + bb] = fmaf(A1l, vl, acc[1][4 * wi + bb]);
+                            acc[1][16 + 4 * wi + bb] = fmaf(A1h, vh, acc[1][16 + 4 * wi + bb]);
                         }
                     }
                 }
@@ -828,7 +849,7 @@ __global__ void __launch_bounds__(kDnThreads) k_dec_down(DecArgs a)
                 acc[1][j] -= zl1;
                 acc[1][16 + j] -= zh1;
             }
-            // reduce the 4 row lanes of this warp (lanes q + 8 r'), then the 4 warps
+            // sum the 4 row lanes (lanes q, q + 8, q + 16, q + 24)
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 acc[0][j] += __shfl_xor_sync(0xffffffffu, acc[0][j], 8);
@@ -838,44 +859,32 @@ __global__ void __launch_bounds__(kDnThreads) k_dec_down(DecArgs a)
                     acc[1][j] += __shfl_xor_sync(0xffffffffu, acc[1][j], 16);
                 }
             }
-            if (lane < 8) {
-                // h offsets within the block: low nibbles 64c + l0 + j, high +32
+            // lane (q, rl) writes token (rl & 1) and the low (rl < 2) or high 16 columns of its chunk
+            const int pt = rl & 1, part = rl >> 1;
+            if (pt < np) {
+                const int as = pt ? as1 : as0;
+                const float wt = a.w[as];
+                const int tok = as / a.k;
+                const int h = 256 * cb + 64 * c + 32 * part + l0;
+                float o[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    s_acc[warp][0][64 * c + l0 + j] = acc[0][j];
-                    s_acc[warp][0][64 * c + 32 + l0 + j] = acc[0][16 + j];
-                    if (np > 1) {
-                        s_acc[warp][1][64 * c + l0 + j] = acc[1][j];
-                        s_acc[warp][1][64 * c + 32 + l0 + j] = acc[1][16 + j];
-                    }
+                    const float lo0 = acc[0][j], hi0 = acc[0][16 + j], lo1 = acc[1][j], hi1 = acc[1][16 + j];
+                    o[j] = (part ? (pt ? hi1 : hi0) : (pt ? lo1 : lo0)) * wt;
                 }
-            }
-            __syncthreads();
-            // 128 threads: token pt = tid / 64, 4 consecutive h each
-            {
-                const int pt = tid >> 6, h4 = (tid & 63) * 4;
-                if (pt < np) {
-                    const int as = pt ? as1 : as0;
-                    const float wt = a.w[as];
-                    float o[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        o[i] = (s_acc[0][pt][h4 + i] + s_acc[1][pt][h4 + i] + s_acc[2][pt][h4 + i] +
-                                s_acc[3][pt][h4 + i]) * wt;
-                    const int tok = as / a.k;
-                    const int h = 256 * cb + h4;
+                for (int v = 0; v < 4; ++v) {
                     if (a.det) {
-                        float *dst = a.slots + ((int64_t)as * FS + fs) * H + h;
-                        *reinterpret_cast<float4 *>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+                        float *dst = a.slots + ((int64_t)as * FS + fs) * H + h + 4 * v;
+                        *reinterpret_cast<float4 *>(dst) = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
                     } else {
-                        float *dst = a.yacc + (int64_t)tok * H + h;
-                        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(o[0]),
-                                     "f"(o[1]), "f"(o[2]), "f"(o[3])
+                        float *dst = a.yacc + (int64_t)tok * H + h + 4 * v;
+                        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(o[4 * v]),
+                                     "f"(o[4 * v + 1]), "f"(o[4 * v + 2]), "f"(o[4 * v + 3])
                                      : "memory");
                     }
                 }
             }
-            __syncthreads();
         }
     }
     cp_async_wait<0>();
@@ -943,9 +952,11 @@ int dec_down_splits(const moe_config &c, int32_t T)
     const int64_t maxu = std::min<int64_t>(c.n_experts, (int64_t)T * c.top_k);
     const int64_t nb = c.hidden / 256;
     int fs = 1;
-    while (c.ff / fs > kDnMaxRows) fs *= 2;
+    while (c.ff % fs || c.ff / fs > kDnMaxRows) ++fs;      // segments of at most kDnMaxRows rows
     if (c.flags & MOE_FLAG_DETERMINISTIC) return fs;
-    while (fs < 64 && maxu * nb * fs < 2 * dec_sms() && c.ff % (fs * 2) == 0 && c.ff / (fs * 2) >= 32) fs *= 2;
+    // more segments while there are fewer units than warps and segments stay >= 32 rows
+    for (int f2 = fs + 1; maxu * nb * fs < (int64_t)kDnWarps * 2 * dec_sms() && f2 <= 64; ++f2)
+        if (c.ff % f2 == 0 && c.ff / f2 >= 32) fs = f2;
     return fs;
 }
 
@@ -966,12 +977,14 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-// Ring depth of the gate/up stages: three when shared memory holds them.
+// Ring depth of the gate/up stages: the deepest (up to four) that shared memory holds.
 int dec_gateup_stages(int H)
 {
     const size_t fixed = (size_t)H * 16 + kGuWarps * 32 * 4 * sizeof(float) + kDecMaxAssign * 2 * (1 + kDecTok) +
                          kDecMaxAssign * sizeof(void *);
-    return fixed + (size_t)kGuWarps * 3 * kGuStage + 1024 <= (size_t)kMaxSmemPerBlock ? 3 : 2;
+    for (int nst = 4; nst > 2; --nst)
+        if (fixed + (size_t)kGuWarps * nst * kGuStage + 1024 <= (size_t)kMaxSmemPerBlock) return nst;
+    return 2;
 }
 
 static size_t gateup_smem(const DecArgs &a, int nst)
@@ -1010,7 +1023,7 @@ cudaError_t launch_decode(const DecArgs &a0, cudaStream_t s)
                                  kDecTok * 8192 * (int)sizeof(uint16_t));
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_dec_down, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     2 * kDnMaxRows * kDnRowStride);
+                                     kDnWarps * 2 * kDnBuf);
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -1043,7 +1056,7 @@ cudaError_t launch_decode(const DecArgs &a0, cudaStream_t s)
     : ks == 4 ? launch_gateup<NS, 4>(a, grid_gu, s) : ks == 5 ? launch_gateup<NS, 5>(a, grid_gu, s)                 \
     : ks == 8 ? launch_gateup<NS, 8>(a, grid_gu, s) : ks == 10 ? launch_gateup<NS, 10>(a, grid_gu, s)               \
               : launch_gateup<NS, 16>(a, grid_gu, s)
-    e = NST == 3 ? (MOE_GU_CASES(3)) : (MOE_GU_CASES(2));
+    e = NST == 4 ? (MOE_GU_CASES(4)) : NST == 3 ? (MOE_GU_CASES(3)) : (MOE_GU_CASES(2));
 #undef MOE_GU_CASES
     prof_end(kPhDecGateUp, s);
     if (e != cudaSuccess) return e;
@@ -1054,9 +1067,9 @@ cudaError_t launch_decode(const DecArgs &a0, cudaStream_t s)
     }
 
     const int64_t units = maxu * nb * a.fs_dn;
-    const int grid_dn = (int)std::max<int64_t>(1, std::min<int64_t>(units, 2 * (int64_t)sms));
+    const int grid_dn = (int)std::max<int64_t>(1, std::min<int64_t>((units + kDnWarps - 1) / kDnWarps, 2 * (int64_t)sms));
     prof_begin(kPhDecDown, s);
-    e = launch_pdl(k_dec_down, dim3(grid_dn), dim3(kDnThreads), 2 * kDnMaxRows * kDnRowStride, s, true, a);
+    e = launch_pdl(k_dec_down, dim3(grid_dn), dim3(kDnThreads), (size_t)kDnWarps * 2 * kDnBuf, s, true, a);
     prof_end(kPhDecDown, s);
     if (e != cudaSuccess) return e;
     const int n4 = a.T * a.H / 4;

@@ -18,11 +18,12 @@
 //            epilogue: * routing weight, atomically added into y (fp32), or
 //              stored to the assignment's slot when the call is deterministic.
 //
-// Warp roles (12 warps): 0-3 epilogue (tensor-memory lane quarters 0-3),
+// Warp roles (16 warps): 0-3 epilogue (tensor-memory lane quarters 0-3),
 // 4 MMA issue + tensor-memory allocation, 5 raw weight bytes (16-byte cp.async
 // pieces into a ring, completion counted on its mbarrier), 6-7 token rows
-// (16-byte cp.async gathers, 128-byte swizzle),
-// 8-11 dequantisation (raw ring -> fp16 A ring).  All hand-offs are mbarriers;
+// (16-byte cp.async gathers into 128-byte-swizzled tiles, completion counted
+// on the B ring's mbarriers),
+// 8-15 dequantisation (raw ring -> fp16 A ring).  All hand-offs are mbarriers;
 // every wait is bounded and sets MOE_ERR_TIMEOUT instead of hanging.
 //
 // Operand precision: fp16 A and B (sub-block scale and min rounded to fp16,
@@ -40,7 +41,8 @@ using namespace ptx;
 enum GemmOp { kOpGateUp = 0, kOpDown = 1 };
 enum WFmt { kWQ4K = 0, kWQ80 = 1 };
 
-constexpr int kGemmThreads = 384;
+constexpr int kGemmThreads = 512;
+constexpr int kDeqThreads = 256;           // warps 8-15: dequantisation
 constexpr int kABytes = 128 * 128;          // 128 rows x 64 fp16
 constexpr long long kWaitCycles = 1ll << 32; // ~2 s at 2 GHz
 
@@ -87,12 +89,15 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs &g, int idx)
 
 // Bounded wait on an mbarrier phase; false on abort (another role gave up) or
 // on timeout (this call records MOE_ERR_TIMEOUT and raises the abort flag).
+// Waiting warps sleep in the try_wait (hardware suspend, up to ~20 us per
+// try) rather than spin, so they do not take issue slots from the working
+// warps.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort, uint32_t *status)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort) return false;
         if (clock64() - t0 > kWaitCycles) {
             *abort = 1;
@@ -146,30 +151,50 @@ __device__ __forceinline__ void q4k_subblock_scales(uint4 hdr, int j, __half &s,
     nz = __float2half_rn(-__fmul_rn(dmin, (float)m));
 }
 
-// gate/up, Q4_K: thread t dequantises row t (64 weights of K-step `sub` of the
-// raw block) into the swizzled fp16 A tile.
-__device__ __forceinline__ void dequant_gu_q4k(const uint8_t *raw, uint32_t a_tile, int row, int sub)
+// Q4_K block header -> fp16 (scale, -min) pairs of its eight sub-blocks:
+// S[i] = (fp16(d sc_2i), fp16(d sc_2i+1)), NZ[i] likewise with -dmin m.  The
+// 6-bit values are exact fp16 integers and each product rounds once, as
+// fp16(fp32(d) * sc) does.
+__device__ __forceinline__ void q4k_block_scales_h(uint4 hdr, uint32_t (&S)[4], uint32_t (&NZ)[4])
+{
+    const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, m_lo = hdr.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    const __half2 k1024 = __float2half2_rn(1024.0f);
+    const __half2 dd = u2h2(__byte_perm(hdr.x, 0, 0x1010)), mm = u2h2(__byte_perm(hdr.x, 0, 0x3232) ^ 0x80008000u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t scw = i < 2 ? sc_lo : sc_hi, mw = i < 2 ? m_lo : m_hi;
+        const uint32_t sel = (i & 1) ? 0x5342u : 0x5140u;
+        S[i] = h22u(__hmul2(dd, __hsub2(u2h2(__byte_perm(scw, 0x64646464u, sel)), k1024)));
+        NZ[i] = h22u(__hmul2(mm, __hsub2(u2h2(__byte_perm(mw, 0x64646464u, sel)), k1024)));
+    }
+}
+
+// gate/up, Q4_K: thread (row, h) dequantises half h of row `row` of K-step
+// `sub` of the raw block column (16 quant bytes: 16 low-nibble weights of
+// sub-block 2 sub and 16 high-nibble weights of sub-block 2 sub + 1) into the
+// swizzled fp16 A tile, with the block's scales decoded beforehand.
+__device__ __forceinline__ void dequant_gu_q4k(const uint8_t *raw, uint32_t a_tile, int row, int h, int sub,
+                                               const uint32_t (&S)[4], const uint32_t (&NZ)[4])
 {
     const uint8_t *rr = raw + row * 144;
-    const uint4 hdr = *reinterpret_cast<const uint4 *>(rr);
-    __half s_lo, nz_lo, s_hi, nz_hi;
-    q4k_subblock_scales(hdr, 2 * sub, s_lo, nz_lo);
-    q4k_subblock_scales(hdr, 2 * sub + 1, s_hi, nz_hi);
-    const __half2 S_lo = __half2half2(s_lo), NZ_lo = __half2half2(nz_lo);
-    const __half2 S_hi = __half2half2(s_hi), NZ_hi = __half2half2(nz_hi);
-    const uint4 qa = *reinterpret_cast<const uint4 *>(rr + 16 + 32 * sub);
-    const uint4 qb = *reinterpret_cast<const uint4 *>(rr + 16 + 32 * sub + 16);
-    const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const uint4 q = *reinterpret_cast<const uint4 *>(rr + 16 + 32 * sub + 16 * h);
+    // sub is a runtime value: select, so that S and NZ stay in registers
+    const uint32_t sp = sub == 0 ? S[0] : sub == 1 ? S[1] : sub == 2 ? S[2] : S[3];
+    const uint32_t np = sub == 0 ? NZ[0] : sub == 1 ? NZ[1] : sub == 2 ? NZ[2] : NZ[3];
+    const __half2 S_lo = __low2half2(u2h2(sp)), S_hi = __high2half2(u2h2(sp));
+    const __half2 NZ_lo = __low2half2(u2h2(np)), NZ_hi = __high2half2(u2h2(np));
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
+    for (int p = 0; p < 2; ++p) {
         __half2 l0, l1, h0, h1, l2, l3, h2, h3;
         nibbles_to_q(words[2 * p], l0, l1, h0, h1);
         nibbles_to_q(words[2 * p + 1], l2, l3, h2, h3);
-        st_shared_v4(a_tile + sw128_off(row, p), h22u(__hfma2(l0, S_lo, NZ_lo)), h22u(__hfma2(l1, S_lo, NZ_lo)),
+        st_shared_v4(a_tile + sw128_off(row, 2 * h + p), h22u(__hfma2(l0, S_lo, NZ_lo)), h22u(__hfma2(l1, S_lo, NZ_lo)),
                      h22u(__hfma2(l2, S_lo, NZ_lo)), h22u(__hfma2(l3, S_lo, NZ_lo)));
-        st_shared_v4(a_tile + sw128_off(row, p + 4), h22u(__hfma2(h0, S_hi, NZ_hi)),
-                     h22u(__hfma2(h1, S_hi, NZ_hi)), h22u(__hfma2(h2, S_hi, NZ_hi)),
-                     h22u(__hfma2(h3, S_hi, NZ_hi)));
+        st_shared_v4(a_tile + sw128_off(row, 4 + 2 * h + p), h22u(__hfma2(h0, S_hi, NZ_hi)),
+                     h22u(__hfma2(h1, S_hi, NZ_hi)), h22u(__hfma2(h2, S_hi, NZ_hi)), h22u(__hfma2(h3, S_hi, NZ_hi)));
     }
 }
 
@@ -180,14 +205,13 @@ __device__ __forceinline__ __half2 i8pair_to_h2(uint32_t pair16)
     return __hsub2(u2h2(p | 0x64006400u), __float2half2_rn(1152.0f));                  // 1024 + q + 128 - 1152
 }
 
-// gate/up, Q8_0: row t, K-step s: two 34-byte blocks at offset (68 s) mod 16
-// of the 80-byte raw row.
-__device__ __forceinline__ void dequant_gu_q80(const uint8_t *raw, uint32_t a_tile, int row, int s)
+// gate/up, Q8_0: thread (row, blk), K-step s: block blk of the two 34-byte
+// blocks at offset (68 s) mod 16 of the 80-byte raw row.
+__device__ __forceinline__ void dequant_gu_q80(const uint8_t *raw, uint32_t a_tile, int row, int blk, int s)
 {
     const uint8_t *rr = raw + row * 80 + ((68 * s) & 15);
     const uint16_t *r16 = reinterpret_cast<const uint16_t *>(rr);   // offset is a multiple of 4
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
+    {
         const __half2 D = __half2half2(__ushort_as_half(r16[17 * blk]));
 #pragma unroll
         for (int cq = 0; cq < 4; ++cq) {          // 4 chunks of 8 weights per block
@@ -207,8 +231,8 @@ __device__ __forceinline__ void dequant_gu_q80(const uint8_t *raw, uint32_t a_ti
 __device__ __forceinline__ void dequant_dn_q4k(const uint8_t *raw, uint32_t a_tile, int dt, int half)
 {
 #pragma unroll
-    for (int it4 = 0; it4 < 4; ++it4) {
-        const int it = dt + 128 * it4;
+    for (int it4 = 0; it4 < 512 / kDeqThreads; ++it4) {
+        const int it = dt + kDeqThreads * it4;
         const int row = it & 63, bg = it >> 6;           // bg 0..7
         const uint8_t *rr = raw + row * 80;
         const uint4 hdr = *reinterpret_cast<const uint4 *>(rr);
@@ -246,8 +270,8 @@ __device__ __forceinline__ void dequant_dn_q4k(const uint8_t *raw, uint32_t a_ti
 __device__ __forceinline__ void dequant_dn_q80(const uint8_t *raw, uint32_t a_tile, int dt, int o8)
 {
 #pragma unroll
-    for (int it8 = 0; it8 < 8; ++it8) {
-        const int it = dt + 128 * it8;
+    for (int it8 = 0; it8 < 1024 / kDeqThreads; ++it8) {
+        const int it = dt + kDeqThreads * it8;
         const int row = it & 63, g = it >> 6;            // g 0..15: 8 columns each
         const int b = g >> 2, hh0 = 8 * (g & 3);
         const uint16_t *blk = reinterpret_cast<const uint16_t *>(raw + row * 144 + o8 + 34 * b);
@@ -328,10 +352,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
             mbar_init(full_raw(i), 32);          // the 32 lanes of the raw-byte warp
-            mbar_init(empty_raw(i), 128);
+            mbar_init(empty_raw(i), kDeqThreads);
         }
         for (int i = 0; i < SA; ++i) {
-            mbar_init(full_a(i), 128);
+            mbar_init(full_a(i), kDeqThreads);
             mbar_init(empty_a(i), 1);
         }
         for (int i = 0; i < SB; ++i) {
@@ -502,6 +526,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
                     const int slot_a = sa_it % SA, slot_b = sb_it % SB;
                     if (!(ok = wait_bar(full_a(slot_a), (sa_it / SA) & 1, abort_flag, g.status))) break;
                     if (!(ok = wait_bar(full_b(slot_b), (sb_it / SB) & 1, abort_flag, g.status))) break;
+                    fence_proxy_async();   // the token rows were written by cp.async (generic proxy)
                     tc_fence_after();
                     const uint32_t a0 = sA + slot_a * kABytes, b0 = sB + slot_b * C::kBBytes;
 #pragma unroll
@@ -539,31 +564,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
                 if (!(ok = wait_bar(empty_raw(slot), ((rs_it / RS) & 1) ^ 1, abort_flag, g.status))) break;
                 uint8_t *dst0 = raw_base + slot * C::kRawStage;
                 // 16-byte asynchronous copies; each lane's completion arrives on full_raw
+                // consecutive lanes take consecutive 16-byte pieces (coalesced requests);
+                // piece p = lane + 32 j is (row p / P, piece p % P), stepped incrementally
                 if (OP == kOpGateUp) {
                     // 128 rows: row 2i = gate f0+i, row 2i+1 = up f0+i
                     constexpr int kPieces = FMT == kWQ4K ? 9 : 5;           // 144 or 80 bytes per row
-                    for (int p = lane; p < 128 * kPieces; p += 32) {
-                        const int i = p / kPieces, pc = p % kPieces;
-                        const int64_t mrow = (int64_t)((i & 1) ? ffop : 0) + ti.m * 64 + (i >> 1);
-                        const uint8_t *rowp = ti.blob + mrow * rb;
-                        const uint8_t *src = FMT == kWQ4K ? rowp + (int64_t)r * 144 : rowp + ((68 * r) & ~15);
-                        cp_async16(smem_addr(dst0 + i * (16 * kPieces) + pc * 16), src + pc * 16);
+                    int i = lane / kPieces, pc = lane % kPieces;
+                    const int64_t col = FMT == kWQ4K ? (int64_t)r * 144 : (int64_t)((68 * r) & ~15);
+                    const uint8_t *gbase = ti.blob + (int64_t)ti.m * 64 * rb + col;
+                    const uint8_t *ubase = gbase + (int64_t)ffop * rb;
+                    for (int j = 0; j < (128 * kPieces) / 32; ++j) {
+                        const uint8_t *src = ((i & 1) ? ubase : gbase) + (int64_t)(i >> 1) * rb + pc * 16;
+                        cp_async16(smem_addr(dst0 + i * (16 * kPieces) + pc * 16), src);
+                        i += 32 / kPieces;
+                        pc += 32 % kPieces;
+                        if (pc >= kPieces) {
+                            pc -= kPieces;
+                            ++i;
+                        }
                     }
                 } else {
                     // 64 ff rows of Wd for this K-step, this tile's 128 hidden columns
                     const int h0 = ti.m * 128;
                     constexpr int kPieces = FMT == kWQ4K ? 5 : 9;           // 16 + 64 or 144 bytes per row
-                    for (int p = lane; p < 64 * kPieces; p += 32) {
-                        const int i = p / kPieces, pc = p % kPieces;
-                        const uint8_t *rowp = ti.blob + ((int64_t)2 * ffop + 64 * r + i) * rb;
-                        const uint8_t *src;
-                        if (FMT == kWQ4K) {
-                            const uint8_t *blk = rowp + (int64_t)(h0 / 256) * 144;
-                            src = pc == 0 ? blk : blk + 16 + 64 * ((h0 / 128) & 1) + (pc - 1) * 16;
-                        } else {
-                            src = rowp + ((34 * (h0 / 32)) & ~15) + pc * 16;
-                        }
+                    const uint8_t *base = ti.blob + ((int64_t)2 * ffop + 64 * r) * rb;
+                    const int64_t blk = FMT == kWQ4K ? (int64_t)(h0 / 256) * 144 : (int64_t)((34 * (h0 / 32)) & ~15);
+                    const int qoff = 16 + 64 * ((h0 / 128) & 1);
+                    int i = lane / kPieces, pc = lane % kPieces;
+                    for (int j = 0; j < (64 * kPieces) / 32; ++j) {
+                        const uint8_t *rowp = base + (int64_t)i * rb + blk;
+                        const uint8_t *src = FMT == kWQ4K ? (pc == 0 ? rowp : rowp + qoff + (pc - 1) * 16) : rowp + pc * 16;
                         cp_async16(smem_addr(dst0 + i * (16 * kPieces) + pc * 16), src);
+                        i += 32 / kPieces;
+                        pc += 32 % kPieces;
+                        if (pc >= kPieces) {
+                            pc -= kPieces;
+                            ++i;
+                        }
                     }
                 }
                 cp_async_arrive_noinc(full_raw(slot));
@@ -578,14 +615,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
     } else if (warp < 8) {
         // ------------------------------------------------------------ token rows (B)
         // thread bt copies 16-byte chunk (bt & 7) of rows j = (bt >> 3) + 8 i;
-        // a stage is announced full once its copies have landed, SB-1 stages
-        // behind the newest one (the lag runs across tiles)
-        constexpr int LAG = SB - 1;
+        // each thread's copies of a stage arrive on full_b when they land, so
+        // the gatherers run up to SB stages ahead of the MMAs
         const int bt = threadIdx.x - 192;   // 0..63
         const int c = bt & 7, r0 = bt >> 3;
         const __half *srcbase = OP == kOpGateUp ? g.x16 : (FMT == kWQ4K ? g.act16 : g.sh_act16);
         const int ld = OP == kOpGateUp ? g.H : (FMT == kWQ4K ? g.FF : g.SFF);
-        uint32_t sb_it = 0, pending = 0;
+        uint32_t sb_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<OP, FMT>(g, tile);
@@ -610,23 +646,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
                     const int j = r0 + 8 * i;
                     if (j < ti.n) cp_async16(b_tile + sw128_off(j, c), srcbase + (int64_t)src[i] * ld + kcol);
                 }
-                cp_async_commit();
-                if (++pending > (uint32_t)LAG) {
-                    cp_async_wait<LAG>();
-                    fence_proxy_async();
-                    mbar_arrive(full_b((sb_it - LAG) % SB));
-                    --pending;
-                }
+                cp_async_arrive_noinc(full_b(slot));
             }
         }
-        cp_async_wait<0>();
-        fence_proxy_async();
-        if (ok)
-            for (; pending > 0; --pending) mbar_arrive(full_b((sb_it - pending) % SB));
+        cp_async_wait<0>();   // nothing may still be writing shared memory when the CTA ends
     } else {
         // ------------------------------------------------------------ dequantisation (A)
-        const int dt = threadIdx.x - 256;   // 0..127
+        const int dt = threadIdx.x - 256;   // 0..255
         uint32_t sa_it = 0, rs_it = 0;
+        uint32_t S[4], NZ[4];
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<OP, FMT>(g, tile);
@@ -642,8 +670,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
                 const uint8_t *raw = raw_base + rslot * C::kRawStage;
                 const uint32_t a_tile = sA + slot * kABytes;
                 if (OP == kOpGateUp) {
-                    if (FMT == kWQ4K) dequant_gu_q4k(raw, a_tile, dt, sub);
-                    else dequant_gu_q80(raw, a_tile, dt, sg);
+                    // thread dt = (row dt & 127, half dt >> 7): a warp covers 32 consecutive
+                    // rows (conflict-free shared-memory accesses)
+                    if (FMT == kWQ4K) {
+                        if (first) q4k_block_scales_h(*reinterpret_cast<const uint4 *>(raw + (dt & 127) * 144), S, NZ);
+                        dequant_gu_q4k(raw, a_tile, dt & 127, dt >> 7, sub, S, NZ);
+                    } else {
+                        dequant_gu_q80(raw, a_tile, dt & 127, dt >> 7, sg);
+                    }
                 } else {
                     if (FMT == kWQ4K) dequant_dn_q4k(raw, a_tile, dt, ti.m & 1);
                     else dequant_dn_q80(raw, a_tile, dt, (34 * (ti.m * 128 / 32)) & 15);
@@ -805,13 +839,12 @@ static cudaError_t launch_gemm(const GemmArgs &g, int grid, cudaStream_t s)
 
 // Configurations: small buckets (every token tile <= 16 wide: decode windows)
 // keep deep A and raw rings; large buckets (prefill) use token tiles of
-// kGemmMaxN with a 5-deep A ring, so that the dequantisation runs ahead of the
-// MMAs.
+// kGemmMaxN with A, B and raw rings of 4, 6 and 3 stages.
 template <int OP, int FMT>
 static cudaError_t launch_gemm_cfg(const GemmArgs &g, int grid, bool small, cudaStream_t s)
 {
     if (small) return launch_gemm<OP, FMT, 16, 6, 8, 92160>(g, grid, s);
-    return launch_gemm<OP, FMT, kGemmMaxN, 5, 4, 55296>(g, grid, s);
+    return launch_gemm<OP, FMT, kGemmMaxN, 4, 6, 55296>(g, grid, s);
 }
 
 static int num_sms()
