@@ -58,7 +58,8 @@ WsLayout ws_layout(const moe_config &c, int32_t T)
     L.act = take(gemv ? TK * c.ff * 4 : 0);
     L.slots = take(det ? TK * H * 4 * (gemv ? dec_down_splits(c, T) : 1) : 0);
     L.yacc = take((size_t)T * H * 4);
-    L.x16 = take(gemv ? 0 : (size_t)T * H * 2);
+    L.xg = take(gemv ? 0 : TK * H * 2);
+    L.x16 = take(gemv || !c.shared_ff ? 0 : (size_t)T * H * 2);
     L.sh_act = take(gemv && c.shared_ff ? (size_t)T * c.shared_ff * 4 : 0);
     L.sh_out = take(c.shared_ff && (gemv || det) ? (size_t)T * H * 4 : 0);
     (void)maxu;
@@ -74,6 +75,7 @@ WsLayout ws_layout(const moe_config &c, int32_t T)
     L.tiles_dn = take(cap_dn * sp.dn * 16);
     L.tiles_gus = take(cap_gus * sp.gus * 16);
     L.tiles_dns = take(cap_dns * sp.dns * 16);
+    L.tmaps = take(gemv ? 0 : gemm_tmap_bytes());
     L.gu = take(sp.gu > 1 ? TK * 2 * c.ff * 4 : 0);
     L.sh_gu = take(sp.gus > 1 ? (size_t)T * 2 * c.shared_ff * 4 : 0);
     L.split_cnt = take(((sp.gu > 1 ? cap_gu : 0) + (sp.gus > 1 ? cap_gus : 0)) * 4);
@@ -318,6 +320,7 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
     a.header = r.header;
     {
         GemmWs gw{};
+        gw.xg = (__half *)(base + L.xg);
         gw.x16 = (__half *)(base + L.x16);
         gw.act16 = (__half *)(base + L.act16);
         gw.sh_act16 = (__half *)(base + L.sh_act16);
@@ -326,6 +329,7 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
         gw.tiles_dn = (int4 *)(base + L.tiles_dn);
         gw.tiles_gus = (int4 *)(base + L.tiles_gus);
         gw.tiles_dns = (int4 *)(base + L.tiles_dns);
+        gw.tmaps = base + L.tmaps;
         gw.splits = gemm_splits(*cfg, T);
         gw.gu = (float *)(base + L.gu);
         gw.sh_gu = (float *)(base + L.sh_gu);

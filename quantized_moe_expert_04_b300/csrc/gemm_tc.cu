@@ -31,6 +31,8 @@
 #include <algorithm>
 #include <cmath>
 
+#include <cuda.h>
+
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -42,7 +44,17 @@ enum GemmOp { kOpGateUp = 0, kOpDown = 1 };
 enum WFmt { kWQ4K = 0, kWQ80 = 1 };
 
 constexpr int kGemmThreads = 512;
-constexpr int kDeqThreads = 256;           // warps 8-15: dequantisation
+// Warp roles: the epilogue runs on warps 0-3, the dequantisation on warps
+// 8-15, unless EW = 8 (down projections whose tiles are short along K, where
+// the epilogue's additions into y outweigh the dequantisation): then warps
+// 12-15 join the epilogue (two groups taking alternate 16-column chunks) and
+// warps 8-11 dequantise.
+template <int EW>
+__host__ __device__ constexpr int deq_threads()
+{
+    return EW == 8 ? 128 : 256;
+}
+
 constexpr int kABytes = 128 * 128;          // 128 rows x 64 fp16
 constexpr long long kWaitCycles = 1ll << 32; // ~2 s at 2 GHz
 
@@ -52,7 +64,8 @@ struct GemmArgs {
     const uint8_t *shared_blob;
     const int32_t *offsets, *assign;
     const float *w;
-    const __half *x16;       // [T][H]
+    const __half *xg;        // [T*k][H] x rows in bucket order (routed gate/up operand)
+    const __half *x16;       // [T][H] (shared expert's gate/up operand; null without one)
     __half *act16;           // [T*k][FF] by bucket position
     __half *sh_act16;        // [T][SFF]
     float *yacc;             // [T][H]
@@ -62,6 +75,7 @@ struct GemmArgs {
     float *gu;               // split-K gate/up partial sums [rows][2 FF] (splits > 1)
     uint32_t *split_cnt;     // split-K arrival counters, one per (expert, m, n) group
     uint32_t *status;
+    CUtensorMap *tmaps;      // [grid][2] per-CTA tensor maps of the current expert's blob
 };
 
 struct TileInfo {
@@ -138,64 +152,19 @@ __device__ __forceinline__ void nibbles_to_q(uint32_t w, __half2 &lo01, __half2 
     hi23 = __hfma2(u2h2((p23 & 0x00F000F0u) | 0x64006400u), k16th, km64);
 }
 
-__device__ __forceinline__ void q4k_subblock_scales(uint4 hdr, int j, __half &s, __half &nz)
-{
-    const float d = f16_bits_to_f32(hdr.x & 0xffff), dmin = f16_bits_to_f32(hdr.x >> 16);
-    uint8_t scales[12];
-    memcpy(scales, &hdr.y, 4);
-    memcpy(scales + 4, &hdr.z, 4);
-    memcpy(scales + 8, &hdr.w, 4);
-    int sc, m;
-    q4k_scale_min(scales, j, sc, m);
-    s = __float2half_rn(__fmul_rn(d, (float)sc));
-    nz = __float2half_rn(-__fmul_rn(dmin, (float)m));
-}
-
-// Q4_K block header -> fp16 (scale, -min) pairs of its eight sub-blocks:
-// S[i] = (fp16(d sc_2i), fp16(d sc_2i+1)), NZ[i] likewise with -dmin m.  The
-// 6-bit values are exact fp16 integers and each product rounds once, as
+// Q4_K block header -> fp16 (scale, -min) of the sub-block pair (2g, 2g+1):
+// S = (fp16(d sc_2g), fp16(d sc_2g+1)), NZ likewise with -dmin m.  The 6-bit
+// values are exact fp16 integers and each product rounds once, as
 // fp16(fp32(d) * sc) does.
-__device__ __forceinline__ void q4k_block_scales_h(uint4 hdr, uint32_t (&S)[4], uint32_t (&NZ)[4])
+__device__ __forceinline__ void q4k_pair_scales_h(uint4 hdr, int g, __half2 &S, __half2 &NZ)
 {
-    const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, m_lo = hdr.z & 0x3F3F3F3Fu;
-    const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
-    const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    const uint32_t scw = g < 2 ? (hdr.y & 0x3F3F3F3Fu) : ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u));
+    const uint32_t mw = g < 2 ? (hdr.z & 0x3F3F3F3Fu) : (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u));
+    const uint32_t sel = (g & 1) ? 0x5342u : 0x5140u;
     const __half2 k1024 = __float2half2_rn(1024.0f);
     const __half2 dd = u2h2(__byte_perm(hdr.x, 0, 0x1010)), mm = u2h2(__byte_perm(hdr.x, 0, 0x3232) ^ 0x80008000u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t scw = i < 2 ? sc_lo : sc_hi, mw = i < 2 ? m_lo : m_hi;
-        const uint32_t sel = (i & 1) ? 0x5342u : 0x5140u;
-        S[i] = h22u(__hmul2(dd, __hsub2(u2h2(__byte_perm(scw, 0x64646464u, sel)), k1024)));
-        NZ[i] = h22u(__hmul2(mm, __hsub2(u2h2(__byte_perm(mw, 0x64646464u, sel)), k1024)));
-    }
-}
-
-// gate/up, Q4_K: thread (row, h) dequantises half h of row `row` of K-step
-// `sub` of the raw block column (16 quant bytes: 16 low-nibble weights of
-// sub-block 2 sub and 16 high-nibble weights of sub-block 2 sub + 1) into the
-// swizzled fp16 A tile, with the block's scales decoded beforehand.
-__device__ __forceinline__ void dequant_gu_q4k(const uint8_t *raw, uint32_t a_tile, int row, int h, int sub,
-                                               const uint32_t (&S)[4], const uint32_t (&NZ)[4])
-{
-    const uint8_t *rr = raw + row * 144;
-    const uint4 q = *reinterpret_cast<const uint4 *>(rr + 16 + 32 * sub + 16 * h);
-    // sub is a runtime value: select, so that S and NZ stay in registers
-    const uint32_t sp = sub == 0 ? S[0] : sub == 1 ? S[1] : sub == 2 ? S[2] : S[3];
-    const uint32_t np = sub == 0 ? NZ[0] : sub == 1 ? NZ[1] : sub == 2 ? NZ[2] : NZ[3];
-    const __half2 S_lo = __low2half2(u2h2(sp)), S_hi = __high2half2(u2h2(sp));
-    const __half2 NZ_lo = __low2half2(u2h2(np)), NZ_hi = __high2half2(u2h2(np));
-    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        __half2 l0, l1, h0, h1, l2, l3, h2, h3;
-        nibbles_to_q(words[2 * p], l0, l1, h0, h1);
-        nibbles_to_q(words[2 * p + 1], l2, l3, h2, h3);
-        st_shared_v4(a_tile + sw128_off(row, 2 * h + p), h22u(__hfma2(l0, S_lo, NZ_lo)), h22u(__hfma2(l1, S_lo, NZ_lo)),
-                     h22u(__hfma2(l2, S_lo, NZ_lo)), h22u(__hfma2(l3, S_lo, NZ_lo)));
-        st_shared_v4(a_tile + sw128_off(row, 4 + 2 * h + p), h22u(__hfma2(h0, S_hi, NZ_hi)),
-                     h22u(__hfma2(h1, S_hi, NZ_hi)), h22u(__hfma2(h2, S_hi, NZ_hi)), h22u(__hfma2(h3, S_hi, NZ_hi)));
-    }
+    S = __hmul2(dd, __hsub2(u2h2(__byte_perm(scw, 0x64646464u, sel)), k1024));
+    NZ = __hmul2(mm, __hsub2(u2h2(__byte_perm(mw, 0x64646464u, sel)), k1024));
 }
 
 // int8 pair (two bytes of a 16-bit word) -> exact fp16 pair
@@ -205,139 +174,205 @@ __device__ __forceinline__ __half2 i8pair_to_h2(uint32_t pair16)
     return __hsub2(u2h2(p | 0x64006400u), __float2half2_rn(1152.0f));                  // 1024 + q + 128 - 1152
 }
 
-// gate/up, Q8_0: thread (row, blk), K-step s: block blk of the two 34-byte
-// blocks at offset (68 s) mod 16 of the 80-byte raw row.
-__device__ __forceinline__ void dequant_gu_q80(const uint8_t *raw, uint32_t a_tile, int row, int blk, int s)
+// gate/up, Q4_K, one 128-wide K stage: thread (row, half h) turns group g of
+// the row's super-block (32 quant bytes at q: 32 weights of sub-block 2g in
+// the low nibbles, 32 of sub-block 2g + 1 in the high ones) into 64 fp16 A
+// values, written to tensor-memory columns `taddr` + 0..31 of its lane (K
+// order: low nibbles, then high nibbles).  hdr: the block's 16-byte header.
+__device__ __forceinline__ void dequant_gu_q4k_tmem(const uint8_t *hdr_p, const uint8_t *q, int g, uint32_t taddr)
 {
-    const uint8_t *rr = raw + row * 80 + ((68 * s) & 15);
-    const uint16_t *r16 = reinterpret_cast<const uint16_t *>(rr);   // offset is a multiple of 4
-    {
-        const __half2 D = __half2half2(__ushort_as_half(r16[17 * blk]));
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(hdr_p);
+    const uint4 qa = *reinterpret_cast<const uint4 *>(q);
+    const uint4 qb = *reinterpret_cast<const uint4 *>(q + 16);
+    __half2 S, NZ;
+    q4k_pair_scales_h(hdr, g, S, NZ);
+    const __half2 S_lo = __low2half2(S), S_hi = __high2half2(S);
+    const __half2 NZ_lo = __low2half2(NZ), NZ_hi = __high2half2(NZ);
+    const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    uint32_t lo[16], hi[16];
 #pragma unroll
-        for (int cq = 0; cq < 4; ++cq) {          // 4 chunks of 8 weights per block
-            uint32_t o[4];
+    for (int i = 0; i < 8; ++i) {
+        __half2 l01, l23, h01, h23;
+        nibbles_to_q(words[i], l01, l23, h01, h23);
+        lo[2 * i] = h22u(__hfma2(l01, S_lo, NZ_lo));
+        lo[2 * i + 1] = h22u(__hfma2(l23, S_lo, NZ_lo));
+        hi[2 * i] = h22u(__hfma2(h01, S_hi, NZ_hi));
+        hi[2 * i + 1] = h22u(__hfma2(h23, S_hi, NZ_hi));
+    }
+    tmem_st16(taddr, lo);
+    tmem_st16(taddr + 16, hi);
+}
+
+// gate/up, Q8_0, one 128-wide K stage: thread (row, half h) turns blocks 2h and
+// 2h + 1 of the stage's four into 64 fp16 A values (tensor-memory columns
+// `taddr` + 0..31).  rr: the row's 144-byte window holding the stage's 136
+// bytes at offset o (0 or 8).
+__device__ __forceinline__ void dequant_gu_q80_tmem(const uint8_t *rr, int o, int h, uint32_t taddr)
+{
+    const uint16_t *r16 = reinterpret_cast<const uint16_t *>(rr + o);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) o[i] = h22u(__hmul2(i8pair_to_h2(r16[17 * blk + 1 + 4 * cq + i]), D));
-            st_shared_v4(a_tile + sw128_off(row, 4 * blk + cq), o[0], o[1], o[2], o[3]);
-        }
+    for (int bi = 0; bi < 2; ++bi) {
+        const int b = 2 * h + bi;
+        const __half2 D = __half2half2(__ushort_as_half(r16[17 * b]));
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = h22u(__hmul2(i8pair_to_h2(r16[17 * b + 1 + i]), D));
+        tmem_st16(taddr + 16 * bi, v);
     }
 }
 
+// Byte offset of element (m, k) in an MN-major 128-byte-swizzled tile of 128
+// M x 64 K fp16: atoms of 64 M x 8 K, 1024 bytes apart along M and 2048 along K.
+__device__ __forceinline__ uint32_t mn_off(uint32_t m, uint32_t k)
+{
+    return ((k >> 3) << 11) + ((m >> 6) << 10) + ((k & 7) << 7) + ((((m & 63) >> 3) ^ (k & 7)) << 4) + ((m & 7) << 1);
+}
+
 // down, Q4_K: A[h][f] = Wd[f][h0 + h] for the tile's 128 hidden columns and
-// the K-step's 64 ff rows.  Raw row i (f = 64 s + i) holds the block header
-// and the 64 quant bytes of this half block (80 bytes).  Item = (row, group of
-// 8 quant bytes): 8 low-nibble weights at h = 64 c + l .. +7 and 8 high-nibble
-// weights at h + 32, stored as 16-bit values into their transposed places.
+// the stage's 64 ff rows, stored MN-major (h contiguous), so eight consecutive
+// weights of a raw row land in one 16-byte chunk.  Raw row i (f = 64 s + i)
+// is the 144-byte block holding the tile's columns; `half` selects its 64
+// quant bytes: group c (32 bytes) holds 32 low-nibble weights at h = 64 c + l
+// and 32 high-nibble ones at h = 64 c + 32 + l.  Thread (row, c, part) takes
+// 32 / P bytes of group c (P = NT / 128 parts), so one scale decode serves all
+// its weights; lanes take consecutive rows (conflict-free stores).
+template <int NT>
 __device__ __forceinline__ void dequant_dn_q4k(const uint8_t *raw, uint32_t a_tile, int dt, int half)
 {
+    constexpr int P = NT / 128, NB = 32 / P;            // parts per group, bytes per thread
+    const int row = dt & 63, c = (dt >> 6) / P, part = (dt >> 6) % P;
+    const uint8_t *rr = raw + row * 144;
+    __half2 S, NZ;
+    q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(rr), 2 * half + c, S, NZ);
+    const __half2 S_lo = __low2half2(S), S_hi = __high2half2(S);
+    const __half2 NZ_lo = __low2half2(NZ), NZ_hi = __high2half2(NZ);
+    const uint8_t *q = rr + 16 + 64 * half + 32 * c + NB * part;
 #pragma unroll
-    for (int it4 = 0; it4 < 512 / kDeqThreads; ++it4) {
-        const int it = dt + kDeqThreads * it4;
-        const int row = it & 63, bg = it >> 6;           // bg 0..7
-        const uint8_t *rr = raw + row * 80;
-        const uint4 hdr = *reinterpret_cast<const uint4 *>(rr);
-        const int c_loc = bg >> 2, l0 = (8 * bg) & 31;
-        const int jsb = 2 * (2 * half + c_loc);
-        __half s_lo, nz_lo, s_hi, nz_hi;
-        q4k_subblock_scales(hdr, jsb, s_lo, nz_lo);
-        q4k_subblock_scales(hdr, jsb + 1, s_hi, nz_hi);
-        const __half2 S_lo = __half2half2(s_lo), NZ_lo = __half2half2(nz_lo);
-        const __half2 S_hi = __half2half2(s_hi), NZ_hi = __half2half2(nz_hi);
-        const uint2 q8 = *reinterpret_cast<const uint2 *>(rr + 16 + 8 * bg);
-        const int h_lo = 64 * c_loc + l0;
-        const uint32_t kchunk = (uint32_t)row >> 3, kbyte = ((uint32_t)row & 7) * 2;
+    for (int u = 0; u < NB / 16; ++u) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(q + 16 * u);
+        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int wsel = 0; wsel < 2; ++wsel) {
-            __half2 l01, l23, h01, h23;
-            nibbles_to_q(wsel ? q8.y : q8.x, l01, l23, h01, h23);
-            const __half2 vl01 = __hfma2(l01, S_lo, NZ_lo), vl23 = __hfma2(l23, S_lo, NZ_lo);
-            const __half2 vh01 = __hfma2(h01, S_hi, NZ_hi), vh23 = __hfma2(h23, S_hi, NZ_hi);
-            const int hb = h_lo + 4 * wsel;
-            st_shared_u16(a_tile + sw128_off(hb + 0, kchunk) + kbyte, __half_as_ushort(__low2half(vl01)));
-            st_shared_u16(a_tile + sw128_off(hb + 1, kchunk) + kbyte, __half_as_ushort(__high2half(vl01)));
-            st_shared_u16(a_tile + sw128_off(hb + 2, kchunk) + kbyte, __half_as_ushort(__low2half(vl23)));
-            st_shared_u16(a_tile + sw128_off(hb + 3, kchunk) + kbyte, __half_as_ushort(__high2half(vl23)));
-            st_shared_u16(a_tile + sw128_off(hb + 32, kchunk) + kbyte, __half_as_ushort(__low2half(vh01)));
-            st_shared_u16(a_tile + sw128_off(hb + 33, kchunk) + kbyte, __half_as_ushort(__high2half(vh01)));
-            st_shared_u16(a_tile + sw128_off(hb + 34, kchunk) + kbyte, __half_as_ushort(__low2half(vh23)));
-            st_shared_u16(a_tile + sw128_off(hb + 35, kchunk) + kbyte, __half_as_ushort(__high2half(vh23)));
+        for (int p = 0; p < 2; ++p) {                   // 8 bytes: 8 low and 8 high weights
+            __half2 l01, l23, h01, h23, l45, l67, h45, h67;
+            nibbles_to_q(words[2 * p], l01, l23, h01, h23);
+            nibbles_to_q(words[2 * p + 1], l45, l67, h45, h67);
+            const int h_lo = 64 * c + NB * part + 16 * u + 8 * p;
+            st_shared_v4(a_tile + mn_off(h_lo, row), h22u(__hfma2(l01, S_lo, NZ_lo)), h22u(__hfma2(l23, S_lo, NZ_lo)),
+                         h22u(__hfma2(l45, S_lo, NZ_lo)), h22u(__hfma2(l67, S_lo, NZ_lo)));
+            st_shared_v4(a_tile + mn_off(h_lo + 32, row), h22u(__hfma2(h01, S_hi, NZ_hi)),
+                         h22u(__hfma2(h23, S_hi, NZ_hi)), h22u(__hfma2(h45, S_hi, NZ_hi)),
+                         h22u(__hfma2(h67, S_hi, NZ_hi)));
         }
     }
 }
 
 // down, Q8_0: raw row i (f = 64 s + i) is a 144-byte window holding the 4
-// blocks of this tile's 128 hidden columns at offset o8 (0 or 8).
+// blocks of this tile's 128 hidden columns at offset o8 (0 or 8); item
+// (row, group g of 8 hidden columns) -> one 16-byte chunk of the MN-major tile.
+template <int NT>
 __device__ __forceinline__ void dequant_dn_q80(const uint8_t *raw, uint32_t a_tile, int dt, int o8)
 {
 #pragma unroll
-    for (int it8 = 0; it8 < 1024 / kDeqThreads; ++it8) {
-        const int it = dt + kDeqThreads * it8;
+    for (int it8 = 0; it8 < 1024 / NT; ++it8) {
+        const int it = dt + NT * it8;
         const int row = it & 63, g = it >> 6;            // g 0..15: 8 columns each
         const int b = g >> 2, hh0 = 8 * (g & 3);
         const uint16_t *blk = reinterpret_cast<const uint16_t *>(raw + row * 144 + o8 + 34 * b);
         const __half2 D = __half2half2(__ushort_as_half(blk[0]));
-        const uint32_t kchunk = (uint32_t)row >> 3, kbyte = ((uint32_t)row & 7) * 2;
+        uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __half2 v = __hmul2(i8pair_to_h2(blk[1 + hh0 / 2 + i]), D);
-            const int h = 32 * b + hh0 + 2 * i;
-            st_shared_u16(a_tile + sw128_off(h, kchunk) + kbyte, __half_as_ushort(__low2half(v)));
-            st_shared_u16(a_tile + sw128_off(h + 1, kchunk) + kbyte, __half_as_ushort(__high2half(v)));
-        }
+        for (int i = 0; i < 4; ++i) o[i] = h22u(__hmul2(i8pair_to_h2(blk[1 + hh0 / 2 + i]), D));
+        st_shared_v4(a_tile + mn_off(32 * b + hh0, row), o[0], o[1], o[2], o[3]);
     }
 }
 
 // ---------------------------------------------------------------- the kernel
 
+// K-steps (64 wide) per pipeline stage: gate/up stages are 128 wide (8 MMAs
+// per hand-off), down stages 64 (its K, FF, is short).
+template <int OP>
+__host__ __device__ constexpr int kstep_per_stage()
+{
+    return OP == kOpGateUp ? 2 : 1;
+}
+
+// Raw bytes of one raw-ring slot, filled by 2-D tensor copies of 144-byte x
+// 64-row boxes of the expert blob: gate/up 64 gate rows then the 64 up rows
+// (Q4_K: a whole block column, the raw of two stages; Q8_0: a 16-byte aligned
+// window over one stage's 136 bytes); down 64 ff rows (Q4_K: the block
+// holding the tile's 128 hidden columns; Q8_0: a window over its 4 blocks).
 template <int OP, int FMT>
 __host__ __device__ constexpr int raw_stage_bytes()
 {
-    return OP == kOpGateUp ? (FMT == kWQ4K ? 128 * 144 : 128 * 80) : (FMT == kWQ4K ? 64 * 80 : 64 * 144);
+    return OP == kOpGateUp ? 128 * 144 : 64 * 144;
 }
 
-// K-steps covered by one raw stage: a whole Q4_K block column (4 K-steps) for
-// gate/up, one K-step otherwise.
+// pipeline stages served by one raw slot
 template <int OP, int FMT>
-__host__ __device__ constexpr int ksteps_per_raw()
+__host__ __device__ constexpr int stages_per_raw()
 {
-    return (OP == kOpGateUp && FMT == kWQ4K) ? 4 : 1;
+    return (OP == kOpGateUp && FMT == kWQ4K) ? 2 : 1;
 }
 
-template <int OP, int FMT, int NMAX, int SA, int SB, int RAW>
+template <int OP, int FMT, int NMAX, int S, int RAW>
 struct GemmCfg {
+    static constexpr int KS = kstep_per_stage<OP>();
     static constexpr int kRawStage = raw_stage_bytes<OP, FMT>();
     static constexpr int RS = RAW / kRawStage;           // raw ring depth
-    static constexpr int kBBytes = NMAX * 128;
+    static constexpr int SPR = stages_per_raw<OP, FMT>();
+    static constexpr int kBSub = NMAX * 128;             // one 64-wide K sub-tile of token rows
+    static constexpr int kBStage = KS * kBSub;
+    static constexpr int kAStage = OP == kOpGateUp ? 0 : kABytes;   // down: A in shared memory
     static constexpr int kOffA = 0;
-    static constexpr int kOffB = kOffA + SA * kABytes;
-    static constexpr int kOffRaw = kOffB + SB * kBBytes;
+    static constexpr int kOffB = kOffA + S * kAStage;
+    static constexpr int kOffRaw = kOffB + S * kBStage;
     static constexpr int kOffBar = kOffRaw + ((RS * kRawStage + 1023) & ~1023);
-    static constexpr int kNumBars = 2 * RS + 2 * SA + 2 * SB + 6;
-    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr int kNumBars = 2 * S + 2 * RS + 6;
+    static constexpr int kOffTmap = (kOffBar + 8 * kNumBars + 127) & ~127;   // 128-byte tensor map
+    static constexpr int kOffMisc = kOffTmap + 128;
     static constexpr int kOffMeta = kOffMisc + 16;              // [2][NMAX] token, weight, slot
     static constexpr int kBytes = kOffMeta + 2 * NMAX * 12 + 1024;
+    // tensor memory: two accumulators of NMAX columns; gate/up adds S A stages
+    // of 64 columns (128 rows x 128 K fp16)
+    static constexpr int kColA = 2 * NMAX;
+    static constexpr int kCols = OP == kOpGateUp ? 512 : (2 * NMAX < 32 ? 32 : 2 * NMAX);
     static_assert(RS >= 2, "raw ring too shallow");
-    static_assert(kBytes <= 232448, "shared memory budget");
+    static_assert(kBytes <= 227 * 1024, "shared memory budget");
+    static_assert(OP != kOpGateUp || kColA + 64 * S <= 512, "tensor memory budget");
+    static_assert((kCols & (kCols - 1)) == 0, "tensor-memory allocations are powers of two");
 };
 
-template <int OP, int FMT, int NMAX, int SA, int SB, int RAW>
-__global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
+// Bounded wait of a whole warp: every lane polls, and the lanes agree on the
+// outcome (false if any lane saw an abort or a timeout).
+__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, volatile int *abort, uint32_t *status)
 {
-    using C = GemmCfg<OP, FMT, NMAX, SA, SB, RAW>;
+    const bool ok = wait_bar(bar, parity, abort, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int OP, int FMT, int NMAX, int S, int RAW, int EW>
+__global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const __grid_constant__ CUtensorMap tmap_b,
+                                                          const __grid_constant__ CUtensorMap tmap_w)
+{
+    using C = GemmCfg<OP, FMT, NMAX, S, RAW>;
     constexpr int RS = C::RS;
-    constexpr int KPR = ksteps_per_raw<OP, FMT>();
+    constexpr int KS = C::KS;
+    constexpr int SPR = C::SPR;
+    static_assert(EW == 4 || (EW == 8 && OP == kOpDown), "8 epilogue warps: down only");
+    constexpr int kDeq = deq_threads<EW>(), kEpi = 32 * EW;
+    constexpr int kEG = kEpi / 128;          // epilogue groups (alternate 16-column chunks)
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_dyn + 1023) & ~(uintptr_t)1023);
     const uint32_t sA = smem_addr(smem + C::kOffA), sB = smem_addr(smem + C::kOffB);
     uint8_t *raw_base = smem + C::kOffRaw;
     const uint32_t bar0 = smem_addr(smem + C::kOffBar);
-    auto full_raw = [&](int i) { return bar0 + 8 * i; };
-    auto empty_raw = [&](int i) { return bar0 + 8 * (RS + i); };
-    auto full_a = [&](int i) { return bar0 + 8 * (2 * RS + i); };
-    auto empty_a = [&](int i) { return bar0 + 8 * (2 * RS + SA + i); };
-    auto full_b = [&](int i) { return bar0 + 8 * (2 * RS + 2 * SA + i); };
-    auto empty_b = [&](int i) { return bar0 + 8 * (2 * RS + 2 * SA + SB + i); };
-    const uint32_t bx = bar0 + 8 * (2 * RS + 2 * SA + 2 * SB);
+    // stage ring: `full` completes when the stage's A (dequantised weights) and
+    // B (token rows) are in place, `empty` when its MMAs have read them
+    auto full = [&](int i) { return bar0 + 8 * i; };
+    auto empty = [&](int i) { return bar0 + 8 * (S + i); };
+    auto full_raw = [&](int i) { return bar0 + 8 * (2 * S + i); };
+    auto empty_raw = [&](int i) { return bar0 + 8 * (2 * S + RS + i); };
+    const uint32_t bx = bar0 + 8 * (2 * S + 2 * RS);
     auto acc_full = [&](int i) { return bx + 8 * i; };
     auto acc_empty = [&](int i) { return bx + 8 * (2 + i); };
     const uint32_t final_bar = bx + 8 * 4, epi_bar = bx + 8 * 5;
@@ -350,30 +385,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full(i), kDeq + KS);          // dequantisers + one expect_tx per B sub-tile
+            mbar_init(empty(i), 1);
+        }
         for (int i = 0; i < RS; ++i) {
-            mbar_init(full_raw(i), 32);          // the 32 lanes of the raw-byte warp
-            mbar_init(empty_raw(i), kDeqThreads);
-        }
-        for (int i = 0; i < SA; ++i) {
-            mbar_init(full_a(i), kDeqThreads);
-            mbar_init(empty_a(i), 1);
-        }
-        for (int i = 0; i < SB; ++i) {
-            mbar_init(full_b(i), 64);
-            mbar_init(empty_b(i), 1);
+            mbar_init(full_raw(i), 1);              // the raw copies' expect_tx
+            mbar_init(empty_raw(i), kDeq);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full(i), 1);
-            mbar_init(acc_empty(i), 128);
+            mbar_init(acc_empty(i), kEpi);
         }
         mbar_init(final_bar, 1);
-        mbar_init(epi_bar, 128);
+        mbar_init(epi_bar, kEpi);
         *abort_flag = 0;
         *last_flag = 0;
         fence_mbar_init();
     }
     if (warp == 4) {
-        tmem_alloc(smem_addr(tmem_slot), 2 * NMAX);
+        tmem_alloc(smem_addr(tmem_slot), C::kCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -382,11 +413,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
     const uint32_t tmem_base = *tmem_slot;
     const int n_tiles = (int)*g.n_tiles;
 
-    if (warp < 4) {
+    if (warp < 4 || (kEG == 2 && warp >= 12)) {
         // ------------------------------------------------------------ epilogue
         uint32_t t_it = 0, epi_it = 0;
-        const int et = threadIdx.x;          // 0..127 = tensor-memory lane
-        auto epi_sync = [&]() -> bool {      // the 4 epilogue warps only, bounded
+        const int wq = warp & 3;             // tensor-memory lane quarter of this warp
+        const int et = 32 * wq + lane;       // 0..127 = tensor-memory lane (row of the tile)
+        const int eg = warp < 4 ? 0 : 1;     // epilogue group
+        const int ei = eg * 128 + et;        // 0 .. kEpi-1
+        auto epi_sync = [&]() -> bool {      // the epilogue warps only, bounded
             mbar_arrive(epi_bar);
             return wait_bar(epi_bar, (epi_it++) & 1, abort_flag, g.status);
         };
@@ -394,13 +428,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<OP, FMT>(g, tile);
             if (!ti.blob) {
-                if (et == 0) set_status(g.status, MOE_ERR_DEVICE_FAULT);
+                if (ei == 0) set_status(g.status, MOE_ERR_DEVICE_FAULT);
                 continue;
             }
             const int acc = t_it & 1;
             if (OP == kOpDown) {
                 // column metadata: token, routing weight and slot of each column
-                for (int j = et; j < ti.n; j += 128) {
+                for (int j = ei; j < ti.n; j += kEpi) {
                     int tok, slot;
                     float wt;
                     if (FMT == kWQ4K) {
@@ -420,20 +454,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
             if (!(ok = wait_bar(acc_full(acc), (t_it >> 1) & 1, abort_flag, g.status))) break;
             tc_fence_after();
             const int ffop = FMT == kWQ4K ? g.FF : g.SFF;
-            for (int cc = 0; cc < ti.nmma / 16; ++cc) {
+            for (int cc = eg; cc < ti.nmma / 16; cc += kEG) {
                 uint32_t v[16];
-                tmem_ld16(tmem_base + ((uint32_t)(32 * warp) << 16) + acc * NMAX + cc * 16, v);
+                tmem_ld16(tmem_base + ((uint32_t)(32 * wq) << 16) + acc * NMAX + cc * 16, v);
                 tmem_wait_ld();
                 if (OP == kOpGateUp) {
                     const int f = ti.m * 64 + (et >> 1);
                     if (g.splits == 1) {
+                        // lanes 2i (gate row) and 2i+1 (up row) of ff index f split the
+                        // columns: the even lane takes the even ones, the odd lane the odd
+                        // ones, after one exchange per column pair
+                        const int par = lane & 1;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float val = __uint_as_float(v[i]);
-                            const float other = __shfl_xor_sync(0xffffffffu, val, 1);
-                            const int j = cc * 16 + i;
-                            if (!(lane & 1) && j < ti.n) {
-                                const float a = val / (1.0f + expf(-val)) * other;
+                        for (int pp = 0; pp < 8; ++pp) {
+                            const float own = __uint_as_float(v[2 * pp + par]);
+                            const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(v[2 * pp + 1 - par]), 1);
+                            const float gg = par ? recv : own, uu = par ? own : recv;
+                            const int j = cc * 16 + 2 * pp + par;
+                            if (j < ti.n) {
+                                const float a = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
                                 __half *dst = FMT == kWQ4K ? g.act16 + (int64_t)(ti.bb + ti.n0 + j) * ffop + f
                                                            : g.sh_act16 + (int64_t)(ti.n0 + j) * ffop + f;
                                 *dst = __float2half_rn(a);
@@ -451,8 +490,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
                     }
                 } else {
                     // 4x4 transposes within lane quads: lane (q, r) ends with the
-                    // values of hidden rows 4q..4q+3 for column 4b + r
-                    const int hq = ti.m * 128 + 32 * warp + (lane & ~3);
+                    // values of hidden rows 4q..4q+3 for column 4b + r, added as one
+                    // 16-byte vector
+                    const int hq = ti.m * 128 + 32 * wq + (lane & ~3);
                     const int r = lane & 3;
 #pragma unroll
                     for (int b = 0; b < 4; ++b) {
@@ -501,7 +541,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
                             const float uu = ld_cg_f32(g.gu + (int64_t)rowi * 2 * ffop + ffop + f);
                             __half *dst = FMT == kWQ4K ? g.act16 + (int64_t)rowi * ffop + f
                                                        : g.sh_act16 + (int64_t)rowi * ffop + f;
-                            *dst = __float2half_rn(gg / (1.0f + expf(-gg)) * uu);
+                            *dst = __float2half_rn(__fdividef(gg, 1.0f + __expf(-gg)) * uu);
                         }
                     }
                     if (et == 0) g.split_cnt[tile / g.splits] = 0;
@@ -511,36 +551,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
         }
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
-            uint32_t sa_it = 0, sb_it = 0, t_it = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-                const TileInfo ti = tile_info<OP, FMT>(g, tile);
-                if (!ti.blob) continue;
-                const int acc = t_it & 1;
-                if (!(ok = wait_bar(acc_empty(acc), ((t_it >> 1) & 1) ^ 1, abort_flag, g.status))) break;
+        // the whole warp walks the stages (waits are warp-wide); lane 0 issues
+        // every MMA and every commit (a commit tracks the issuing thread's MMAs)
+        uint32_t st_it = 0, t_it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+            const TileInfo ti = tile_info<OP, FMT>(g, tile);
+            if (!ti.blob) continue;
+            const int acc = t_it & 1;
+            if (!(ok = warp_wait_bar(acc_empty(acc), ((t_it >> 1) & 1) ^ 1, abort_flag, g.status))) break;
+            tc_fence_after();
+            const uint32_t idesc = idesc_f16_f32(128, ti.nmma) | (OP == kOpDown ? kIdescAMnMajor : 0u);
+            const uint32_t d_tmem = tmem_base + acc * NMAX;
+            const int nst = (ti.ksteps + KS - 1) / KS;
+            for (int st = 0; st < nst; ++st, ++st_it) {
+                const int slot = st_it % S;
+                if (!(ok = warp_wait_bar(full(slot), (st_it / S) & 1, abort_flag, g.status))) break;
                 tc_fence_after();
-                const uint32_t idesc = idesc_f16_f32(128, ti.nmma);
-                const uint32_t d_tmem = tmem_base + acc * NMAX;
-                for (int s = 0; s < ti.ksteps; ++s, ++sa_it, ++sb_it) {
-                    const int slot_a = sa_it % SA, slot_b = sb_it % SB;
-                    if (!(ok = wait_bar(full_a(slot_a), (sa_it / SA) & 1, abort_flag, g.status))) break;
-                    if (!(ok = wait_bar(full_b(slot_b), (sb_it / SB) & 1, abort_flag, g.status))) break;
-                    fence_proxy_async();   // the token rows were written by cp.async (generic proxy)
-                    tc_fence_after();
-                    const uint32_t a0 = sA + slot_a * kABytes, b0 = sB + slot_b * C::kBBytes;
+                // straight-line issue: no branch between the MMAs of a stage (the
+                // issue rate halves otherwise); gate/up stages always hold 8 K16 steps
+                // (tiles cover whole Q4_K block columns), down stages 4
+                if (lane == 0) {
+                    const uint64_t bdesc0 = sdesc_kmajor_sw128(sB + slot * C::kBStage);
+                    const uint32_t acc0 = st != 0;
+                    if (OP == kOpGateUp) {
+                        const uint32_t a0 = tmem_base + C::kColA + 64 * slot;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_f16(d_tmem, sdesc_kmajor_sw128(a0 + 32 * kk), sdesc_kmajor_sw128(b0 + 32 * kk), idesc,
-                                (s | kk) != 0);
-                    mma_commit(empty_a(slot_a));
-                    mma_commit(empty_b(slot_b));
+                        for (int kk = 0; kk < 4 * KS; ++kk)
+                            mma_f16_ta(d_tmem, a0 + 8 * kk,
+                                       bdesc0 + (uint64_t)(((kk >> 2) * C::kBSub + 32 * (kk & 3)) >> 4), idesc,
+                                       kk == 0 ? acc0 : 1u);
+                    } else {
+                        const uint64_t adesc0 = sdesc_mnmajor_sw128(sA + slot * C::kAStage, 1024, 2048);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f16(d_tmem, adesc0 + (uint64_t)((4096 * kk) >> 4),
+                                    bdesc0 + (uint64_t)((32 * kk) >> 4), idesc, kk == 0 ? acc0 : 1u);
+                    }
+                    mma_commit(empty(slot));
                 }
-                if (!ok) break;
-                mma_commit(acc_full(acc));
-                ++t_it;
+                __syncwarp();
             }
-            // every issued MMA must be complete before the tensor memory is freed
+            if (!ok) break;
+            if (lane == 0) mma_commit(acc_full(acc));
+            __syncwarp();
+            ++t_it;
+        }
+        // every issued MMA must be complete before the tensor memory is freed
+        if (lane == 0) {
             mma_commit(final_bar);
             const long long t0 = clock64();
             while (!mbar_try_wait(final_bar, 0) && clock64() - t0 < kWaitCycles) {
@@ -549,141 +607,154 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
         __syncwarp();
     } else if (warp == 5) {
         // ------------------------------------------------------------ raw weight bytes
+        // 2-D tensor copies of 144-byte x 64-row boxes of the blob, issued by
+        // lane 0.  Q8_0 (the shared expert) copies through the launch's map;
+        // Q4_K through a per-CTA map whose global address is rewritten for
+        // each new expert (two global slots used in turn: a slot is reused only
+        // once the copies that named it have landed).
         uint32_t rs_it = 0;
-        const int H = g.H;
-        const int64_t rb = FMT == kWQ4K ? (int64_t)(H / 256) * 144 : (int64_t)(H / 32) * 34;   // row bytes
         const int ffop = FMT == kWQ4K ? g.FF : g.SFF;
+        const void *tm = &tmap_w;
+        const uint32_t s_tmap = smem_addr(smem + C::kOffTmap);
+        int cur_e = -2, nmaps = 0;
+        uint32_t last_rs0 = 0, last_rs1 = 0;   // raw index after the last copy that named slot 0 / 1
+        if (FMT == kWQ4K) {
+            reinterpret_cast<uint32_t *>(smem + C::kOffTmap)[lane] = reinterpret_cast<const uint32_t *>(&tmap_w)[lane];
+            __syncwarp();
+        }
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<OP, FMT>(g, tile);
             if (!ti.blob) continue;
-            const int nraw = ti.ksteps / KPR, r0 = ti.k0 / KPR;
-            for (int rr = 0; rr < nraw; ++rr, ++rs_it) {
-                const int r = r0 + rr;                    // raw stage (block column / K-step) index
-                const int slot = rs_it % RS;
-                if (!(ok = wait_bar(empty_raw(slot), ((rs_it / RS) & 1) ^ 1, abort_flag, g.status))) break;
-                uint8_t *dst0 = raw_base + slot * C::kRawStage;
-                // 16-byte asynchronous copies; each lane's completion arrives on full_raw
-                // consecutive lanes take consecutive 16-byte pieces (coalesced requests);
-                // piece p = lane + 32 j is (row p / P, piece p % P), stepped incrementally
-                if (OP == kOpGateUp) {
-                    // 128 rows: row 2i = gate f0+i, row 2i+1 = up f0+i
-                    constexpr int kPieces = FMT == kWQ4K ? 9 : 5;           // 144 or 80 bytes per row
-                    int i = lane / kPieces, pc = lane % kPieces;
-                    const int64_t col = FMT == kWQ4K ? (int64_t)r * 144 : (int64_t)((68 * r) & ~15);
-                    const uint8_t *gbase = ti.blob + (int64_t)ti.m * 64 * rb + col;
-                    const uint8_t *ubase = gbase + (int64_t)ffop * rb;
-                    for (int j = 0; j < (128 * kPieces) / 32; ++j) {
-                        const uint8_t *src = ((i & 1) ? ubase : gbase) + (int64_t)(i >> 1) * rb + pc * 16;
-                        cp_async16(smem_addr(dst0 + i * (16 * kPieces) + pc * 16), src);
-                        i += 32 / kPieces;
-                        pc += 32 % kPieces;
-                        if (pc >= kPieces) {
-                            pc -= kPieces;
-                            ++i;
-                        }
-                    }
-                } else {
-                    // 64 ff rows of Wd for this K-step, this tile's 128 hidden columns
-                    const int h0 = ti.m * 128;
-                    constexpr int kPieces = FMT == kWQ4K ? 5 : 9;           // 16 + 64 or 144 bytes per row
-                    const uint8_t *base = ti.blob + ((int64_t)2 * ffop + 64 * r) * rb;
-                    const int64_t blk = FMT == kWQ4K ? (int64_t)(h0 / 256) * 144 : (int64_t)((34 * (h0 / 32)) & ~15);
-                    const int qoff = 16 + 64 * ((h0 / 128) & 1);
-                    int i = lane / kPieces, pc = lane % kPieces;
-                    for (int j = 0; j < (64 * kPieces) / 32; ++j) {
-                        const uint8_t *rowp = base + (int64_t)i * rb + blk;
-                        const uint8_t *src = FMT == kWQ4K ? (pc == 0 ? rowp : rowp + qoff + (pc - 1) * 16) : rowp + pc * 16;
-                        cp_async16(smem_addr(dst0 + i * (16 * kPieces) + pc * 16), src);
-                        i += 32 / kPieces;
-                        pc += 32 % kPieces;
-                        if (pc >= kPieces) {
-                            pc -= kPieces;
-                            ++i;
-                        }
+            if (FMT == kWQ4K && ti.e != cur_e) {
+                const int ms = nmaps & 1;
+                // the copies that last named this slot must have landed (a raw slot is
+                // refilled only after it was consumed, which settles every older copy)
+                const uint32_t lr = ms ? last_rs1 : last_rs0;
+                if (nmaps >= 2 && lr > 0 && rs_it < lr - 1 + RS && lane == 0) {
+                    const uint32_t i = lr - 1;
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(full_raw(i % RS), (i / RS) & 1) && clock64() - t0 < kWaitCycles) {
                     }
                 }
-                cp_async_arrive_noinc(full_raw(slot));
+                __syncwarp();
+                CUtensorMap *gslot = g.tmaps + 2 * blockIdx.x + ms;
+                if (lane == 0) tmap_set_addr_smem(s_tmap, ti.blob);
+                __syncwarp();
+                tmap_copy_release(gslot, s_tmap);
+                if (lane == 0) tmap_acquire(gslot);
+                __syncwarp();
+                tm = gslot;
+                cur_e = ti.e;
+                ++nmaps;
+            }
+            const int nrs = ((ti.ksteps + KS - 1) / KS + SPR - 1) / SPR;
+            for (int rsi = 0; rsi < nrs; ++rsi, ++rs_it) {
+                const int slot = rs_it % RS;
+                if (!(ok = warp_wait_bar(empty_raw(slot), ((rs_it / RS) & 1) ^ 1, abort_flag, g.status))) break;
+                if (lane == 0) {
+                    const uint32_t dst0 = smem_addr(raw_base + slot * C::kRawStage);
+                    mbar_arrive_expect_tx(full_raw(slot), C::kRawStage);
+                    if (OP == kOpGateUp) {
+                        const int kst0 = ti.k0 / KS + rsi * SPR;               // first 128-wide K stage
+                        const int x = FMT == kWQ4K ? (kst0 >> 1) * 144 : (136 * kst0) & ~15;
+                        tma_load_2d(dst0, tm, x, ti.m * 64, full_raw(slot));
+                        tma_load_2d(dst0 + 64 * 144, tm, x, ffop + ti.m * 64, full_raw(slot));
+                    } else {
+                        const int h0 = ti.m * 128;
+                        const int x = FMT == kWQ4K ? (h0 / 256) * 144 : (34 * (h0 / 32)) & ~15;
+                        tma_load_2d(dst0, tm, x, 2 * ffop + 64 * (ti.k0 + rsi), full_raw(slot));
+                    }
+                }
+                __syncwarp();
+            }
+            if (FMT == kWQ4K) {
+                if ((nmaps - 1) & 1) last_rs1 = rs_it;
+                else last_rs0 = rs_it;
             }
         }
         // copies still in flight (an early exit) must land before the CTA ends
-        for (uint32_t i = rs_it > (uint32_t)RS ? rs_it - RS : 0; i < rs_it; ++i) {
-            const long long t0 = clock64();
-            while (!mbar_try_wait(full_raw(i % RS), (i / RS) & 1) && clock64() - t0 < kWaitCycles) {
+        if (lane == 0) {
+            for (uint32_t i = rs_it > (uint32_t)RS ? rs_it - RS : 0; i < rs_it; ++i) {
+                const long long t0 = clock64();
+                while (!mbar_try_wait(full_raw(i % RS), (i / RS) & 1) && clock64() - t0 < kWaitCycles) {
+                }
             }
         }
+        __syncwarp();
     } else if (warp < 8) {
         // ------------------------------------------------------------ token rows (B)
-        // thread bt copies 16-byte chunk (bt & 7) of rows j = (bt >> 3) + 8 i;
-        // each thread's copies of a stage arrive on full_b when they land, so
-        // the gatherers run up to SB stages ahead of the MMAs
-        const int bt = threadIdx.x - 192;   // 0..63
-        const int c = bt & 7, r0 = bt >> 3;
-        const __half *srcbase = OP == kOpGateUp ? g.x16 : (FMT == kWQ4K ? g.act16 : g.sh_act16);
-        const int ld = OP == kOpGateUp ? g.H : (FMT == kWQ4K ? g.FF : g.SFF);
-        uint32_t sb_it = 0;
+        // the tile's rows are consecutive (xg and a are in bucket order): one
+        // tensor box of NMAX rows per 64-wide K sub-tile, sub-tile i issued by
+        // lane 0 of warp 6 + i (two issuing warps keep two copies in flight)
+        const int sub = warp - 6;
+        uint32_t st_it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-            const TileInfo ti = tile_info<OP, FMT>(g, tile);
-            if (!ti.blob) continue;
-            int src[NMAX / 8];
-#pragma unroll
-            for (int i = 0; i < NMAX / 8; ++i) {
-                const int j = r0 + 8 * i;
-                src[i] = 0;
-                if (j < ti.n) {
-                    if (OP == kOpGateUp) src[i] = FMT == kWQ4K ? g.assign[ti.bb + ti.n0 + j] / g.k : ti.n0 + j;
-                    else src[i] = FMT == kWQ4K ? ti.bb + ti.n0 + j : ti.n0 + j;
+        if (sub < KS) {
+            for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+                const TileInfo ti = tile_info<OP, FMT>(g, tile);
+                if (!ti.blob) continue;
+                const int row0 = FMT == kWQ4K ? ti.bb + ti.n0 : ti.n0;
+                const int nst = (ti.ksteps + KS - 1) / KS;
+                for (int st = 0; st < nst; ++st, ++st_it) {
+                    const int slot = st_it % S;
+                    if (!(ok = warp_wait_bar(empty(slot), ((st_it / S) & 1) ^ 1, abort_flag, g.status))) break;
+                    if (lane == 0) {
+                        const bool has = st * KS + sub < ti.ksteps;
+                        mbar_arrive_expect_tx(full(slot), has ? (uint32_t)C::kBSub : 0u);
+                        if (has)
+                            tma_load_2d(sB + slot * C::kBStage + sub * C::kBSub, &tmap_b,
+                                        (ti.k0 + st * KS + sub) * 64, row0, full(slot));
+                    }
+                    __syncwarp();
                 }
             }
-            for (int s = 0; s < ti.ksteps; ++s, ++sb_it) {
-                const int slot = sb_it % SB;
-                if (!(ok = wait_bar(empty_b(slot), ((sb_it / SB) & 1) ^ 1, abort_flag, g.status))) break;
-                const uint32_t b_tile = sB + slot * C::kBBytes;
-                const int kcol = (ti.k0 + s) * 64 + c * 8;
-#pragma unroll
-                for (int i = 0; i < NMAX / 8; ++i) {
-                    const int j = r0 + 8 * i;
-                    if (j < ti.n) cp_async16(b_tile + sw128_off(j, c), srcbase + (int64_t)src[i] * ld + kcol);
+            // tensor copies still in flight (an early exit) must land before the
+            // CTA ends; they complete within microseconds, so a short bounded wait
+            if (lane == 0) {
+                for (uint32_t i = st_it > (uint32_t)S ? st_it - S : 0; i < st_it; ++i) {
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(full(i % S), (i / S) & 1) && clock64() - t0 < (1 << 21)) {
+                    }
                 }
-                cp_async_arrive_noinc(full_b(slot));
             }
+            __syncwarp();
         }
-        cp_async_wait<0>();   // nothing may still be writing shared memory when the CTA ends
     } else {
         // ------------------------------------------------------------ dequantisation (A)
-        const int dt = threadIdx.x - 256;   // 0..255
-        uint32_t sa_it = 0, rs_it = 0;
-        uint32_t S[4], NZ[4];
+        const int dt = threadIdx.x - 256;   // 0 .. kDeq-1
+        // gate/up: thread (row, half) with row = tensor-memory lane 32 (warp % 4) + lane
+        const int q_lane = 32 * (warp & 3), row = q_lane + lane, hh = (warp - 8) >> 2;
+        uint32_t st_it = 0, rs_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<OP, FMT>(g, tile);
             if (!ti.blob) continue;
-            for (int s = 0; s < ti.ksteps; ++s, ++sa_it) {
-                const int sg = ti.k0 + s;                 // global K-step
-                const int sub = sg % KPR;
-                const bool first = s == 0 || sub == 0, last = s == ti.ksteps - 1 || sub == KPR - 1;
+            const int nst = (ti.ksteps + KS - 1) / KS;
+            for (int st = 0; st < nst; ++st, ++st_it) {
+                // warp-wide waits: the tensor-memory stores below are warp-collective
+                const int kst = ti.k0 / KS + st;                  // global stage index along K
+                const bool first = SPR == 1 || (kst & 1) == 0, last = SPR == 1 || (kst & 1) == 1;
                 const int rslot = rs_it % RS;
-                if (first && !(ok = wait_bar(full_raw(rslot), (rs_it / RS) & 1, abort_flag, g.status))) break;
-                const int slot = sa_it % SA;
-                if (!(ok = wait_bar(empty_a(slot), ((sa_it / SA) & 1) ^ 1, abort_flag, g.status))) break;
+                if (first && !(ok = warp_wait_bar(full_raw(rslot), (rs_it / RS) & 1, abort_flag, g.status))) break;
+                const int slot = st_it % S;
+                if (!(ok = warp_wait_bar(empty(slot), ((st_it / S) & 1) ^ 1, abort_flag, g.status))) break;
                 const uint8_t *raw = raw_base + rslot * C::kRawStage;
-                const uint32_t a_tile = sA + slot * kABytes;
                 if (OP == kOpGateUp) {
-                    // thread dt = (row dt & 127, half dt >> 7): a warp covers 32 consecutive
-                    // rows (conflict-free shared-memory accesses)
-                    if (FMT == kWQ4K) {
-                        if (first) q4k_block_scales_h(*reinterpret_cast<const uint4 *>(raw + (dt & 127) * 144), S, NZ);
-                        dequant_gu_q4k(raw, a_tile, dt & 127, dt >> 7, sub, S, NZ);
-                    } else {
-                        dequant_gu_q80(raw, a_tile, dt & 127, dt >> 7, sg);
-                    }
+                    tc_fence_after();
+                    const uint32_t taddr = tmem_base + ((uint32_t)q_lane << 16) + C::kColA + 64 * slot + 32 * hh;
+                    const uint8_t *rr = raw + ((row & 1) * 64 + (row >> 1)) * 144;   // lane 2i: gate, 2i+1: up
+                    if (FMT == kWQ4K) dequant_gu_q4k_tmem(rr, rr + 16 + 64 * (kst & 1) + 32 * hh, 2 * (kst & 1) + hh, taddr);
+                    else dequant_gu_q80_tmem(rr, (136 * kst) & 15, hh, taddr);
+                    tmem_wait_st();
+                    tc_fence_before();
                 } else {
-                    if (FMT == kWQ4K) dequant_dn_q4k(raw, a_tile, dt, ti.m & 1);
-                    else dequant_dn_q80(raw, a_tile, dt, (34 * (ti.m * 128 / 32)) & 15);
+                    const uint32_t a_tile = sA + slot * C::kAStage;
+                    if (FMT == kWQ4K) dequant_dn_q4k<kDeq>(raw, a_tile, dt, ti.m & 1);
+                    else dequant_dn_q80<kDeq>(raw, a_tile, dt, (34 * (ti.m * 128 / 32)) & 15);
+                    fence_proxy_async();
                 }
-                fence_proxy_async();
-                mbar_arrive(full_a(slot));
+                mbar_arrive(full(slot));
                 if (last) {
                     mbar_arrive(empty_raw(rslot));
                     ++rs_it;
@@ -696,30 +767,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g)
     __syncthreads();
     if (warp == 4) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, 2 * NMAX);
+        tmem_dealloc(tmem_base, C::kCols);
     }
 }
 
 // ---------------------------------------------------------------- helpers
 
-// x -> fp16 operand copy; zero the fp32 output accumulator, the split-K
-// partial sums and their counters.
-__global__ void __launch_bounds__(256) k_gemm_prep(const uint16_t *__restrict__ x, __half *__restrict__ x16,
-                                                   float *__restrict__ yacc, int64_t n, float *__restrict__ gu,
-                                                   int64_t n_gu, uint32_t *__restrict__ cnt, int64_t n_cnt,
-                                                   uint32_t *status)
+// fp16 operand copies of x: xg, the rows in bucket order (row p holds token
+// assign[p] / k), and x16 in token order when a shared expert needs it; zero
+// the fp32 output accumulator, the split-K partial sums and their counters.
+// Eight elements per item (16-byte loads and stores).
+__global__ void __launch_bounds__(256) k_gemm_prep(const uint16_t *__restrict__ x, const int32_t *__restrict__ assign,
+                                                   int k, int T, int H, __half *__restrict__ xg,
+                                                   __half *__restrict__ x16, float *__restrict__ yacc,
+                                                   float *__restrict__ gu, int64_t n_gu, uint32_t *__restrict__ cnt,
+                                                   int64_t n_cnt, uint32_t *status)
 {
     bool bad = false;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const float v = bf16_bits_to_f32(x[i]);
-        const __half hv = __float2half_rn(v);
-        bad |= isfinite(v) && !isfinite(__half2float(hv));    // beyond the fp16 range
-        x16[i] = hv;
-        if (yacc) yacc[i] = 0.0f;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int cpr = H / 8;                               // 8-element chunks per row
+    auto convert = [&](const uint16_t *src, __half *dst) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float lo = bf16_bits_to_f32(w[i] & 0xffffu), hi = bf16_bits_to_f32(w[i] >> 16);
+            const __half2 h = __floats2half2_rn(lo, hi);
+            bad |= (isfinite(lo) && !isfinite(__low2float(h))) || (isfinite(hi) && !isfinite(__high2float(h)));
+            memcpy(&o[i], &h, 4);
+        }
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    const int64_t n_xg = (int64_t)T * k * cpr;
+    for (int64_t i = tid; i < n_xg; i += stride) {
+        const int64_t p = i / cpr, c = i % cpr;
+        const int t = assign[p] / k;
+        convert(x + (int64_t)t * H + 8 * c, xg + p * H + 8 * c);
     }
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_gu; i += stride) gu[i] = 0.0f;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_cnt; i += stride) cnt[i] = 0u;
+    const int64_t n_x = (int64_t)T * cpr;
+    if (x16)
+        for (int64_t i = tid; i < n_x; i += stride) convert(x + 8 * i, x16 + 8 * i);
+    if (yacc)
+        for (int64_t i = tid; i < 2 * n_x; i += stride)
+            reinterpret_cast<float4 *>(yacc)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int64_t i = tid; i < n_gu; i += stride) gu[i] = 0.0f;
+    for (int64_t i = tid; i < n_cnt; i += stride) cnt[i] = 0u;
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, MOE_ERR_DEVICE_FAULT);
 }
 
@@ -822,29 +916,113 @@ __global__ void __launch_bounds__(256) k_gemm_finish(const float *__restrict__ y
 
 // ---------------------------------------------------------------- launch
 
-template <int OP, int FMT, int NMAX, int SA, int SB, int RAW>
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime (no
+// link against the driver library)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// Tensor map of an fp16 matrix [rows][cols] (row-major, cols % 8 == 0, base
+// 16-byte aligned): boxes of 64 columns x box_rows rows, 128-byte swizzle
+// (the K-major layout the MMA descriptors expect), zero fill past the edges.
+static bool make_tmap_f16(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn || rows <= 0 || cols <= 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of the raw bytes of a blob of 3 matrices [rows][row_bytes]
+// (uint8 elements, no swizzle): boxes of 144 bytes x 64 rows.
+static bool make_tmap_raw(CUtensorMap *m, const void *base, int64_t rows, int64_t row_bytes)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn || rows <= 0 || row_bytes <= 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {144, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The weight tensor map of one launch: the shared expert's blob (Q8_0), or
+// for the routed experts (Q4_K) a template whose address each CTA rewrites.
+template <int FMT>
+static bool make_tmap_w(CUtensorMap *m, const GemmArgs &g)
+{
+    if (FMT == kWQ80) return make_tmap_raw(m, g.shared_blob, 3 * (int64_t)g.SFF, (int64_t)(g.H / 32) * 34);
+    return make_tmap_raw(m, g.tmaps, 3 * (int64_t)g.FF, (int64_t)(g.H / 256) * 144);
+}
+
+// The B operand's tensor map of one launch: boxes of NMAX consecutive rows of
+// xg (routed gate/up), x16 (shared gate/up) or a (down).
+template <int OP, int FMT, int NMAX>
+static bool make_tmap_b(CUtensorMap *m, const GemmArgs &g)
+{
+    if (OP == kOpGateUp) {
+        if (FMT == kWQ4K) return make_tmap_f16(m, g.xg, (int64_t)g.T * g.k, g.H, NMAX);
+        return make_tmap_f16(m, g.x16, g.T, g.H, NMAX);
+    }
+    if (FMT == kWQ4K) return make_tmap_f16(m, g.act16, (int64_t)g.T * g.k, g.FF, NMAX);
+    return make_tmap_f16(m, g.sh_act16, g.T, g.SFF, NMAX);
+}
+
+template <int OP, int FMT, int NMAX, int S, int RAW, int EW>
 static cudaError_t launch_gemm(const GemmArgs &g, int grid, cudaStream_t s)
 {
-    using C = GemmCfg<OP, FMT, NMAX, SA, SB, RAW>;
+    using C = GemmCfg<OP, FMT, NMAX, S, RAW>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<OP, FMT, NMAX, SA, SB, RAW>,
+        cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<OP, FMT, NMAX, S, RAW, EW>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    k_moe_gemm<OP, FMT, NMAX, SA, SB, RAW><<<grid, kGemmThreads, C::kBytes, s>>>(g);
+    CUtensorMap tmap_b, tmap_w;
+    if (!make_tmap_b<OP, FMT, NMAX>(&tmap_b, g) || !make_tmap_w<FMT>(&tmap_w, g)) return cudaErrorInvalidValue;
+    k_moe_gemm<OP, FMT, NMAX, S, RAW, EW><<<grid, kGemmThreads, C::kBytes, s>>>(g, tmap_b, tmap_w);
     return cudaGetLastError();
 }
 
-// Configurations: small buckets (every token tile <= 16 wide: decode windows)
-// keep deep A and raw rings; large buckets (prefill) use token tiles of
-// kGemmMaxN with A, B and raw rings of 4, 6 and 3 stages.
+// Configurations: small buckets (every token tile <= 16 wide) keep a 6-stage
+// ring; large buckets (prefill) use token tiles of kGemmMaxN and 4 stages
+// (gate/up: the A stages fill the tensor memory beside the two accumulators).
+// The raw-byte rings take what shared memory is left.  Down projections with
+// few 64-row K-steps per token column (ff / tokens per expert below 8) give
+// the epilogue 8 warps.
 template <int OP, int FMT>
-static cudaError_t launch_gemm_cfg(const GemmArgs &g, int grid, bool small, cudaStream_t s)
+static cudaError_t launch_gemm_cfg(const GemmArgs &g, int grid, bool small, bool epi8, cudaStream_t s)
 {
-    if (small) return launch_gemm<OP, FMT, 16, 6, 8, 92160>(g, grid, s);
-    return launch_gemm<OP, FMT, kGemmMaxN, 4, 6, 55296>(g, grid, s);
+    if constexpr (OP == kOpDown) {
+        if (epi8) {
+            if (small) return launch_gemm<OP, FMT, 16, 6, 98304, 8>(g, grid, s);
+            return launch_gemm<OP, FMT, kGemmMaxN, 4, 81920, 8>(g, grid, s);
+        }
+    }
+    if (small) return launch_gemm<OP, FMT, 16, 6, OP == kOpGateUp ? 163840 : 98304, 4>(g, grid, s);
+    return launch_gemm<OP, FMT, kGemmMaxN, 4, 81920, 4>(g, grid, s);
 }
 
 static int num_sms()
@@ -858,6 +1036,8 @@ static int num_sms()
     }
     return n;
 }
+
+size_t gemm_tmap_bytes() { return (size_t)num_sms() * 2 * sizeof(CUtensorMap); }
 
 size_t gemm_tile_capacity(int mt, int64_t TK, int E)
 {
@@ -912,8 +1092,10 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     const bool small = a.T <= kGemmSmallTokens;
     const GemmSplits sp = w.splits;
     prof_begin(kPhGemmPrep, s);
-    k_gemm_prep<<<(unsigned)std::min<int64_t>((std::max<int64_t>(n, w.n_gu) + 255) / 256, 148 * 8), 256, 0, s>>>(
-        a.x, w.x16, det ? nullptr : w.yacc, n, w.gu, w.n_gu, w.split_cnt, w.n_cnt, a.header + kHdrStatus);
+    const int64_t items = std::max<int64_t>((int64_t)a.T * a.k * (a.H / 8), w.n_gu);
+    k_gemm_prep<<<(unsigned)std::min<int64_t>((items + 255) / 256, 148 * 8), 256, 0, s>>>(
+        a.x, a.assign, a.k, a.T, a.H, w.xg, a.shared_blob ? w.x16 : nullptr, det ? nullptr : w.yacc, w.gu, w.n_gu,
+        w.split_cnt, w.n_cnt, a.header + kHdrStatus);
     PlanArgs p{a.H, a.FF, a.SFF, a.T, sp.gu, sp.dn, sp.gus, sp.dns, a.offsets, a.active, a.header,
                w.tiles_gu, w.tiles_dn, w.tiles_gus, w.tiles_dns};
     k_gemm_plan<<<1, 1024, 0, s>>>(p);
@@ -931,6 +1113,7 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     g.offsets = a.offsets;
     g.assign = a.assign;
     g.w = a.w;
+    g.xg = w.xg;
     g.x16 = w.x16;
     g.act16 = w.act16;
     g.sh_act16 = w.sh_act16;
@@ -938,6 +1121,7 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     g.slots = a.slots;
     g.sh_out = a.sh_out;
     g.status = a.header + kHdrStatus;
+    g.tmaps = reinterpret_cast<CUtensorMap *>(w.tmaps);
     const int grid = num_sms();
     cudaError_t e;
 
@@ -947,14 +1131,14 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     g.splits = sp.gu;
     g.gu = w.gu;
     g.split_cnt = w.split_cnt;
-    e = launch_gemm_cfg<kOpGateUp, kWQ4K>(g, grid, small, s);
+    e = launch_gemm_cfg<kOpGateUp, kWQ4K>(g, grid, small, false, s);
     if (e == cudaSuccess && a.shared_blob) {
         g.tiles = w.tiles_gus;
         g.n_tiles = a.header + kHdrTilesGUS;
         g.splits = sp.gus;
         g.gu = w.sh_gu;
         g.split_cnt = w.split_cnt + w.n_cnt_routed;
-        e = launch_gemm_cfg<kOpGateUp, kWQ80>(g, grid, small, s);
+        e = launch_gemm_cfg<kOpGateUp, kWQ80>(g, grid, small, false, s);
     }
     prof_end(kPhGemmGateUp, s);
     if (e != cudaSuccess) return e;
@@ -963,12 +1147,15 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     g.tiles = w.tiles_dn;
     g.n_tiles = a.header + kHdrTilesDN;
     g.splits = sp.dn;
-    e = launch_gemm_cfg<kOpDown, kWQ4K>(g, grid, small, s);
+    // a tile's K against its token columns (tokens per expert on average, at
+    // most kGemmMaxN)
+    const int64_t n_avg = std::min<int64_t>((int64_t)a.T * a.k / std::max(1, a.E), kGemmMaxN);
+    e = launch_gemm_cfg<kOpDown, kWQ4K>(g, grid, small, a.FF < 8 * n_avg, s);
     if (e == cudaSuccess && a.shared_blob) {
         g.tiles = w.tiles_dns;
         g.n_tiles = a.header + kHdrTilesDNS;
         g.splits = sp.dns;
-        e = launch_gemm_cfg<kOpDown, kWQ80>(g, grid, small, s);
+        e = launch_gemm_cfg<kOpDown, kWQ80>(g, grid, small, a.SFF < 8 * std::min<int64_t>(a.T, kGemmMaxN), s);
     }
     prof_end(kPhGemmDown, s);
     if (e != cudaSuccess) return e;

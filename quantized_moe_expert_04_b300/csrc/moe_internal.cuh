@@ -71,8 +71,8 @@ void prof_end(int phase, cudaStream_t s);
 // Workspace regions (byte offsets from the workspace base) for one call shape.
 struct WsLayout {
     size_t header, logits, ids, w, counts, offsets, assign, active, plan, xfrag;
-    size_t act, slots, yacc, x16, sh_act, sh_out;
-    size_t act16, sh_act16, tiles_gu, tiles_dn, tiles_gus, tiles_dns, gu, sh_gu, split_cnt;
+    size_t act, slots, yacc, xg, x16, sh_act, sh_out;
+    size_t act16, sh_act16, tiles_gu, tiles_dn, tiles_gus, tiles_dns, tmaps, gu, sh_gu, split_cnt;
     size_t total;
 };
 
@@ -163,17 +163,19 @@ struct GemmSplits {
     int gu, dn, gus, dns;                // K splits: routed gate/up, down; shared gate/up, down
 };
 struct GemmWs {
-    __half *x16, *act16, *sh_act16;
+    __half *xg, *x16, *act16, *sh_act16;
     float *yacc;
     float *gu, *sh_gu;                   // split-K partial sums of g and u
     int64_t n_gu;                        // floats to zero in gu and sh_gu (contiguous)
     uint32_t *split_cnt;                 // split-K counters (routed groups, then shared groups)
     int64_t n_cnt, n_cnt_routed;
     int4 *tiles_gu, *tiles_dn, *tiles_gus, *tiles_dns;
+    void *tmaps;                         // two 128-byte tensor-map slots per GEMM CTA
     GemmSplits splits;
     int det;
 };
 size_t gemm_tile_capacity(int mt, int64_t TK, int E);
+size_t gemm_tmap_bytes();
 GemmSplits gemm_splits(const moe_config &c, int32_t T);
 cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream_t s);
 

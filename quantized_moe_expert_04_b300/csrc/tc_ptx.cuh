@@ -70,6 +70,55 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  : "memory");
 }
 
+// 2-D tiled tensor load (the tensor map's box at column x, row y) into shared
+// memory, completing its bytes on `bar`.  x * element size must be a multiple
+// of 16 bytes; rows past the tensor's extent are filled with zeros.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Four rows y0..y3 of a 2-D tensor (box: one row of the map's box width, at
+// column x) gathered into consecutive box rows of shared memory, completing
+// on `bar`.  Same alignment rule for x as tma_load_2d.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int y0, int y1, int y2, int y3,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+        : "memory");
+}
+
+// Tensor maps edited on the device: rewrite the global address of a map held
+// in shared memory (128-byte aligned) ...
+__device__ __forceinline__ void tmap_set_addr_smem(uint32_t smem_tmap, const void *addr)
+{
+    asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(smem_tmap), "l"(addr)
+                 : "memory");
+}
+
+// ... copy it (warp-collective) to a 128-byte slot in global memory, releasing
+// it to the tensor-map proxy ...
+__device__ __forceinline__ void tmap_copy_release(void *gmem_tmap, uint32_t smem_tmap)
+{
+    asm volatile(
+        "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned [%0], [%1], 128;" ::"l"(
+            gmem_tmap),
+        "r"(smem_tmap)
+        : "memory");
+}
+
+// ... and acquire it before the first tensor copy that names it.
+__device__ __forceinline__ void tmap_acquire(const void *gmem_tmap)
+{
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(gmem_tmap) : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared (L2 only), tracked by commit groups.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
 {
@@ -122,6 +171,19 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T: A read from tensor memory (row i of A
+// in lane i, two fp16 of consecutive K per 32-bit column), fp32 accumulation.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // arrive (once) on `bar` when every MMA issued so far by this thread has completed
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
@@ -143,6 +205,31 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 32 lanes x 16 consecutive 32-bit columns from registers: thread i writes lane (base lane + i)
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// one lane of the (converged) warp returns true
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t p;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t.reg .b32 rl;\n\t"
+        "elect.sync rl|P1, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P1;\n\t}"
+        : "=r"(p));
+    return p != 0;
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
 // core groups 1024 bytes apart (SBO), version 1, base offset 0 (the tile
 // must start on a 1024-byte boundary).
@@ -156,6 +243,24 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     d |= (uint64_t)2 << 61;                      // swizzle: 128 B              [61,64)
     return d;
 }
+
+// Shared-memory matrix descriptor: MN-major operand (the M or N index is the
+// contiguous one), 128-byte swizzle.  A swizzle atom is 8 K-rows of 64 fp16
+// along M (1024 bytes, 1024-byte aligned); atoms `mn_stride` bytes apart along
+// M (leading byte offset) and `k_stride` bytes apart along K (stride byte offset).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride, uint32_t k_stride)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((k_stride >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// instruction-descriptor bit: A is MN-major
+constexpr uint32_t kIdescAMnMajor = 1u << 15;
 
 // Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major, M x N.
 __host__ __device__ __forceinline__ uint32_t idesc_f16_f32(int M, int N)
