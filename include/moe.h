@@ -93,11 +93,12 @@ enum {
                                         order on every path (bit-identical reruns)        */
     MOE_FLAG_FORCE_GEMV = 2,         /* use the decode (grouped GEMV) path; T <= 8 only  */
     MOE_FLAG_FORCE_GEMM = 4,         /* use the prefill (tensor-core GEMM) path at any T */
-    MOE_FLAG_STATIC_WEIGHTS = 8      /* the caller guarantees that router_w, router_bias
-                                        and the expert blobs are not written by the work
-                                        enqueued just before this call on the stream: a
-                                        decode call may then start reading the router
-                                        rows while that work is still running (its other
+    MOE_FLAG_STATIC_WEIGHTS = 8      /* the caller guarantees that router_w, router_bias,
+                                        the expert table and the expert blobs are not
+                                        written by the work enqueued just before this call
+                                        on the stream: a decode call may then start
+                                        reading the router rows and the expert table
+                                        while that work is still running (its other
                                         inputs are read only after it has finished)     */
 };
 

@@ -267,6 +267,7 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
         d.det = (cfg->flags & MOE_FLAG_DETERMINISTIC) != 0;
         d.route_parts = dec_route_parts(cfg->hidden);
         d.fs_dn = dec_down_splits(*cfg, T);
+        d.dn_nbuf = dec_down_nbuf(*cfg, T, d.fs_dn);
         d.overlap_prev = (cfg->flags & MOE_FLAG_STATIC_WEIGHTS) != 0;
         d.prefetch_down = 0;   // measured: the bulk L2 prefetch slows both projections
         d.prefetch_budget = kDecPrefetchBudget;

@@ -135,10 +135,11 @@ __device__ __forceinline__ uint32_t key_bits(float f)
 // each round takes the warp maximum (redux), the lowest expert id among equal
 // keys, and only the winning lane clears that key and recomputes its best.
 // Weights: softmax over the k selected logits (= the full softmax
-// renormalised over the k) or s / sum of the selected s, from the logits in
-// global memory.  Lane r < k receives selection r.
+// renormalised over the k) or s / sum of the selected s; vals[e] (shared
+// memory) holds expert e's logit (softmax) or s = sigmoid(logit).  Lane r < k
+// receives selection r.
 template <int NPER>
-__device__ void warp_topk(const uint32_t *keys, const float *logit_row, int E, int k, int score_fn, int lane,
+__device__ void warp_topk(const uint32_t *keys, const float *vals, int E, int k, int score_fn, int lane,
                           int &out_id, float &out_w, bool &fault)
 {
     uint32_t key[NPER];
@@ -184,13 +185,13 @@ __device__ void warp_topk(const uint32_t *keys, const float *logit_row, int E, i
         }
     }
     const bool sel = lane < k;
-    const float lv = sel ? __ldcg(logit_row + my_id) : 0.0f;
+    const float lv = sel ? vals[my_id] : 0.0f;
     float num;
     if (score_fn == MOE_SCORE_SOFTMAX) {
         const float lmax = __shfl_sync(0xffffffffu, lv, 0);   // the first pick is the largest
         num = sel ? expf(lv - lmax) : 0.0f;
     } else {
-        num = sel ? 1.0f / (1.0f + expf(-lv)) : 0.0f;
+        num = sel ? lv : 0.0f;
     }
     float den = num;
 #pragma unroll
@@ -313,6 +314,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_dec_route(DecArgs a)
 // sort; the plan (active experts and their tokens) stays in `pe` / `ptok`.
 struct RouteScratch {
     uint32_t *key;       // [T][E] selection keys
+    float *val;          // [T][E] logit (softmax) or sigmoid(logit): what the weight uses
     int32_t *ids;        // [T*k]
     float *w;            // [T*k]
     int32_t *rank;       // [T*k]
@@ -339,8 +341,11 @@ __device__ void route_window(const DecArgs &a, const RouteScratch &sc, int16_t *
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int i = i0 + j * nthr;
-            if (i < T * E)
-                sc.key[i] = key_bits(a.score_fn == MOE_SCORE_SOFTMAX ? v[j] : 1.0f / (1.0f + expf(-v[j])) + b[j]);
+            if (i < T * E) {
+                const float sv = a.score_fn == MOE_SCORE_SOFTMAX ? v[j] : 1.0f / (1.0f + expf(-v[j]));
+                sc.val[i] = sv;
+                sc.key[i] = key_bits(a.score_fn == MOE_SCORE_SOFTMAX ? sv : sv + b[j]);
+            }
         }
     }
     if (threadIdx.x < 32) sc.bits[threadIdx.x] = 0u;
@@ -350,7 +355,7 @@ __device__ void route_window(const DecArgs &a, const RouteScratch &sc, int16_t *
         float wt;
         bool f;
         const uint32_t *kr = sc.key + warp * E;
-        const float *lr = a.logits + (int64_t)warp * E;
+        const float *lr = sc.val + warp * E;
         if (E <= 256) warp_topk<8>(kr, lr, E, k, a.score_fn, lane, id, wt, f);
         else if (E <= 512) warp_topk<16>(kr, lr, E, k, a.score_fn, lane, id, wt, f);
         else warp_topk<32>(kr, lr, E, k, a.score_fn, lane, id, wt, f);
@@ -512,12 +517,18 @@ __global__ void __launch_bounds__(kGuWarps * 32, 1) k_dec_gateup(DecArgs a)
     int16_t *pe = reinterpret_cast<int16_t *>(s_red + kGuWarps * 32 * 4);          // [256]
     int16_t(*ptok)[kDecTok] = reinterpret_cast<int16_t(*)[kDecTok]>(pe + kDecMaxAssign);
     const uint8_t **s_blob = reinterpret_cast<const uint8_t **>(ptok + kDecMaxAssign);   // [256]
+    const uint8_t **s_tab = s_blob + kDecMaxAssign;                                         // [E]
     __shared__ int s_nact;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     uint8_t *myring = ring + warp * NST * kGuStage;
 
+    // the expert table: before the dependency wait when the weights are static
+    if (a.overlap_prev)
+        for (int e = threadIdx.x; e < E; e += blockDim.x) s_tab[e] = a.blobs[e];
     griddep_wait();
+    if (!a.overlap_prev)
+        for (int e = threadIdx.x; e < E; e += blockDim.x) s_tab[e] = a.blobs[e];
     // x fragments into shared memory, asynchronously while the window is routed
     for (int i = threadIdx.x; i < nb * 256; i += blockDim.x) cp_async16(s_xf + i, a.xfrag + i);
     cp_async_commit();
@@ -526,6 +537,8 @@ __global__ void __launch_bounds__(kGuWarps * 32, 1) k_dec_gateup(DecArgs a)
         RouteScratch sc;
         uint8_t *p = ring;
         sc.key = reinterpret_cast<uint32_t *>(p);
+        p += (size_t)T * E * 4;
+        sc.val = reinterpret_cast<float *>(p);
         p += (size_t)T * E * 4;
         sc.ids = reinterpret_cast<int32_t *>(p);
         p += kDecMaxAssign * 4;
@@ -549,7 +562,7 @@ __global__ void __launch_bounds__(kGuWarps * 32, 1) k_dec_gateup(DecArgs a)
     const bool in_group = warp < ipg * KS;          // KS not dividing 16 leaves warps idle
     const int cpi = nb / KS;                                               // stages per item part
 
-    for (int u = threadIdx.x; u < U; u += blockDim.x) s_blob[u] = a.blobs[pe[u]];
+    for (int u = threadIdx.x; u < U; u += blockDim.x) s_blob[u] = s_tab[pe[u]];
     __syncthreads();
     // L2 prefetch of the down matrices of the selected experts (up to a budget),
     // one chunk per thread over the whole grid, so their bytes stream while
@@ -715,7 +728,9 @@ constexpr int kDnWarps = 4;                 // warps (independent units) per CTA
 constexpr int kDnThreads = kDnWarps * 32;
 constexpr int kDnMaxRows = 80;
 constexpr int kDnRowStride = 160;           // 144 + 16 padding
-constexpr int kDnBuf = kDnMaxRows * kDnRowStride + 2 * kDnMaxRows * 4;   // rows + activations of 2 tokens
+// one unit buffer: FR rows + the activations of 2 tokens for them
+__host__ __device__ constexpr int dn_buf_bytes(int FR) { return (FR * kDnRowStride + 2 * FR * 4 + 15) & ~15; }
+constexpr int kDnRegCtas = 3;               // CTAs per SM the kernel's registers allow
 
 // fp32 scale and min of the sub-block pair (2c, 2c + 1) of a Q4_K header:
 // d * sc and dmin * m, each one rounding (exact integer conversions).
@@ -738,7 +753,7 @@ __device__ __forceinline__ void q4k_pair_scales_f(uint4 hdr, int c, float &s0, f
     z1 = __fmul_rn(dmin, m1);
 }
 
-__global__ void __launch_bounds__(kDnThreads) k_dec_down(DecArgs a)
+__global__ void __launch_bounds__(kDnThreads, kDnRegCtas) k_dec_down(DecArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];     // [warp][2][kDnBuf]
     griddep_wait();
@@ -750,7 +765,8 @@ __global__ void __launch_bounds__(kDnThreads) k_dec_down(DecArgs a)
     const int q = lane & 7, rl = lane >> 3;
     const int c = q >> 1, l0 = 16 * (q & 1);
     const int FR = FF / FS;
-    uint8_t *wbuf = smem + warp * 2 * kDnBuf;
+    const int NB = a.dn_nbuf, BB = dn_buf_bytes(FR);
+    uint8_t *wbuf = smem + warp * NB * BB;
     const int gw = blockIdx.x * kDnWarps + warp, nw = gridDim.x * kDnWarps;
 
     auto unit_of = [&](int unit, int &u, int &cb, int &fs) {
@@ -766,7 +782,7 @@ __global__ void __launch_bounds__(kDnThreads) k_dec_down(DecArgs a)
             const uint8_t *blob = a.blobs[a.plan[u].e];
             if (blob) {
                 const uint8_t *src = blob + (2 * (int64_t)FF + (int64_t)fs * FR) * rb + (int64_t)cb * 144;
-                uint8_t *dst = wbuf + buf * kDnBuf;
+                uint8_t *dst = wbuf + buf * BB;
                 for (int p = lane; p < FR * 9; p += 32) {
                     const int row = p / 9, pc = p % 9;
                     cp_async16(dst + row * kDnRowStride + pc * 16, src + row * rb + pc * 16);
@@ -776,37 +792,54 @@ __global__ void __launch_bounds__(kDnThreads) k_dec_down(DecArgs a)
         cp_async_commit();
     };
 
+    // two buffers: the next unit is staged while this one computes; one buffer
+    // (a warp with a single unit, the usual case): the next unit, if any, is
+    // staged after this one
     issue(gw, 0);
     int buf = 0;
-    for (int unit = gw; unit < units; unit += nw, buf ^= 1) {
-        issue(unit + nw, buf ^ 1);
+    for (int unit = gw; unit < units; unit += nw, buf ^= (NB - 1)) {
+        if (NB == 2) issue(unit + nw, buf ^ 1);
         int u, cb, fs;
         unit_of(unit, u, cb, fs);
         if (!a.blobs[a.plan[u].e]) {
             if (lane == 0) set_status(a.header + kHdrStatus, MOE_ERR_DEVICE_FAULT);
+            if (NB == 1) {
+                cp_async_wait<0>();
+                __syncwarp();
+                issue(unit + nw, 0);
+            }
             continue;
         }
-        int tok_a[kDecTok];
-        int n = 0;
+        // the window tokens routed to this expert (bit t: token t), taken two per pass
+        int tok_as[kDecTok];
+        uint32_t pm = 0;
 #pragma unroll
         for (int tt = 0; tt < kDecTok; ++tt) {
-            const int as = a.plan[u].tok_assign[tt];
-            tok_a[tt] = -1;
-            if (as >= 0) tok_a[n++] = as;
+            tok_as[tt] = a.plan[u].tok_assign[tt];
+            if (tok_as[tt] >= 0) pm |= 1u << tt;
         }
-        uint8_t *tile = wbuf + buf * kDnBuf;
-        float *s_act = reinterpret_cast<float *>(tile + kDnMaxRows * kDnRowStride);   // [2][kDnMaxRows]
+        const int n = __popc(pm);
+        uint8_t *tile = wbuf + buf * BB;
+        float *s_act = reinterpret_cast<float *>(tile + FR * kDnRowStride);   // [2][FR]
         for (int p0 = 0; p0 < n; p0 += 2) {
             const int np = min(2, n - p0);
-            const int as0 = tok_a[p0], as1 = np > 1 ? tok_a[p0 + 1] : -1;
+            int as0 = -1, as1 = -1, seen = 0;
+#pragma unroll
+            for (int tt = 0; tt < kDecTok; ++tt)
+                if ((pm >> tt) & 1u) {
+                    if (seen == p0) as0 = tok_as[tt];
+                    if (seen == p0 + 1) as1 = tok_as[tt];
+                    ++seen;
+                }
             // activations of the pass's tokens for the segment's rows (written by the previous kernel)
             __syncwarp();
             for (int i = lane; i < 2 * FR; i += 32) {
                 const int tk = i / FR, row = i % FR;
                 const int as = tk ? as1 : as0;
-                s_act[tk * kDnMaxRows + row] = as >= 0 ? __ldg(a.act + (int64_t)as * FF + fs * FR + row) : 0.0f;
+                s_act[tk * FR + row] = as >= 0 ? __ldg(a.act + (int64_t)as * FF + fs * FR + row) : 0.0f;
             }
-            cp_async_wait<1>();
+            if (NB == 2) cp_async_wait<1>();
+            else cp_async_wait<0>();
             __syncwarp();
             float acc[2][32];
 #pragma unroll
@@ -816,7 +849,7 @@ __global__ void __launch_bounds__(kDnThreads) k_dec_down(DecArgs a)
             for (int row = rl; row < FR; row += 4) {
                 const uint4 hv = *reinterpret_cast<const uint4 *>(tile + row * kDnRowStride);
                 const uint4 qv = *reinterpret_cast<const uint4 *>(tile + row * kDnRowStride + 16 + 16 * q);
-                const float av0 = s_act[row], av1 = s_act[kDnMaxRows + row];
+                const float av0 = s_act[row], av1 = s_act[FR + row];
                 float sl, zl, sh, zh;
                 q4k_pair_scales_f(hv, c, sl, zl, sh, zh);
                 const float A0l = 256.0f * av0 * sl, A0h = 256.0f * av0 * sh;
@@ -886,6 +919,10 @@ __global__ void __launch_bounds__(kDnThreads) k_dec_down(DecArgs a)
                 }
             }
         }
+        if (NB == 1) {
+            __syncwarp();              // every lane is done with the buffer
+            issue(unit + nw, 0);
+        }
     }
     cp_async_wait<0>();
     griddep_launch();
@@ -947,6 +984,25 @@ int dec_route_parts(int H)
 
 // ff segments per down unit: at most kDnMaxRows rows each, and enough units
 // for two per SM.
+// Down units (expert, block column, ff segment) are spread over the warps of
+// the grid.  A unit buffer holds FR = ff / fs rows; with one buffer per warp
+// (every warp has at most one unit) more CTAs fit on an SM than with two.
+static int64_t dn_warps(int64_t units, int FR, int nbuf)
+{
+    const int64_t smem = (int64_t)kDnWarps * nbuf * dn_buf_bytes(FR);
+    const int64_t by_smem = 233472 / (smem + 1024);
+    const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(by_smem, kDnRegCtas));
+    const int64_t ctas = std::min<int64_t>((units + kDnWarps - 1) / kDnWarps, per_sm * dec_sms());
+    return ctas * kDnWarps;
+}
+
+int dec_down_nbuf(const moe_config &c, int32_t T, int fs)
+{
+    const int64_t maxu = std::min<int64_t>(c.n_experts, (int64_t)T * c.top_k);
+    const int64_t units = maxu * (c.hidden / 256) * fs;
+    return units <= dn_warps(units, c.ff / fs, 1) ? 1 : 2;
+}
+
 int dec_down_splits(const moe_config &c, int32_t T)
 {
     const int64_t maxu = std::min<int64_t>(c.n_experts, (int64_t)T * c.top_k);
@@ -954,10 +1010,24 @@ int dec_down_splits(const moe_config &c, int32_t T)
     int fs = 1;
     while (c.ff % fs || c.ff / fs > kDnMaxRows) ++fs;      // segments of at most kDnMaxRows rows
     if (c.flags & MOE_FLAG_DETERMINISTIC) return fs;
-    // more segments while there are fewer units than warps and segments stay >= 32 rows
-    for (int f2 = fs + 1; maxu * nb * fs < (int64_t)kDnWarps * 2 * dec_sms() && f2 <= 64; ++f2)
-        if (c.ff % f2 == 0 && c.ff / f2 >= 32) fs = f2;
-    return fs;
+    // The slowest warp takes ceil(units / warps) units: pick the segmentation
+    // with the least work on that warp (its rows' bytes plus a per-unit cost:
+    // the unit's additions into y and its fixed latency).
+    int64_t best_cost = -1;
+    int best = fs;
+    for (int f2 = fs; f2 <= 64; ++f2) {
+        if (c.ff % f2 || (f2 > fs && c.ff / f2 < 32)) continue;     // segments of >= 32 rows
+
+        const int64_t units = maxu * nb * f2;
+        const int64_t warps = dn_warps(units, c.ff / f2, dec_down_nbuf(c, T, f2));
+        const int64_t rounds = (units + warps - 1) / warps;
+        const int64_t cost = rounds * ((int64_t)(c.ff / f2) * 144 + (int64_t)T * 2048 + 2048);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = f2;
+        }
+    }
+    return best;
 }
 
 template <typename K>
@@ -978,10 +1048,10 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
 }
 
 // Ring depth of the gate/up stages: the deepest (up to four) that shared memory holds.
-int dec_gateup_stages(int H)
+int dec_gateup_stages(int H, int E)
 {
     const size_t fixed = (size_t)H * 16 + kGuWarps * 32 * 4 * sizeof(float) + kDecMaxAssign * 2 * (1 + kDecTok) +
-                         kDecMaxAssign * sizeof(void *);
+                         kDecMaxAssign * sizeof(void *) + (size_t)E * sizeof(void *);
     for (int nst = 4; nst > 2; --nst)
         if (fixed + (size_t)kGuWarps * nst * kGuStage + 1024 <= (size_t)kMaxSmemPerBlock) return nst;
     return 2;
@@ -991,9 +1061,9 @@ static size_t gateup_smem(const DecArgs &a, int nst)
 {
     const size_t ring = (size_t)kGuWarps * nst * kGuStage;
     // the routing scratch lives in the ring before the first stage
-    const size_t route = (size_t)a.T * a.E * 4 + 5 * kDecMaxAssign * 4 + 64 * 4;
+    const size_t route = (size_t)a.T * a.E * 8 + 5 * kDecMaxAssign * 4 + 64 * 4;
     return (size_t)a.H * 16 + std::max(ring, route) + kGuWarps * 32 * 4 * sizeof(float) +
-           kDecMaxAssign * 2 * (1 + kDecTok) + kDecMaxAssign * sizeof(void *);
+           kDecMaxAssign * 2 * (1 + kDecTok) + kDecMaxAssign * sizeof(void *) + (size_t)a.E * sizeof(void *);
 }
 
 template <int NST, int KS>
@@ -1023,7 +1093,7 @@ cudaError_t launch_decode(const DecArgs &a0, cudaStream_t s)
                                  kDecTok * 8192 * (int)sizeof(uint16_t));
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_dec_down, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kDnWarps * 2 * kDnBuf);
+                                     kDnWarps * 2 * dn_buf_bytes(kDnMaxRows));
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -1037,15 +1107,23 @@ cudaError_t launch_decode(const DecArgs &a0, cudaStream_t s)
     const int sms = dec_sms();
     const int64_t maxu = std::min<int64_t>(a.E, (int64_t)a.T * a.k);
     const int nb = a.H / 256;
-    const int NST = dec_gateup_stages(a.H);
+    const int NST = dec_gateup_stages(a.H, a.E);
     const int64_t items = maxu * (a.FF / 8);
-    // K split of an item: the smallest divisor of the block count (1, 2, 4, 5,
-    // 8, 10, 16) that gives every warp of the grid some work, when possible
+    // K split of an item: a divisor of the block count (1, 2, 4, 5, 8, 10, 16);
+    // groups of 16 / ks items go round-robin to the CTAs, so the slowest CTA
+    // runs ceil(groups / CTAs) groups of nb / ks block columns per warp (plus
+    // the ks-way reduction); pick the split with the least of that
     int ks = 1;
+    double best_cost = -1.0;
     for (int cand : {1, 2, 4, 5, 8, 10, 16}) {
         if (nb % cand) continue;
-        ks = cand;
-        if (items * cand >= (int64_t)kGuWarps * sms) break;
+        const int64_t grp = (items + kGuWarps / cand - 1) / (kGuWarps / cand);
+        const int64_t rounds = (grp + sms - 1) / sms;
+        const double cost = (double)rounds * ((double)(nb / cand) + (cand > 1 ? 0.25 : 0.0));
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            ks = cand;
+        }
     }
     const int ipg = kGuWarps / ks;
     const int64_t groups = (items + ipg - 1) / ipg;
@@ -1067,9 +1145,11 @@ cudaError_t launch_decode(const DecArgs &a0, cudaStream_t s)
     }
 
     const int64_t units = maxu * nb * a.fs_dn;
-    const int grid_dn = (int)std::max<int64_t>(1, std::min<int64_t>((units + kDnWarps - 1) / kDnWarps, 2 * (int64_t)sms));
+    const int FR = a.FF / a.fs_dn;
+    const int grid_dn = (int)std::max<int64_t>(1, dn_warps(units, FR, a.dn_nbuf) / kDnWarps);
     prof_begin(kPhDecDown, s);
-    e = launch_pdl(k_dec_down, dim3(grid_dn), dim3(kDnThreads), (size_t)kDnWarps * 2 * kDnBuf, s, true, a);
+    e = launch_pdl(k_dec_down, dim3(grid_dn), dim3(kDnThreads), (size_t)kDnWarps * a.dn_nbuf * dn_buf_bytes(FR), s,
+                   true, a);
     prof_end(kPhDecDown, s);
     if (e != cudaSuccess) return e;
     const int n4 = a.T * a.H / 4;

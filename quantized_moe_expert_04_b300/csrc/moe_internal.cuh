@@ -131,6 +131,7 @@ struct DecArgs {
     int H, E, FF, k, T, SFF, score_fn, det;
     int route_parts;             // router row split per CTA (1, 2, 4 or 8)
     int fs_dn;                   // ff segments per down unit
+    int dn_nbuf;                 // shared-memory buffers per down warp (2: the next unit is staged ahead)
     int overlap_prev;            // router rows may be read before the previous kernel ends
     int prefetch_down;           // ask L2 for the down matrices during gate/up
     int64_t prefetch_budget;     // at most this many bytes of them
@@ -153,6 +154,7 @@ struct DecArgs {
 };
 int dec_route_parts(int H);
 int dec_down_splits(const moe_config &c, int32_t T);
+int dec_down_nbuf(const moe_config &c, int32_t T, int fs);
 cudaError_t launch_decode(const DecArgs &a, cudaStream_t s);
 cudaError_t launch_shared_gemv(const DecArgs &a, cudaStream_t s);
 
