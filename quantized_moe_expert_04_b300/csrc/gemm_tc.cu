@@ -9,21 +9,27 @@
 // one expert's 128 weight rows x up to kGemmMaxN of its tokens:
 //
 //   gate/up  A = 64 gate rows and the 64 up rows of the same ff indices,
-//              interleaved (row 2i = gate f0+i, row 2i+1 = up f0+i), K = H;
-//            B = the tile's token rows of x (fp16);
+//              interleaved (row 2i = gate f0+i, row 2i+1 = up f0+i), K = H,
+//              dequantised by the dequantisation warps straight into tensor
+//              memory (thread = tensor-memory lane = weight row) and read from
+//              there by the MMA;
+//            B = the tile's rows of xg (x in fp16, permuted into bucket order,
+//              so a tile's token rows are consecutive);
 //            epilogue: lanes 2i / 2i+1 hold g / u of one ff index ->
 //              a = SiLU(g) * u, stored fp16 at the assignment's bucket position.
-//   down     A = Wd^T tile (128 hidden rows, K = FF; Wd is stored [FF][H], so the
-//              dequantiser writes it transposed), B = the tile's rows of a;
+//   down     A = Wd^T tile (128 hidden rows, K = FF), written MN-major into
+//              shared memory (Wd is stored [FF][H]: eight consecutive weights
+//              of a row are eight consecutive M indices), B = the tile's rows of a;
 //            epilogue: * routing weight, atomically added into y (fp32), or
 //              stored to the assignment's slot when the call is deterministic.
 //
-// Warp roles (16 warps): 0-3 epilogue (tensor-memory lane quarters 0-3),
-// 4 MMA issue + tensor-memory allocation, 5 raw weight bytes (16-byte cp.async
-// pieces into a ring, completion counted on its mbarrier), 6-7 token rows
-// (16-byte cp.async gathers into 128-byte-swizzled tiles, completion counted
-// on the B ring's mbarriers),
-// 8-15 dequantisation (raw ring -> fp16 A ring).  All hand-offs are mbarriers;
+// Warp roles (16 warps): 0-3 epilogue (tensor-memory lane quarters 0-3; down
+// projections short along K add warps 12-15), 4 MMA issue + tensor-memory
+// allocation, 5 raw weight bytes (2-D tensor copies of 144-byte x 64-row boxes
+// of the expert blob, through a per-CTA tensor map rewritten for each expert),
+// 6-7 B rows (2-D tensor copies, one per 64-wide K sub-tile), 8-15 (or 8-11)
+// dequantisation.  All hand-offs are mbarriers: per pipeline stage one "full"
+// (dequantised A and B rows in place) and one "empty" (the stage's MMAs done);
 // every wait is bounded and sets MOE_ERR_TIMEOUT instead of hanging.
 //
 // Operand precision: fp16 A and B (sub-block scale and min rounded to fp16,
