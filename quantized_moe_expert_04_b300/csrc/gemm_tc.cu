@@ -806,11 +806,14 @@ __global__ void __launch_bounds__(256) k_gemm_prep(const uint16_t *__restrict__ 
         }
         *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
     };
-    const int64_t n_xg = (int64_t)T * k * cpr;
-    for (int64_t i = tid; i < n_xg; i += stride) {
-        const int64_t p = i / cpr, c = i % cpr;
+    // one warp per row: lanes take consecutive 16-byte chunks
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarp = tid >> 5, nwarps = stride >> 5;
+    for (int64_t p = gwarp; p < (int64_t)T * k; p += nwarps) {
         const int t = assign[p] / k;
-        convert(x + (int64_t)t * H + 8 * c, xg + p * H + 8 * c);
+        const uint16_t *src = x + (int64_t)t * H;
+        __half *dst = xg + p * H;
+        for (int c = lane; c < cpr; c += 32) convert(src + 8 * c, dst + 8 * c);
     }
     const int64_t n_x = (int64_t)T * cpr;
     if (x16)
@@ -845,6 +848,7 @@ __device__ __forceinline__ void split_tokens(int n_e, int &tn, int &nt)
 __global__ void __launch_bounds__(1024) k_gemm_plan(PlanArgs p)
 {
     __shared__ int scan_gu[1024], scan_dn[1024];
+    __shared__ int s_e[1024], s_n[1024], s_tn[1024];
     const int u = threadIdx.x;
     const int n_active = (int)p.header[kHdrNActive];
     const int mt_gu = p.FF / 64, mt_dn = p.H / 128;
@@ -854,6 +858,9 @@ __global__ void __launch_bounds__(1024) k_gemm_plan(PlanArgs p)
         n_e = p.offsets[e + 1] - p.offsets[e];
         split_tokens(n_e, tn, nt);
     }
+    s_e[u] = e;
+    s_n[u] = n_e;
+    s_tn[u] = tn;
     scan_gu[u] = nt * mt_gu * p.split_gu;
     scan_dn[u] = nt * mt_dn * p.split_dn;
     __syncthreads();
@@ -864,14 +871,26 @@ __global__ void __launch_bounds__(1024) k_gemm_plan(PlanArgs p)
         scan_dn[u] += b;
         __syncthreads();
     }
-    int at_gu = scan_gu[u] - nt * mt_gu * p.split_gu, at_dn = scan_dn[u] - nt * mt_dn * p.split_dn;
-    for (int j = 0; j < nt; ++j) {
-        const int n0 = j * tn, n = min(tn, n_e - n0);
-        for (int m = 0; m < mt_gu; ++m)
-            for (int ks = 0; ks < p.split_gu; ++ks) p.gu[at_gu++] = make_int4(e, m | (ks << 16), n0, n);
-        for (int m = 0; m < mt_dn; ++m)
-            for (int ks = 0; ks < p.split_dn; ++ks) p.dn[at_dn++] = make_int4(e, m | (ks << 16), n0, n);
-    }
+    // every thread writes tiles: tile i of a list belongs to the expert whose
+    // inclusive prefix first exceeds i (binary search); within an expert the
+    // order is token tile j, then weight tile m, then K split ks
+    auto fill = [&](const int *scan, int mt, int split, int4 *out) {
+        const int total = scan[1023];
+        for (int i = u; i < total; i += 1024) {
+            int lo = 0, hi = 1023;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (scan[mid] > i) hi = mid;
+                else lo = mid + 1;
+            }
+            const int l = i - (lo ? scan[lo - 1] : 0);
+            const int ks = l % split, m = (l / split) % mt, j = l / (split * mt);
+            const int n0 = j * s_tn[lo];
+            out[i] = make_int4(s_e[lo], m | (ks << 16), n0, min(s_tn[lo], s_n[lo] - n0));
+        }
+    };
+    fill(scan_gu, mt_gu, p.split_gu, p.gu);
+    fill(scan_dn, mt_dn, p.split_dn, p.dn);
     if (u == 1023) {
         p.header[kHdrTilesGU] = (uint32_t)scan_gu[1023];
         p.header[kHdrTilesDN] = (uint32_t)scan_dn[1023];

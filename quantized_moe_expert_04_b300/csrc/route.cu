@@ -249,9 +249,21 @@ __global__ void __launch_bounds__(256) k_router_mma(const uint16_t *__restrict__
 }
 
 // One warp per token.  Keys: the logit (softmax: the order of p equals the
-// order of the logits) or s_e + b_e (sigmoid).  Weights: softmax over the k
-// selected logits (= the full softmax renormalised over the k), or
-// s_e / sum of the selected s.
+// order of the logits) or s_e + b_e (sigmoid), as order-preserving integers
+// (NaN -> 0, never selected).  Lane l keeps experts l, l + 32, ... (NPER) in
+// registers with its best untaken key (a reduction tree, equal keys to the
+// lower id); each round takes the warp maximum (redux), the lowest expert id
+// among equal keys, and only the winning lane recomputes its best.  Weights:
+// softmax over the k selected logits (= the full softmax renormalised over
+// the k), or s_e / sum of the selected s.
+__device__ __forceinline__ uint32_t topk_key(float f)
+{
+    if (isnan(f)) return 0u;
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int NPER>
 __global__ void __launch_bounds__(256)
 k_topk(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k,
        int score_fn, int32_t *__restrict__ ids, float *__restrict__ wout, uint32_t *status)
@@ -260,68 +272,69 @@ k_topk(const float *__restrict__ logits, const float *__restrict__ bias, int T, 
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
     const float *lrow = logits + (int64_t)t * E;
-    float key[kMaxPerLane], val[kMaxPerLane];
+    uint32_t key[NPER];
+    float val[NPER];
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < NPER; ++i) {
         const int e = lane + 32 * i;
-        key[i] = -INFINITY;
+        key[i] = 0u;
         val[i] = 0.0f;
         if (e < E) {
-            const float l = lrow[e];
+            const float l = __ldg(lrow + e);
             if (score_fn == MOE_SCORE_SOFTMAX) {
-                key[i] = l;
                 val[i] = l;
+                key[i] = topk_key(l);
             } else {
                 const float sg = 1.0f / (1.0f + expf(-l));
                 val[i] = sg;
-                key[i] = sg + (bias ? bias[e] : 0.0f);
+                key[i] = topk_key(sg + (bias ? __ldg(bias + e) : 0.0f));
             }
         }
     }
-    uint32_t taken = 0;
+    uint32_t bk = 0u;
+    int bi = 0;
+    float bv = 0.0f;
+    auto best = [&]() {
+        uint32_t kk[NPER];
+        int ii[NPER];
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) {
+            kk[i] = key[i];
+            ii[i] = i;
+        }
+#pragma unroll
+        for (int w = 1; w < NPER; w <<= 1)
+#pragma unroll
+            for (int i = 0; i + w < NPER; i += 2 * w)
+                if (kk[i + w] > kk[i]) {        // strict: equal keys keep the lower index
+                    kk[i] = kk[i + w];
+                    ii[i] = ii[i + w];
+                }
+        bk = kk[0];
+        bi = ii[0];
+        bv = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i)
+            if (i == bi) bv = val[i];
+    };
+    best();
     int my_id = 0;
     float my_val = 0.0f;
     bool fault = false;
     for (int r = 0; r < k; ++r) {
-        // this lane's best untaken key (ascending ids: '>' keeps the lower id)
-        float bv = -INFINITY, bval = 0.0f;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u) && (be == 0x7fffffff || key[i] > bv)) {
-                bv = key[i];
-                be = e;
-                bval = val[i];
-            }
-        }
-        // warp arg-max; equal keys -> lower id; NaN loses to any number
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            const float oval = __shfl_xor_sync(0xffffffffu, bval, off);
-            bool take = false;
-            if (oe != 0x7fffffff) {
-                if (be == 0x7fffffff) take = true;
-                else if (isnan(bv)) take = !isnan(ov) || oe < be;
-                else if (!isnan(ov)) take = ov > bv || (ov == bv && oe < be);
-            }
-            if (take) {
-                bv = ov;
-                be = oe;
-                bval = oval;
-            }
-        }
-        if (be == 0x7fffffff || isnan(bv)) {  // nothing selectable: non-finite router input
-            fault = true;
-            be = r;
-            bval = 0.0f;
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const int e = (int)__reduce_min_sync(0xffffffffu, bk == mk ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
+        const float pv = __shfl_sync(0xffffffffu, bv, e & 31);
+        if (mk == 0u) fault = true;          // nothing selectable (non-finite scores)
         if (lane == r) {
-            my_id = be;
-            my_val = bval;
+            my_id = mk == 0u ? r : e;
+            my_val = mk == 0u ? 0.0f : pv;
+        }
+        if (mk != 0u && lane == (e & 31)) {
+#pragma unroll
+            for (int i = 0; i < NPER; ++i)
+                if (i == (e >> 5)) key[i] = 0u;
+            best();
         }
     }
     // weights over the k selected (lane r holds selection r)
@@ -495,9 +508,13 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
     prof_end(kPhRouterLogits, s);
     const int warps_per_block = 8;
     prof_begin(kPhTopk, s);
-    k_topk<<<(a.T + warps_per_block - 1) / warps_per_block, warps_per_block * 32, 0, s>>>(
-        a.logits, a.score_fn == MOE_SCORE_SIGMOID_BIAS ? a.bias : nullptr, a.T, a.E, a.k, a.score_fn,
-        a.ids, a.w, a.header + kHdrStatus);
+    {
+        const dim3 g((a.T + warps_per_block - 1) / warps_per_block), b(warps_per_block * 32);
+        const float *bias = a.score_fn == MOE_SCORE_SIGMOID_BIAS ? a.bias : nullptr;
+        if (a.E <= 256) k_topk<8><<<g, b, 0, s>>>(a.logits, bias, a.T, a.E, a.k, a.score_fn, a.ids, a.w, a.header + kHdrStatus);
+        else if (a.E <= 512) k_topk<16><<<g, b, 0, s>>>(a.logits, bias, a.T, a.E, a.k, a.score_fn, a.ids, a.w, a.header + kHdrStatus);
+        else k_topk<32><<<g, b, 0, s>>>(a.logits, bias, a.T, a.E, a.k, a.score_fn, a.ids, a.w, a.header + kHdrStatus);
+    }
     prof_end(kPhTopk, s);
     const size_t sh = (size_t)(kBucketWarps * a.E + kBucketThreads) * sizeof(int32_t);
     prof_begin(kPhBucket, s);
