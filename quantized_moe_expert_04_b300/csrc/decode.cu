@@ -755,8 +755,9 @@ __device__ __forceinline__ void q4k_pair_scales_f(uint4 hdr, int c, float &s0, f
 
 __global__ void __launch_bounds__(kDnThreads, kDnRegCtas) k_dec_down(DecArgs a)
 {
-    extern __shared__ __align__(16) uint8_t smem[];     // [warp][2][kDnBuf]
+    extern __shared__ __align__(16) uint8_t smem[];     // [warp][nbuf][buffer]
     griddep_wait();
+    griddep_launch();   // the finish kernel may launch now (it waits for this grid before reading)
     const int U = (int)a.header[kHdrNActive];
     const int H = a.H, FF = a.FF, nb = H / 256, FS = a.fs_dn;
     const int64_t rb = (int64_t)nb * 144;
@@ -925,13 +926,15 @@ __global__ void __launch_bounds__(kDnThreads, kDnRegCtas) k_dec_down(DecArgs a)
         }
     }
     cp_async_wait<0>();
-    griddep_launch();
 }
 
 // y = bf16(accumulated y), or the fixed-order sum of the slots in
 // deterministic mode, plus the shared expert's output; float4 per thread.
 __global__ void __launch_bounds__(256) k_dec_finish(DecArgs a)
 {
+    // the next call's router may launch now: before its own dependency wait it
+    // reads only the (static) router rows
+    griddep_launch();
     griddep_wait();
     const int H = a.H, FS = a.fs_dn, k = a.k;
     const int n4 = a.T * H / 4;
