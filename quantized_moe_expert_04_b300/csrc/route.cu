@@ -382,10 +382,17 @@ k_bucket(const int32_t *__restrict__ ids, int TK, int E, int32_t *__restrict__ c
     const int S = (TK + kBucketWarps - 1) / kBucketWarps;
     const int a0 = warp * S, a1 = min(TK, a0 + S);
     bool bad = false;
-    for (int a = a0 + lane; a < a1; a += 32) {
-        const int e = ids[a];
-        if (e >= 0 && e < E) atomicAdd(&hist[warp * E + e], 1);
-        else bad = true;
+    // 8 loads in flight per lane (the walk is latency-bound otherwise)
+    for (int ab = a0 + lane; ab < a1; ab += 32 * 8) {
+        int ev[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ev[j] = ab + 32 * j < a1 ? __ldg(ids + ab + 32 * j) : -2;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (ev[j] == -2) continue;
+            if (ev[j] >= 0 && ev[j] < E) atomicAdd(&hist[warp * E + ev[j]], 1);
+            else bad = true;
+        }
     }
     __syncthreads();
     // per expert: prefix over warps (in place), expert total
@@ -446,11 +453,13 @@ k_bucket(const int32_t *__restrict__ ids, int TK, int E, int32_t *__restrict__ c
         header[kHdrNActive] = (uint32_t)n_active_before;
     }
     __syncthreads();
-    // stable scatter
+    // stable scatter; the next chunk's ids are loaded while this one is ranked
+    int e_next = a0 + lane < a1 ? __ldg(ids + a0 + lane) : -1;
     for (int c0 = a0; c0 < a1; c0 += 32) {
         const int a = c0 + lane;
         const bool valid = a < a1;
-        int e = valid ? ids[a] : -1;
+        int e = valid ? e_next : -1;
+        e_next = c0 + 32 + lane < a1 ? __ldg(ids + c0 + 32 + lane) : -1;
         if (e < 0 || e >= E) e = -1 - lane;      // unique non-matching key for invalid lanes
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(peers & ((1u << lane) - 1u));
