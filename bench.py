@@ -211,10 +211,18 @@ def algorithmic(wl, T, ids_per_layer):
     return np.mean(total_bytes), {n: float(np.mean(v)) for n, v in per_kernel.items()}, flops, gemm_gateup_flops
 
 
-def kernel_source_hash():
+# The sources a kernel's code comes from: its own file and the shared headers.
+KERNEL_SOURCES = {
+    "dec": ["decode.cu", "moe_internal.cuh", "tc_ptx.cuh"],
+    "gemm": ["gemm_tc.cu", "moe_internal.cuh", "tc_ptx.cuh"],
+}
+
+
+def kernel_source_hash(kernel):
+    """Hash of the CUDA sources the kernel is built from (traffic figures go stale when it changes)."""
     import hashlib
     h = hashlib.sha256()
-    for fn in sorted(os.listdir(os.path.join(ROOT, "quantized_moe_expert_04_b300", "csrc"))):
+    for fn in KERNEL_SOURCES[kernel.split("_")[0]]:
         with open(os.path.join(ROOT, "quantized_moe_expert_04_b300", "csrc", fn), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -227,7 +235,7 @@ def profiled_traffic(kernel, workload, T):
         with open(path) as fh:
             d = json.load(fh)
         rec = d.get("%s:%s:T%d" % (kernel, workload, T))
-        if rec and rec.get("source_hash") == kernel_source_hash():
+        if rec and rec.get("source_hash") == kernel_source_hash(kernel):
             return rec["dram_bytes_per_launch"]
     except Exception:
         pass

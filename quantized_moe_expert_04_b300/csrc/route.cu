@@ -21,7 +21,6 @@ namespace moe {
 
 constexpr int kRouterTokens = 8;     // tokens per CTA in the logits kernel
 constexpr int kRouterWarps = 4;      // warps per CTA (one expert row at a time each)
-constexpr int kMaxPerLane = 32;      // E <= 1024 logits per warp
 
 __global__ void __launch_bounds__(kRouterWarps * 32)
 k_router_logits(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H, int E,
