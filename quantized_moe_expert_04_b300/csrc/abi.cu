@@ -51,6 +51,7 @@ WsLayout ws_layout(const moe_config &c, int32_t T)
     L.offsets = take((E + 1) * 4);
     L.assign = take(TK * 4);
     L.active = take((E + 1) * 4);
+    L.bhist = take((TK + kBucketItems - 1) / kBucketItems * E * 4);
     const bool gemv = use_gemv(c, T), det = (c.flags & MOE_FLAG_DETERMINISTIC) != 0;
     const size_t maxu = std::min<size_t>(E, TK);
     L.plan = take(gemv ? maxu * sizeof(DecPlan) : 0);
@@ -211,6 +212,7 @@ static RouteArgs route_args(const moe_config *cfg, const uint16_t *x, const floa
     r.offsets = (int32_t *)(base + L.offsets);
     r.assign = (int32_t *)(base + L.assign);
     r.active = (int32_t *)(base + L.active);
+    r.bhist = (int32_t *)(base + L.bhist);
     r.header = (uint32_t *)(base + L.header);
     return r;
 }

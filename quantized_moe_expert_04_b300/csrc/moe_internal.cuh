@@ -71,7 +71,7 @@ void prof_end(int phase, cudaStream_t s);
 // Workspace regions (byte offsets from the workspace base) for one call shape.
 struct WsLayout {
     size_t header, logits, ids, w, counts, offsets, assign, active, plan, xfrag;
-    size_t act, slots, yacc, xg, x16, sh_act, sh_out;
+    size_t act, slots, yacc, xg, x16, sh_act, sh_out, bhist;
     size_t act16, sh_act16, tiles_gu, tiles_dn, tiles_gus, tiles_dns, tmaps, gu, sh_gu, split_cnt;
     size_t total;
 };
@@ -96,8 +96,10 @@ struct RouteArgs {
     int32_t *ids;
     float *w;
     int32_t *counts, *offsets, *assign, *active;
+    int32_t *bhist;                      // bucketing: [ceil(T*k / kBucketItems)][E] per-CTA counts
     uint32_t *header;
 };
+constexpr int kBucketItems = 1024;       // assignments per CTA of the parallel bucketing
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s);
 
 struct ExpertArgs {

@@ -14,7 +14,7 @@
 //                    router row is read once per 8 tokens.
 //   k_topk           one warp per token, E/32 logits per lane in registers,
 //                    k rounds of a warp arg-max (equal keys: lower id).
-//   k_bucket         one CTA: stable counting sort of the T*k assignments.
+//   k_bucket_*       stable counting sort of the T*k assignments over the grid.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -354,124 +354,108 @@ k_topk(const float *__restrict__ logits, const float *__restrict__ bias, int T, 
     if (fault && lane == 0) set_status(status, MOE_ERR_DEVICE_FAULT);
 }
 
-// Stable counting sort of the T*k assignments by expert, one CTA of 1024
-// threads.  Warp w owns the contiguous assignment range [w*S, (w+1)*S):
-//   1. per-warp histograms hist[w][e] (shared memory);
-//   2. for each expert, the warps' counts are prefix-summed in warp order and
-//      the expert totals scanned -> offsets; base[w][e] = where warp w's
-//      first assignment to e goes;
-//   3. each warp walks its range in order, 32 at a time; lanes with the same
-//      expert are ranked by lane index (__match_any_sync) so the order of
-//      equal keys is the input order -- the sort is stable.
-// Also writes the ascending list of experts that received tokens.
-constexpr int kBucketThreads = 1024;
-constexpr int kBucketWarps = kBucketThreads / 32;
-
-__global__ void __launch_bounds__(kBucketThreads)
-k_bucket(const int32_t *__restrict__ ids, int TK, int E, int32_t *__restrict__ counts,
-         int32_t *__restrict__ offsets, int32_t *__restrict__ assign, int32_t *__restrict__ active,
-         uint32_t *header)
+// Stable counting sort of the T*k assignments by expert, over the grid: CTA
+// b owns the kBucketItems assignments [b*kBucketItems, (b+1)*kBucketItems).
+//   1. k_bucket_hist: each CTA's per-expert counts (shared-memory atomics);
+//   2. k_bucket_scan (one CTA): per expert, the CTAs' counts prefix-summed in
+//      CTA order and the expert totals scanned -> counts, offsets, the
+//      ascending list of experts that received tokens; base[b][e] = where
+//      CTA b's first assignment to e goes;
+//   3. k_bucket_scatter: within a CTA, lanes with the same expert are ranked
+//      by lane (__match_any_sync) and warps by a per-expert prefix over the
+//      warps, so equal keys keep the input order -- the sort is stable.
+__global__ void __launch_bounds__(kBucketItems)
+k_bucket_hist(const int32_t *__restrict__ ids, int TK, int E, int32_t *__restrict__ bhist, uint32_t *header)
 {
-    extern __shared__ int32_t sh[];              // hist[kBucketWarps][E], then scan scratch
-    int32_t *hist = sh;
-    int32_t *scan = sh + kBucketWarps * E;       // [kBucketThreads]
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < kBucketWarps * E; i += kBucketThreads) hist[i] = 0;
+    extern __shared__ int32_t h[];               // [E]
+    for (int i = threadIdx.x; i < E; i += blockDim.x) h[i] = 0;
     __syncthreads();
-    const int S = (TK + kBucketWarps - 1) / kBucketWarps;
-    const int a0 = warp * S, a1 = min(TK, a0 + S);
+    const int a = blockIdx.x * kBucketItems + threadIdx.x;
     bool bad = false;
-    // 8 loads in flight per lane (the walk is latency-bound otherwise)
-    for (int ab = a0 + lane; ab < a1; ab += 32 * 8) {
-        int ev[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ev[j] = ab + 32 * j < a1 ? __ldg(ids + ab + 32 * j) : -2;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (ev[j] == -2) continue;
-            if (ev[j] >= 0 && ev[j] < E) atomicAdd(&hist[warp * E + ev[j]], 1);
-            else bad = true;
+    if (a < TK) {
+        const int e = __ldg(ids + a);
+        if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+        else bad = true;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x) bhist[(int64_t)blockIdx.x * E + i] = h[i];
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(header + kHdrStatus, MOE_ERR_DEVICE_FAULT);
+}
+
+__global__ void __launch_bounds__(1024)
+k_bucket_scan(int nblk, int E, int32_t *__restrict__ bhist, int32_t *__restrict__ counts,
+              int32_t *__restrict__ offsets, int32_t *__restrict__ active, uint32_t *header)
+{
+    __shared__ int32_t scan[1024];
+    const int e = threadIdx.x;                   // one thread per expert (E <= 1024)
+    int tot = 0;
+    if (e < E) {
+#pragma unroll 8
+        for (int b = 0; b < nblk; ++b) {
+            const int c = bhist[(int64_t)b * E + e];
+            bhist[(int64_t)b * E + e] = tot;
+            tot += c;
+        }
+        counts[e] = tot;
+    }
+    // exclusive scans over the experts: of the totals, and of (total > 0)
+    scan[e] = tot;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+        const int v = e >= off ? scan[e - off] : 0;
+        __syncthreads();
+        scan[e] += v;
+        __syncthreads();
+    }
+    const int base = scan[e] - tot, total = scan[1023];
+    __syncthreads();
+    scan[e] = tot > 0 ? 1 : 0;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+        const int v = e >= off ? scan[e - off] : 0;
+        __syncthreads();
+        scan[e] += v;
+        __syncthreads();
+    }
+    if (e < E) {
+        offsets[e] = base;
+        if (tot > 0) active[scan[e] - 1] = e;
+#pragma unroll 8
+        for (int b = 0; b < nblk; ++b) bhist[(int64_t)b * E + e] += base;
+    }
+    if (e == 1023) {
+        offsets[E] = total;                      // = number of valid assignments
+        header[kHdrNActive] = (uint32_t)scan[1023];
+    }
+}
+
+__global__ void __launch_bounds__(kBucketItems)
+k_bucket_scatter(const int32_t *__restrict__ ids, int TK, int E, const int32_t *__restrict__ bhist,
+                 int32_t *__restrict__ assign)
+{
+    extern __shared__ int32_t wh[];              // [32 warps][E]
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wh[i] = 0;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int a = blockIdx.x * kBucketItems + threadIdx.x;
+    int e = a < TK ? __ldg(ids + a) : -1;
+    const bool valid = e >= 0 && e < E;
+    if (!valid) e = -1 - lane;                   // a key no other lane holds
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0) wh[warp * E + e] = __popc(peers);
+    __syncthreads();
+    for (int x = threadIdx.x; x < E; x += blockDim.x) {
+        int run = 0;
+#pragma unroll 8
+        for (int w = 0; w < 32; ++w) {
+            const int c = wh[w * E + x];
+            wh[w * E + x] = run;
+            run += c;
         }
     }
     __syncthreads();
-    // per expert: prefix over warps (in place), expert total
-    const int per_thread = (E + kBucketThreads - 1) / kBucketThreads;
-    int local_total = 0;
-    for (int j = 0; j < per_thread; ++j) {
-        const int e = threadIdx.x * per_thread + j;
-        if (e < E) {
-            int run = 0;
-            for (int w = 0; w < kBucketWarps; ++w) {
-                const int c = hist[w * E + e];
-                hist[w * E + e] = run;
-                run += c;
-            }
-            counts[e] = run;
-            local_total += run;
-        }
-    }
-    // block exclusive scan of the per-thread totals (contiguous expert ranges)
-    scan[threadIdx.x] = local_total;
-    __syncthreads();
-    for (int off = 1; off < kBucketThreads; off <<= 1) {
-        const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
-        __syncthreads();
-        scan[threadIdx.x] += v;
-        __syncthreads();
-    }
-    int base = scan[threadIdx.x] - local_total;
-    int n_active_before = 0;
-    // count actives in earlier threads: second scan on (count > 0)
-    int local_active = 0;
-    for (int j = 0; j < per_thread; ++j) {
-        const int e = threadIdx.x * per_thread + j;
-        if (e < E && counts[e] > 0) ++local_active;
-    }
-    __syncthreads();
-    scan[threadIdx.x] = local_active;
-    __syncthreads();
-    for (int off = 1; off < kBucketThreads; off <<= 1) {
-        const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
-        __syncthreads();
-        scan[threadIdx.x] += v;
-        __syncthreads();
-    }
-    n_active_before = scan[threadIdx.x] - local_active;
-    for (int j = 0; j < per_thread; ++j) {
-        const int e = threadIdx.x * per_thread + j;
-        if (e < E) {
-            const int c = counts[e];
-            offsets[e] = base;
-            for (int w = 0; w < kBucketWarps; ++w) hist[w * E + e] += base;
-            base += c;
-            if (c > 0) active[n_active_before++] = e;
-        }
-    }
-    if (threadIdx.x == kBucketThreads - 1) {
-        offsets[E] = base;                        // = number of valid assignments
-        header[kHdrNActive] = (uint32_t)n_active_before;
-    }
-    __syncthreads();
-    // stable scatter; the next chunk's ids are loaded while this one is ranked
-    int e_next = a0 + lane < a1 ? __ldg(ids + a0 + lane) : -1;
-    for (int c0 = a0; c0 < a1; c0 += 32) {
-        const int a = c0 + lane;
-        const bool valid = a < a1;
-        int e = valid ? e_next : -1;
-        e_next = c0 + 32 + lane < a1 ? __ldg(ids + c0 + 32 + lane) : -1;
-        if (e < 0 || e >= E) e = -1 - lane;      // unique non-matching key for invalid lanes
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        int pos = 0;
-        if (valid && e >= 0) pos = hist[warp * E + e] + rank;
-        __syncwarp();
-        if (valid && e >= 0) {
-            assign[pos] = a;
-            if (rank == 0) hist[warp * E + e] += __popc(peers);
-        }
-        __syncwarp();
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(header + kHdrStatus, MOE_ERR_DEVICE_FAULT);
+    if (valid) assign[bhist[(int64_t)blockIdx.x * E + e] + wh[warp * E + e] + rank] = a;
 }
 
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
@@ -488,8 +472,8 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
     if (!attrs_set) {
         cudaFuncSetAttribute(k_router_logits, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(kRouterTokens * 8192 * sizeof(uint16_t)));
-        cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((kBucketWarps * 1024 + kBucketThreads) * sizeof(int32_t)));
+        cudaFuncSetAttribute(k_bucket_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(32 * 1024 * sizeof(int32_t)));
         attrs_set = true;
     }
     const size_t xs_bytes = (size_t)kRouterTokens * a.H * sizeof(uint16_t);
@@ -524,10 +508,11 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
         else k_topk<32><<<g, b, 0, s>>>(a.logits, bias, a.T, a.E, a.k, a.score_fn, a.ids, a.w, a.header + kHdrStatus);
     }
     prof_end(kPhTopk, s);
-    const size_t sh = (size_t)(kBucketWarps * a.E + kBucketThreads) * sizeof(int32_t);
+    const int TK = a.T * a.k, nblk = (TK + kBucketItems - 1) / kBucketItems;
     prof_begin(kPhBucket, s);
-    k_bucket<<<1, kBucketThreads, sh, s>>>(a.ids, a.T * a.k, a.E, a.counts, a.offsets, a.assign, a.active,
-                                           a.header);
+    k_bucket_hist<<<nblk, kBucketItems, a.E * sizeof(int32_t), s>>>(a.ids, TK, a.E, a.bhist, a.header);
+    k_bucket_scan<<<1, 1024, 0, s>>>(nblk, a.E, a.bhist, a.counts, a.offsets, a.active, a.header);
+    k_bucket_scatter<<<nblk, kBucketItems, 32 * a.E * sizeof(int32_t), s>>>(a.ids, TK, a.E, a.bhist, a.assign);
     prof_end(kPhBucket, s);
     return cudaGetLastError();
 }
