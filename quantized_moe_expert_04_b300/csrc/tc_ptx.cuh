@@ -61,15 +61,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 }
 
 // ---------------------------------------------------------------- copies
-// 1-D bulk copy global -> shared, completing `bytes` of transaction on `bar`.
-// dst, src 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 // 2-D tiled tensor load (the tensor map's box at column x, row y) into shared
 // memory, completing its bytes on `bar`.  x * element size must be a multiple
 // of 16 bytes; rows past the tensor's extent are filled with zeros.
@@ -78,19 +69,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// Four rows y0..y3 of a 2-D tensor (box: one row of the map's box width, at
-// column x) gathered into consecutive box rows of shared memory, completing
-// on `bar`.  Same alignment rule for x as tma_load_2d.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int y0, int y1, int y2, int y3,
-                                            uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
         : "memory");
 }
 
@@ -126,13 +104,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-// arrive (once per calling thread) on `bar` when all cp.async of this thread
-// issued so far have completed; the barrier counts these arrivals
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
 
 template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
@@ -218,18 +189,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// one lane of the (converged) warp returns true
-__device__ __forceinline__ bool elect_one()
-{
-    uint32_t p;
-    asm volatile(
-        "{\n\t.reg .pred P1;\n\t.reg .b32 rl;\n\t"
-        "elect.sync rl|P1, 0xffffffff;\n\t"
-        "selp.u32 %0, 1, 0, P1;\n\t}"
-        : "=r"(p));
-    return p != 0;
-}
-
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
 // core groups 1024 bytes apart (SBO), version 1, base offset 0 (the tile
 // must start on a 1024-byte boundary).
@@ -271,21 +230,9 @@ __host__ __device__ __forceinline__ uint32_t idesc_f16_f32(int M, int N)
            | ((uint32_t)(M >> 4) << 24);      // M >> 4
 }
 
-// Byte offset of 16-byte chunk c (0..7) of row r in a K-major tile with
-// 128-byte rows and the 128-byte swizzle (8-row, 1024-byte atoms).
-__device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c)
-{
-    return ((r >> 3) << 10) + ((r & 7) << 7) + (((c ^ (r & 7)) & 7) << 4);
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v)
-{
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
 __device__ __forceinline__ void red_add_f32(float *p, float v)
