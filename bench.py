@@ -218,13 +218,39 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text):
+    """C/CUDA source with comments and whitespace removed (string literals kept)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':                                   # string literal, copied as is
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c.isspace():
+            i += 1
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash(kernel):
-    """Hash of the CUDA sources the kernel is built from (traffic figures go stale when it changes)."""
+    """Hash of the code (comments and whitespace aside) of the CUDA sources the kernel is
+    built from: its DRAM traffic figures go stale when that code changes."""
     import hashlib
     h = hashlib.sha256()
     for fn in KERNEL_SOURCES[kernel.split("_")[0]]:
-        with open(os.path.join(ROOT, "quantized_moe_expert_04_b300", "csrc", fn), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "quantized_moe_expert_04_b300", "csrc", fn), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -3,7 +3,7 @@
 // The teardown page ("Strata 引擎深度拆解", lcz.me/topic/2098/5, section 一,
 // CPU ledger) computes each selected expert once for all tokens of a 3-token
 // verify window; the decode critical path there is the expert arithmetic
-// (section 二 item 5).  Here a window is three kernels chained with
+// (section 二 item 5).  Here a window is four kernels chained with
 // programmatic dependent launch, so each one is scheduled while its
 // predecessor drains:
 //
@@ -20,10 +20,13 @@
 //                 through a private cp.async ring; the bytes are dequantised
 //                 straight into MMA A fragments (fp16, fp32 accumulation)
 //                 with the window's tokens as the 8 MMA columns; SiLU(g)*u in
-//                 registers.  It also asks L2 to prefetch the down matrices
-//                 of the selected experts.
+//                 registers.  (An L2 prefetch of the selected experts' down
+//                 matrices during gate/up exists behind a switch; measured
+//                 slower, it is off.)
 //   k_dec_down    down projection: units of (expert, 256 hidden columns, ff
-//                 segment) staged in shared memory with cp.async; Q4_K
+//                 segment) staged in shared memory with cp.async (segments
+//                 chosen so the slowest warp has the fewest rows; one buffer
+//                 per warp and 3 CTAs per SM when every warp has one unit); Q4_K
 //                 nibbles become exact fp32 values through the mantissa, the
 //                 sub-block scale and min are factored out of the sum over ff;
 //                 the weighted result is added into an fp32 accumulator of y
