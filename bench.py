@@ -148,40 +148,71 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle leg
 
-def oracle_sample(wl, T, layers, x_layers, time_budget_s=12.0, max_tokens=None, gen_device="cuda"):
+def oracle_sample(wl, T, layers, x_layers, gpu_ids=None, gpu_y32=None, time_budget_s=10.0, wall_budget_s=40.0,
+                  max_tokens=None, gen_device="cuda"):
     """Time the CPU oracle on a bounded sample: the first layers (and, for
     large T, the first max_tokens tokens) of the same workload.  Packing the
     oracle's blobs is untimed set-up; routing, bucketing, dequantisation and
-    the FFNs are timed.  Returns (tokens/s per layer, threads, description)."""
+    the FFNs are timed.  Where the GPU's ids and fp32 outputs of those layers
+    are given, the sample doubles as a parity check: ids compared (differences
+    are near-ties, counted), y compared by rel-L2 / max-abs (the oracle rerun
+    with the GPU's ids where they differ).
+    Returns (tokens/s per layer, threads, description, parity or None)."""
     import oracle
     threads = oracle.set_threads(0)
     done_tok, spent, used_layers = 0, 0.0, 0
+    num = den = 0.0
+    max_err = max_ref = 0.0
+    ties = compared = 0
+    wall0 = time.perf_counter()
     for l in layers:
         x = x_layers[l].cpu()
         if max_tokens is not None:
             x = x[:max_tokens]
         xb = synth.bf16_bits(x)
+        Ts = xb.shape[0]
         wr = synth.router_weight(wl, 0, l, device=gen_device).cpu().numpy()
         b = synth.router_bias(wl, 0, l, device=gen_device)
         b = None if b is None else b.cpu().numpy()
-        ids, _, _, _ = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
+        oids, _, kth, nxt = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
+        forced = None
+        if gpu_ids is not None:
+            g = gpu_ids[l][:Ts]
+            diff = [t for t in range(Ts) if not np.array_equal(g[t], oids[t])]
+            ties += len(diff)
+            compared += Ts
+            if diff:
+                forced = g
+        used = set(oids.reshape(-1).tolist()) | (set(forced.reshape(-1).tolist()) if forced is not None else set())
         blobs = [None] * wl.n_experts
-        for e in sorted(set(ids.reshape(-1).tolist())):
+        for e in sorted(used):
             blobs[e] = oracle.pack_expert_q4k(synth.expert_weight(wl, e, 0, l, device=gen_device).cpu().numpy())
         sblob = None
         if wl.has_shared:
             sblob = oracle.pack_shared_q8_0(synth.shared_weight(wl, 0, l, device=gen_device).cpu().numpy())
         t0 = time.perf_counter()
-        oracle.moe_forward(wl.hidden, wl.n_experts, wl.ff, wl.top_k, wl.score_fn, xb, wr, b, blobs,
-                           wl.shared_ff, sblob)
+        ref = oracle.moe_forward(wl.hidden, wl.n_experts, wl.ff, wl.top_k, wl.score_fn, xb, wr, b, blobs,
+                                 wl.shared_ff, sblob, forced_ids=forced)
         spent += time.perf_counter() - t0
-        done_tok += xb.shape[0]
+        if gpu_y32 is not None and l in gpu_y32:
+            got = gpu_y32[l][:Ts].astype(np.float64)
+            num += float(((got - ref) ** 2).sum())
+            den += float((ref ** 2).sum())
+            max_err = max(max_err, float(np.abs(got - ref).max()))
+            max_ref = max(max_ref, float(np.abs(ref).max()))
+        done_tok += Ts
         used_layers += 1
-        if spent >= time_budget_s:
+        if spent >= time_budget_s or time.perf_counter() - wall0 >= wall_budget_s:
             break
     desc = "%d layer(s) x %d token(s) of %s (oracle: fp64 route+bucket+dequant+FFN; packing untimed)" % (
         used_layers, done_tok // max(used_layers, 1), wl.name)
-    return done_tok / spent, threads, desc
+    parity = None
+    if gpu_y32 is not None and den > 0:
+        parity = {"rel_l2": float("%.3e" % math.sqrt(num / den)), "max_abs_over_max_ref": float("%.3e" % (max_err / max_ref)),
+                  "near_tie_tokens": ties, "tokens_compared": compared, "bar": {"rel_l2": 5e-3, "max_abs": 2e-2},
+                  "ok": math.sqrt(num / den) <= 5e-3 and max_err <= 2e-2 * max_ref,
+                  "sample": desc.split(" (")[0]}
+    return done_tok / spent, threads, desc, parity
 
 
 # ------------------------------------------------------------------ algorithmic work
@@ -197,7 +228,7 @@ def algorithmic(wl, T, ids_per_layer):
     counted."""
     E, H, FF, k = wl.n_experts, wl.hidden, wl.ff, wl.top_k
     rb = (H // 256) * 144
-    total_bytes, per_kernel = [], {"dec_route": [], "dec_gateup": [], "dec_down": []}
+    total_bytes, per_kernel = [], {"dec_route": [], "dec_gateup": [], "dec_down": [], "dec_layer": []}
     for ids in ids_per_layer:
         U = len(np.unique(ids))
         b = U * wl.blob_bytes + wl.shared_blob_bytes + E * H * 4 + (E * 4 if wl.bias != "none" else 0)
@@ -206,6 +237,7 @@ def algorithmic(wl, T, ids_per_layer):
         per_kernel["dec_route"].append(E * H * 4 + T * H * 2)
         per_kernel["dec_gateup"].append(U * 2 * FF * rb)
         per_kernel["dec_down"].append(U * FF * rb)
+        per_kernel["dec_layer"].append(U * wl.blob_bytes + wl.shared_blob_bytes)
     flops = 2 * T * E * H + 2 * T * k * 3 * H * FF + (2 * T * 3 * H * wl.shared_ff if wl.has_shared else 0)
     gemm_gateup_flops = 2 * T * k * 2 * H * FF
     return np.mean(total_bytes), {n: float(np.mean(v)) for n, v in per_kernel.items()}, flops, gemm_gateup_flops
@@ -270,12 +302,20 @@ def profiled_traffic(kernel, workload, T):
 
 # ------------------------------------------------------------------ arms
 
-def run_ours(args, world, rank, local):
-    wl = synth.WORKLOADS[args.workload]
-    T = args.tokens or DEFAULT_TOKENS[args.workload]
-    torch.cuda.set_device(local)
+# The five workloads: the headline (the Qwen-shaped MTP window of 3 tokens)
+# plus every other window size and the two prefill batches, each measured in
+# the same process after the headline.
+CONFIG_SET = [("qwen_decode", 1), ("qwen_decode", 3), ("qwen_decode", 5), ("deepseek_decode", 1),
+              ("deepseek_decode", 4), ("deepseek_decode", 8), ("qwen_prefill", 4096),
+              ("deepseek_prefill_skewed", 4096)]
+
+
+def measure(args, wl, T, nL, world, rank, local, K=None, soak_s=0.0, target_s=0.3, e2e=False,
+            cpu_budget=None, parity_layers=2):
+    """Pack nL distinct layers of workload wl, then time K graph replays of one
+    step (the nL layer calls with T-token inputs).  Returns the measurement
+    dict (value, roofline, clocks, ...)."""
     dev = torch.device("cuda", local)
-    nL = wl.layers if args.layers is None else args.layers
     flags = {"auto": 0, "gemv": moe.MOE_FLAG_FORCE_GEMV, "gemm": moe.MOE_FLAG_FORCE_GEMM}[args.path]
     flags |= moe.MOE_FLAG_STATIC_WEIGHTS     # the layers' weights are never rewritten
     cfg = moe.config_for(wl, flags)
@@ -294,22 +334,26 @@ def run_ours(args, world, rank, local):
             moe.moe_forward(cfg, xs[l], pl.router_w, pl.router_bias, pl.table, pl.shared, T, ys[l], None, ws,
                             stream)
 
-    # routing of each layer (for the algorithmic byte counts) + correctness status
-    ids_per_layer = []
+    # routing of each layer (for the algorithmic byte counts), fp32 outputs of
+    # the first layers (for the parity sample) and the device status
+    ids_per_layer, y32 = [], {}
     with torch.cuda.stream(stream):
         for l in range(nL):
             pl = layers[l]
-            moe.moe_forward(cfg, xs[l], pl.router_w, pl.router_bias, pl.table, pl.shared, T, ys[l], None, ws,
+            yf = torch.empty(T, wl.hidden, dtype=torch.float32, device=dev) if l < parity_layers else None
+            moe.moe_forward(cfg, xs[l], pl.router_w, pl.router_bias, pl.table, pl.shared, T, ys[l], yf, ws,
                             stream)
             ids, _, _, _ = routing_views(cfg, T, ws)
             ids_per_layer.append(ids.cpu().numpy().copy())
+            if yf is not None:
+                y32[l] = yf.cpu().numpy()
     st = moe.moe_last_device_status(ws, stream)
     if st != moe.MOE_OK:
-        raise moe.MoeError(st, "device status after the first pass")
+        raise moe.MoeError(st, "device status after the first pass (%s T=%d)" % (wl.name, T))
 
-    # launches per layer call + per-kernel durations (eager, profiled pass)
+    # launches per layer call + per-kernel durations (eager, event-bracketed pass)
     moe.moe_profile_enable(True)
-    prof_steps = max(3, min(args.steps or 20, 20))
+    prof_steps = max(3, min(K or 20, 20))
     with torch.cuda.stream(stream):
         for _ in range(prof_steps):
             step()
@@ -321,126 +365,164 @@ def run_ours(args, world, rank, local):
     # CUDA graph of one step
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        step()                                   # warm
+        step()
         stream.synchronize()
         with torch.cuda.graph(graph, stream=stream):
             step()
     torch.cuda.synchronize()
-
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
-    # steps: fixed by the caller, else enough for ~3 s of timed work
-    K = args.steps
+    t0 = time.perf_counter()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    per = (time.perf_counter() - t0) / 3
     if K is None:
-        t0 = time.perf_counter()
-        for _ in range(5):
-            graph.replay()
-        torch.cuda.synchronize()
-        per = (time.perf_counter() - t0) / 5
-        K = int(max(10, min(5000, 3.0 / max(per, 1e-6))))
+        K = int(max(10, min(20000, target_s / max(per, 1e-7))))
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # the soak keeps the GPU busy with the same replays for >= soak_s inside the
+        # sampled window (untimed), so the clock record reflects the timed steps
+        n_soak = int(soak_s / max(per, 1e-7)) if soak_s > 0 else 0
         with torch.cuda.stream(stream):
+            for _ in range(n_soak):
+                graph.replay()
             ev0.record(stream)
             for _ in range(K):
                 graph.replay()
             ev1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    ms = ev0.elapsed_time(ev1)
-    ms = all_max(ms, world)
+    ms = all_max(ev0.elapsed_time(ev1), world)
     clocks = clk.summary()
     step_ms = ms / K
-    tokens = T * nL * K * world
-    value = tokens / (ms / 1e3)
+    value = T * nL * K * world / (ms / 1e3)
 
-    # end to end through the C ABI with host buffers
-    xh = [x.cpu().pin_memory() for x in xs]
-    yh = [torch.empty(T, wl.hidden, dtype=torch.bfloat16).pin_memory() for _ in range(nL)]
-    xd = [torch.empty_like(x) for x in xs]
-    Ke = max(3, min(K, 50))
+    out = {"workload": wl.name, "tokens_per_window": T, "distinct_layers": nL, "value": round(value, 2),
+           "unit": UNIT, "steps": K, "ms_per_step": round(step_ms, 5), "us_per_layer": round(step_ms * 1e3 / nL, 3),
+           "setup_s": round(setup_s, 1), "clocks": clocks,
+           "timed_region_s": round(ms / 1e3, 3), "soak_replays": n_soak}
 
-    def e2e_step():
-        for l in range(nL):
-            pl = layers[l]
-            xd[l].copy_(xh[l], non_blocking=True)
-            moe.moe_forward(cfg, xd[l], pl.router_w, pl.router_bias, pl.table, pl.shared, T, ys[l], None, ws,
-                            stream)
-            yh[l].copy_(ys[l], non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
-        stream.synchronize()
-        barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(Ke):
-            e2e_step()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = all_max(e0.elapsed_time(e1), world)
-    e2e_value = T * nL * Ke * world / (e2e_ms / 1e3)
-
-    # roofline of the dominant kernel
+    # roofline: whole layer and the dominant kernel
     pk = peaks()
     step_bytes, kernel_bytes, flops, gemm_flops = algorithmic(wl, T, ids_per_layer)
     kernel_ms = {name: (v[2] / v[1] if v[1] else float("nan")) for name, v in prof.items()}
     share = {name: v[2] for name, v in prof.items()}
-    top = max(share, key=share.get)
-    decode = "dec_gateup" in prof
+    decode = any(n in prof for n in ("dec_layer", "dec_gateup"))
+    layer_s = step_ms / 1e3 / nL
+    out["hbm"] = {"algorithmic_bytes_per_call": int(step_bytes), "gbs": round(step_bytes / layer_s / 1e9, 1),
+                  "frac": round(step_bytes / layer_s / 1e9 / pk["hbm_gbs"], 4)}
+    out["tflops"] = {"algorithmic_flops_per_call": int(flops), "achieved": round(flops / layer_s / 1e12, 3),
+                     "frac": round(flops / layer_s / 1e12 / pk["bf16_tflops"], 4)}
     if decode:
-        dom = max((n for n in kernel_bytes if n in share), key=lambda n: share[n])
+        cands = [n for n in kernel_bytes if n in share]
+        dom = max(cands, key=lambda n: share[n])
         achieved = kernel_bytes[dom] / (kernel_ms[dom] / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": profiled_traffic(dom, wl.name, T), "peak_source": pk["source"] + " (burst copy)",
-                "avg_launch_us": round(kernel_ms[dom] * 1e3, 3),
-                "algorithmic_bytes_per_launch": int(kernel_bytes[dom]),
-                "per_kernel_gbs": {n: round(kernel_bytes[n] / (kernel_ms[n] / 1e3) / 1e9, 1)
-                                   for n in kernel_bytes if n in kernel_ms}}
+        out["roofline"] = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                           "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                           "traffic": profiled_traffic(dom, wl.name, T),
+                           "peak_source": pk["source"] + " (burst copy)",
+                           "avg_launch_us": round(kernel_ms[dom] * 1e3, 3),
+                           "algorithmic_bytes_per_launch": int(kernel_bytes[dom]),
+                           "per_kernel_gbs": {n: round(kernel_bytes[n] / (kernel_ms[n] / 1e3) / 1e9, 1)
+                                              for n in kernel_bytes if n in kernel_ms}}
     else:
-        dom = "gemm_gateup" if "gemm_gateup" in prof else top
+        dom = "gemm_gateup" if "gemm_gateup" in prof else max(share, key=share.get)
         achieved = gemm_flops / (kernel_ms[dom] / 1e3) / 1e12
-        peak = pk["bf16_tflops"]
-        roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(dom, wl.name, T),
-                "peak_source": pk["source"] + " (fp16 operands; same nominal rate as bf16)",
-                "avg_launch_us": round(kernel_ms[dom] * 1e3, 3), "algorithmic_flops_per_launch": int(gemm_flops)}
+        out["roofline"] = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2),
+                           "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
+                           "traffic": profiled_traffic(dom, wl.name, T),
+                           "peak_source": pk["source"] + " (fp16 operands; same nominal rate as bf16)",
+                           "avg_launch_us": round(kernel_ms[dom] * 1e3, 3),
+                           "algorithmic_flops_per_launch": int(gemm_flops)}
+    out["kernels_ms_per_launch"] = {k: round(v, 5) for k, v in kernel_ms.items()}
+    out["kernel_share"] = {k: round(v / sum(share.values()), 4) for k, v in share.items()}
+    out["gpu_launches"] = int(round(launches_per_call * nL * K))
+    out["dtype"] = "f16xf16->f32 (tensor-core MMAs), f32 combine"
 
+    if e2e:
+        # end to end through the C ABI with host buffers
+        xh = [x.cpu().pin_memory() for x in xs]
+        yh = [torch.empty(T, wl.hidden, dtype=torch.bfloat16).pin_memory() for _ in range(nL)]
+        xd = [torch.empty_like(x) for x in xs]
+        Ke = max(3, min(K, 50))
+
+        def e2e_step():
+            for l in range(nL):
+                pl = layers[l]
+                xd[l].copy_(xh[l], non_blocking=True)
+                moe.moe_forward(cfg, xd[l], pl.router_w, pl.router_bias, pl.table, pl.shared, T, ys[l], None, ws,
+                                stream)
+                yh[l].copy_(ys[l], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                e2e_step()
+            stream.synchronize()
+            barrier(world)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(Ke):
+                e2e_step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = all_max(e0.elapsed_time(e1), world)
+        out["e2e"] = {"value": round(T * nL * Ke * world / (e2e_ms / 1e3), 2), "unit": UNIT,
+                      "h2d_bytes_per_step": int(nL * T * wl.hidden * 2),
+                      "d2h_bytes_per_step": int(nL * T * wl.hidden * 2),
+                      "path": "pinned H2D x -> moe_forward -> D2H y, per layer, eager"}
+
+    if rank == 0 and cpu_budget is not None:
+        v, threads, desc, parity = oracle_sample(wl, T, list(range(nL)), xs, gpu_ids=ids_per_layer, gpu_y32=y32,
+                                                 time_budget_s=cpu_budget, wall_budget_s=4 * cpu_budget + 10,
+                                                 max_tokens=args.cpu_tokens if T > 64 else None)
+        out["cpu_baseline"] = {"value": round(v, 3), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+        out["parity"] = parity
+    del graph, layers, xs, ys, ws
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, world, rank, local):
+    torch.cuda.set_device(local)
+    wl = synth.WORKLOADS[args.workload or "qwen_decode"]
+    T = args.tokens or DEFAULT_TOKENS[wl.name]
+    nL = wl.layers if args.layers is None else args.layers
+    cpu = None if args.no_cpu_baseline else args.cpu_budget
+    head = measure(args, wl, T, nL, world, rank, local, K=args.steps, soak_s=args.soak, target_s=3.0, e2e=True,
+                   cpu_budget=cpu)
     out = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16xf16->f32 (gate/up), f32 (down)" if decode else "f16xf16->f32",
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": head["steps"],
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
         "data": "synthetic (seeded; x~N(0,1) bf16, router W~N(0,1/H), experts N(0,0.02^2) packed to Q4_K)",
         "config": {"workload": wl.name, "tokens_per_window": T, "hidden": wl.hidden, "experts": wl.n_experts,
                    "top_k": wl.top_k, "ff": wl.ff, "shared_ff": wl.shared_ff, "distinct_layers": nL,
                    "resident_expert_gb": round(nL * (wl.n_experts * wl.blob_bytes + wl.shared_blob_bytes) / 1e9, 2),
-                   "l2": "inputs larger than L2 (distinct layers rotated)", "graph": "one CUDA graph per step", "static_weights": True,
-                   "path": args.path,
-                   "parallelism": "replicas x%d" % world},
-        "hbm": {"algorithmic_bytes_per_call": int(step_bytes),
-                "gbs": round(step_bytes * nL * K / (ms / 1e3) / 1e9 * 1, 1),
-                "frac": round(step_bytes * nL * K / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)},
-        "tflops": round(flops * nL * K / (ms / 1e3) / 1e12, 3),
-        "roofline": roof,
-        "kernels_ms_per_launch": {k: round(v, 5) for k, v in kernel_ms.items()},
-        "gpu_launches": int(round(launches_per_call * nL * K)),
-        "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
-                "h2d_bytes_per_step": int(nL * T * wl.hidden * 2), "d2h_bytes_per_step": int(nL * T * wl.hidden * 2),
-                "path": "pinned H2D x -> moe_forward -> D2H y, per layer, eager"},
-        "clocks": clocks,
-        "setup_s": round(setup_s, 1),
+                   "l2": "inputs larger than L2 (distinct layers rotated)", "graph": "one CUDA graph per step",
+                   "static_weights": True, "path": args.path, "parallelism": "replicas x%d" % world},
+        "hbm": head["hbm"], "tflops": head["tflops"], "roofline": head["roofline"],
+        "kernels_ms_per_launch": head["kernels_ms_per_launch"], "kernel_share": head["kernel_share"],
+        "gpu_launches": head["gpu_launches"], "e2e": head["e2e"], "clocks": head["clocks"],
+        "timed_region_s": head["timed_region_s"], "soak_replays": head["soak_replays"], "setup_s": head["setup_s"],
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        v, threads, desc = oracle_sample(wl, T, list(range(nL)), xs, time_budget_s=args.cpu_budget,
-                                         max_tokens=args.cpu_tokens if T > 64 else None)
-        out["cpu_baseline"] = {"value": round(v, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-                               "sample": desc}
+    if "cpu_baseline" in head:
+        out["cpu_baseline"] = head["cpu_baseline"]
+        out["parity"] = head["parity"]
+    if args.workload is None and not args.no_configs:
+        confs = []
+        for name, Tc in CONFIG_SET:
+            wlc = synth.WORKLOADS[name]
+            r = measure(args, wlc, Tc, wlc.layers, world, rank, local, K=None, soak_s=0.0, target_s=0.3,
+                        e2e=False, cpu_budget=None if cpu is None else min(cpu, 4.0))
+            confs.append({k: r[k] for k in ("workload", "tokens_per_window", "distinct_layers", "value", "unit",
+                                            "steps", "ms_per_step", "us_per_layer", "hbm", "tflops", "roofline",
+                                            "kernel_share", "clocks", "cpu_baseline", "parity") if k in r})
+        out["configs"] = confs
     if rank == 0:
         print(json.dumps(out), flush=True)
 
@@ -449,8 +531,8 @@ def run_reference(args, world, rank):
     """The CPU oracle as the reference arm, on this arm's workload and metric."""
     if rank != 0:
         return
-    wl = synth.WORKLOADS[args.workload]
-    T = args.tokens or DEFAULT_TOKENS[args.workload]
+    wl = synth.WORKLOADS[args.workload or "qwen_decode"]
+    T = args.tokens or DEFAULT_TOKENS[wl.name]
     gen = "cuda" if torch.cuda.is_available() else "cpu"
     nL = min(wl.layers if args.layers is None else args.layers, 8)
     Ts = T if T <= 64 else args.cpu_tokens
@@ -502,12 +584,16 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="qwen_decode")
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default=None,
+                    help="one workload only (default: the qwen_decode T=3 headline, then every config)")
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--cpu-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="headline only")
+    ap.add_argument("--soak", type=float, default=1.2,
+                    help="seconds of untimed replays inside the clock-sampled window before the timed steps")
     ap.add_argument("--path", choices=["auto", "gemv", "gemm"], default="auto",
                     help="expert kernels: auto (GEMV for T <= 8, tensor-core GEMM above), or force one")
     args = ap.parse_args()

@@ -169,6 +169,18 @@ MOE_API moe_status moe_dequant_q4k(const uint8_t *blocks, int64_t rows, int64_t 
 MOE_API moe_status moe_dequant_q8_0(const uint8_t *blocks, int64_t rows, int64_t cols, float *out,
                             moe_stream_t stream);
 
+/* Test hooks of the tensor-core operand rounding: the fp16 weights that the
+ * fused decode and prefill kernels multiply, produced by the same device
+ * functions those kernels call, as binary16 bit patterns out[rows][cols]
+ * (device).  Q4_K: S_j = fp16(d*sc_j), NZ_j = fp16(-(dmin*m_j)),
+ * w = fp16(q*S_j + NZ_j) rounded once; Q8_0: w = fp16(d*q).  The pages fix no
+ * precision; this rounding is the library's (see moe_forward).  Errors as
+ * moe_dequant_q4k (Q8_0: out 4-byte aligned). */
+MOE_API moe_status moe_dequant_q4k_f16(const uint8_t *blocks, int64_t rows, int64_t cols, uint16_t *out,
+                               moe_stream_t stream);
+MOE_API moe_status moe_dequant_q8_0_f16(const uint8_t *blocks, int64_t rows, int64_t cols, uint16_t *out,
+                                moe_stream_t stream);
+
 /* ---------------------------------------------------------------- workspace */
 
 /*
@@ -208,7 +220,9 @@ MOE_API moe_status moe_route(const moe_config *cfg, const uint16_t *x, const flo
  * dequantised weights by the fp16 hidden states with fp32 accumulation (warp
  * MMAs), the down projection runs in fp32.  Larger T runs the tensor-core
  * grouped GEMM with fp16 operands and fp32 accumulation.  Both paths need
- * |x| < 65504 (fp16 range; larger values set MOE_ERR_DEVICE_FAULT).
+ * |x| < 65504 (fp16 range; larger values set MOE_ERR_DEVICE_FAULT), and the
+ * tensor-core path also needs |SiLU(g)*u| <= 65504 (its down projection
+ * multiplies fp16 activations; a larger one sets MOE_ERR_DEVICE_FAULT).
  */
 MOE_API moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *router_w,
                        const float *router_bias, const uint8_t *const *expert_blobs,
@@ -244,20 +258,27 @@ MOE_API moe_status moe_last_device_status(void *ws, moe_stream_t stream);
  * scratch is a file-scope device array of MOE_STATIC_WS_BYTES bytes inside
  * the library, which every GPU that loads the library holds until the
  * process exits.  Calls whose moe_workspace_bytes(cfg, T) exceeds it return
- * MOE_ERR_WORKSPACE_TOO_SMALL (4 MiB fits decode windows of up to 8 tokens of
- * both the 2560x512x320 and the 4096x256x2048 + shared layer shapes).
- * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ * MOE_ERR_WORKSPACE_TOO_SMALL; with the default flags 4 MiB fits decode
+ * windows of up to 8 tokens of both the 2560x512x320 and the 4096x256x2048
+ * + shared layer shapes (MOE_FLAG_DETERMINISTIC needs more: see
+ * moe_workspace_bytes).  Nothing is allocated: no cudaMalloc, cudaFree or
+ * allocating library call.
  *
- * dev_status (device uint32, may be NULL) receives the call's device-side
- * status (0 = MOE_OK, else a moe_status), as moe_last_device_status reports
- * it for an ordinary workspace.
+ * Every argument is checked before the array is touched; a rejected call
+ * enqueues nothing and leaves *dev_status as it was.  Otherwise dev_status
+ * (device uint32, 4-byte aligned, may be NULL) receives the call's
+ * device-side status (0 = MOE_OK, else a moe_status), as
+ * moe_last_device_status reports it for an ordinary workspace; a call with
+ * T == 0 writes MOE_OK there.
  *
  * Every call on a device shares the one array, which keeps the previous
  * call's contents (the call clears its header itself).  Calls that overlap on
  * the GPU -- different streams without ordering, or several host threads --
  * race on it: order them.  The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress, with that device current);
- * make that first call before any stream capture.
+ * array's device address (cudaGetSymbolAddress, with that device current)
+ * and keeps it for the life of the process; make that first call before any
+ * stream capture, and do not call cudaDeviceReset on a device after it (the
+ * kept address would then be stale).
  */
 #define MOE_STATIC_WS_BYTES (4u << 20)
 MOE_API moe_status moe_forward_static_ws(const moe_config *cfg, const uint16_t *x, const float *router_w,

@@ -40,6 +40,11 @@ def lib() -> ctypes.CDLL:
         L.orc_f32_to_f16.restype = ctypes.c_uint16
         L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
         L.orc_f16_to_f32.restype = ctypes.c_float
+        L.orc_f64_to_f16.argtypes = [ctypes.c_double]
+        L.orc_f64_to_f16.restype = ctypes.c_uint16
+        for name in ("orc_q4k_dequantize_f16", "orc_q8_0_dequantize_f16"):
+            getattr(L, name).argtypes = [_p, _i64, _i64, _p]
+            getattr(L, name).restype = None
         L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
         L.orc_bf16_to_f32.restype = ctypes.c_float
         for name in ("orc_q4k_quantize", "orc_q8_0_quantize"):
@@ -80,6 +85,10 @@ def f32_to_f16_bits(v: float) -> int:
     return int(lib().orc_f32_to_f16(float(v)))
 
 
+def f64_to_f16_bits(v: float) -> int:
+    return int(lib().orc_f64_to_f16(float(v)))
+
+
 def f16_bits_to_f32(b: int) -> float:
     return float(lib().orc_f16_to_f32(int(b)))
 
@@ -101,6 +110,24 @@ def q4k_dequantize(blob: np.ndarray, rows: int, cols: int) -> np.ndarray:
     assert blob.size == rows * (cols // QK_K) * Q4K_BYTES
     out = np.empty((rows, cols), np.float32)
     lib().orc_q4k_dequantize(_ptr(blob), rows, cols, _ptr(out))
+    return out
+
+
+def q4k_dequantize_f16(blob: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """The fp16 operand rounding of the Q4_K weights (R9): uint16 bit patterns [rows, cols]."""
+    blob = _c(blob, np.uint8)
+    assert blob.size == rows * (cols // QK_K) * Q4K_BYTES
+    out = np.empty((rows, cols), np.uint16)
+    lib().orc_q4k_dequantize_f16(_ptr(blob), rows, cols, _ptr(out))
+    return out
+
+
+def q8_0_dequantize_f16(blob: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """fp16(d*q) of the Q8_0 weights (R9): uint16 bit patterns [rows, cols]."""
+    blob = _c(blob, np.uint8)
+    assert blob.size == rows * (cols // QK8) * Q8_BYTES
+    out = np.empty((rows, cols), np.uint16)
+    lib().orc_q8_0_dequantize_f16(_ptr(blob), rows, cols, _ptr(out))
     return out
 
 

@@ -72,6 +72,15 @@
  *  R8  y_t = sum_r w_r * o_{t,r} over r ascending, plus (when present) the
  *      always-on shared expert's FFN of x_t with weight 1 and Q8_0 weights.
  *
+ *  R9  Tensor-core operand rounding of the dequantised weights (the GPU path
+ *      multiplies fp16 weights; the pages fix no precision, so this is the
+ *      rounding the GPU path states for itself, written out here so that its
+ *      fused dequantisation can be checked bit for bit):
+ *        Q4_K: S_j = fp16(d*sc_j), NZ_j = fp16(-(dmin*m_j)) (each product exact
+ *              in fp32, rounded once to fp16), w = fp16(q*S_j + NZ_j) with the
+ *              sum taken exactly and rounded once;
+ *        Q8_0: w = fp16(d*q) (exact product, rounded once).
+ *
  * Precision: quantise/dequantise in fp32 exactly as R1-R3 state; router,
  * scores, weights and every FFN product and sum in fp64.
  *
@@ -131,6 +140,28 @@ uint16_t orc_f32_to_f16(float f)
     if (r >= 2048.0) { r = 1024.0; ex += 1; }   /* carried into the next binade */
     if (ex > 15) return sign | 0x7c00;           /* overflow -> infinity */
     if (r < 1024.0) return sign | (uint16_t)r;   /* subnormal (ex == -14) */
+    return sign | (uint16_t)(((ex + 15) << 10) | ((int)r - 1024));
+}
+
+/* fp64 -> IEEE binary16, round to nearest, ties to even: the same steps as
+ * orc_f32_to_f16 applied to a double, for values that need more than fp32 to
+ * be held exactly before their one rounding (R9). */
+uint16_t orc_f64_to_f16(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    if (isnan(v)) return 0x7e00;
+    if (isinf(v)) return sign | 0x7c00;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    int e2;
+    frexp(a, &e2);
+    int ex = e2 - 1;
+    if (ex < -14) ex = -14;
+    double ulp = ldexp(1.0, ex - 10);
+    double r = rint(a / ulp);
+    if (r >= 2048.0) { r = 1024.0; ex += 1; }
+    if (ex > 15) return sign | 0x7c00;
+    if (r < 1024.0) return sign | (uint16_t)r;
     return sign | (uint16_t)(((ex + 15) << 10) | ((int)r - 1024));
 }
 
@@ -307,6 +338,53 @@ void orc_q8_0_dequantize(const uint8_t *blob, int64_t rows, int64_t cols, float 
 #pragma omp parallel for schedule(static)
     for (int64_t b = 0; b < nb; ++b)
         orc_q8_0_dequantize_block(blob + b * ORC_Q8_BYTES, out + b * ORC_QK8);
+}
+
+/* ------------------------------------------------------------------ */
+/* fp16 operand rounding of the dequantised weights (R9)               */
+/* ------------------------------------------------------------------ */
+
+/* One Q4_K block -> 256 binary16 bit patterns: per sub-block j the scale
+ * and negated min rounded to fp16, then q*S + NZ taken exactly (every term
+ * fits a double) and rounded once. */
+void orc_q4k_dequantize_f16_block(const uint8_t *blk, uint16_t *y)
+{
+    float d = orc_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+    float dmin = orc_f16_to_f32((uint16_t)(blk[2] | (blk[3] << 8)));
+    const uint8_t *scales = blk + 4, *qs = blk + 16;
+    for (int c = 0; c < 4; ++c) {
+        for (int half = 0; half < 2; ++half) {
+            int j = 2 * c + half, sc, m;
+            q4k_get_scale_min(scales, j, &sc, &m);
+            double S = orc_f16_to_f32(orc_f32_to_f16(d * (float)sc));       /* d*sc exact in fp32 */
+            double NZ = orc_f16_to_f32(orc_f32_to_f16(-(dmin * (float)m)));
+            for (int l = 0; l < 32; ++l) {
+                int q = half ? (qs[32 * c + l] >> 4) : (qs[32 * c + l] & 15);
+                y[64 * c + 32 * half + l] = orc_f64_to_f16((double)q * S + NZ);
+            }
+        }
+    }
+}
+
+void orc_q4k_dequantize_f16(const uint8_t *blob, int64_t rows, int64_t cols, uint16_t *out)
+{
+    int64_t nb = rows * (cols / ORC_QK_K);
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nb; ++b)
+        orc_q4k_dequantize_f16_block(blob + b * ORC_Q4K_BYTES, out + b * ORC_QK_K);
+}
+
+/* One Q8_0 block -> 32 binary16 patterns fp16(d*q) (d*q exact in fp32). */
+void orc_q8_0_dequantize_f16(const uint8_t *blob, int64_t rows, int64_t cols, uint16_t *out)
+{
+    int64_t nb = rows * (cols / ORC_QK8);
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nb; ++b) {
+        const uint8_t *blk = blob + b * ORC_Q8_BYTES;
+        float d = orc_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+        for (int i = 0; i < ORC_QK8; ++i)
+            out[b * ORC_QK8 + i] = orc_f32_to_f16(d * (float)(int8_t)blk[2 + i]);
+    }
 }
 
 /* ------------------------------------------------------------------ */

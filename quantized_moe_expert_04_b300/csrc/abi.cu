@@ -88,6 +88,41 @@ static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK 
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+static moe_status check_call(const moe_config *cfg, const uint16_t *x, const float *router_w,
+                             const float *router_bias, int32_t T, void *ws, size_t ws_bytes)
+{
+    if (!cfg_valid(cfg)) {
+        if (!cfg) return MOE_ERR_INVALID_ARG;
+        if (cfg->score_fn != MOE_SCORE_SOFTMAX && cfg->score_fn != MOE_SCORE_SIGMOID_BIAS)
+            return MOE_ERR_INVALID_ARG;
+        if (cfg->reserved != 0 || cfg->top_k < 1 || cfg->top_k > cfg->n_experts) return MOE_ERR_INVALID_ARG;
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !router_w)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ws) || (x && !aligned16(x)) || (router_w && !aligned16(router_w)))
+        return MOE_ERR_MISALIGNED;
+    (void)router_bias;
+    if (ws_bytes < ws_layout(*cfg, T).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return MOE_OK;
+}
+
+// Every host-side check of moe_forward (also run by moe_forward_static_ws
+// before it touches its array): nothing is enqueued when one fails.
+moe_status forward_checks(const moe_config *cfg, const uint16_t *x, const float *router_w, const float *router_bias,
+                          const uint8_t *const *expert_blobs, const uint8_t *shared_blob, int32_t T, uint16_t *y,
+                          float *y_f32, void *ws, size_t ws_bytes)
+{
+    moe_status st = check_call(cfg, x, router_w, router_bias, T, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (T > 0 && (!y || !expert_blobs)) return MOE_ERR_INVALID_ARG;
+    if (cfg->shared_ff > 0 && T > 0 && !shared_blob) return MOE_ERR_INVALID_ARG;
+    if ((y && !aligned16(y)) || (y_f32 && !aligned16(y_f32)) || (shared_blob && !aligned16(shared_blob)))
+        return MOE_ERR_MISALIGNED;
+    if (T > 0 && (cfg->flags & MOE_FLAG_FORCE_GEMV) && !use_gemv(*cfg, T)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
 }  // namespace moe
 
 using namespace moe;
@@ -159,6 +194,27 @@ moe_status moe_dequant_q8_0(const uint8_t *blocks, int64_t rows, int64_t cols, f
     return cuda_status(launch_dequant_q8_0(blocks, rows * (cols / kQK8), out, (cudaStream_t)stream));
 }
 
+moe_status moe_dequant_q4k_f16(const uint8_t *blocks, int64_t rows, int64_t cols, uint16_t *out, moe_stream_t stream)
+{
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % kQK) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(blocks) || !aligned16(out)) return MOE_ERR_MISALIGNED;
+    return cuda_status(launch_dequant_q4k_f16(blocks, rows * (cols / kQK), out, (cudaStream_t)stream));
+}
+
+moe_status moe_dequant_q8_0_f16(const uint8_t *blocks, int64_t rows, int64_t cols, uint16_t *out,
+                                moe_stream_t stream)
+{
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % kQK8) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !out) return MOE_ERR_INVALID_ARG;
+    if (((uintptr_t)out & 3u) != 0) return MOE_ERR_MISALIGNED;
+    return cuda_status(launch_dequant_q8_0_f16(blocks, rows * (cols / kQK8), out, (cudaStream_t)stream));
+}
+
 size_t moe_workspace_bytes(const moe_config *cfg, int32_t max_tokens)
 {
     if (!cfg_valid(cfg) || max_tokens < 0) return 0;
@@ -171,25 +227,6 @@ moe_status moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream)
     return cuda_status(cudaMemsetAsync(ws, 0, kHeaderBytes, (cudaStream_t)stream));
 }
 
-static moe_status check_call(const moe_config *cfg, const uint16_t *x, const float *router_w,
-                             const float *router_bias, int32_t T, void *ws, size_t ws_bytes)
-{
-    if (!cfg_valid(cfg)) {
-        if (!cfg) return MOE_ERR_INVALID_ARG;
-        if (cfg->score_fn != MOE_SCORE_SOFTMAX && cfg->score_fn != MOE_SCORE_SIGMOID_BIAS)
-            return MOE_ERR_INVALID_ARG;
-        if (cfg->reserved != 0 || cfg->top_k < 1 || cfg->top_k > cfg->n_experts) return MOE_ERR_INVALID_ARG;
-        return MOE_ERR_UNSUPPORTED_SHAPE;
-    }
-    if (T < 0) return MOE_ERR_INVALID_ARG;
-    if (!ws) return MOE_ERR_INVALID_ARG;
-    if (T > 0 && (!x || !router_w)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(ws) || (x && !aligned16(x)) || (router_w && !aligned16(router_w)))
-        return MOE_ERR_MISALIGNED;
-    (void)router_bias;
-    if (ws_bytes < ws_layout(*cfg, T).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-    return MOE_OK;
-}
 
 static RouteArgs route_args(const moe_config *cfg, const uint16_t *x, const float *router_w,
                             const float *router_bias, int32_t T, void *ws)
@@ -240,19 +277,15 @@ moe_status moe_route(const moe_config *cfg, const uint16_t *x, const float *rout
     return cuda_status(e);
 }
 
+
 moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *router_w,
                        const float *router_bias, const uint8_t *const *expert_blobs,
                        const uint8_t *shared_blob, int32_t T, uint16_t *y, float *y_f32, void *ws,
                        size_t ws_bytes, moe_stream_t stream)
 {
-    moe_status st = check_call(cfg, x, router_w, router_bias, T, ws, ws_bytes);
+    moe_status st = forward_checks(cfg, x, router_w, router_bias, expert_blobs, shared_blob, T, y, y_f32, ws, ws_bytes);
     if (st != MOE_OK) return st;
-    if (T > 0 && (!y || !expert_blobs)) return MOE_ERR_INVALID_ARG;
-    if (cfg->shared_ff > 0 && T > 0 && !shared_blob) return MOE_ERR_INVALID_ARG;
-    if ((y && !aligned16(y)) || (y_f32 && !aligned16(y_f32)) || (shared_blob && !aligned16(shared_blob)))
-        return MOE_ERR_MISALIGNED;
     if (T == 0) return MOE_OK;
-    if ((cfg->flags & MOE_FLAG_FORCE_GEMV) && !use_gemv(*cfg, T)) return MOE_ERR_UNSUPPORTED_SHAPE;
     cudaStream_t s = (cudaStream_t)stream;
     const WsLayout L = ws_layout(*cfg, T);
     char *base = (char *)ws;

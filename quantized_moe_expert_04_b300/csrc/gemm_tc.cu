@@ -41,6 +41,7 @@
 
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
+#include "dequant_f16.cuh"
 
 namespace moe {
 
@@ -107,6 +108,15 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs &g, int idx)
     return ti;
 }
 
+// a = SiLU(g) * u as the fp16 operand of the down projection.  A value
+// beyond the fp16 range (it would become +-inf, or NaN) is a device fault:
+// the call reports MOE_ERR_DEVICE_FAULT rather than a silently infinite y.
+__device__ __forceinline__ __half act_to_f16(float a, uint32_t *status)
+{
+    if (!(fabsf(a) <= 65504.0f)) set_status(status, MOE_ERR_DEVICE_FAULT);
+    return __float2half_rn(a);
+}
+
 // Bounded wait on an mbarrier phase; false on abort (another role gave up) or
 // on timeout (this call records MOE_ERR_TIMEOUT and raises the abort flag).
 // Waiting warps sleep in the try_wait (hardware suspend, up to ~20 us per
@@ -127,58 +137,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-__device__ __forceinline__ __half2 u2h2(uint32_t u)
-{
-    __half2 h;
-    memcpy(&h, &u, 4);
-    return h;
-}
-
-__device__ __forceinline__ uint32_t h22u(__half2 h)
-{
-    uint32_t u;
-    memcpy(&u, &h, 4);
-    return u;
-}
-
 // ---------------------------------------------------------------- dequant
-
-// 4-bit quants of 4 consecutive bytes -> fp16 pairs (exact integers), low and
-// high nibbles: 1024 + q via the fp16 exponent trick, then remove the offset.
-__device__ __forceinline__ void nibbles_to_q(uint32_t w, __half2 &lo01, __half2 &lo23, __half2 &hi01, __half2 &hi23)
-{
-    const uint32_t p01 = __byte_perm(w, 0, 0x4140);   // bytes b0, b1 into the two halves
-    const uint32_t p23 = __byte_perm(w, 0, 0x4342);   // b2, b3
-    const __half2 k1024 = __float2half2_rn(1024.0f);
-    const __half2 k16th = __float2half2_rn(0.0625f);
-    const __half2 km64 = __float2half2_rn(-64.0f);
-    lo01 = __hsub2(u2h2((p01 & 0x000F000Fu) | 0x64006400u), k1024);          // q
-    lo23 = __hsub2(u2h2((p23 & 0x000F000Fu) | 0x64006400u), k1024);
-    hi01 = __hfma2(u2h2((p01 & 0x00F000F0u) | 0x64006400u), k16th, km64);    // (1024 + 16q)/16 - 64 = q
-    hi23 = __hfma2(u2h2((p23 & 0x00F000F0u) | 0x64006400u), k16th, km64);
-}
-
-// Q4_K block header -> fp16 (scale, -min) of the sub-block pair (2g, 2g+1):
-// S = (fp16(d sc_2g), fp16(d sc_2g+1)), NZ likewise with -dmin m.  The 6-bit
-// values are exact fp16 integers and each product rounds once, as
-// fp16(fp32(d) * sc) does.
-__device__ __forceinline__ void q4k_pair_scales_h(uint4 hdr, int g, __half2 &S, __half2 &NZ)
-{
-    const uint32_t scw = g < 2 ? (hdr.y & 0x3F3F3F3Fu) : ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u));
-    const uint32_t mw = g < 2 ? (hdr.z & 0x3F3F3F3Fu) : (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u));
-    const uint32_t sel = (g & 1) ? 0x5342u : 0x5140u;
-    const __half2 k1024 = __float2half2_rn(1024.0f);
-    const __half2 dd = u2h2(__byte_perm(hdr.x, 0, 0x1010)), mm = u2h2(__byte_perm(hdr.x, 0, 0x3232) ^ 0x80008000u);
-    S = __hmul2(dd, __hsub2(u2h2(__byte_perm(scw, 0x64646464u, sel)), k1024));
-    NZ = __hmul2(mm, __hsub2(u2h2(__byte_perm(mw, 0x64646464u, sel)), k1024));
-}
-
-// int8 pair (two bytes of a 16-bit word) -> exact fp16 pair
-__device__ __forceinline__ __half2 i8pair_to_h2(uint32_t pair16)
-{
-    const uint32_t p = (__byte_perm(pair16, 0, 0x4140) ^ 0x00800080u) & 0x00FF00FFu;   // q + 128
-    return __hsub2(u2h2(p | 0x64006400u), __float2half2_rn(1152.0f));                  // 1024 + q + 128 - 1152
-}
+// (the fp16 operand recipe lives in dequant_f16.cuh, shared with the decode
+// kernel and the test hooks)
 
 // gate/up, Q4_K, one 128-wide K stage: thread (row, half h) turns group g of
 // the row's super-block (32 quant bytes at q: 32 weights of sub-block 2g in
@@ -198,12 +159,12 @@ __device__ __forceinline__ void dequant_gu_q4k_tmem(const uint8_t *hdr_p, const 
     uint32_t lo[16], hi[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        __half2 l01, l23, h01, h23;
-        nibbles_to_q(words[i], l01, l23, h01, h23);
-        lo[2 * i] = h22u(__hfma2(l01, S_lo, NZ_lo));
-        lo[2 * i + 1] = h22u(__hfma2(l23, S_lo, NZ_lo));
-        hi[2 * i] = h22u(__hfma2(h01, S_hi, NZ_hi));
-        hi[2 * i + 1] = h22u(__hfma2(h23, S_hi, NZ_hi));
+        uint32_t o[4];
+        q4k_word_f16(words[i], S_lo, NZ_lo, S_hi, NZ_hi, o);
+        lo[2 * i] = o[0];
+        lo[2 * i + 1] = o[1];
+        hi[2 * i] = o[2];
+        hi[2 * i + 1] = o[3];
     }
     tmem_st16(taddr, lo);
     tmem_st16(taddr + 16, hi);
@@ -222,7 +183,7 @@ __device__ __forceinline__ void dequant_gu_q80_tmem(const uint8_t *rr, int o, in
         const __half2 D = __half2half2(__ushort_as_half(r16[17 * b]));
         uint32_t v[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = h22u(__hmul2(i8pair_to_h2(r16[17 * b + 1 + i]), D));
+        for (int i = 0; i < 16; ++i) v[i] = q80_pair_f16(r16[17 * b + 1 + i], D);
         tmem_st16(taddr + 16 * bi, v);
     }
 }
@@ -259,15 +220,12 @@ __device__ __forceinline__ void dequant_dn_q4k(const uint8_t *raw, uint32_t a_ti
         const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int p = 0; p < 2; ++p) {                   // 8 bytes: 8 low and 8 high weights
-            __half2 l01, l23, h01, h23, l45, l67, h45, h67;
-            nibbles_to_q(words[2 * p], l01, l23, h01, h23);
-            nibbles_to_q(words[2 * p + 1], l45, l67, h45, h67);
+            uint32_t a[4], b[4];
+            q4k_word_f16(words[2 * p], S_lo, NZ_lo, S_hi, NZ_hi, a);
+            q4k_word_f16(words[2 * p + 1], S_lo, NZ_lo, S_hi, NZ_hi, b);
             const int h_lo = 64 * c + NB * part + 16 * u + 8 * p;
-            st_shared_v4(a_tile + mn_off(h_lo, row), h22u(__hfma2(l01, S_lo, NZ_lo)), h22u(__hfma2(l23, S_lo, NZ_lo)),
-                         h22u(__hfma2(l45, S_lo, NZ_lo)), h22u(__hfma2(l67, S_lo, NZ_lo)));
-            st_shared_v4(a_tile + mn_off(h_lo + 32, row), h22u(__hfma2(h01, S_hi, NZ_hi)),
-                         h22u(__hfma2(h23, S_hi, NZ_hi)), h22u(__hfma2(h45, S_hi, NZ_hi)),
-                         h22u(__hfma2(h67, S_hi, NZ_hi)));
+            st_shared_v4(a_tile + mn_off(h_lo, row), a[0], a[1], b[0], b[1]);
+            st_shared_v4(a_tile + mn_off(h_lo + 32, row), a[2], a[3], b[2], b[3]);
         }
     }
 }
@@ -287,7 +245,7 @@ __device__ __forceinline__ void dequant_dn_q80(const uint8_t *raw, uint32_t a_ti
         const __half2 D = __half2half2(__ushort_as_half(blk[0]));
         uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = h22u(__hmul2(i8pair_to_h2(blk[1 + hh0 / 2 + i]), D));
+        for (int i = 0; i < 4; ++i) o[i] = q80_pair_f16(blk[1 + hh0 / 2 + i], D);
         st_shared_v4(a_tile + mn_off(32 * b + hh0, row), o[0], o[1], o[2], o[3]);
     }
 }
@@ -481,7 +439,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
                                 const float a = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
                                 __half *dst = FMT == kWQ4K ? g.act16 + (int64_t)(ti.bb + ti.n0 + j) * ffop + f
                                                            : g.sh_act16 + (int64_t)(ti.n0 + j) * ffop + f;
-                                *dst = __float2half_rn(a);
+                                *dst = act_to_f16(a, g.status);
                             }
                         }
                     } else {
@@ -547,7 +505,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
                             const float uu = ld_cg_f32(g.gu + (int64_t)rowi * 2 * ffop + ffop + f);
                             __half *dst = FMT == kWQ4K ? g.act16 + (int64_t)rowi * ffop + f
                                                        : g.sh_act16 + (int64_t)rowi * ffop + f;
-                            *dst = __float2half_rn(__fdividef(gg, 1.0f + __expf(-gg)) * uu);
+                            *dst = act_to_f16(__fdividef(gg, 1.0f + __expf(-gg)) * uu, g.status);
                         }
                     }
                     if (et == 0) g.split_cnt[tile / g.splits] = 0;

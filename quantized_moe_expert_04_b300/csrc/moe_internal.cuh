@@ -76,6 +76,10 @@ struct WsLayout {
     size_t total;
 };
 
+moe_status forward_checks(const moe_config *cfg, const uint16_t *x, const float *router_w, const float *router_bias,
+                          const uint8_t *const *expert_blobs, const uint8_t *shared_blob, int32_t T, uint16_t *y,
+                          float *y_f32, void *ws, size_t ws_bytes);
+
 // Routing path choice for T tokens under cfg flags.
 bool use_gemv(const moe_config &c, int32_t T);
 WsLayout ws_layout(const moe_config &c, int32_t T);
@@ -87,6 +91,8 @@ cudaError_t launch_pack_q8_0(const float *w, int64_t nblocks, uint8_t *out, uint
                              cudaStream_t s);
 cudaError_t launch_dequant_q4k(const uint8_t *blk, int64_t nblocks, float *out, cudaStream_t s);
 cudaError_t launch_dequant_q8_0(const uint8_t *blk, int64_t nblocks, float *out, cudaStream_t s);
+cudaError_t launch_dequant_q4k_f16(const uint8_t *blk, int64_t nblocks, uint16_t *out, cudaStream_t s);
+cudaError_t launch_dequant_q8_0_f16(const uint8_t *blk, int64_t nblocks, uint16_t *out, cudaStream_t s);
 
 struct RouteArgs {
     int H, E, k, T, score_fn;

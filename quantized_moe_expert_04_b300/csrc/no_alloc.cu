@@ -53,19 +53,29 @@ extern "C" moe_status moe_forward_static_ws(const moe_config *cfg, const uint16_
                                            const uint8_t *shared_blob, int32_t T, uint16_t *y, float *y_f32,
                                            uint32_t *dev_status, moe_stream_t stream)
 {
+    // every argument check first, before the array is touched: a rejected
+    // call enqueues nothing (in particular it does not clear the header of a
+    // call that may still be running)
+    if (dev_status && ((uintptr_t)dev_status & 3u)) return MOE_ERR_MISALIGNED;
+    const size_t need = moe_workspace_bytes(cfg, T < 0 ? 0 : T);
+    if (need > (size_t)MOE_STATIC_WS_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;   // call too large for the array
+    const void *const kAligned = reinterpret_cast<const void *>(256);               // stands in for the array
+    moe_status st = forward_checks(cfg, x, router_w, router_bias, expert_blobs, shared_blob, T, y, y_f32,
+                                   const_cast<void *>(kAligned), MOE_STATIC_WS_BYTES);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {
+        if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
     void *ws = nullptr;
     if (static_ws_address(&ws) != cudaSuccess) return MOE_ERR_CUDA;
-    const size_t need = moe_workspace_bytes(cfg, T);
-    if (need > (size_t)MOE_STATIC_WS_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;   // call too large for the array
-    cudaStream_t s = (cudaStream_t)stream;
-    if (need > 0) {
-        // the array still holds the previous call's header: its status word and
-        // counters must start at zero
-        if (cudaMemsetAsync(ws, 0, kHeaderBytes, s) != cudaSuccess) return MOE_ERR_CUDA;
-    }
-    const moe_status st = moe_forward(cfg, x, router_w, router_bias, expert_blobs, shared_blob, T, y, y_f32, ws,
-                                      MOE_STATIC_WS_BYTES, stream);
-    if (st == MOE_OK && dev_status && T > 0) {
+    // the array still holds the previous call's header: its status word and
+    // counters must start at zero
+    if (cudaMemsetAsync(ws, 0, kHeaderBytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+    st = moe_forward(cfg, x, router_w, router_bias, expert_blobs, shared_blob, T, y, y_f32, ws, MOE_STATIC_WS_BYTES,
+                     stream);
+    if (st == MOE_OK && dev_status) {
         if (cudaMemcpyAsync(dev_status, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
             return MOE_ERR_CUDA;
     }

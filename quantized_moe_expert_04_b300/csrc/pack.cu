@@ -9,6 +9,7 @@
 // ("Qwen3.8-Flash-Next UD-Q4_K_XL 引擎对比", lcz.me/user/wml-ai/posts,
 // section 一, pack conversions); the quantiser itself is not on the pages.
 #include "moe_internal.cuh"
+#include "dequant_f16.cuh"
 
 namespace moe {
 
@@ -190,6 +191,46 @@ __global__ void __launch_bounds__(256) k_dequant_q8_0(const uint8_t *__restrict_
     }
 }
 
+// The fp16 operand rounding of the tensor-core paths, through the very
+// functions their fused kernels call (dequant_f16.cuh): thread per (block,
+// 4-byte word of the quants) -> 8 fp16 weights.
+__global__ void __launch_bounds__(256) k_dequant_q4k_f16(const uint8_t *__restrict__ blocks, int64_t nblocks,
+                                                         uint16_t *__restrict__ out)
+{
+    const int64_t n = nblocks * 32;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = i >> 5;
+        const int wi = (int)(i & 31), c = wi >> 3, i4 = wi & 7;     // chunk c (sub-blocks 2c, 2c+1), word i4
+        const uint8_t *blk = blocks + b * kQ4KBytes;
+        const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+        __half2 S, NZ;
+        q4k_pair_scales_h(hdr, c, S, NZ);
+        uint32_t o[4];
+        q4k_word_f16(*reinterpret_cast<const uint32_t *>(blk + 16 + 32 * c + 4 * i4), __low2half2(S), __low2half2(NZ),
+                     __high2half2(S), __high2half2(NZ), o);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(out + b * kQK + 64 * c + 4 * i4);
+        dst[0] = o[0];
+        dst[1] = o[1];
+        dst[16] = o[2];            // elements 64c + 32 + 4 i4 ...
+        dst[17] = o[3];
+    }
+}
+
+__global__ void __launch_bounds__(256) k_dequant_q8_0_f16(const uint8_t *__restrict__ blocks, int64_t nblocks,
+                                                          uint16_t *__restrict__ out)
+{
+    const int64_t n = nblocks * 16;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint8_t *blk = blocks + (i >> 4) * kQ8Bytes;
+        const int p = (int)(i & 15);
+        const __half2 D = __half2half2(__ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8))));
+        const uint32_t pair = (uint32_t)blk[2 + 2 * p] | ((uint32_t)blk[3 + 2 * p] << 8);
+        reinterpret_cast<uint32_t *>(out)[i] = q80_pair_f16(pair, D);
+    }
+}
+
 static unsigned grid_for(int64_t work_items, int per_block)
 {
     int64_t g = (work_items + per_block - 1) / per_block;
@@ -219,6 +260,18 @@ cudaError_t launch_dequant_q4k(const uint8_t *blk, int64_t nblocks, float *out, 
 cudaError_t launch_dequant_q8_0(const uint8_t *blk, int64_t nblocks, float *out, cudaStream_t s)
 {
     if (nblocks > 0) k_dequant_q8_0<<<grid_for(nblocks * 32, 256), 256, 0, s>>>(blk, nblocks, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_q4k_f16(const uint8_t *blk, int64_t nblocks, uint16_t *out, cudaStream_t s)
+{
+    if (nblocks > 0) k_dequant_q4k_f16<<<grid_for(nblocks * 32, 256), 256, 0, s>>>(blk, nblocks, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_q8_0_f16(const uint8_t *blk, int64_t nblocks, uint16_t *out, cudaStream_t s)
+{
+    if (nblocks > 0) k_dequant_q8_0_f16<<<grid_for(nblocks * 16, 256), 256, 0, s>>>(blk, nblocks, out);
     return cudaGetLastError();
 }
 

@@ -38,6 +38,7 @@ EXPORTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_forward",
     "moe_workspace_routing", "moe_last_device_status", "moe_status_string",
     "moe_profile_enable", "moe_profile_read", "moe_forward_static_ws",
+    "moe_dequant_q4k_f16", "moe_dequant_q8_0_f16",
 )
 
 MOE_STATIC_WS_BYTES = 4 << 20
@@ -94,6 +95,8 @@ def lib() -> ctypes.CDLL:
             "moe_pack_q8_0": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
             "moe_dequant_q4k": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
             "moe_dequant_q8_0": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
+            "moe_dequant_q4k_f16": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
+            "moe_dequant_q8_0_f16": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
             "moe_workspace_bytes": (_SZ, [_CFG, _I32]),
             "moe_workspace_init": (ctypes.c_int, [_P, _SZ, _P]),
             "moe_route": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -198,6 +201,19 @@ def moe_dequant_q4k(blocks: torch.Tensor, rows: int, cols: int, out: torch.Tenso
 def moe_dequant_q8_0(blocks: torch.Tensor, rows: int, cols: int, out: torch.Tensor, stream=None) -> torch.Tensor:
     assert out.dtype == torch.float32 and out.numel() == rows * cols
     _check(lib().moe_dequant_q8_0(_ptr(blocks), rows, cols, _ptr(out), _stream(stream)), "moe_dequant_q8_0")
+    return out
+
+
+def moe_dequant_q4k_f16(blocks: torch.Tensor, rows: int, cols: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """fp16 operand weights (bit patterns in an int16/uint16 tensor) of a Q4_K matrix."""
+    assert out.element_size() == 2 and out.numel() == rows * cols
+    _check(lib().moe_dequant_q4k_f16(_ptr(blocks), rows, cols, _ptr(out), _stream(stream)), "moe_dequant_q4k_f16")
+    return out
+
+
+def moe_dequant_q8_0_f16(blocks: torch.Tensor, rows: int, cols: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    assert out.element_size() == 2 and out.numel() == rows * cols
+    _check(lib().moe_dequant_q8_0_f16(_ptr(blocks), rows, cols, _ptr(out), _stream(stream)), "moe_dequant_q8_0_f16")
     return out
 
 

@@ -80,3 +80,23 @@ def test_host_checks_reject_before_launch():
 def test_status_strings():
     for code in range(8):
         assert moe.status_string(code) and moe.status_string(code) != "unknown status"
+
+
+def test_static_ws_checks_arguments_before_any_cuda_call():
+    """moe_forward_static_ws rejects bad arguments on the host before it
+    looks up or clears its device array (no GPU in this process)."""
+    L = moe.lib()
+    p = ctypes.c_void_p(4096)
+    cfg = moe.make_config(256, 16, 128, 2)
+    args = lambda **kw: [ctypes.byref(kw.get("cfg", cfg)), kw.get("x", p), p, None, kw.get("table", p), None,
+                         kw.get("T", 4), kw.get("y", p), None, kw.get("st", None), None]
+    assert L.moe_forward_static_ws(*args(y=None)) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_forward_static_ws(*args(table=None)) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_forward_static_ws(*args(x=ctypes.c_void_p(4098))) == moe.MOE_ERR_MISALIGNED
+    assert L.moe_forward_static_ws(*args(y=ctypes.c_void_p(4100))) == moe.MOE_ERR_MISALIGNED
+    assert L.moe_forward_static_ws(*args(st=ctypes.c_void_p(4098))) == moe.MOE_ERR_MISALIGNED
+    assert L.moe_forward_static_ws(*args(T=-1)) == moe.MOE_ERR_INVALID_ARG
+    gemv = moe.make_config(256, 16, 128, 2, flags=moe.MOE_FLAG_FORCE_GEMV)
+    assert L.moe_forward_static_ws(*args(cfg=gemv, T=9)) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    big = moe.make_config(2560, 512, 320, 10)
+    assert L.moe_forward_static_ws(*args(cfg=big, T=4096)) == moe.MOE_ERR_WORKSPACE_TOO_SMALL

@@ -1,8 +1,10 @@
 """The whole layer on the GPU against the oracle.
 
 Small shapes (oracle over every token, several warps/tiles and ragged tails)
-and the full workload sizes in the benchmark's launch configuration (oracle on
-a sample of tokens; the layer is token-parallel, so a sample is exact).
+and the full workload sizes in the benchmark's launch configuration: every
+token of the 4096-token Qwen-shaped prefill, and for the skewed DeepSeek-shaped
+prefill the tokens that sit at every tile of the grouped GEMM (the layer is
+token-parallel, so checking a token checks every tile it passed through).
 Ids must match up to reported near-ties; y within rel-L2 5e-3 and max-abs
 2e-2 * max|ref|; for a near-tie token the oracle is rerun with the GPU's ids.
 """
@@ -33,6 +35,37 @@ SMALL = [
 ]
 
 
+def tile_sample(offsets, assign, k, T, shared, tile=128):
+    """Tokens that put the oracle on every tile of the grouped GEMM.
+
+    The GEMM's work tiles run over bucket order: each expert's bucket is cut
+    into token tiles of at most `tile` rows (equal sizes, multiples of 16), and
+    every token of a tile meets all of its weight tiles and K splits.  So the
+    first and last token of every token tile of every expert -- and of the
+    shared expert's tiles over tokens 0..T-1 -- cover every (expert, weight
+    tile, K split, token tile) position.  Bucket positions 16j and 16j - 1 are
+    taken as well, so the sample does not depend on where exactly a tile ends."""
+    toks = set()
+    for e in range(len(offsets) - 1):
+        b0, b1 = int(offsets[e]), int(offsets[e + 1])
+        n = b1 - b0
+        if n == 0:
+            continue
+        nt = (n + tile - 1) // tile
+        tn = ((n + nt - 1) // nt + 15) // 16 * 16
+        for p in list(range(0, n, tn)) + [min(j + tn, n) - 1 for j in range(0, n, tn)]:
+            toks.add(int(assign[b0 + p]) // k)
+        for p in range(0, n, 64):
+            toks.add(int(assign[b0 + p]) // k)
+        toks.add(int(assign[b1 - 1]) // k)
+    if shared:
+        nt = (T + tile - 1) // tile
+        tn = ((T + nt - 1) // nt + 15) // 16 * 16
+        for j in range(0, T, tn):
+            toks.update((j, min(j + tn, T) - 1))
+    return sorted(toks)
+
+
 def _run(wl, T, gen_device, sample=None, flags=0, seed=0, layer=0):
     x = synth.hidden_states(wl, T, seed, layer)
     pl = pack_layer(wl, seed, layer, gen_device=gen_device)
@@ -42,6 +75,8 @@ def _run(wl, T, gen_device, sample=None, flags=0, seed=0, layer=0):
     y = forward(pl, x.cuda(), ws, y_f32=y32, cfg=cfg)
     assert moe.moe_last_device_status(ws) == moe.MOE_OK
     ids, w, offs, assign = routing_views(cfg, T, ws)
+    if isinstance(sample, str) and sample == "tiles":
+        sample = tile_sample(offs.cpu().numpy(), assign.cpu().numpy(), wl.top_k, T, wl.has_shared)
     toks = np.arange(T) if sample is None else np.asarray(sample)
     gids = ids.cpu().numpy()[toks]
     xb, wr, b = oracle_inputs(wl, T, seed, layer, gen_device=gen_device, x=x)
@@ -113,8 +148,8 @@ def test_static_weights_flag_matches():
 FULL = [
     (W["qwen_decode"], 1, None), (W["qwen_decode"], 3, None), (W["qwen_decode"], 5, None),
     (W["deepseek_decode"], 1, None), (W["deepseek_decode"], 4, None), (W["deepseek_decode"], 8, None),
-    (W["qwen_prefill"], 4096, [0, 1, 2, 777, 1500, 2047, 2048, 3001, 4000, 4094, 4095]),
-    (W["deepseek_prefill_skewed"], 4096, [0, 5, 999, 2048, 3333, 4095]),
+    (W["qwen_prefill"], 4096, None),                    # every token (the oracle takes ~15 s)
+    (W["deepseek_prefill_skewed"], 4096, "tiles"),      # every GEMM tile position
 ]
 
 
@@ -191,3 +226,25 @@ FULL_GEMM = [(W["qwen_decode"], 1), (W["qwen_decode"], 3), (W["deepseek_decode"]
 def test_full_size_decode_on_tensor_cores(wl, T):
     """Decode windows through the tensor-core path (K split across CTAs)."""
     _run(wl, T, gen_device="cuda", flags=moe.MOE_FLAG_FORCE_GEMM)
+
+
+def test_prefill_activation_beyond_fp16_is_reported():
+    """The tensor-core path multiplies fp16 activations: |SiLU(g) u| > 65504
+    must raise MOE_ERR_DEVICE_FAULT instead of an infinite y."""
+    wl = sv(W["qwen_decode"], name="qwen_e16", n_experts=16)
+    T = 40
+    pl = pack_layer(wl, gen_device="cpu", experts=[])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for e in range(wl.n_experts):
+        w = synth.expert_weight(wl, e).clone()
+        w[:2] *= 1000.0                                  # gate and up: |g|, |u| ~ 1e3, a ~ 1e6
+        moe.moe_pack_q4k(w.reshape(3 * wl.ff, wl.hidden).cuda(), pl.blobs[e], st)
+    assert int(st.item()) == 0
+    cfg = moe.config_for(wl, moe.MOE_FLAG_FORCE_GEMM)
+    ws = workspace(cfg, T)
+    forward(pl, synth.hidden_states(wl, T).cuda(), ws, cfg=cfg)
+    assert moe.moe_last_device_status(ws) == moe.MOE_ERR_DEVICE_FAULT
+    # the same layer at the normal scale is fine
+    pl2 = pack_layer(wl, gen_device="cpu")
+    forward(pl2, synth.hidden_states(wl, T).cuda(), ws, cfg=cfg)
+    assert moe.moe_last_device_status(ws) == moe.MOE_OK

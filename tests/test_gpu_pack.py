@@ -97,3 +97,30 @@ def test_pack_flags_bad_input(bad):
     out8 = torch.zeros(moe.moe_q8_0_bytes(2, 512), dtype=torch.uint8, device="cuda")
     moe.moe_pack_q8_0(w.cuda(), out8, st)
     assert int(st.item()) == moe.MOE_ERR_DEVICE_FAULT     # 3e38/127 overflows fp16 too
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("rows,cols", [(1, 256), (37, 2560), (130, 4096)])
+def test_fused_dequant_f16_bit_exact(kind, rows, cols):
+    """The fp16 weights the fused tensor-core kernels multiply (their own
+    device functions, through moe_dequant_q4k_f16) equal the oracle's R9
+    rounding bit for bit, every sub-block j = 0..7 of every block."""
+    w = _inputs(kind, rows, cols, seed=3 * rows + cols)
+    blob = oracle.q4k_quantize(w.numpy())
+    ref = oracle.q4k_dequantize_f16(blob, rows, cols)
+    out = torch.empty(rows, cols, dtype=torch.int16, device="cuda")
+    moe.moe_dequant_q4k_f16(torch.from_numpy(blob).cuda(), rows, cols, out)
+    got = out.cpu().numpy().view(np.uint16)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, "first differing weights at %s" % (bad[:3],)
+
+
+@pytest.mark.parametrize("kind", ["normal", "wide", "ties", "zeros_signed"])
+def test_fused_dequant_q8_0_f16_bit_exact(kind):
+    rows, cols = 33, 4096
+    w = _inputs(kind, rows, cols, seed=11)
+    blob = oracle.q8_0_quantize(w.numpy())
+    ref = oracle.q8_0_dequantize_f16(blob, rows, cols)
+    out = torch.empty(rows, cols, dtype=torch.int16, device="cuda")
+    moe.moe_dequant_q8_0_f16(torch.from_numpy(blob).cuda(), rows, cols, out)
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), ref)
