@@ -3,6 +3,7 @@
 // The ABI itself (argument meaning, layouts, ownership, errors) is specified
 // in include/moe.h.
 #include <algorithm>
+#include <atomic>
 
 #include "moe_internal.cuh"
 
@@ -24,14 +25,22 @@ static bool cfg_valid(const moe_config *c)
 }
 
 // Decode path (windows of up to kDecTok tokens) unless the tensor-core GEMM
-// is forced or the hidden width has no router split.
+// is forced, the call is deterministic (the decode kernel combines with
+// atomic additions; the GEMM path has the fixed-order slots), or the shape
+// does not fit the decode kernel.
 bool use_gemv(const moe_config &c, int32_t T)
 {
-    if (c.flags & MOE_FLAG_FORCE_GEMM) return false;
-    if (T > kDecTok || dec_route_parts(c.hidden) == 0) return false;
+    if (c.flags & (MOE_FLAG_FORCE_GEMM | MOE_FLAG_DETERMINISTIC)) return false;
+    if (T > kDecTok || !dec_supported(c, T)) return false;
     if (c.flags & MOE_FLAG_FORCE_GEMV) return true;
     return T <= kGemvMaxTokens;
 }
+
+// ---- test hooks of the bounded device waits (moe_debug_set)
+static std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
+static std::atomic<int64_t> g_skip_stage{-1};
+long long debug_wait_cycles() { return g_wait_cycles.load(); }
+int64_t debug_take_skip_stage() { return g_skip_stage.exchange(-1); }
 
 WsLayout ws_layout(const moe_config &c, int32_t T)
 {
@@ -53,17 +62,11 @@ WsLayout ws_layout(const moe_config &c, int32_t T)
     L.active = take((E + 1) * 4);
     L.bhist = take((TK + kBucketItems - 1) / kBucketItems * E * 4);
     const bool gemv = use_gemv(c, T), det = (c.flags & MOE_FLAG_DETERMINISTIC) != 0;
-    const size_t maxu = std::min<size_t>(E, TK);
-    L.plan = take(gemv ? maxu * sizeof(DecPlan) : 0);
-    L.xfrag = take(gemv ? (size_t)H * 16 : 0);
-    L.act = take(gemv ? TK * c.ff * 4 : 0);
-    L.slots = take(det ? TK * H * 4 * (gemv ? dec_down_splits(c, T) : 1) : 0);
+    L.slots = take(det ? TK * H * 4 : 0);
     L.yacc = take((size_t)T * H * 4);
     L.xg = take(gemv ? 0 : TK * H * 2);
     L.x16 = take(gemv || !c.shared_ff ? 0 : (size_t)T * H * 2);
-    L.sh_act = take(gemv && c.shared_ff ? (size_t)T * c.shared_ff * 4 : 0);
-    L.sh_out = take(c.shared_ff && (gemv || det) ? (size_t)T * H * 4 : 0);
-    (void)maxu;
+    L.sh_out = take(!gemv && c.shared_ff && det ? (size_t)T * H * 4 : 0);
     L.act16 = take(gemv ? 0 : TK * c.ff * 2);
     L.sh_act16 = take(!gemv && c.shared_ff ? (size_t)T * c.shared_ff * 2 : 0);
     const size_t sh_tiles = (size_t)((T + kGemmMaxN - 1) / kGemmMaxN + 1);
@@ -299,13 +302,12 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
         d.T = T;
         d.SFF = cfg->shared_ff;
         d.score_fn = cfg->score_fn;
-        d.det = (cfg->flags & MOE_FLAG_DETERMINISTIC) != 0;
         d.route_parts = dec_route_parts(cfg->hidden);
-        d.fs_dn = dec_down_splits(*cfg, T);
-        d.dn_nbuf = dec_down_nbuf(*cfg, T, d.fs_dn);
+        d.nc = dec_consumers(cfg->hidden);
+        d.ring_bytes = dec_ring_bytes(*cfg, T);
         d.overlap_prev = (cfg->flags & MOE_FLAG_STATIC_WEIGHTS) != 0;
-        d.prefetch_down = 0;   // measured: the bulk L2 prefetch slows both projections
-        d.prefetch_budget = kDecPrefetchBudget;
+        d.wait_cycles = debug_wait_cycles();
+        d.skip_stage = debug_take_skip_stage();
         d.x = x;
         d.wr = router_w;
         d.bias = cfg->score_fn == MOE_SCORE_SIGMOID_BIAS ? router_bias : nullptr;
@@ -318,13 +320,7 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
         d.offsets = r.offsets;
         d.assign = r.assign;
         d.active = r.active;
-        d.plan = (DecPlan *)(base + L.plan);
-        d.xfrag = (uint4 *)(base + L.xfrag);
-        d.act = (float *)(base + L.act);
-        d.sh_act = cfg->shared_ff ? (float *)(base + L.sh_act) : nullptr;
-        d.sh_out = cfg->shared_ff ? (float *)(base + L.sh_out) : nullptr;
         d.yacc = (float *)(base + L.yacc);
-        d.slots = d.det ? (float *)(base + L.slots) : nullptr;
         d.y = y;
         d.y_f32 = y_f32;
         d.header = r.header;
@@ -347,9 +343,7 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
     a.assign = r.assign;
     a.active = r.active;
     a.w = r.w;
-    a.act = (float *)(base + L.act);
     a.slots = (float *)(base + L.slots);
-    a.sh_act = cfg->shared_ff ? (float *)(base + L.sh_act) : nullptr;
     a.sh_out = cfg->shared_ff ? (float *)(base + L.sh_out) : nullptr;
     a.y = y;
     a.y_f32 = y_f32;
@@ -410,6 +404,21 @@ moe_status moe_last_device_status(void *ws, moe_stream_t stream)
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     return (moe_status)v;
+}
+
+moe_status moe_debug_set(int32_t what, int64_t value)
+{
+    switch (what) {
+    case MOE_DEBUG_WAIT_CYCLES:
+        if (value < 0) return MOE_ERR_INVALID_ARG;
+        g_wait_cycles.store(value == 0 ? kDefaultWaitCycles : (long long)value);
+        return MOE_OK;
+    case MOE_DEBUG_SKIP_STAGE:
+        if (value < -1) return MOE_ERR_INVALID_ARG;
+        g_skip_stage.store(value);
+        return MOE_OK;
+    }
+    return MOE_ERR_INVALID_ARG;
 }
 
 const char *moe_status_string(moe_status status)

@@ -61,17 +61,16 @@ __device__ __forceinline__ void q4k_scale_min(const uint8_t *scales, int j, int 
 
 // Kernels counted / timed by the diagnostics API (moe_profile_*).
 enum Phase : int {
-    kPhRouterLogits = 0, kPhTopk, kPhBucket, kPhGateUp, kPhGateUpShared, kPhDown, kPhDownShared,
-    kPhCombine, kPhGemmPrep, kPhGemmGateUp, kPhGemmDown, kPhGemmFinish, kPhDecRoute, kPhDecGateUp,
-    kPhDecDown, kPhDecFinish, kNumPhases
+    kPhRouterLogits = 0, kPhTopk, kPhBucket, kPhGemmPrep, kPhGemmGateUp, kPhGemmDown, kPhGemmFinish,
+    kPhDecRoute, kPhDecLayer, kNumPhases
 };
 void prof_begin(int phase, cudaStream_t s);   // no-ops unless profiling is enabled
 void prof_end(int phase, cudaStream_t s);
 
 // Workspace regions (byte offsets from the workspace base) for one call shape.
 struct WsLayout {
-    size_t header, logits, ids, w, counts, offsets, assign, active, plan, xfrag;
-    size_t act, slots, yacc, xg, x16, sh_act, sh_out, bhist;
+    size_t header, logits, ids, w, counts, offsets, assign, active;
+    size_t slots, yacc, xg, x16, sh_out, bhist;
     size_t act16, sh_act16, tiles_gu, tiles_dn, tiles_gus, tiles_dns, tmaps, gu, sh_gu, split_cnt;
     size_t total;
 };
@@ -115,34 +114,30 @@ struct ExpertArgs {
     const uint8_t *shared_blob;         // Q8_0 or null
     const int32_t *offsets, *assign, *active;
     const float *w;                     // routing weights [T*k]
-    float *act;                         // [T*k][FF] by bucket position
-    float *slots;                       // [T*k][H]
-    float *sh_act;                      // [T][SFF]
-    float *sh_out;                      // [T][H]
+    float *slots;                       // [T*k][H] (deterministic combine)
+    float *sh_out;                      // [T][H] (deterministic combine)
     uint16_t *y;                        // bf16 [T][H]
     float *y_f32;                       // optional
     uint32_t *header;
 };
 
-// ---- decode path (T <= kDecTok): route + grouped gate/up (mma) + down, chained with PDL
+// ---- decode path (T <= kDecTok): router logits, then one persistent kernel
+// ---- (routing, gate/up + SiLU*mul, down, combine), chained with PDL
 constexpr int kDecTok = 8;                         // window tokens = MMA N columns
 constexpr int kDecMaxAssign = kDecTok * 32;        // T * k
 constexpr int kRouteMaxVec = 10;                   // router float4 per lane and warp
-constexpr int64_t kDecPrefetchBudget = 64ll << 20; // down bytes asked of L2 ahead of use
-
-struct DecPlan {                 // one active expert of the window
-    int32_t e, count;
-    int32_t tok_assign[kDecTok]; // assignment t*k + r of token t to this expert, -1 if none
-};
+constexpr int kDecSmemBudget = 232448;             // dynamic shared memory of the layer kernel (227 KB)
+constexpr int kSmemPerSM = 233472;                 // shared memory of one SM (228 KB)
+constexpr long long kDefaultWaitCycles = 1ll << 32; // bounded device waits: ~2 s at 2 GHz
 
 struct DecArgs {
-    int H, E, FF, k, T, SFF, score_fn, det;
+    int H, E, FF, k, T, SFF, score_fn;
     int route_parts;             // router row split per CTA (1, 2, 4 or 8)
-    int fs_dn;                   // ff segments per down unit
-    int dn_nbuf;                 // shared-memory buffers per down warp (2: the next unit is staged ahead)
-    int overlap_prev;            // router rows may be read before the previous kernel ends
-    int prefetch_down;           // ask L2 for the down matrices during gate/up
-    int64_t prefetch_budget;     // at most this many bytes of them
+    int nc;                      // consumer warps of the layer kernel
+    uint32_t ring_bytes;         // its staging ring
+    int overlap_prev;            // weights may be read before the previous kernel ends
+    long long wait_cycles;       // limit of every bounded wait
+    int64_t skip_stage;          // test hook: CTA 0 never arms this ring stage (-1: none)
     const uint16_t *x;
     const float *wr, *bias;
     const uint8_t *const *blobs;
@@ -151,20 +146,21 @@ struct DecArgs {
     int32_t *ids;
     float *w;
     int32_t *counts, *offsets, *assign, *active;
-    DecPlan *plan;
-    uint4 *xfrag;                // fp16 MMA B fragments of x: [H/256][8][32 lanes] x 16 B
-    float *act;                  // [T*k][FF] by assignment
-    float *sh_act, *sh_out;      // shared expert [T][SFF], [T][H]
-    float *yacc, *slots;         // [T][H] fp32 accumulator; [T*k][fs_dn][H] (deterministic)
+    float *yacc;                 // [T][H] fp32 accumulator
     uint16_t *y;
     float *y_f32;
     uint32_t *header;
 };
 int dec_route_parts(int H);
-int dec_down_splits(const moe_config &c, int32_t T);
-int dec_down_nbuf(const moe_config &c, int32_t T, int fs);
+int dec_consumers(int H);
+uint32_t dec_ring_bytes(const moe_config &c, int32_t T);
+bool dec_supported(const moe_config &c, int32_t T);
 cudaError_t launch_decode(const DecArgs &a, cudaStream_t s);
-cudaError_t launch_shared_gemv(const DecArgs &a, cudaStream_t s);
+
+// Test hooks (moe_debug_set): limit of the bounded device waits and a ring
+// stage of the decode kernel that is never armed.
+long long debug_wait_cycles();
+int64_t debug_take_skip_stage();
 
 // Tensor-core (tcgen05) grouped GEMM path: its workspace regions.
 constexpr int kGemmSmallTokens = 16;   // calls with T <= 16 use the small-bucket GEMM configuration

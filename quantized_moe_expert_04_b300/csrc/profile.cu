@@ -9,9 +9,8 @@
 namespace moe {
 
 static const char *kPhaseNames[kNumPhases] = {
-    "router_logits", "topk", "bucket", "gemv_gateup", "gemv_gateup_shared", "gemv_down",
-    "gemv_down_shared", "combine", "gemm_prep", "gemm_gateup", "gemm_down", "gemm_finish",
-    "dec_route", "dec_gateup", "dec_down", "dec_finish",
+    "router_logits", "topk", "bucket", "gemm_prep", "gemm_gateup", "gemm_down", "gemm_finish",
+    "dec_route", "dec_layer",
 };
 
 namespace {

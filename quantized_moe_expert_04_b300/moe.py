@@ -38,8 +38,11 @@ EXPORTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_forward",
     "moe_workspace_routing", "moe_last_device_status", "moe_status_string",
     "moe_profile_enable", "moe_profile_read", "moe_forward_static_ws",
-    "moe_dequant_q4k_f16", "moe_dequant_q8_0_f16",
+    "moe_dequant_q4k_f16", "moe_dequant_q8_0_f16", "moe_debug_set",
 )
+
+MOE_DEBUG_WAIT_CYCLES = 1
+MOE_DEBUG_SKIP_STAGE = 2
 
 MOE_STATIC_WS_BYTES = 4 << 20
 
@@ -106,6 +109,7 @@ def lib() -> ctypes.CDLL:
             "moe_last_device_status": (ctypes.c_int, [_P, _P]),
             "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "moe_profile_enable": (ctypes.c_int, [_I32]),
+            "moe_debug_set": (ctypes.c_int, [_I32, _I64]),
             "moe_forward_static_ws": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P]),
             "moe_profile_read": (_I32, [ctypes.POINTER(moe_profile_entry), _I32]),
         }
@@ -270,6 +274,11 @@ def moe_last_device_status(ws: torch.Tensor, stream=None) -> int:
 
 
 # ---------------------------------------------------------------- diagnostics
+
+def moe_debug_set(what: int, value: int):
+    """Test hooks of the bounded device waits (see include/moe.h)."""
+    _check(lib().moe_debug_set(int(what), int(value)), "moe_debug_set")
+
 
 def moe_profile_enable(on: bool = True):
     _check(lib().moe_profile_enable(1 if on else 0), "moe_profile_enable")

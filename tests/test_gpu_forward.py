@@ -131,6 +131,27 @@ def test_decode_deterministic_mode_matches_oracle(T):
     assert torch.equal(forward(pl, x, ws, cfg=cfg), y)
 
 
+def test_static_weights_flag_decode_path():
+    """Decode windows chained with MOE_FLAG_STATIC_WEIGHTS (router rows and the
+    expert table read before the previous call has finished), several calls
+    back to back on one stream, each checked against the oracle."""
+    wl = sv(W["qwen_decode"], name="qwen_e64", n_experts=64)
+    pl = pack_layer(wl, gen_device="cpu")
+    cfg = moe.config_for(wl, moe.MOE_FLAG_STATIC_WEIGHTS | moe.MOE_FLAG_FORCE_GEMV)
+    T = 5
+    ws = workspace(cfg, T)
+    xs = [synth.hidden_states(wl, T, seed=s).cuda() for s in range(4)]
+    outs = [torch.empty(T, wl.hidden, dtype=torch.float32, device="cuda") for _ in xs]
+    for x, y32 in zip(xs, outs):
+        forward(pl, x, ws, y_f32=y32, cfg=cfg)
+    assert moe.moe_last_device_status(ws) == moe.MOE_OK
+    for s, (x, y32) in enumerate(zip(xs, outs)):
+        xb, wr, b = oracle_inputs(wl, T, x=x.cpu())
+        ids, _, _, _ = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
+        blobs, sblob = oracle_blobs(wl, ids.reshape(-1))
+        check_close(y32.cpu().numpy(), oracle_forward(wl, xb, wr, b, blobs, sblob), what="call %d" % s)
+
+
 def test_static_weights_flag_matches():
     """Calls that may start reading the router early give the same result."""
     wl = sv(W["qwen_decode"], name="qwen_e64", n_experts=64)

@@ -1,0 +1,51 @@
+"""Failure detection on the GPU without a fault: a bounded wait that runs out.
+
+moe_debug_set shortens every device wait and makes CTA 0 of the decode
+kernel leave one staging stage unarmed, so the waits for it give up.  The call
+must end (no hang), report MOE_ERR_TIMEOUT through the workspace status word,
+and leave the context usable: the next call, with the hooks cleared, matches
+the oracle.  Nothing here faults, traps or spins without a limit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from quantized_moe_expert_04_b300 import moe, synth
+from quantized_moe_expert_04_b300.layer import forward, pack_layer, workspace
+from parity import check_close, oracle_blobs, oracle_forward, oracle_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("stage", [0, 2, 4])
+def test_decode_wait_timeout_is_reported_and_the_context_survives(stage):
+    wl = synth.small_variant(synth.WORKLOADS["qwen_decode"], name="qwen_e64", n_experts=64)
+    T = 3
+    pl = pack_layer(wl, gen_device="cpu")
+    cfg = moe.config_for(wl, moe.MOE_FLAG_FORCE_GEMV)
+    ws = workspace(cfg, T)
+    x = synth.hidden_states(wl, T).cuda()
+    try:
+        moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, 1 << 22)      # ~2 ms
+        moe.moe_debug_set(moe.MOE_DEBUG_SKIP_STAGE, stage)
+        forward(pl, x, ws, cfg=cfg)
+        assert moe.moe_last_device_status(ws) == moe.MOE_ERR_TIMEOUT
+    finally:
+        moe.moe_debug_set(moe.MOE_DEBUG_SKIP_STAGE, -1)
+        moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, 0)
+    # the skip is one-shot and the context is intact: the next call is right
+    y32 = torch.empty(T, wl.hidden, dtype=torch.float32, device="cuda")
+    forward(pl, x, ws, y_f32=y32, cfg=cfg)
+    assert moe.moe_last_device_status(ws) == moe.MOE_OK
+    xb, wr, b = oracle_inputs(wl, T, x=x.cpu())
+    import oracle
+    ids, _, _, _ = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
+    blobs, sblob = oracle_blobs(wl, ids.reshape(-1))
+    check_close(y32.cpu().numpy(), oracle_forward(wl, xb, wr, b, blobs, sblob))
+
+
+def test_debug_hook_rejects_bad_values():
+    with pytest.raises(moe.MoeError):
+        moe.moe_debug_set(99, 0)
+    with pytest.raises(moe.MoeError):
+        moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, -5)
