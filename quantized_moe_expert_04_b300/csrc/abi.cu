@@ -64,6 +64,7 @@ WsLayout ws_layout(const moe_config &c, int32_t T)
     const bool gemv = use_gemv(c, T), det = (c.flags & MOE_FLAG_DETERMINISTIC) != 0;
     L.slots = take(det ? TK * H * 4 : 0);
     L.yacc = take((size_t)T * H * 4);
+    L.xfrag = take(gemv ? (size_t)T * H * 2 : 0);
     L.xg = take(gemv ? 0 : TK * H * 2);
     L.x16 = take(gemv || !c.shared_ff ? 0 : (size_t)T * H * 2);
     L.sh_out = take(!gemv && c.shared_ff && det ? (size_t)T * H * 4 : 0);
@@ -305,15 +306,20 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
         d.route_parts = dec_route_parts(cfg->hidden);
         d.nc = dec_consumers(cfg->hidden);
         d.ring_bytes = dec_ring_bytes(*cfg, T);
+        d.srows = dec_shared_rows(*cfg, T);
+        d.n_slot = dec_slots(*cfg, T);
+        d.slot_bytes = dec_slot_bytes(*cfg, T);
+        d.pf_dist = dec_prefetch_distance(*cfg, T);
         d.overlap_prev = (cfg->flags & MOE_FLAG_STATIC_WEIGHTS) != 0;
         d.wait_cycles = debug_wait_cycles();
-        d.skip_stage = debug_take_skip_stage();
+        d.skip_stage = (int)debug_take_skip_stage();
         d.x = x;
         d.wr = router_w;
         d.bias = cfg->score_fn == MOE_SCORE_SIGMOID_BIAS ? router_bias : nullptr;
         d.blobs = expert_blobs;
         d.shared_blob = cfg->shared_ff > 0 ? shared_blob : nullptr;
         d.logits = r.logits;
+        d.xfrag = (uint2 *)(base + L.xfrag);
         d.ids = r.ids;
         d.w = r.w;
         d.counts = r.counts;

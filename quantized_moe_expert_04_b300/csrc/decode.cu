@@ -86,6 +86,25 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` of the mbarrier's transaction count.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
@@ -253,6 +272,23 @@ __global__ void __maxnreg__(88) k_dec_route(DecArgs a)
     for (int i = gtid; i < T * H / 4; i += gthreads)
         reinterpret_cast<float4 *>(a.yacc)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     __syncthreads();
+    // x -> fp16 MMA B fragments, once for the window (every layer CTA copies them whole):
+    // xf[((cb*16 + s)*4 + tq)*T + g] = x[g][e .. e+3], e = 256 cb + 64 tq + (s < 8 ? 4 s : 32 + 4 (s - 8))
+    {
+        bool bad = false;
+        const int n = (H / 256) * 64 * T;
+        for (int i = gtid; i < n; i += gthreads) {
+            const int g = i % T, r = i / T, tq = r & 3, sx = (r >> 2) & 15, cb = r >> 6;
+            const int e = 256 * cb + 64 * tq + (sx < 8 ? 4 * sx : 32 + 4 * (sx - 8));
+            const uint2 xb = *reinterpret_cast<const uint2 *>(s_x + g * H + e);
+            const float x0 = bf16_bits_to_f32(xb.x & 0xffff), x1 = bf16_bits_to_f32(xb.x >> 16);
+            const float x2 = bf16_bits_to_f32(xb.y & 0xffff), x3 = bf16_bits_to_f32(xb.y >> 16);
+            const float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+            bad |= !(m < 65504.0f);      // beyond the fp16 range, or NaN
+            a.xfrag[i] = make_uint2(dq_h22u(__floats2half2_rn(x0, x1)), dq_h22u(__floats2half2_rn(x2, x3)));
+        }
+        if (bad) set_status(a.header + kHdrStatus, MOE_ERR_DEVICE_FAULT);
+    }
 
     float acc[kDecTok];
 #pragma unroll
@@ -294,12 +330,14 @@ __global__ void __maxnreg__(88) k_dec_route(DecArgs a)
 // ---------------------------------------------------------------- the layer
 
 constexpr int kUnitRows = 8;            // ff rows per unit (and rows per ring stage)
-constexpr int kNSlot = 16;              // ring stages tracked at once (mbarrier pairs)
+constexpr int kMaxSlot = 32;            // staging-ring slots at most (one mbarrier each)
+constexpr int kMinSlot = 6;             // at least two units' slabs
+constexpr int64_t kPrefetchBytes = 128 * 1024;   // per SM, requested into L2 beyond the ring
 constexpr int kMaxCons = 16;            // consumer warps (256-column blocks of H per pass)
 
 // Shared-memory carve of k_dec_layer (byte offsets); see dec_layer_smem().
 struct LayerSmem {
-    uint32_t tab, xf, ids, w, pe, ptok, tmask, bits, pre, red, sa, bar, misc, ring, ring_bytes, total;
+    uint32_t tab, xf, ids, w, pe, ptok, tmask, bits, pre, red, sa, bar, cnt, last, misc, ring, ring_bytes, total;
 };
 
 __host__ __device__ inline uint32_t al16(uint32_t v) { return (v + 15u) & ~15u; }
@@ -319,7 +357,9 @@ __host__ __device__ inline LayerSmem layer_smem(int E, int T, int H, int nc, uin
     L.pre = o;   o = al16(o + 4u * 32);
     L.red = o;   o = al16(o + 8u * nc * kDecTok * kUnitRows);    // [warp][token slot][f] (g, u) partial sums
     L.sa = o;    o = al16(o + 2u * kDecTok * kUnitRows);          // [token][f] weighted activations (fp16)
-    L.bar = o;   o = al16(o + 16u * kNSlot);
+    L.bar = o;   o = al16(o + 8u * (kMaxSlot + 1));
+    L.cnt = o;   o = al16(o + 4u * kMaxSlot);                     // per slot: warps done with its stages
+    L.last = o;  o = al16(o + 4u * kMaxSlot);                     // per slot: last stage requested
     L.misc = o;  o = al16(o + 64u);
     o = (o + 127u) & ~127u;
     L.ring = o;
@@ -343,22 +383,6 @@ __device__ __forceinline__ int64_t first_unit(const Units &u, int64_t byte)
     return u.nr + (byte - rbytes + u.bs - 1) / u.bs;
 }
 
-// The byte ring: stages are allocated in order; one that would run past the
-// end starts again at 0.  Producer and consumers walk the same sequence of
-// stage sizes, so both compute the same offsets.
-struct RingPos {
-    uint32_t size;
-    uint64_t head;           // virtual byte position of the next stage
-    __device__ __forceinline__ uint64_t next(uint32_t bytes, uint32_t &phys)
-    {
-        uint64_t s = head;
-        if ((s % size) + bytes > size) s = (s / size + 1) * size;
-        phys = (uint32_t)(s % size);
-        head = s + bytes;
-        return head;         // virtual end of the stage
-    }
-};
-
 struct UnitInfo {
     const uint8_t *blob;
     int fmt;                 // 0: Q4_K routed, 1: Q8_0 shared
@@ -366,23 +390,27 @@ struct UnitInfo {
     int f0;                  // first ff row
     int ffm;                 // rows of one matrix in the blob (FF or SFF)
     int rowb;                // row bytes
+    int rows;                // ff rows of the unit: 8, or a.srows for the shared expert
 };
 
+// Unit i of the window (32-bit arithmetic: this runs once per stage).
 __device__ __forceinline__ UnitInfo unit_info(const DecArgs &a, const Units &un, const int16_t *pe,
-                                              const uint8_t *const *tab, int64_t i)
+                                              const uint8_t *const *tab, int i)
 {
     UnitInfo ui;
-    if (i < un.nr) {
+    if (i < (int)un.nr) {
         const int mt = a.FF / kUnitRows;
-        ui.u = (int)(i / mt);
-        ui.f0 = (int)(i % mt) * kUnitRows;
+        ui.u = i / mt;
+        ui.rows = kUnitRows;
+        ui.f0 = (i - ui.u * mt) * kUnitRows;
         ui.blob = tab[pe[ui.u]];
         ui.fmt = 0;
         ui.ffm = a.FF;
         ui.rowb = un.rb;
     } else {
         ui.u = -1;
-        ui.f0 = (int)(i - un.nr) * kUnitRows;
+        ui.rows = a.srows;
+        ui.f0 = (i - (int)un.nr) * a.srows;
         ui.blob = a.shared_blob;
         ui.fmt = 1;
         ui.ffm = a.SFF;
@@ -414,8 +442,8 @@ __device__ __forceinline__ __half2 i8_pair(uint32_t w0, uint32_t w1, int b)
     return __hsub2(dq_u2h2(((p ^ 0x00800080u) & 0x00FF00FFu) | 0x64006400u), __float2half2_rn(1152.0f));
 }
 
-// 120 registers a thread: 17 warps (16 consumers + the producer) fit one SM.
-__global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
+// 128 registers a thread: 16 warps (4 on each SM sub-partition) fit one SM.
+__global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int T = a.T, H = a.H, E = a.E, k = a.k, nb = H / 256, NC = a.nc;
@@ -433,24 +461,30 @@ __global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
     __half *s_wa = reinterpret_cast<__half *>(smem + L.sa);       // [kDecTok][8]
     const uint32_t bar0 = sm_addr(smem + L.bar);
     auto full = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    auto empty = [&](int i) { return bar0 + 8u * (uint32_t)(kNSlot + i); };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc);
     int *s_nact = reinterpret_cast<int *>(smem + L.misc + 4);
-    int *s_last = reinterpret_cast<int *>(smem + L.misc + 8);
+    int *s_is_last = reinterpret_cast<int *>(smem + L.misc + 8);
     uint8_t *ring = smem + L.ring;
+    uint32_t *s_cnt = reinterpret_cast<uint32_t *>(smem + L.cnt);
+    int *s_last = reinterpret_cast<int *>(smem + L.last);   // per slot: last stage requested
     const uint32_t ring_s = sm_addr(ring);
     uint32_t *status = a.header + kHdrStatus;
     const long long limit = a.wait_cycles;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNSlot; ++i) {
-            mbar_init(full(i), 1);
-            mbar_init(empty(i), NC);
+        for (int i = 0; i < a.n_slot; ++i) mbar_init(full(i), 1);
+        mbar_init(bar0 + 8u * kMaxSlot, 1);
+        for (int i = 0; i < kMaxSlot; ++i) {
+            s_cnt[i] = 0u;
+            s_last[i] = -1;
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    // no thread may touch a barrier (or the abort flag) before they are initialised:
+    // warps start independently, and a wait on an uninitialised barrier is undefined
+    __syncthreads();
     // the expert table: before the dependency wait when the weights are static
     if (a.overlap_prev)
         for (int e = threadIdx.x; e < E; e += nthr) s_tab[e] = a.blobs[e];
@@ -461,34 +495,35 @@ __global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
     if (!a.overlap_prev)
         for (int e = threadIdx.x; e < E; e += nthr) s_tab[e] = a.blobs[e];
 
-    // ---- x -> fp16 MMA B fragments: xf[((cb*16 + s)*4 + tq)*T + g] = x[g][e .. e+3],
-    //      e = 256 cb + 64 tq + (s < 8 ? 4 s : 32 + 4 (s - 8))
+    // ---- the window's x fragments (built by the router kernel) and logits: one bulk
+    //      copy each (every CTA reads the same bytes: whole copies keep that cheap).
+    //      The selection keys follow in the ring, which is not in use yet.
+    float *s_lg = reinterpret_cast<float *>(ring);
+    uint32_t *s_key = reinterpret_cast<uint32_t *>(ring + 4 * T * E);
+    float *s_val = reinterpret_cast<float *>(ring + 8 * T * E);
     {
-        bool bad = false;
-        const int n = nb * 64 * T;
-        for (int i = threadIdx.x; i < n; i += nthr) {
-            const int g = i % T, r = i / T, tq = r & 3, s = (r >> 2) & 15, cb = r >> 6;
-            const int e = 256 * cb + 64 * tq + (s < 8 ? 4 * s : 32 + 4 * (s - 8));
-            const uint2 xb = __ldcg(reinterpret_cast<const uint2 *>(a.x + (int64_t)g * H + e));
-            const float x0 = bf16_bits_to_f32(xb.x & 0xffff), x1 = bf16_bits_to_f32(xb.x >> 16);
-            const float x2 = bf16_bits_to_f32(xb.y & 0xffff), x3 = bf16_bits_to_f32(xb.y >> 16);
-            const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
-            const float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-            bad |= !(m < 65504.0f);      // beyond the fp16 range, or NaN
-            s_xf[i] = make_uint2(dq_h22u(h01), dq_h22u(h23));
+        const uint32_t xbytes = 2u * T * H, lbytes = (4u * T * E + 15u) & ~15u;
+        const uint32_t bx = bar0 + 8u * kMaxSlot;                // the prologue's own mbarrier
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(bx, xbytes + lbytes);
+            bulk_g2s(sm_addr(s_xf), a.xfrag, xbytes, bx);
+            bulk_g2s(sm_addr(s_lg), a.logits, lbytes, bx);
         }
-        if (bad) set_status(status, MOE_ERR_DEVICE_FAULT);
-    }
-
-    // ---- route the window: selection keys (scratch in the ring, not in use yet)
-    uint32_t *s_key = reinterpret_cast<uint32_t *>(ring);
-    float *s_val = reinterpret_cast<float *>(ring + 4 * T * E);
-    for (int i = threadIdx.x; i < T * E; i += nthr) {
-        const float l = __ldcg(a.logits + i);
-        const float sv = a.score_fn == MOE_SCORE_SOFTMAX ? l : 1.0f / (1.0f + expf(-l));
-        const float b = (a.score_fn != MOE_SCORE_SOFTMAX && a.bias) ? __ldg(a.bias + i % E) : 0.0f;
-        s_val[i] = sv;
-        s_key[i] = key_bits(a.score_fn == MOE_SCORE_SOFTMAX ? sv : sv + b);
+        const bool sig = a.score_fn != MOE_SCORE_SOFTMAX;
+        if (!wait_phase(bx, 0u, abort_flag, status, limit) && threadIdx.x == 0) {
+            *abort_flag = 1;
+            // the two copies must land before the CTA ends (bounded)
+            const long long t0 = clock64();
+            while (!mbar_poll(bx, 0u) && clock64() - t0 < limit) {
+            }
+        }
+        for (int i = threadIdx.x; i < T * E; i += nthr) {
+            const float l = s_lg[i];
+            const float sv = sig ? 1.0f / (1.0f + expf(-l)) : l;
+            const float b = (sig && a.bias) ? __ldg(a.bias + i % E) : 0.0f;
+            s_val[i] = sv;
+            s_key[i] = key_bits(sig ? sv + b : sv);
+        }
     }
     if (threadIdx.x < 32) s_bits[threadIdx.x] = 0u;
     __syncthreads();
@@ -594,68 +629,76 @@ __global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
     un.rb = nb * 144;
     un.rbs = (H / 32) * 34;
     un.nr = (int64_t)U * (a.FF / kUnitRows);
-    un.ns = a.shared_blob ? a.SFF / kUnitRows : 0;
+    un.ns = a.shared_blob ? a.SFF / a.srows : 0;
     un.br = 3ll * kUnitRows * un.rb;
-    un.bs = 3ll * kUnitRows * un.rbs;
+    un.bs = 3ll * a.srows * un.rbs;
     const int64_t total = un.nr * un.br + un.ns * un.bs;
     const int64_t u_begin = first_unit(un, total * blockIdx.x / gridDim.x);
     const int64_t u_end = first_unit(un, total * (blockIdx.x + 1) / gridDim.x);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic accesses before the copies
     __syncthreads();   // the routing scratch in the ring is free from here on
 
-    if (warp == NC) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            RingPos rp{L.ring_bytes, 0};
-            uint64_t vstart[kNSlot];
-            int64_t issued = 0, released = 0;
-            bool ok = true;
-            for (int64_t i = u_begin; ok && i < u_end; ++i) {
-                const UnitInfo ui = unit_info(a, un, s_pe, s_tab, i);
-                const uint32_t bytes = (uint32_t)(kUnitRows * ui.rowb);
-                for (int part = 0; ok && part < 3; ++part) {
-                    uint32_t phys;
-                    const uint64_t ve = rp.next(bytes, phys);
-                    // wait until the stages this one overwrites (and the barrier pair it reuses) are free
-                    while (released < issued &&
-                           (issued - released >= kNSlot || vstart[released % kNSlot] + L.ring_bytes < ve)) {
-                        const int sl = (int)(released % kNSlot);
-                        if (!wait_phase(empty(sl), (uint32_t)((released / kNSlot) & 1), abort_flag, status, limit)) {
-                            ok = false;
-                            break;
-                        }
-                        ++released;
-                    }
-                    if (!ok) break;
-                    const int sl = (int)(issued % kNSlot);
-                    vstart[sl] = ve - bytes;
-                    const uint8_t *src =
-                        ui.blob ? ui.blob + ((int64_t)part * ui.ffm + ui.f0) * ui.rowb : nullptr;
-                    if (issued == a.skip_stage && blockIdx.x == 0) {
-                        // test hook: this stage is never armed, so its consumers' waits run out
-                    } else if (src) {
-                        mbar_arrive_expect_tx(full(sl), bytes);
-                        bulk_g2s(ring_s + phys, src, bytes, full(sl));
-                    } else {
-                        mbar_arrive(full(sl));   // no blob: the consumers skip the unit
-                    }
-                    ++issued;
-                }
-            }
-            // copies still in flight (an early exit) must land before the CTA ends
-            for (int64_t j = released; j < issued; ++j) {
-                if (j == a.skip_stage && blockIdx.x == 0) continue;
-                const int sl = (int)(j % kNSlot);
-                const long long t0 = clock64();
-                while (!mbar_test(full(sl), (uint32_t)((j / kNSlot) & 1)) && clock64() - t0 < limit) {
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp < NC) {
+    if (warp < NC) {
         // ------------------------------------------------------------ consumers
         const int g = lane >> 2, tq = lane & 3;          // MMA fragment coordinates
-        RingPos rp{L.ring_bytes, 0};
-        int64_t stage = 0;
+        // ---- the staging ring: n_slot fixed slots of slot_bytes; stage j (the CTA's
+        // j-th slab: unit j / 3, matrix j % 3) goes to slot j % n_slot.  The copy of
+        // stage j + n_slot is issued, as one bulk copy of the whole slab, by the last
+        // warp to finish reading stage j (counted per slot): a slab is requested the
+        // moment its slot frees, by whichever warp frees it.  Progress: a warp waits
+        // for stages of its current unit only, and the warps stay within one unit of
+        // each other (the barriers below), so with n_slot >= 6 every stage it waits
+        // for has been requested.
+        const int n_stage = 3 * (int)(u_end - u_begin);
+        // L2 prefetch of stage j (the ring holds only a few stages: the prefetches keep
+        // about 128 KB more per SM on their way from DRAM, so the ring copies of
+        // those stages come from L2)
+        auto prefetch = [&](int j) {                     // by one lane
+            if (j >= n_stage) return;
+            const UnitInfo ui = unit_info(a, un, s_pe, s_tab, (int)u_begin + j / 3);
+            if (ui.blob)
+                prefetch_l2(ui.blob + ((int64_t)(j % 3) * ui.ffm + ui.f0) * ui.rowb, (uint32_t)(ui.rows * ui.rowb));
+        };
+        auto issue = [&](int j) {                        // by one lane
+            if (j >= n_stage || *abort_flag) return;
+            const int sl = j % a.n_slot;
+            const UnitInfo ui = unit_info(a, un, s_pe, s_tab, (int)u_begin + j / 3);
+            const uint32_t bytes = (uint32_t)(ui.rows * ui.rowb);
+            const uint8_t *src = ui.blob ? ui.blob + ((int64_t)(j % 3) * ui.ffm + ui.f0) * ui.rowb : nullptr;
+            s_last[sl] = j;
+            if (j == a.skip_stage && blockIdx.x == 0) {
+                // test hook: this stage is never armed nor filled, so the waits for it run out
+            } else if (src) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(full(sl), bytes);
+                bulk_g2s(ring_s + (uint32_t)sl * a.slot_bytes, src, bytes, full(sl));
+            } else {
+                mbar_arrive(full(sl));                   // no blob: the consumers skip the unit
+            }
+            if (a.pf_dist > a.n_slot) prefetch(j + a.pf_dist);
+        };
+        auto release = [&](int j) {                      // this warp is done with stage j
+            __syncwarp();
+            if (lane == 0) {
+                const int sl = j % a.n_slot;
+                // acquire-release: the other warps' reads of the slot happen before the
+                // copy that the last of them issues into it
+                uint32_t old;
+                asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                             : "=r"(old) : "r"(sm_addr(&s_cnt[sl])) : "memory");
+                const uint32_t done = old + 1u;
+                if (done == (uint32_t)NC * (uint32_t)(j / a.n_slot + 1)) issue(j + a.n_slot);
+            }
+        };
+        auto wait_full = [&](int j) -> bool {
+            const int sl = j % a.n_slot;
+            return wait_phase(full(sl), (uint32_t)((j / a.n_slot) & 1), abort_flag, status, limit);
+        };
+        if (warp == 0 && lane == 0) {
+            for (int j = 0; j < a.n_slot; ++j) issue(j);
+            for (int j = a.n_slot; j < a.pf_dist; ++j) prefetch(j);
+        }
+        int stage = 0;
         // down accumulators: block cb = warp, tile i (16 hidden rows x the
         // 8 window tokens): d0/d1 = columns hl(g, i) for tokens 2tq, 2tq+1, d2/d3 =
         // columns hl(g, i) + 32, with hl(g, i) = 256 cb + 64 (g / 2) + 16 (g % 2) + i
@@ -663,18 +706,10 @@ __global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
 #pragma unroll
         for (int i4 = 0; i4 < 16; ++i4) D[i4][0] = D[i4][1] = D[i4][2] = D[i4][3] = 0.0f;
         uint32_t touched = 0;                             // window tokens this CTA's units served
-        for (int64_t i = u_begin; i < u_end; ++i) {
-            const UnitInfo ui = unit_info(a, un, s_pe, s_tab, i);
-            const uint32_t bytes = (uint32_t)(kUnitRows * ui.rowb);
+        for (int iu = (int)u_begin; iu < (int)u_end; ++iu, stage += 3) {
+            const UnitInfo ui = unit_info(a, un, s_pe, s_tab, iu);
             uint32_t off[3];
-            int sl[3];
-            uint32_t par[3];
-            for (int p = 0; p < 3; ++p) {
-                rp.next(bytes, off[p]);
-                sl[p] = (int)((stage + p) % kNSlot);
-                par[p] = (uint32_t)(((stage + p) / kNSlot) & 1);
-            }
-            stage += 3;
+            for (int p = 0; p < 3; ++p) off[p] = (uint32_t)((stage + p) % a.n_slot) * a.slot_bytes;
             const bool live = ui.blob != nullptr;
             if (!live && warp == 0 && lane == 0) set_status(status, MOE_ERR_DEVICE_FAULT);
             // tokens of this unit: the expert's, or every token (shared)
@@ -682,8 +717,8 @@ __global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
             touched |= tmask;
 
             // ---- gate / up over this warp's block
-            bool ok = wait_phase(full(sl[0]), par[0], abort_flag, status, limit) &&
-                      wait_phase(full(sl[1]), par[1], abort_flag, status, limit);
+            bool ok = wait_full(stage) && wait_full(stage + 1);
+            ok = __all_sync(0xffffffffu, ok);           // the MMAs below need the whole warp
             float c4[2][4];
 #pragma unroll
             for (int i2 = 0; i2 < 2; ++i2) c4[i2][0] = c4[i2][1] = c4[i2][2] = c4[i2][3] = 0.0f;
@@ -714,10 +749,13 @@ __global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
                             mma16816(c4[1], og[2], ou[2], og[3], ou[3], xh.x, xh.y);
                         }
                     } else {
+                        // units shorter than 8 rows: MMA rows g >= rows read row 0 (their
+                        // outputs are not used)
+                        const int gr_ = g < ui.rows ? g : 0;
                         const uint32_t *gw =
-                            reinterpret_cast<const uint32_t *>(gst + g * ui.rowb + 272 * cb + 68 * tq);
+                            reinterpret_cast<const uint32_t *>(gst + gr_ * ui.rowb + 272 * cb + 68 * tq);
                         const uint32_t *uw =
-                            reinterpret_cast<const uint32_t *>(ust + g * ui.rowb + 272 * cb + 68 * tq);
+                            reinterpret_cast<const uint32_t *>(ust + gr_ * ui.rowb + 272 * cb + 68 * tq);
                         const __half2 Dg0 = __half2half2(__ushort_as_half((unsigned short)(gw[0] & 0xffff)));
                         const __half2 Dg1 = __half2half2(__ushort_as_half((unsigned short)(gw[8] >> 16)));
                         const __half2 Du0 = __half2half2(__ushort_as_half((unsigned short)(uw[0] & 0xffff)));
@@ -737,22 +775,21 @@ __global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
                     }
                 }
             }
-            // the gate and up slabs are no longer read by this warp
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(empty(sl[0]));
-                mbar_arrive(empty(sl[1]));
-            }
+            release(stage);                               // the gate and up slabs are read
+            release(stage + 1);
             // partial sums of this warp: (g, u) of ff row f0 + g for window token n
             {
                 const float c0 = c4[0][0] + c4[1][0], c1 = c4[0][1] + c4[1][1];
                 const float c2 = c4[0][2] + c4[1][2], c3 = c4[0][3] + c4[1][3];
-                if ((tmask >> (2 * tq)) & 1u) s_red[(warp * kDecTok + 2 * tq) * kUnitRows + g] = make_float2(c0, c2);
-                if ((tmask >> (2 * tq + 1)) & 1u)
-                    s_red[(warp * kDecTok + 2 * tq + 1) * kUnitRows + g] = make_float2(c1, c3);
+                if (g < ui.rows) {
+                    if ((tmask >> (2 * tq)) & 1u) s_red[(warp * kDecTok + 2 * tq) * kUnitRows + g] = make_float2(c0, c2);
+                    if ((tmask >> (2 * tq + 1)) & 1u)
+                        s_red[(warp * kDecTok + 2 * tq + 1) * kUnitRows + g] = make_float2(c1, c3);
+                }
             }
             // barrier among the consumer warps that also ORs their view of the abort
             // flag, so that every warp takes the same decision
+            __syncwarp();
             {
                 uint32_t any;
                 asm volatile(
@@ -769,7 +806,7 @@ __global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
             for (int ct = warp * 32 + lane; ct < kUnitRows * kDecTok; ct += NC * 32) {
                 const int f = ct & 7, n = ct >> 3;
                 float v = 0.0f;
-                if ((tmask >> n) & 1u) {
+                if (((tmask >> n) & 1u) && f < ui.rows) {
                     float gs = 0.0f, us = 0.0f;
                     for (int w2 = 0; w2 < NC; ++w2) {
                         const float2 pv = s_red[(w2 * kDecTok + n) * kUnitRows + f];
@@ -782,15 +819,20 @@ __global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
                 }
                 s_wa[n * kUnitRows + f] = __float2half_rn(v);
             }
+            __syncwarp();
             asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
 
             // ---- down rows of the unit (the 8 rows are the MMA K), for this warp's block
-            ok = ok && wait_phase(full(sl[2]), par[2], abort_flag, status, limit);
+            ok = ok && wait_full(stage + 2);
+            ok = __all_sync(0xffffffffu, ok);
             if (ok && live) {
                 const uint8_t *dn = ring + off[2];
                 // B fragment: rows f = 2tq, 2tq + 1 of token g
                 const uint32_t bfr = *reinterpret_cast<const uint32_t *>(s_wa + g * kUnitRows + 2 * tq);
-                const uint8_t *r0 = dn + (2 * tq) * ui.rowb, *r1 = dn + (2 * tq + 1) * ui.rowb;
+                // rows 2tq, 2tq + 1 (K of the MMA); beyond a short unit they read row 0, whose
+                // product with the zero activations of those rows adds nothing
+                const uint8_t *r0 = dn + (2 * tq < ui.rows ? 2 * tq : 0) * ui.rowb;
+                const uint8_t *r1 = dn + (2 * tq + 1 < ui.rows ? 2 * tq + 1 : 0) * ui.rowb;
                 {
                     const int cb = warp;
                     {
@@ -841,9 +883,21 @@ __global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty(sl[2]));
+            release(stage + 2);
         }
+        // copies still in flight (an early exit) must land before the CTA ends: the
+        // last stage requested into each slot
+        __syncwarp();
+        asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
+        if (warp == 0 && lane < a.n_slot) {
+            const int j = s_last[lane];
+            if (j >= 0 && !(j == a.skip_stage && blockIdx.x == 0)) {
+                const long long t0 = clock64();
+                while (!mbar_poll(full(lane), (uint32_t)((j / a.n_slot) & 1)) && clock64() - t0 < limit) {
+                }
+            }
+        }
+        __syncwarp();
         // ---- this CTA's share of y, for the window tokens its units served
         {
             const int hl = 256 * warp + 64 * (g >> 1) + 16 * (g & 1);
@@ -868,10 +922,10 @@ __global__ void __maxnreg__(120) k_dec_layer(DecArgs a)
     __syncthreads();
     if (threadIdx.x == 0) {
         const uint32_t ticket = atomicAdd(a.header + kHdrTicketDown, 1u);
-        *s_last = ticket == gridDim.x - 1;
+        *s_is_last = ticket == gridDim.x - 1;
     }
     __syncthreads();
-    if (*s_last) {
+    if (*s_is_last) {
         __threadfence();
         const int n4 = T * H / 4;
         for (int i = threadIdx.x; i < n4; i += nthr) {
@@ -907,30 +961,57 @@ int dec_route_parts(int H)
 
 int dec_consumers(int H) { return H / 256; }
 
-// Ring bytes of a call.  The ring takes what the shared-memory budget leaves,
-// less room for one CTA of the next call's router kernel beside it on the SM
-// (it loads its router rows while this window streams), but never fewer than
-// four stages; 0 when not even three stages (or the routing scratch) fit.
-uint32_t dec_ring_bytes(const moe_config &c, int32_t T)
+// The staging ring takes all the shared memory the rest of the kernel leaves,
+// cut into slots of the largest slab (8 rows of a routed matrix, or the
+// shared expert's rows per unit); at least kMinSlot slots are needed.
+static int64_t dec_base_ring(const moe_config &c, int32_t T)
 {
-    const int nc = dec_consumers(c.hidden);
-    const LayerSmem base = layer_smem(c.n_experts, T, c.hidden, nc, 0);
-    const int64_t max_ring = (int64_t)kDecSmemBudget - (int64_t)base.total;
-    const int64_t route_peer = (int64_t)T * c.hidden * 2 + 512;            // its dynamic + static shared memory
-    const int64_t beside = (int64_t)kSmemPerSM - 2 * 1024 - route_peer - (int64_t)base.total;
+    const LayerSmem base = layer_smem(c.n_experts, T, c.hidden, dec_consumers(c.hidden), 0);
+    return ((int64_t)kDecSmemBudget - (int64_t)base.total) & ~(int64_t)127;
+}
+
+static int64_t slot_for(const moe_config &c, int srows)
+{
     const int64_t rb = (int64_t)(c.hidden / 256) * 144, rbs = (int64_t)(c.hidden / 32) * 34;
-    const int64_t stage = kUnitRows * std::max(rb, c.shared_ff ? rbs : (int64_t)0);
-    const int64_t scratch = (int64_t)T * c.n_experts * 8;
-    int64_t ring = std::min(max_ring, std::max(beside, std::max(4 * stage, scratch)));
-    if (ring < std::max(3 * stage, scratch)) return 0;
-    return (uint32_t)(ring & ~(int64_t)127);
+    const int64_t slab = std::max<int64_t>(kUnitRows * rb, c.shared_ff ? srows * rbs : 0);
+    return (slab + 127) & ~(int64_t)127;
+}
+
+// Rows per shared-expert unit: 8, or fewer when 8-row Q8_0 slabs would leave
+// fewer than kMinSlot slots (0: not even 2 rows do).
+int dec_shared_rows(const moe_config &c, int32_t T)
+{
+    if (!c.shared_ff) return kUnitRows;
+    const int64_t ring = dec_base_ring(c, T);
+    for (int r = kUnitRows; r >= 2; r /= 2)
+        if (ring / slot_for(c, r) >= kMinSlot) return r;
+    return 0;
+}
+
+uint32_t dec_slot_bytes(const moe_config &c, int32_t T) { return (uint32_t)slot_for(c, std::max(2, dec_shared_rows(c, T))); }
+
+int dec_slots(const moe_config &c, int32_t T)
+{
+    const int64_t ring = dec_base_ring(c, T);
+    if (dec_shared_rows(c, T) == 0 || ring < (int64_t)T * c.n_experts * 12 + 16) return 0;
+    const int64_t n = ring / dec_slot_bytes(c, T);
+    return n < kMinSlot ? 0 : (int)std::min<int64_t>(n, kMaxSlot);
+}
+
+uint32_t dec_ring_bytes(const moe_config &c, int32_t T) { return (uint32_t)dec_base_ring(c, T); }
+
+// Stages between a stage's ring copy and the L2 prefetch issued with it: the
+// slots plus about 128 KB (per SM, 19 MB over the GPU: well inside L2).
+int dec_prefetch_distance(const moe_config &c, int32_t T)
+{
+    const int n = dec_slots(c, T);
+    return n + (int)((kPrefetchBytes + dec_slot_bytes(c, T) - 1) / dec_slot_bytes(c, T));
 }
 
 bool dec_supported(const moe_config &c, int32_t T)
 {
     return T >= 0 && T <= kDecTok && dec_route_parts(c.hidden) != 0 && c.hidden / 256 <= kMaxCons &&
-           c.ff % kUnitRows == 0 &&
-           (c.shared_ff == 0 || c.shared_ff % kUnitRows == 0) && dec_ring_bytes(c, T) > 0;
+           c.ff % kUnitRows == 0 && dec_slots(c, T) > 0;
 }
 
 template <typename K>
@@ -984,7 +1065,7 @@ cudaError_t launch_decode(const DecArgs &a0, cudaStream_t s)
     if (e != cudaSuccess) return e;
     const LayerSmem L = layer_smem(a.E, a.T, a.H, a.nc, a.ring_bytes);
     prof_begin(kPhDecLayer, s);
-    const int warps = std::max(a.nc + 1, kDecTok);   // consumers + producer; at least one warp per token
+    const int warps = std::max(a.nc, kDecTok);   // consumer warps; at least one warp per token
     e = launch_pdl(k_dec_layer, dim3(dec_sms()), dim3(32 * warps), L.total, s, true, a);
     prof_end(kPhDecLayer, s);
     return e;

@@ -1061,9 +1061,9 @@ GemmSplits gemm_splits(const moe_config &c, int32_t T)
         sp.dns = pick_split(c.hidden / 128, c.shared_ff / 64, c.shared_ff / 64, sms);
     }
     if (c.flags & MOE_FLAG_DETERMINISTIC) {
-        // the deterministic down epilogue stores each slot once: no K split there
-        sp.dn = 1;
-        sp.dns = 1;
+        // no K split anywhere: the split gate/up sums meet through atomic additions
+        // (their order varies), and the deterministic down epilogue stores each slot once
+        sp = GemmSplits{1, 1, 1, 1};
     }
     return sp;
 }

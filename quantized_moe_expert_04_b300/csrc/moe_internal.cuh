@@ -70,7 +70,7 @@ void prof_end(int phase, cudaStream_t s);
 // Workspace regions (byte offsets from the workspace base) for one call shape.
 struct WsLayout {
     size_t header, logits, ids, w, counts, offsets, assign, active;
-    size_t slots, yacc, xg, x16, sh_out, bhist;
+    size_t slots, yacc, xg, x16, sh_out, bhist, xfrag;
     size_t act16, sh_act16, tiles_gu, tiles_dn, tiles_gus, tiles_dns, tmaps, gu, sh_gu, split_cnt;
     size_t total;
 };
@@ -135,14 +135,19 @@ struct DecArgs {
     int route_parts;             // router row split per CTA (1, 2, 4 or 8)
     int nc;                      // consumer warps of the layer kernel
     uint32_t ring_bytes;         // its staging ring
+    int srows;                   // ff rows per shared-expert unit (8, 4 or 2)
+    int n_slot;                  // staging-ring slots
+    int pf_dist;                 // L2 prefetch distance in stages (<= n_slot: none)
+    uint32_t slot_bytes;         // bytes of one slot
     int overlap_prev;            // weights may be read before the previous kernel ends
     long long wait_cycles;       // limit of every bounded wait
-    int64_t skip_stage;          // test hook: CTA 0 never arms this ring stage (-1: none)
+    int skip_stage;              // test hook: CTA 0 never arms this ring stage (-1: none)
     const uint16_t *x;
     const float *wr, *bias;
     const uint8_t *const *blobs;
     const uint8_t *shared_blob;
     float *logits;
+    uint2 *xfrag;                // [H/256][16][4][T] fp16 MMA B fragments of x (built by the router kernel)
     int32_t *ids;
     float *w;
     int32_t *counts, *offsets, *assign, *active;
@@ -154,6 +159,10 @@ struct DecArgs {
 int dec_route_parts(int H);
 int dec_consumers(int H);
 uint32_t dec_ring_bytes(const moe_config &c, int32_t T);
+int dec_shared_rows(const moe_config &c, int32_t T);
+int dec_slots(const moe_config &c, int32_t T);
+uint32_t dec_slot_bytes(const moe_config &c, int32_t T);
+int dec_prefetch_distance(const moe_config &c, int32_t T);
 bool dec_supported(const moe_config &c, int32_t T);
 cudaError_t launch_decode(const DecArgs &a, cudaStream_t s);
 
