@@ -312,14 +312,16 @@ MOE_API int32_t moe_profile_read(moe_profile_entry *out, int32_t max_entries);
  *   MOE_DEBUG_WAIT_CYCLES  value > 0: every bounded wait of the kernels
  *                          launched afterwards gives up after `value` clock
  *                          cycles (0 restores the default, ~2 s).
- *   MOE_DEBUG_SKIP_STAGE   value >= 0: in the next decode-path call, CTA 0 of
- *                          the layer kernel never arms staging-ring stage
- *                          `value`, so the waits for it run out: the call
- *                          then ends with MOE_ERR_TIMEOUT in its status word
- *                          (the context stays usable).  -1 clears it.
- * Errors: MOE_ERR_INVALID_ARG for an unknown `what` or a negative value.
+ *   MOE_DEBUG_SKIP_COPY    value >= 0: in the next decode-path call, CTA
+ *                          `value` of the layer kernel never issues the bulk
+ *                          copy of the window's x fragments and logits, so its
+ *                          wait for them runs out: the call then ends with
+ *                          MOE_ERR_TIMEOUT in its status word (the context
+ *                          stays usable; a value past the grid does nothing).
+ *                          -1 clears it.
+ * Errors: MOE_ERR_INVALID_ARG for an unknown `what` or a value out of range.
  */
-enum { MOE_DEBUG_WAIT_CYCLES = 1, MOE_DEBUG_SKIP_STAGE = 2 };
+enum { MOE_DEBUG_WAIT_CYCLES = 1, MOE_DEBUG_SKIP_COPY = 2 };
 MOE_API moe_status moe_debug_set(int32_t what, int64_t value);
 
 /* Static string for a status code. */

@@ -38,9 +38,9 @@ bool use_gemv(const moe_config &c, int32_t T)
 
 // ---- test hooks of the bounded device waits (moe_debug_set)
 static std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
-static std::atomic<int64_t> g_skip_stage{-1};
+static std::atomic<int> g_skip_copy{-1};
 long long debug_wait_cycles() { return g_wait_cycles.load(); }
-int64_t debug_take_skip_stage() { return g_skip_stage.exchange(-1); }
+int debug_take_skip_copy() { return g_skip_copy.exchange(-1); }
 
 WsLayout ws_layout(const moe_config &c, int32_t T)
 {
@@ -306,13 +306,10 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
         d.route_parts = dec_route_parts(cfg->hidden);
         d.nc = dec_consumers(cfg->hidden);
         d.ring_bytes = dec_ring_bytes(*cfg, T);
-        d.srows = dec_shared_rows(*cfg, T);
-        d.n_slot = dec_slots(*cfg, T);
-        d.slot_bytes = dec_slot_bytes(*cfg, T);
-        d.pf_dist = dec_prefetch_distance(*cfg, T);
+        d.stages = dec_stages(*cfg, T);
         d.overlap_prev = (cfg->flags & MOE_FLAG_STATIC_WEIGHTS) != 0;
         d.wait_cycles = debug_wait_cycles();
-        d.skip_stage = (int)debug_take_skip_stage();
+        d.skip_cta = debug_take_skip_copy();
         d.x = x;
         d.wr = router_w;
         d.bias = cfg->score_fn == MOE_SCORE_SIGMOID_BIAS ? router_bias : nullptr;
@@ -419,9 +416,9 @@ moe_status moe_debug_set(int32_t what, int64_t value)
         if (value < 0) return MOE_ERR_INVALID_ARG;
         g_wait_cycles.store(value == 0 ? kDefaultWaitCycles : (long long)value);
         return MOE_OK;
-    case MOE_DEBUG_SKIP_STAGE:
-        if (value < -1) return MOE_ERR_INVALID_ARG;
-        g_skip_stage.store(value);
+    case MOE_DEBUG_SKIP_COPY:
+        if (value < -1 || value > (1 << 20)) return MOE_ERR_INVALID_ARG;
+        g_skip_copy.store((int)value);
         return MOE_OK;
     }
     return MOE_ERR_INVALID_ARG;

@@ -86,11 +86,6 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // Non-blocking test of an mbarrier phase.
 __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity)
 {
@@ -329,15 +324,16 @@ __global__ void __maxnreg__(88) k_dec_route(DecArgs a)
 
 // ---------------------------------------------------------------- the layer
 
-constexpr int kUnitRows = 8;            // ff rows per unit (and rows per ring stage)
-constexpr int kMaxSlot = 32;            // staging-ring slots at most (one mbarrier each)
-constexpr int kMinSlot = 6;             // at least two units' slabs
-constexpr int64_t kPrefetchBytes = 128 * 1024;   // per SM, requested into L2 beyond the ring
-constexpr int kMaxCons = 16;            // consumer warps (256-column blocks of H per pass)
+constexpr int kUnitRows = 8;            // ff rows of a routed unit (the 8 MMA rows of each of gate, up)
+constexpr int kSharedRows = 4;          // ff rows of a shared-expert unit
+constexpr int kPieceQ4K = 144;          // bytes of one row's 256-column block: one Q4_K super-block
+constexpr int kPieceQ80 = 272;          // the same block in Q8_0: eight 34-byte blocks
+constexpr uint32_t kSlotBytes = 1152;   // one stage of one warp: 8 x 144 (>= 4 x 272)
+constexpr int kMaxCons = 16;            // consumer warps (256-column blocks of H)
 
-// Shared-memory carve of k_dec_layer (byte offsets); see dec_layer_smem().
+// Shared-memory carve of k_dec_layer (byte offsets).
 struct LayerSmem {
-    uint32_t tab, xf, ids, w, pe, ptok, tmask, bits, pre, red, sa, bar, cnt, last, misc, ring, ring_bytes, total;
+    uint32_t tab, xf, ids, w, pe, ptok, tmask, bits, pre, red, sa, bar, misc, ring, ring_bytes, total;
 };
 
 __host__ __device__ inline uint32_t al16(uint32_t v) { return (v + 15u) & ~15u; }
@@ -355,11 +351,9 @@ __host__ __device__ inline LayerSmem layer_smem(int E, int T, int H, int nc, uin
     L.tmask = o; o = al16(o + 4u * kDecMaxAssign);               // [u] tokens routed to active expert u
     L.bits = o;  o = al16(o + 4u * 32);
     L.pre = o;   o = al16(o + 4u * 32);
-    L.red = o;   o = al16(o + 8u * nc * kDecTok * kUnitRows);    // [warp][token slot][f] (g, u) partial sums
-    L.sa = o;    o = al16(o + 2u * kDecTok * kUnitRows);          // [token][f] weighted activations (fp16)
-    L.bar = o;   o = al16(o + 8u * (kMaxSlot + 1));
-    L.cnt = o;   o = al16(o + 4u * kMaxSlot);                     // per slot: warps done with its stages
-    L.last = o;  o = al16(o + 4u * kMaxSlot);                     // per slot: last stage requested
+    L.red = o;   o = al16(o + 2u * 8u * nc * kDecTok * kUnitRows); // [2][warp][token][f] (g, u) partial sums
+    L.sa = o;    o = al16(o + 2u * 2u * kDecTok * kUnitRows);      // [2][token][f] weighted activations (fp16)
+    L.bar = o;   o = al16(o + 8u);                                 // the prologue's mbarrier
     L.misc = o;  o = al16(o + 64u);
     o = (o + 127u) & ~127u;
     L.ring = o;
@@ -369,10 +363,10 @@ __host__ __device__ inline LayerSmem layer_smem(int E, int T, int H, int nc, uin
 }
 
 // Unit geometry of a window: Nr routed units (8 ff rows of one active expert)
-// then Ns shared-expert units, split over the CTAs by bytes.
+// then Ns shared-expert units (4 rows), split over the CTAs by bytes.
 struct Units {
     int64_t nr, ns;          // unit counts
-    int64_t br, bs;          // bytes of one unit (3 slabs of 8 rows)
+    int64_t br, bs;          // bytes of one unit (3 slabs)
     int rb, rbs;             // row bytes: Q4_K routed, Q8_0 shared
 };
 
@@ -390,10 +384,10 @@ struct UnitInfo {
     int f0;                  // first ff row
     int ffm;                 // rows of one matrix in the blob (FF or SFF)
     int rowb;                // row bytes
-    int rows;                // ff rows of the unit: 8, or a.srows for the shared expert
+    int rows;                // ff rows of the unit
 };
 
-// Unit i of the window (32-bit arithmetic: this runs once per stage).
+// Unit i of the window.
 __device__ __forceinline__ UnitInfo unit_info(const DecArgs &a, const Units &un, const int16_t *pe,
                                               const uint8_t *const *tab, int i)
 {
@@ -409,14 +403,40 @@ __device__ __forceinline__ UnitInfo unit_info(const DecArgs &a, const Units &un,
         ui.rowb = un.rb;
     } else {
         ui.u = -1;
-        ui.rows = a.srows;
-        ui.f0 = (i - (int)un.nr) * a.srows;
+        ui.rows = kSharedRows;
+        ui.f0 = (i - (int)un.nr) * kSharedRows;
         ui.blob = a.shared_blob;
         ui.fmt = 1;
         ui.ffm = a.SFF;
         ui.rowb = un.rbs;
     }
     return ui;
+}
+
+// The unit after c.i (c.ui describes unit c.i): consecutive routed units walk an
+// expert's ff rows 8 at a time, then the next active expert's; the shared expert's
+// units follow the routed ones.  No division: this runs once per stage.
+struct UnitCursor {
+    UnitInfo ui;
+    int i;
+};
+
+__device__ __forceinline__ void unit_next(UnitCursor &c, const DecArgs &a, const Units &un, const int16_t *pe,
+                                          const uint8_t *const *tab)
+{
+    ++c.i;
+    if (c.i < (int)un.nr) {
+        c.ui.f0 += kUnitRows;
+        if (c.ui.f0 == a.FF) {
+            c.ui.f0 = 0;
+            ++c.ui.u;
+            c.ui.blob = tab[pe[c.ui.u]];
+        }
+    } else if (c.i == (int)un.nr) {
+        c.ui = unit_info(a, un, pe, tab, c.i);
+    } else {
+        c.ui.f0 += kSharedRows;
+    }
 }
 
 __device__ __forceinline__ void mma16808(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0)
@@ -442,9 +462,36 @@ __device__ __forceinline__ __half2 i8_pair(uint32_t w0, uint32_t w1, int b)
     return __hsub2(dq_u2h2(((p ^ 0x00800080u) & 0x00FF00FFu) | 0x64006400u), __float2half2_rn(1152.0f));
 }
 
-// 128 registers a thread: 16 warps (4 on each SM sub-partition) fit one SM.
+__device__ __forceinline__ void cp16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// One warp copies its column block (P 16-byte pieces) of ROWS consecutive rows
+// (`rowb` bytes apart in global memory) into a packed [ROWS][16 P] slab: piece
+// i = lane + 32 k (ROWS * P <= 96 pieces).
+template <int P, int ROWS>
+__device__ __forceinline__ void copy_block(uint32_t dst, const uint8_t *src, int rowb, int lane)
+{
+    static_assert(ROWS * P <= 96, "three pieces a lane");
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const int i = lane + 32 * k;
+        if (i < ROWS * P) {
+            const int r = i / P, p = i - r * P;
+            cp16(dst + (uint32_t)(r * 16 * P + 16 * p), src + r * rowb + 16 * p);
+        }
+    }
+}
+
+// The layer kernel, S stages per consumer warp.  128 registers a thread: 16
+// warps (4 on each SM sub-partition) fit one SM.
+template <int S>
 __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
 {
+    static_assert(S >= 4, "the lagging down projection keeps 3 stages busy");
     extern __shared__ __align__(128) uint8_t smem[];
     const int T = a.T, H = a.H, E = a.E, k = a.k, nb = H / 256, NC = a.nc;
     const LayerSmem L = layer_smem(E, T, H, NC, a.ring_bytes);
@@ -457,32 +504,23 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
     uint32_t *s_tmask = reinterpret_cast<uint32_t *>(smem + L.tmask);
     uint32_t *s_bits = reinterpret_cast<uint32_t *>(smem + L.bits);
     int32_t *s_pre = reinterpret_cast<int32_t *>(smem + L.pre);
-    float2 *s_red = reinterpret_cast<float2 *>(smem + L.red);     // [NC][window token][8]
-    __half *s_wa = reinterpret_cast<__half *>(smem + L.sa);       // [kDecTok][8]
-    const uint32_t bar0 = sm_addr(smem + L.bar);
-    auto full = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    float2 *s_red = reinterpret_cast<float2 *>(smem + L.red);     // [2][NC][window token][8]
+    __half *s_wa = reinterpret_cast<__half *>(smem + L.sa);       // [2][kDecTok][8]
+    const uint32_t bx = sm_addr(smem + L.bar);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc);
     int *s_nact = reinterpret_cast<int *>(smem + L.misc + 4);
     int *s_is_last = reinterpret_cast<int *>(smem + L.misc + 8);
     uint8_t *ring = smem + L.ring;
-    uint32_t *s_cnt = reinterpret_cast<uint32_t *>(smem + L.cnt);
-    int *s_last = reinterpret_cast<int *>(smem + L.last);   // per slot: last stage requested
-    const uint32_t ring_s = sm_addr(ring);
     uint32_t *status = a.header + kHdrStatus;
     const long long limit = a.wait_cycles;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < a.n_slot; ++i) mbar_init(full(i), 1);
-        mbar_init(bar0 + 8u * kMaxSlot, 1);
-        for (int i = 0; i < kMaxSlot; ++i) {
-            s_cnt[i] = 0u;
-            s_last[i] = -1;
-        }
+        mbar_init(bx, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // no thread may touch a barrier (or the abort flag) before they are initialised:
+    // no thread may touch the barrier (or the abort flag) before they are initialised:
     // warps start independently, and a wait on an uninitialised barrier is undefined
     __syncthreads();
     // the expert table: before the dependency wait when the weights are static
@@ -503,18 +541,19 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
     float *s_val = reinterpret_cast<float *>(ring + 8 * T * E);
     {
         const uint32_t xbytes = 2u * T * H, lbytes = (4u * T * E + 15u) & ~15u;
-        const uint32_t bx = bar0 + 8u * kMaxSlot;                // the prologue's own mbarrier
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(bx, xbytes + lbytes);
-            bulk_g2s(sm_addr(s_xf), a.xfrag, xbytes, bx);
-            bulk_g2s(sm_addr(s_lg), a.logits, lbytes, bx);
+            if ((int)blockIdx.x != a.skip_cta) {      // test hook: never issued, so the wait runs out
+                bulk_g2s(sm_addr(s_xf), a.xfrag, xbytes, bx);
+                bulk_g2s(sm_addr(s_lg), a.logits, lbytes, bx);
+            }
         }
         const bool sig = a.score_fn != MOE_SCORE_SOFTMAX;
         if (!wait_phase(bx, 0u, abort_flag, status, limit) && threadIdx.x == 0) {
             *abort_flag = 1;
-            // the two copies must land before the CTA ends (bounded)
+            // copies in flight must land before the CTA ends (bounded)
             const long long t0 = clock64();
-            while (!mbar_poll(bx, 0u) && clock64() - t0 < limit) {
+            while ((int)blockIdx.x != a.skip_cta && !mbar_poll(bx, 0u) && clock64() - t0 < limit) {
             }
         }
         for (int i = threadIdx.x; i < T * E; i += nthr) {
@@ -626,190 +665,199 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
 
     // ---- this CTA's share of the window's units
     Units un;
-    un.rb = nb * 144;
-    un.rbs = (H / 32) * 34;
+    un.rb = nb * kPieceQ4K;
+    un.rbs = nb * kPieceQ80;
     un.nr = (int64_t)U * (a.FF / kUnitRows);
-    un.ns = a.shared_blob ? a.SFF / a.srows : 0;
+    un.ns = a.shared_blob ? a.SFF / kSharedRows : 0;
     un.br = 3ll * kUnitRows * un.rb;
-    un.bs = 3ll * a.srows * un.rbs;
+    un.bs = 3ll * kSharedRows * un.rbs;
     const int64_t total = un.nr * un.br + un.ns * un.bs;
     const int64_t u_begin = first_unit(un, total * blockIdx.x / gridDim.x);
     const int64_t u_end = first_unit(un, total * (blockIdx.x + 1) / gridDim.x);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic accesses before the copies
-    __syncthreads();   // the routing scratch in the ring is free from here on
+    __syncthreads();   // the routing scratch in the ring is free from here on; the abort flag is settled
 
-    if (warp < NC) {
+    if (warp < NC && !*abort_flag) {
         // ------------------------------------------------------------ consumers
-        const int g = lane >> 2, tq = lane & 3;          // MMA fragment coordinates
-        // ---- the staging ring: n_slot fixed slots of slot_bytes; stage j (the CTA's
-        // j-th slab: unit j / 3, matrix j % 3) goes to slot j % n_slot.  The copy of
-        // stage j + n_slot is issued, as one bulk copy of the whole slab, by the last
-        // warp to finish reading stage j (counted per slot): a slab is requested the
-        // moment its slot frees, by whichever warp frees it.  Progress: a warp waits
-        // for stages of its current unit only, and the warps stay within one unit of
-        // each other (the barriers below), so with n_slot >= 6 every stage it waits
-        // for has been requested.
-        const int n_stage = 3 * (int)(u_end - u_begin);
-        // L2 prefetch of stage j (the ring holds only a few stages: the prefetches keep
-        // about 128 KB more per SM on their way from DRAM, so the ring copies of
-        // those stages come from L2)
-        auto prefetch = [&](int j) {                     // by one lane
-            if (j >= n_stage) return;
-            const UnitInfo ui = unit_info(a, un, s_pe, s_tab, (int)u_begin + j / 3);
-            if (ui.blob)
-                prefetch_l2(ui.blob + ((int64_t)(j % 3) * ui.ffm + ui.f0) * ui.rowb, (uint32_t)(ui.rows * ui.rowb));
-        };
-        auto issue = [&](int j) {                        // by one lane
-            if (j >= n_stage || *abort_flag) return;
-            const int sl = j % a.n_slot;
-            const UnitInfo ui = unit_info(a, un, s_pe, s_tab, (int)u_begin + j / 3);
-            const uint32_t bytes = (uint32_t)(ui.rows * ui.rowb);
-            const uint8_t *src = ui.blob ? ui.blob + ((int64_t)(j % 3) * ui.ffm + ui.f0) * ui.rowb : nullptr;
-            s_last[sl] = j;
-            if (j == a.skip_stage && blockIdx.x == 0) {
-                // test hook: this stage is never armed nor filled, so the waits for it run out
-            } else if (src) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive_expect_tx(full(sl), bytes);
-                bulk_g2s(ring_s + (uint32_t)sl * a.slot_bytes, src, bytes, full(sl));
-            } else {
-                mbar_arrive(full(sl));                   // no blob: the consumers skip the unit
+        // Warp w owns the 256-column block w of H, and reads nothing else of a
+        // row: of every slab (8 rows of gate, up or down of a unit) it stages its
+        // own block -- 144 bytes a Q4_K row, 272 a Q8_0 row -- into its own ring
+        // of S stages with 16-byte cp.async, so the warps stream independently and
+        // no copy is issued on another warp's behalf.  Stage j (unit j / 3, matrix
+        // j % 3) sits in slot j % S.  The down projection of unit u runs one unit
+        // late, after the gate/up of unit u + 1, so one barrier per unit orders
+        // both the partial sums (gate/up) and the activations (down).
+        const int g = lane >> 2, tq = lane & 3, cb = warp;
+        const int n_unit = (int)(u_end - u_begin), n_stage = 3 * n_unit;
+        const uint32_t wring = sm_addr(ring) + (uint32_t)(warp * S) * kSlotBytes;
+        const uint8_t *wring_p = ring + (size_t)warp * S * kSlotBytes;
+        // the next stage to copy: stage js, matrix im of the unit under the cursor ic
+        const UnitInfo ui0 = unit_info(a, un, s_pe, s_tab, (int)u_begin);
+        UnitCursor ic{ui0, (int)u_begin};
+        int js = 0, im = 0;
+        auto issue = [&]() {
+            if (js < n_stage && ic.ui.blob) {
+                const uint8_t *src = ic.ui.blob + ((int64_t)im * ic.ui.ffm + ic.ui.f0) * ic.ui.rowb;
+                const uint32_t dst = wring + (uint32_t)(js % S) * kSlotBytes;
+                if (ic.ui.fmt == 0) copy_block<kPieceQ4K / 16, kUnitRows>(dst, src + cb * kPieceQ4K, ic.ui.rowb, lane);
+                else copy_block<kPieceQ80 / 16, kSharedRows>(dst, src + cb * kPieceQ80, ic.ui.rowb, lane);
             }
-            if (a.pf_dist > a.n_slot) prefetch(j + a.pf_dist);
-        };
-        auto release = [&](int j) {                      // this warp is done with stage j
-            __syncwarp();
-            if (lane == 0) {
-                const int sl = j % a.n_slot;
-                // acquire-release: the other warps' reads of the slot happen before the
-                // copy that the last of them issues into it
-                uint32_t old;
-                asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
-                             : "=r"(old) : "r"(sm_addr(&s_cnt[sl])) : "memory");
-                const uint32_t done = old + 1u;
-                if (done == (uint32_t)NC * (uint32_t)(j / a.n_slot + 1)) issue(j + a.n_slot);
+            cp_commit();                                 // one group a stage, empty or not
+            ++js;
+            if (++im == 3) {
+                im = 0;
+                if (js < n_stage) unit_next(ic, a, un, s_pe, s_tab);
             }
         };
-        auto wait_full = [&](int j) -> bool {
-            const int sl = j % a.n_slot;
-            return wait_phase(full(sl), (uint32_t)((j / a.n_slot) & 1), abort_flag, status, limit);
-        };
-        if (warp == 0 && lane == 0) {
-            for (int j = 0; j < a.n_slot; ++j) issue(j);
-            for (int j = a.n_slot; j < a.pf_dist; ++j) prefetch(j);
-        }
-        int stage = 0;
-        // down accumulators: block cb = warp, tile i (16 hidden rows x the
-        // 8 window tokens): d0/d1 = columns hl(g, i) for tokens 2tq, 2tq+1, d2/d3 =
-        // columns hl(g, i) + 32, with hl(g, i) = 256 cb + 64 (g / 2) + 16 (g % 2) + i
+        for (int j = 0; j < S - 1; ++j) issue();
+        // B fragment of k-step s: x[token g][e .. e+3] in fp16 (zero for g >= T)
+        auto xb = [&](int s) { return g < T ? s_xf[((cb * 16 + s) * 4 + tq) * T + g] : make_uint2(0u, 0u); };
+        // down accumulators: tile i (16 hidden rows x the 8 window tokens): d0/d1 =
+        // columns hl(g, i) for tokens 2tq, 2tq+1, d2/d3 = columns hl(g, i) + 32, with
+        // hl(g, i) = 256 cb + 64 (g / 2) + 16 (g % 2) + i
         float D[16][4];
 #pragma unroll
         for (int i4 = 0; i4 < 16; ++i4) D[i4][0] = D[i4][1] = D[i4][2] = D[i4][3] = 0.0f;
+        auto down = [&](const UnitInfo &ui, const uint8_t *dn, const __half *wa) {
+            // B fragment: rows f = 2tq, 2tq + 1 of token g
+            const uint32_t bfr = *reinterpret_cast<const uint32_t *>(wa + g * kUnitRows + 2 * tq);
+            // rows 2tq, 2tq + 1 (K of the MMA); beyond a short unit they read row 0, whose
+            // product with the zero activations of those rows adds nothing
+            if (ui.fmt == 0) {
+                const uint8_t *r0 = dn + (2 * tq) * kPieceQ4K, *r1 = r0 + kPieceQ4K;
+                // Q4_K: lane g takes quant bytes 16 g .. 16 g + 15 of the block: chunk c = g / 2
+                // (sub-blocks 2c low nibbles, 2c + 1 high), columns hl(g, i)
+                const int c = g >> 1;
+                __half2 S0, N0, S1, N1;
+                q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(r0), c, S0, N0);
+                q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(r1), c, S1, N1);
+                const __half2 Slo = __lows2half2(S0, S1), Shi = __highs2half2(S0, S1);
+                const __half2 Nlo = __lows2half2(N0, N1), Nhi = __highs2half2(N0, N1);
+                const uint4 q0 = *reinterpret_cast<const uint4 *>(r0 + 16 + 16 * g);
+                const uint4 q1 = *reinterpret_cast<const uint4 *>(r1 + 16 + 16 * g);
+                const uint32_t w0[4] = {q0.x, q0.y, q0.z, q0.w}, w1[4] = {q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                for (int t16 = 0; t16 < 16; ++t16) {
+                    __half2 ql, qh;
+                    nib_pair(w0[t16 >> 2], w1[t16 >> 2], t16 & 3, ql, qh);
+                    mma16808(D[t16], dq_h22u(__hfma2(ql, Slo, Nlo)), dq_h22u(__hfma2(qh, Shi, Nhi)), bfr);
+                }
+            } else {
+                const uint8_t *r0 = dn + (2 * tq < ui.rows ? 2 * tq : 0) * kPieceQ80;
+                const uint8_t *r1 = dn + (2 * tq + 1 < ui.rows ? 2 * tq + 1 : 0) * kPieceQ80;
+                // Q8_0: the same columns: hl(g, i) lies in block 2c of this 256-column
+                // window at position 16 (g % 2) + i, hl + 32 in block 2c + 1
+                const int c = g >> 1, h1 = g & 1;
+                const uint32_t *p0 = reinterpret_cast<const uint32_t *>(r0 + 68 * c);   // block 2c (2c + 1 at + 34)
+                const uint32_t *p1 = reinterpret_cast<const uint32_t *>(r1 + 68 * c);
+                const __half2 dlo = __halves2half2(__ushort_as_half((unsigned short)(p0[0] & 0xffff)),
+                                                   __ushort_as_half((unsigned short)(p1[0] & 0xffff)));
+                const __half2 dhi = __halves2half2(__ushort_as_half((unsigned short)(p0[8] >> 16)),
+                                                   __ushort_as_half((unsigned short)(p1[8] >> 16)));
+#pragma unroll
+                for (int wq = 0; wq < 4; ++wq) {
+                    // block 2c bytes 2 + 16 h1 + 4 wq ..: words (16 h1 + 4 wq) / 4 .. shifted 16
+                    const int wl = 4 * h1 + wq;
+                    const uint32_t l0 = __funnelshift_r(p0[wl], p0[wl + 1], 16);
+                    const uint32_t l1 = __funnelshift_r(p1[wl], p1[wl + 1], 16);
+                    // block 2c + 1 bytes 36 + 16 h1 + 4 wq: word 9 + 4 h1 + wq (aligned)
+                    const uint32_t u0 = p0[9 + wl], u1 = p1[9 + wl];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        mma16808(D[4 * wq + b], dq_h22u(__hmul2(i8_pair(l0, l1, b), dlo)),
+                                 dq_h22u(__hmul2(i8_pair(u0, u1, b), dhi)), bfr);
+                }
+            }
+        };
         uint32_t touched = 0;                             // window tokens this CTA's units served
-        for (int iu = (int)u_begin; iu < (int)u_end; ++iu, stage += 3) {
-            const UnitInfo ui = unit_info(a, un, s_pe, s_tab, iu);
-            uint32_t off[3];
-            for (int p = 0; p < 3; ++p) off[p] = (uint32_t)((stage + p) % a.n_slot) * a.slot_bytes;
+        UnitInfo prev{};
+        bool prev_live = false;
+        UnitCursor cc{ui0, (int)u_begin};                   // the unit being computed
+        for (int u = 0; u < n_unit; ++u) {
+            if (u > 0) unit_next(cc, a, un, s_pe, s_tab);
+            const UnitInfo ui = cc.ui;
             const bool live = ui.blob != nullptr;
             if (!live && warp == 0 && lane == 0) set_status(status, MOE_ERR_DEVICE_FAULT);
             // tokens of this unit: the expert's, or every token (shared)
             const uint32_t tmask = live ? (ui.u >= 0 ? s_tmask[ui.u] : ((1u << T) - 1u)) : 0u;
             touched |= tmask;
-
+            cp_wait<S - 3>();                            // stages up to 3u + 1 have landed
+            __syncwarp();
             // ---- gate / up over this warp's block
-            bool ok = wait_full(stage) && wait_full(stage + 1);
-            ok = __all_sync(0xffffffffu, ok);           // the MMAs below need the whole warp
             float c4[2][4];
 #pragma unroll
             for (int i2 = 0; i2 < 2; ++i2) c4[i2][0] = c4[i2][1] = c4[i2][2] = c4[i2][3] = 0.0f;
-            if (ok && live) {
-                const uint8_t *gst = ring + off[0], *ust = ring + off[1];
-                {
-                    const int cb = warp;
-                    // B fragment of k-step s: x[token g][e .. e+3] in fp16 (zero for g >= T)
-                    auto xb = [&](int s) {
-                        return g < T ? s_xf[((cb * 16 + s) * 4 + tq) * T + g] : make_uint2(0u, 0u);
-                    };
-                    if (ui.fmt == 0) {
-                        const uint8_t *gr = gst + g * ui.rowb + cb * 144, *ur = ust + g * ui.rowb + cb * 144;
-                        __half2 Sg, NZg, Su, NZu;
-                        q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(gr), tq, Sg, NZg);
-                        q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(ur), tq, Su, NZu);
-                        const uint32_t *gq = reinterpret_cast<const uint32_t *>(gr + 16 + 32 * tq);
-                        const uint32_t *uq = reinterpret_cast<const uint32_t *>(ur + 16 + 32 * tq);
+            if (live) {
+                const uint8_t *gst = wring_p + (uint32_t)((3 * u) % S) * kSlotBytes;
+                const uint8_t *ust = wring_p + (uint32_t)((3 * u + 1) % S) * kSlotBytes;
+                if (ui.fmt == 0) {
+                    const uint8_t *gr = gst + g * kPieceQ4K, *ur = ust + g * kPieceQ4K;
+                    __half2 Sg, NZg, Su, NZu;
+                    q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(gr), tq, Sg, NZg);
+                    q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(ur), tq, Su, NZu);
+                    const uint4 ga = *reinterpret_cast<const uint4 *>(gr + 16 + 32 * tq);
+                    const uint4 gb = *reinterpret_cast<const uint4 *>(gr + 32 + 32 * tq);
+                    const uint4 ua = *reinterpret_cast<const uint4 *>(ur + 16 + 32 * tq);
+                    const uint4 ub = *reinterpret_cast<const uint4 *>(ur + 32 + 32 * tq);
+                    const uint32_t gq[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                    const uint32_t uq[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-                        for (int s = 0; s < 8; ++s) {
-                            uint32_t og[4], ou[4];
-                            q4k_word_f16(gq[s], __low2half2(Sg), __low2half2(NZg), __high2half2(Sg),
-                                         __high2half2(NZg), og);
-                            q4k_word_f16(uq[s], __low2half2(Su), __low2half2(NZu), __high2half2(Su),
-                                         __high2half2(NZu), ou);
-                            const uint2 xl = xb(s), xh = xb(8 + s);
-                            mma16816(c4[0], og[0], ou[0], og[1], ou[1], xl.x, xl.y);
-                            mma16816(c4[1], og[2], ou[2], og[3], ou[3], xh.x, xh.y);
-                        }
-                    } else {
-                        // units shorter than 8 rows: MMA rows g >= rows read row 0 (their
-                        // outputs are not used)
-                        const int gr_ = g < ui.rows ? g : 0;
-                        const uint32_t *gw =
-                            reinterpret_cast<const uint32_t *>(gst + gr_ * ui.rowb + 272 * cb + 68 * tq);
-                        const uint32_t *uw =
-                            reinterpret_cast<const uint32_t *>(ust + gr_ * ui.rowb + 272 * cb + 68 * tq);
-                        const __half2 Dg0 = __half2half2(__ushort_as_half((unsigned short)(gw[0] & 0xffff)));
-                        const __half2 Dg1 = __half2half2(__ushort_as_half((unsigned short)(gw[8] >> 16)));
-                        const __half2 Du0 = __half2half2(__ushort_as_half((unsigned short)(uw[0] & 0xffff)));
-                        const __half2 Du1 = __half2half2(__ushort_as_half((unsigned short)(uw[8] >> 16)));
+                    for (int s = 0; s < 8; ++s) {
+                        uint32_t og[4], ou[4];
+                        q4k_word_f16(gq[s], __low2half2(Sg), __low2half2(NZg), __high2half2(Sg), __high2half2(NZg), og);
+                        q4k_word_f16(uq[s], __low2half2(Su), __low2half2(NZu), __high2half2(Su), __high2half2(NZu), ou);
+                        const uint2 xl = xb(s), xh = xb(8 + s);
+                        mma16816(c4[0], og[0], ou[0], og[1], ou[1], xl.x, xl.y);
+                        mma16816(c4[1], og[2], ou[2], og[3], ou[3], xh.x, xh.y);
+                    }
+                } else {
+                    // units shorter than 8 rows: MMA rows g >= rows read row 0 (their
+                    // outputs are not used)
+                    const int gr_ = g < ui.rows ? g : 0;
+                    const uint32_t *gw = reinterpret_cast<const uint32_t *>(gst + gr_ * kPieceQ80 + 68 * tq);
+                    const uint32_t *uw = reinterpret_cast<const uint32_t *>(ust + gr_ * kPieceQ80 + 68 * tq);
+                    const __half2 Dg0 = __half2half2(__ushort_as_half((unsigned short)(gw[0] & 0xffff)));
+                    const __half2 Dg1 = __half2half2(__ushort_as_half((unsigned short)(gw[8] >> 16)));
+                    const __half2 Du0 = __half2half2(__ushort_as_half((unsigned short)(uw[0] & 0xffff)));
+                    const __half2 Du1 = __half2half2(__ushort_as_half((unsigned short)(uw[8] >> 16)));
 #pragma unroll
-                        for (int s = 0; s < 8; ++s) {
-                            // block 2tq: q8 bytes 2 + 4s .. 5 + 4s; block 2tq + 1: bytes 36 + 4s ..
-                            const uint32_t gl = __funnelshift_r(gw[s], gw[s + 1], 16);
-                            const uint32_t ul = __funnelshift_r(uw[s], uw[s + 1], 16);
-                            const uint32_t gh = gw[9 + s], uh = uw[9 + s];
-                            const uint2 xl = xb(s), xh = xb(8 + s);
-                            mma16816(c4[0], q80_pair_f16(gl, Dg0), q80_pair_f16(ul, Du0),
-                                     q80_pair_f16(gl >> 16, Dg0), q80_pair_f16(ul >> 16, Du0), xl.x, xl.y);
-                            mma16816(c4[1], q80_pair_f16(gh, Dg1), q80_pair_f16(uh, Du1),
-                                     q80_pair_f16(gh >> 16, Dg1), q80_pair_f16(uh >> 16, Du1), xh.x, xh.y);
-                        }
+                    for (int s = 0; s < 8; ++s) {
+                        // block 2tq: q8 bytes 2 + 4s .. 5 + 4s; block 2tq + 1: bytes 36 + 4s ..
+                        const uint32_t gl = __funnelshift_r(gw[s], gw[s + 1], 16);
+                        const uint32_t ul = __funnelshift_r(uw[s], uw[s + 1], 16);
+                        const uint32_t gh = gw[9 + s], uh = uw[9 + s];
+                        const uint2 xl = xb(s), xh = xb(8 + s);
+                        mma16816(c4[0], q80_pair_f16(gl, Dg0), q80_pair_f16(ul, Du0), q80_pair_f16(gl >> 16, Dg0),
+                                 q80_pair_f16(ul >> 16, Du0), xl.x, xl.y);
+                        mma16816(c4[1], q80_pair_f16(gh, Dg1), q80_pair_f16(uh, Du1), q80_pair_f16(gh >> 16, Dg1),
+                                 q80_pair_f16(uh >> 16, Du1), xh.x, xh.y);
                     }
                 }
             }
-            release(stage);                               // the gate and up slabs are read
-            release(stage + 1);
             // partial sums of this warp: (g, u) of ff row f0 + g for window token n
+            const int buf = u & 1;
             {
+                float2 *red = s_red + (size_t)buf * NC * kDecTok * kUnitRows;
                 const float c0 = c4[0][0] + c4[1][0], c1 = c4[0][1] + c4[1][1];
                 const float c2 = c4[0][2] + c4[1][2], c3 = c4[0][3] + c4[1][3];
                 if (g < ui.rows) {
-                    if ((tmask >> (2 * tq)) & 1u) s_red[(warp * kDecTok + 2 * tq) * kUnitRows + g] = make_float2(c0, c2);
+                    if ((tmask >> (2 * tq)) & 1u) red[(warp * kDecTok + 2 * tq) * kUnitRows + g] = make_float2(c0, c2);
                     if ((tmask >> (2 * tq + 1)) & 1u)
-                        s_red[(warp * kDecTok + 2 * tq + 1) * kUnitRows + g] = make_float2(c1, c3);
+                        red[(warp * kDecTok + 2 * tq + 1) * kUnitRows + g] = make_float2(c1, c3);
                 }
             }
-            // barrier among the consumer warps that also ORs their view of the abort
-            // flag, so that every warp takes the same decision
+            // every warp's partial sums of unit u, and the activations of unit u - 1, are
+            // complete past this barrier
             __syncwarp();
-            {
-                uint32_t any;
-                asm volatile(
-                    "{\n\t.reg .pred pi, po;\n\t"
-                    "setp.ne.u32 pi, %1, 0;\n\t"
-                    "bar.red.or.pred po, 1, %2, pi;\n\t"
-                    "selp.u32 %0, 1, 0, po;\n\t}"
-                    : "=r"(any)
-                    : "r"((uint32_t)(*abort_flag)), "r"(NC * 32)
-                    : "memory");
-                if (any) break;
-            }
-            // B operand of the down projection: w_{n,e} * SiLU(g) * u in fp16, [token n][ff row f]
+            asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
+            // B operand of the down projection of unit u: w_{n,e} * SiLU(g) * u in fp16, [token n][ff row f]
             for (int ct = warp * 32 + lane; ct < kUnitRows * kDecTok; ct += NC * 32) {
+                const float2 *red = s_red + (size_t)buf * NC * kDecTok * kUnitRows;
                 const int f = ct & 7, n = ct >> 3;
                 float v = 0.0f;
                 if (((tmask >> n) & 1u) && f < ui.rows) {
                     float gs = 0.0f, us = 0.0f;
                     for (int w2 = 0; w2 < NC; ++w2) {
-                        const float2 pv = s_red[(w2 * kDecTok + n) * kUnitRows + f];
+                        const float2 pv = red[(w2 * kDecTok + n) * kUnitRows + f];
                         gs += pv.x;
                         us += pv.y;
                     }
@@ -817,87 +865,27 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
                     v = silu_mul(gs, us) * wt;
                     if (!(fabsf(v) <= 65504.0f)) set_status(status, MOE_ERR_DEVICE_FAULT);
                 }
-                s_wa[n * kUnitRows + f] = __float2half_rn(v);
+                s_wa[buf * kDecTok * kUnitRows + n * kUnitRows + f] = __float2half_rn(v);
             }
+            // ---- down rows of unit u - 1 (the 8 rows are the MMA K), for this warp's block
+            if (u > 0 && prev_live)
+                down(prev, wring_p + (uint32_t)((3 * u - 1) % S) * kSlotBytes, s_wa + (buf ^ 1) * kDecTok * kUnitRows);
+            // the slots of stages 3u - 1, 3u and 3u + 1 are read: refill them
             __syncwarp();
-            asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
-
-            // ---- down rows of the unit (the 8 rows are the MMA K), for this warp's block
-            ok = ok && wait_full(stage + 2);
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok && live) {
-                const uint8_t *dn = ring + off[2];
-                // B fragment: rows f = 2tq, 2tq + 1 of token g
-                const uint32_t bfr = *reinterpret_cast<const uint32_t *>(s_wa + g * kUnitRows + 2 * tq);
-                // rows 2tq, 2tq + 1 (K of the MMA); beyond a short unit they read row 0, whose
-                // product with the zero activations of those rows adds nothing
-                const uint8_t *r0 = dn + (2 * tq < ui.rows ? 2 * tq : 0) * ui.rowb;
-                const uint8_t *r1 = dn + (2 * tq + 1 < ui.rows ? 2 * tq + 1 : 0) * ui.rowb;
-                {
-                    const int cb = warp;
-                    {
-                        if (ui.fmt == 0) {
-                            // Q4_K: lane g takes quant bytes 16 g .. 16 g + 15 of the block: chunk
-                            // c = g / 2 (sub-blocks 2c low nibbles, 2c + 1 high), columns hl(g, i)
-                            const int c = g >> 1;
-                            __half2 S0, N0, S1, N1;
-                            q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(r0 + cb * 144), c, S0, N0);
-                            q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(r1 + cb * 144), c, S1, N1);
-                            const __half2 Slo = __lows2half2(S0, S1), Shi = __highs2half2(S0, S1);
-                            const __half2 Nlo = __lows2half2(N0, N1), Nhi = __highs2half2(N0, N1);
-                            const uint4 q0 = *reinterpret_cast<const uint4 *>(r0 + cb * 144 + 16 + 16 * g);
-                            const uint4 q1 = *reinterpret_cast<const uint4 *>(r1 + cb * 144 + 16 + 16 * g);
-                            const uint32_t w0[4] = {q0.x, q0.y, q0.z, q0.w}, w1[4] = {q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-                            for (int t16 = 0; t16 < 16; ++t16) {
-                                __half2 ql, qh;
-                                nib_pair(w0[t16 >> 2], w1[t16 >> 2], t16 & 3, ql, qh);
-                                mma16808(D[t16], dq_h22u(__hfma2(ql, Slo, Nlo)), dq_h22u(__hfma2(qh, Shi, Nhi)),
-                                         bfr);
-                            }
-                        } else {
-                            // Q8_0: the same columns: hl(g, i) lies in block 2c of this 256-column
-                            // window at position 16 (g % 2) + i, hl + 32 in block 2c + 1
-                            const int c = g >> 1, h1 = g & 1;
-                            const int o0 = 272 * cb + 68 * c;            // block 2c (block 2c + 1 at + 34)
-                            const uint32_t *p0 = reinterpret_cast<const uint32_t *>(r0 + o0);
-                            const uint32_t *p1 = reinterpret_cast<const uint32_t *>(r1 + o0);
-                            const __half2 dlo = __halves2half2(__ushort_as_half((unsigned short)(p0[0] & 0xffff)),
-                                                               __ushort_as_half((unsigned short)(p1[0] & 0xffff)));
-                            const __half2 dhi = __halves2half2(__ushort_as_half((unsigned short)(p0[8] >> 16)),
-                                                               __ushort_as_half((unsigned short)(p1[8] >> 16)));
-#pragma unroll
-                            for (int wq = 0; wq < 4; ++wq) {
-                                // block 2c bytes 2 + 16 h1 + 4 wq ..: words (16 h1 + 4 wq) / 4 .. shifted 16
-                                const int wl = 4 * h1 + wq;
-                                const uint32_t l0 = __funnelshift_r(p0[wl], p0[wl + 1], 16);
-                                const uint32_t l1 = __funnelshift_r(p1[wl], p1[wl + 1], 16);
-                                // block 2c + 1 bytes 36 + 16 h1 + 4 wq: word 9 + 4 h1 + wq (aligned)
-                                const uint32_t u0 = p0[9 + wl], u1 = p1[9 + wl];
-#pragma unroll
-                                for (int b = 0; b < 4; ++b)
-                                    mma16808(D[4 * wq + b], dq_h22u(__hmul2(i8_pair(l0, l1, b), dlo)),
-                                             dq_h22u(__hmul2(i8_pair(u0, u1, b), dhi)), bfr);
-                            }
-                        }
-                    }
-                }
-            }
-            release(stage + 2);
+            issue();                                     // stages 3u - 1 + S .. 3u + 1 + S
+            issue();
+            issue();
+            prev = ui;
+            prev_live = live;
         }
-        // copies still in flight (an early exit) must land before the CTA ends: the
-        // last stage requested into each slot
-        __syncwarp();
-        asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
-        if (warp == 0 && lane < a.n_slot) {
-            const int j = s_last[lane];
-            if (j >= 0 && !(j == a.skip_stage && blockIdx.x == 0)) {
-                const long long t0 = clock64();
-                while (!mbar_poll(full(lane), (uint32_t)((j / a.n_slot) & 1)) && clock64() - t0 < limit) {
-                }
-            }
+        if (n_unit > 0) {
+            cp_wait<0>();
+            __syncwarp();
+            asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");   // the last activations
+            if (prev_live)
+                down(prev, wring_p + (uint32_t)((3 * n_unit - 1) % S) * kSlotBytes,
+                     s_wa + ((n_unit - 1) & 1) * kDecTok * kUnitRows);
         }
-        __syncwarp();
         // ---- this CTA's share of y, for the window tokens its units served
         {
             const int hl = 256 * warp + 64 * (g >> 1) + 16 * (g & 1);
@@ -961,57 +949,34 @@ int dec_route_parts(int H)
 
 int dec_consumers(int H) { return H / 256; }
 
-// The staging ring takes all the shared memory the rest of the kernel leaves,
-// cut into slots of the largest slab (8 rows of a routed matrix, or the
-// shared expert's rows per unit); at least kMinSlot slots are needed.
+// The staging rings take all the shared memory the rest of the kernel leaves.
 static int64_t dec_base_ring(const moe_config &c, int32_t T)
 {
     const LayerSmem base = layer_smem(c.n_experts, T, c.hidden, dec_consumers(c.hidden), 0);
     return ((int64_t)kDecSmemBudget - (int64_t)base.total) & ~(int64_t)127;
 }
 
-static int64_t slot_for(const moe_config &c, int srows)
-{
-    const int64_t rb = (int64_t)(c.hidden / 256) * 144, rbs = (int64_t)(c.hidden / 32) * 34;
-    const int64_t slab = std::max<int64_t>(kUnitRows * rb, c.shared_ff ? srows * rbs : 0);
-    return (slab + 127) & ~(int64_t)127;
-}
-
-// Rows per shared-expert unit: 8, or fewer when 8-row Q8_0 slabs would leave
-// fewer than kMinSlot slots (0: not even 2 rows do).
-int dec_shared_rows(const moe_config &c, int32_t T)
-{
-    if (!c.shared_ff) return kUnitRows;
-    const int64_t ring = dec_base_ring(c, T);
-    for (int r = kUnitRows; r >= 2; r /= 2)
-        if (ring / slot_for(c, r) >= kMinSlot) return r;
-    return 0;
-}
-
-uint32_t dec_slot_bytes(const moe_config &c, int32_t T) { return (uint32_t)slot_for(c, std::max(2, dec_shared_rows(c, T))); }
-
-int dec_slots(const moe_config &c, int32_t T)
-{
-    const int64_t ring = dec_base_ring(c, T);
-    if (dec_shared_rows(c, T) == 0 || ring < (int64_t)T * c.n_experts * 12 + 16) return 0;
-    const int64_t n = ring / dec_slot_bytes(c, T);
-    return n < kMinSlot ? 0 : (int)std::min<int64_t>(n, kMaxSlot);
-}
-
 uint32_t dec_ring_bytes(const moe_config &c, int32_t T) { return (uint32_t)dec_base_ring(c, T); }
 
-// Stages between a stage's ring copy and the L2 prefetch issued with it: the
-// slots plus about 128 KB (per SM, 19 MB over the GPU: well inside L2).
-int dec_prefetch_distance(const moe_config &c, int32_t T)
+// Stages of each consumer warp's ring: the largest of the compiled counts that
+// fits (0: none does, or the routing scratch does not fit the ring).
+static const int kStageCounts[] = {16, 12, 10, 8, 6};
+
+int dec_stages(const moe_config &c, int32_t T)
 {
-    const int n = dec_slots(c, T);
-    return n + (int)((kPrefetchBytes + dec_slot_bytes(c, T) - 1) / dec_slot_bytes(c, T));
+    const int64_t ring = dec_base_ring(c, T);
+    const int nc = dec_consumers(c.hidden);
+    if (nc <= 0 || ring < (int64_t)T * c.n_experts * 12 + 16) return 0;
+    const int64_t per = ring / ((int64_t)nc * kSlotBytes);
+    for (int s : kStageCounts)
+        if (per >= s) return s;
+    return 0;
 }
 
 bool dec_supported(const moe_config &c, int32_t T)
 {
     return T >= 0 && T <= kDecTok && dec_route_parts(c.hidden) != 0 && c.hidden / 256 <= kMaxCons &&
-           c.ff % kUnitRows == 0 && dec_slots(c, T) > 0;
+           c.ff % kUnitRows == 0 && c.shared_ff % kSharedRows == 0 && dec_stages(c, T) > 0;
 }
 
 template <typename K>
@@ -1045,8 +1010,11 @@ static cudaError_t dec_set_attributes()
     if (done[dev]) return cudaSuccess;
     e = cudaFuncSetAttribute(k_dec_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kDecTok * 8192 * (int)sizeof(uint16_t));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_dec_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBudget);
+    const void *layers[] = {(const void *)k_dec_layer<16>, (const void *)k_dec_layer<12>,
+                            (const void *)k_dec_layer<10>, (const void *)k_dec_layer<8>,
+                            (const void *)k_dec_layer<6>};
+    for (const void *f : layers)
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBudget);
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
@@ -1064,9 +1032,16 @@ cudaError_t launch_decode(const DecArgs &a0, cudaStream_t s)
     prof_end(kPhDecRoute, s);
     if (e != cudaSuccess) return e;
     const LayerSmem L = layer_smem(a.E, a.T, a.H, a.nc, a.ring_bytes);
+    const dim3 grid(dec_sms()), block(32 * std::max(a.nc, kDecTok));   // at least one warp per token
     prof_begin(kPhDecLayer, s);
-    const int warps = std::max(a.nc, kDecTok);   // consumer warps; at least one warp per token
-    e = launch_pdl(k_dec_layer, dim3(dec_sms()), dim3(32 * warps), L.total, s, true, a);
+    switch (a.stages) {
+    case 16: e = launch_pdl(k_dec_layer<16>, grid, block, L.total, s, true, a); break;
+    case 12: e = launch_pdl(k_dec_layer<12>, grid, block, L.total, s, true, a); break;
+    case 10: e = launch_pdl(k_dec_layer<10>, grid, block, L.total, s, true, a); break;
+    case 8: e = launch_pdl(k_dec_layer<8>, grid, block, L.total, s, true, a); break;
+    case 6: e = launch_pdl(k_dec_layer<6>, grid, block, L.total, s, true, a); break;
+    default: e = cudaErrorInvalidValue;
+    }
     prof_end(kPhDecLayer, s);
     return e;
 }

@@ -134,14 +134,11 @@ struct DecArgs {
     int H, E, FF, k, T, SFF, score_fn;
     int route_parts;             // router row split per CTA (1, 2, 4 or 8)
     int nc;                      // consumer warps of the layer kernel
-    uint32_t ring_bytes;         // its staging ring
-    int srows;                   // ff rows per shared-expert unit (8, 4 or 2)
-    int n_slot;                  // staging-ring slots
-    int pf_dist;                 // L2 prefetch distance in stages (<= n_slot: none)
-    uint32_t slot_bytes;         // bytes of one slot
+    uint32_t ring_bytes;         // their staging rings
+    int stages;                  // stages of each consumer warp's ring
     int overlap_prev;            // weights may be read before the previous kernel ends
     long long wait_cycles;       // limit of every bounded wait
-    int skip_stage;              // test hook: CTA 0 never arms this ring stage (-1: none)
+    int skip_cta;                // test hook: this CTA never issues its first bulk copy (-1: none)
     const uint16_t *x;
     const float *wr, *bias;
     const uint8_t *const *blobs;
@@ -159,17 +156,14 @@ struct DecArgs {
 int dec_route_parts(int H);
 int dec_consumers(int H);
 uint32_t dec_ring_bytes(const moe_config &c, int32_t T);
-int dec_shared_rows(const moe_config &c, int32_t T);
-int dec_slots(const moe_config &c, int32_t T);
-uint32_t dec_slot_bytes(const moe_config &c, int32_t T);
-int dec_prefetch_distance(const moe_config &c, int32_t T);
+int dec_stages(const moe_config &c, int32_t T);
 bool dec_supported(const moe_config &c, int32_t T);
 cudaError_t launch_decode(const DecArgs &a, cudaStream_t s);
 
-// Test hooks (moe_debug_set): limit of the bounded device waits and a ring
-// stage of the decode kernel that is never armed.
+// Test hooks (moe_debug_set): limit of the bounded device waits, and a CTA of
+// the next call's main kernel that never issues its first bulk copy.
 long long debug_wait_cycles();
-int64_t debug_take_skip_stage();
+int debug_take_skip_copy();
 
 // Tensor-core (tcgen05) grouped GEMM path: its workspace regions.
 constexpr int kGemmSmallTokens = 16;   // calls with T <= 16 use the small-bucket GEMM configuration

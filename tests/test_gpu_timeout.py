@@ -1,7 +1,8 @@
 """Failure detection on the GPU without a fault: a bounded wait that runs out.
 
-moe_debug_set shortens every device wait and makes CTA 0 of the decode
-kernel leave one staging stage unarmed, so the waits for it give up.  The call
+moe_debug_set shortens every device wait and makes one CTA of the decode
+layer kernel arm its prologue barrier without issuing the copy it waits for,
+so the wait gives up.  The call
 must end (no hang), report MOE_ERR_TIMEOUT through the workspace status word,
 and leave the context usable: the next call, with the hooks cleared, matches
 the oracle.  Nothing here faults, traps or spins without a limit.
@@ -17,8 +18,8 @@ from parity import check_close, oracle_blobs, oracle_forward, oracle_inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("stage", [0, 2, 4])
-def test_decode_wait_timeout_is_reported_and_the_context_survives(stage):
+@pytest.mark.parametrize("cta", [0, 1, 7])
+def test_decode_wait_timeout_is_reported_and_the_context_survives(cta):
     wl = synth.small_variant(synth.WORKLOADS["qwen_decode"], name="qwen_e64", n_experts=64)
     T = 3
     pl = pack_layer(wl, gen_device="cpu")
@@ -27,11 +28,11 @@ def test_decode_wait_timeout_is_reported_and_the_context_survives(stage):
     x = synth.hidden_states(wl, T).cuda()
     try:
         moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, 1 << 22)      # ~2 ms
-        moe.moe_debug_set(moe.MOE_DEBUG_SKIP_STAGE, stage)
+        moe.moe_debug_set(moe.MOE_DEBUG_SKIP_COPY, cta)
         forward(pl, x, ws, cfg=cfg)
         assert moe.moe_last_device_status(ws) == moe.MOE_ERR_TIMEOUT
     finally:
-        moe.moe_debug_set(moe.MOE_DEBUG_SKIP_STAGE, -1)
+        moe.moe_debug_set(moe.MOE_DEBUG_SKIP_COPY, -1)
         moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, 0)
     # the skip is one-shot and the context is intact: the next call is right
     y32 = torch.empty(T, wl.hidden, dtype=torch.float32, device="cuda")
@@ -49,3 +50,5 @@ def test_debug_hook_rejects_bad_values():
         moe.moe_debug_set(99, 0)
     with pytest.raises(moe.MoeError):
         moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, -5)
+    with pytest.raises(moe.MoeError):
+        moe.moe_debug_set(moe.MOE_DEBUG_SKIP_COPY, -2)
