@@ -222,21 +222,18 @@ def algorithmic(wl, T, ids_per_layer):
 
     Bytes: each selected expert's blob once per window (+ shared blob), the
     fp32 router matrix, bias, x in, y out, ids and weights.  Per kernel of the
-    decode path: router E*H*4 + T*H*2; gate/up U*2*FF*(H/256)*144; down
-    U*FF*(H/256)*144 (U = distinct experts the window selected).  Flops:
+    decode path: router E*H*4 + T*H*2; layer U*blob + shared blob (U = distinct
+    experts the window selected).  Flops:
     router 2*T*E*H + 2*T*k*3*H*FF (+ 2*T*3*H*FF_s shared); padding not
     counted."""
     E, H, FF, k = wl.n_experts, wl.hidden, wl.ff, wl.top_k
-    rb = (H // 256) * 144
-    total_bytes, per_kernel = [], {"dec_route": [], "dec_gateup": [], "dec_down": [], "dec_layer": []}
+    total_bytes, per_kernel = [], {"dec_route": [], "dec_layer": []}
     for ids in ids_per_layer:
         U = len(np.unique(ids))
         b = U * wl.blob_bytes + wl.shared_blob_bytes + E * H * 4 + (E * 4 if wl.bias != "none" else 0)
         b += 2 * T * H * 2 + T * k * 8
         total_bytes.append(b)
         per_kernel["dec_route"].append(E * H * 4 + T * H * 2)
-        per_kernel["dec_gateup"].append(U * 2 * FF * rb)
-        per_kernel["dec_down"].append(U * FF * rb)
         per_kernel["dec_layer"].append(U * wl.blob_bytes + wl.shared_blob_bytes)
     flops = 2 * T * E * H + 2 * T * k * 3 * H * FF + (2 * T * 3 * H * wl.shared_ff if wl.has_shared else 0)
     gemm_gateup_flops = 2 * T * k * 2 * H * FF
@@ -411,7 +408,7 @@ def measure(args, wl, T, nL, world, rank, local, K=None, soak_s=0.0, target_s=0.
     step_bytes, kernel_bytes, flops, gemm_flops = algorithmic(wl, T, ids_per_layer)
     kernel_ms = {name: (v[2] / v[1] if v[1] else float("nan")) for name, v in prof.items()}
     share = {name: v[2] for name, v in prof.items()}
-    decode = any(n in prof for n in ("dec_layer", "dec_gateup"))
+    decode = "dec_layer" in prof
     layer_s = step_ms / 1e3 / nL
     out["hbm"] = {"algorithmic_bytes_per_call": int(step_bytes), "gbs": round(step_bytes / layer_s / 1e9, 1),
                   "frac": round(step_bytes / layer_s / 1e9 / pk["hbm_gbs"], 4)}
