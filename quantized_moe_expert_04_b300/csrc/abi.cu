@@ -304,7 +304,8 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
         d.SFF = cfg->shared_ff;
         d.score_fn = cfg->score_fn;
         d.route_parts = dec_route_parts(cfg->hidden);
-        d.nc = dec_consumers(cfg->hidden);
+        d.nc = dec_consumers(*cfg);
+        d.half = dec_half(*cfg) ? 1 : 0;
         d.ring_bytes = dec_ring_bytes(*cfg, T);
         d.stages = dec_stages(*cfg, T);
         d.overlap_prev = (cfg->flags & MOE_FLAG_STATIC_WEIGHTS) != 0;

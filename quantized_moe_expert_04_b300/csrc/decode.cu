@@ -329,7 +329,9 @@ constexpr int kSharedRows = 4;          // ff rows of a shared-expert unit
 constexpr int kPieceQ4K = 144;          // bytes of one row's 256-column block: one Q4_K super-block
 constexpr int kPieceQ80 = 272;          // the same block in Q8_0: eight 34-byte blocks
 constexpr uint32_t kSlotBytes = 1152;   // one stage of one warp: 8 x 144 (>= 4 x 272)
-constexpr int kMaxCons = 16;            // consumer warps (256-column blocks of H)
+constexpr uint32_t kSlotHalf = 640;     // ... of a half-block warp: 8 x 64 quant bytes, then 8 x 16 header bytes
+constexpr int kMaxCons = 16;            // consumer warps of 256 columns
+constexpr int kMaxConsHalf = 20;        // consumer warps of 128 columns (96 registers a thread)
 
 // Shared-memory carve of k_dec_layer (byte offsets).
 struct LayerSmem {
@@ -486,10 +488,31 @@ __device__ __forceinline__ void copy_block(uint32_t dst, const uint8_t *src, int
     }
 }
 
-// The layer kernel, S stages per consumer warp.  128 registers a thread: 16
-// warps (4 on each SM sub-partition) fit one SM.
-template <int S>
-__global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
+// A half-block warp's copy of a Q4_K slab: of each of the 8 rows, the 16-byte
+// header (piece 0) and the 64 quant bytes of its half hh (pieces 1..4), packed
+// as [8][64] quant bytes then [8][16] headers (a 64-byte row stride keeps the
+// gate/up reads of two rows on disjoint banks).
+__device__ __forceinline__ void copy_half(uint32_t dst, const uint8_t *src, int rowb, int hh, int lane)
+{
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = lane + 32 * k;
+        if (i < kUnitRows * 5) {
+            const int r = i / 5, p = i - r * 5;
+            const uint32_t d = p == 0 ? 512u + 16u * r : (uint32_t)(64 * r + 16 * (p - 1));
+            const int o = p == 0 ? 0 : 16 + 64 * hh + 16 * (p - 1);
+            cp16(dst + d, src + r * rowb + o);
+        }
+    }
+}
+
+// The layer kernel, S stages per consumer warp.  HALF: each consumer warp owns
+// 128 columns (half a Q4_K super-block) instead of 256, for twice the warps;
+// only for layers without a shared expert.  128 registers a thread at 256
+// columns (16 warps, 4 on each SM sub-partition, fit one SM), 96 at 128
+// columns (20 warps).
+template <int S, bool HALF>
+__global__ void __maxnreg__(HALF ? 96 : 128) k_dec_layer(DecArgs a)
 {
     static_assert(S >= 4, "the lagging down projection keeps 3 stages busy");
     extern __shared__ __align__(128) uint8_t smem[];
@@ -686,10 +709,15 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
         // j % 3) sits in slot j % S.  The down projection of unit u runs one unit
         // late, after the gate/up of unit u + 1, so one barrier per unit orders
         // both the partial sums (gate/up) and the activations (down).
-        const int g = lane >> 2, tq = lane & 3, cb = warp;
+        // (HALF: warp w owns the 128-column half w % 2 of block w / 2, and stages the
+        // row headers and its half of the quant bytes.)
+        constexpr uint32_t SLOT = HALF ? kSlotHalf : kSlotBytes;
+        constexpr int NT = HALF ? 8 : 16;                // down tiles of 16 columns (x 2) per warp
+        const int g = lane >> 2, tq = lane & 3;
+        const int cb = HALF ? warp >> 1 : warp, hh = HALF ? warp & 1 : 0;
         const int n_unit = (int)(u_end - u_begin), n_stage = 3 * n_unit;
-        const uint32_t wring = sm_addr(ring) + (uint32_t)(warp * S) * kSlotBytes;
-        const uint8_t *wring_p = ring + (size_t)warp * S * kSlotBytes;
+        const uint32_t wring = sm_addr(ring) + (uint32_t)(warp * S) * SLOT;
+        const uint8_t *wring_p = ring + (size_t)warp * S * SLOT;
         // the next stage to copy: stage js, matrix im of the unit under the cursor ic
         const UnitInfo ui0 = unit_info(a, un, s_pe, s_tab, (int)u_begin);
         UnitCursor ic{ui0, (int)u_begin};
@@ -697,8 +725,9 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
         auto issue = [&]() {
             if (js < n_stage && ic.ui.blob) {
                 const uint8_t *src = ic.ui.blob + ((int64_t)im * ic.ui.ffm + ic.ui.f0) * ic.ui.rowb;
-                const uint32_t dst = wring + (uint32_t)(js % S) * kSlotBytes;
-                if (ic.ui.fmt == 0) copy_block<kPieceQ4K / 16, kUnitRows>(dst, src + cb * kPieceQ4K, ic.ui.rowb, lane);
+                const uint32_t dst = wring + (uint32_t)(js % S) * SLOT;
+                if (HALF) copy_half(dst, src + cb * kPieceQ4K, ic.ui.rowb, hh, lane);   // routed units only
+                else if (ic.ui.fmt == 0) copy_block<kPieceQ4K / 16, kUnitRows>(dst, src + cb * kPieceQ4K, ic.ui.rowb, lane);
                 else copy_block<kPieceQ80 / 16, kSharedRows>(dst, src + cb * kPieceQ80, ic.ui.rowb, lane);
             }
             cp_commit();                                 // one group a stage, empty or not
@@ -709,20 +738,43 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
             }
         };
         for (int j = 0; j < S - 1; ++j) issue();
-        // B fragment of k-step s: x[token g][e .. e+3] in fp16 (zero for g >= T)
-        auto xb = [&](int s) { return g < T ? s_xf[((cb * 16 + s) * 4 + tq) * T + g] : make_uint2(0u, 0u); };
+        // B fragment x[token g][e .. e+3] in fp16 (zero for g >= T), e = 256 cb + 64 c +
+        // (s < 8 ? 4 s : 32 + 4 (s - 8)): sub-block pair c, word s of its quant bytes
+        auto xb = [&](int s, int c) { return g < T ? s_xf[((cb * 16 + s) * 4 + c) * T + g] : make_uint2(0u, 0u); };
         // down accumulators: tile i (16 hidden rows x the 8 window tokens): d0/d1 =
         // columns hl(g, i) for tokens 2tq, 2tq+1, d2/d3 = columns hl(g, i) + 32, with
-        // hl(g, i) = 256 cb + 64 (g / 2) + 16 (g % 2) + i
-        float D[16][4];
+        // hl(g, i) = 256 cb + 64 (g / 2) + 16 (g % 2) + i, or (HALF) 256 cb + 64 c +
+        // 8 (g % 4) + i with c = 2 hh + g / 4
+        float D[NT][4];
 #pragma unroll
-        for (int i4 = 0; i4 < 16; ++i4) D[i4][0] = D[i4][1] = D[i4][2] = D[i4][3] = 0.0f;
+        for (int i4 = 0; i4 < NT; ++i4) D[i4][0] = D[i4][1] = D[i4][2] = D[i4][3] = 0.0f;
         auto down = [&](const UnitInfo &ui, const uint8_t *dn, const __half *wa) {
             // B fragment: rows f = 2tq, 2tq + 1 of token g
             const uint32_t bfr = *reinterpret_cast<const uint32_t *>(wa + g * kUnitRows + 2 * tq);
             // rows 2tq, 2tq + 1 (K of the MMA); beyond a short unit they read row 0, whose
             // product with the zero activations of those rows adds nothing
-            if (ui.fmt == 0) {
+            if (HALF) {
+                // lane g takes quant bytes 8 (g % 4) .. + 7 of pair c = 2 hh + g / 4, i.e. bytes
+                // 8 g .. 8 g + 7 of the staged half: columns 64 c + 8 (g % 4) + i (low
+                // nibbles) and + 32 (high)
+                const uint8_t *q0p = dn + (2 * tq) * 64, *q1p = q0p + 64;
+                const uint8_t *h0p = dn + 512 + (2 * tq) * 16, *h1p = h0p + 16;
+                const int c = 2 * hh + (g >> 2);
+                __half2 S0, N0, S1, N1;
+                q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(h0p), c, S0, N0);
+                q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(h1p), c, S1, N1);
+                const __half2 Slo = __lows2half2(S0, S1), Shi = __highs2half2(S0, S1);
+                const __half2 Nlo = __lows2half2(N0, N1), Nhi = __highs2half2(N0, N1);
+                const uint2 q0 = *reinterpret_cast<const uint2 *>(q0p + 8 * g);
+                const uint2 q1 = *reinterpret_cast<const uint2 *>(q1p + 8 * g);
+                const uint32_t w0[2] = {q0.x, q0.y}, w1[2] = {q1.x, q1.y};
+#pragma unroll
+                for (int t8 = 0; t8 < NT; ++t8) {
+                    __half2 ql, qh;
+                    nib_pair(w0[(t8 >> 2) & 1], w1[(t8 >> 2) & 1], t8 & 3, ql, qh);
+                    mma16808(D[t8], dq_h22u(__hfma2(ql, Slo, Nlo)), dq_h22u(__hfma2(qh, Shi, Nhi)), bfr);
+                }
+            } else if (ui.fmt == 0) {
                 const uint8_t *r0 = dn + (2 * tq) * kPieceQ4K, *r1 = r0 + kPieceQ4K;
                 // Q4_K: lane g takes quant bytes 16 g .. 16 g + 15 of the block: chunk c = g / 2
                 // (sub-blocks 2c low nibbles, 2c + 1 high), columns hl(g, i)
@@ -736,9 +788,9 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
                 const uint4 q1 = *reinterpret_cast<const uint4 *>(r1 + 16 + 16 * g);
                 const uint32_t w0[4] = {q0.x, q0.y, q0.z, q0.w}, w1[4] = {q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-                for (int t16 = 0; t16 < 16; ++t16) {
+                for (int t16 = 0; t16 < NT; ++t16) {
                     __half2 ql, qh;
-                    nib_pair(w0[t16 >> 2], w1[t16 >> 2], t16 & 3, ql, qh);
+                    nib_pair(w0[(t16 >> 2) & 3], w1[(t16 >> 2) & 3], t16 & 3, ql, qh);
                     mma16808(D[t16], dq_h22u(__hfma2(ql, Slo, Nlo)), dq_h22u(__hfma2(qh, Shi, Nhi)), bfr);
                 }
             } else {
@@ -763,7 +815,7 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
                     const uint32_t u0 = p0[9 + wl], u1 = p1[9 + wl];
 #pragma unroll
                     for (int b = 0; b < 4; ++b)
-                        mma16808(D[4 * wq + b], dq_h22u(__hmul2(i8_pair(l0, l1, b), dlo)),
+                        mma16808(D[(4 * wq + b) % NT], dq_h22u(__hmul2(i8_pair(l0, l1, b), dlo)),
                                  dq_h22u(__hmul2(i8_pair(u0, u1, b), dhi)), bfr);
                 }
             }
@@ -787,9 +839,31 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
 #pragma unroll
             for (int i2 = 0; i2 < 2; ++i2) c4[i2][0] = c4[i2][1] = c4[i2][2] = c4[i2][3] = 0.0f;
             if (live) {
-                const uint8_t *gst = wring_p + (uint32_t)((3 * u) % S) * kSlotBytes;
-                const uint8_t *ust = wring_p + (uint32_t)((3 * u + 1) % S) * kSlotBytes;
-                if (ui.fmt == 0) {
+                const uint8_t *gst = wring_p + (uint32_t)((3 * u) % S) * SLOT;
+                const uint8_t *ust = wring_p + (uint32_t)((3 * u + 1) % S) * SLOT;
+                if (HALF) {
+                    // lane tq takes quant bytes 16 tq .. 16 tq + 15 of the staged half: words
+                    // 4 (tq % 2) .. + 3 of pair c = 2 hh + tq / 2
+                    const uint8_t *gr = gst + g * 64, *ur = ust + g * 64;
+                    const int c = 2 * hh + (tq >> 1);
+                    __half2 Sg, NZg, Su, NZu;
+                    q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(gst + 512 + g * 16), c, Sg, NZg);
+                    q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(ust + 512 + g * 16), c, Su, NZu);
+                    const uint4 ga = *reinterpret_cast<const uint4 *>(gr + 16 * tq);
+                    const uint4 ua = *reinterpret_cast<const uint4 *>(ur + 16 * tq);
+                    const uint32_t gq[4] = {ga.x, ga.y, ga.z, ga.w};
+                    const uint32_t uq[4] = {ua.x, ua.y, ua.z, ua.w};
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        uint32_t og[4], ou[4];
+                        q4k_word_f16(gq[s], __low2half2(Sg), __low2half2(NZg), __high2half2(Sg), __high2half2(NZg), og);
+                        q4k_word_f16(uq[s], __low2half2(Su), __low2half2(NZu), __high2half2(Su), __high2half2(NZu), ou);
+                        const int w = 4 * (tq & 1) + s;
+                        const uint2 xl = xb(w, c), xh = xb(8 + w, c);
+                        mma16816(c4[0], og[0], ou[0], og[1], ou[1], xl.x, xl.y);
+                        mma16816(c4[1], og[2], ou[2], og[3], ou[3], xh.x, xh.y);
+                    }
+                } else if (ui.fmt == 0) {
                     const uint8_t *gr = gst + g * kPieceQ4K, *ur = ust + g * kPieceQ4K;
                     __half2 Sg, NZg, Su, NZu;
                     q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(gr), tq, Sg, NZg);
@@ -805,7 +879,7 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
                         uint32_t og[4], ou[4];
                         q4k_word_f16(gq[s], __low2half2(Sg), __low2half2(NZg), __high2half2(Sg), __high2half2(NZg), og);
                         q4k_word_f16(uq[s], __low2half2(Su), __low2half2(NZu), __high2half2(Su), __high2half2(NZu), ou);
-                        const uint2 xl = xb(s), xh = xb(8 + s);
+                        const uint2 xl = xb(s, tq), xh = xb(8 + s, tq);
                         mma16816(c4[0], og[0], ou[0], og[1], ou[1], xl.x, xl.y);
                         mma16816(c4[1], og[2], ou[2], og[3], ou[3], xh.x, xh.y);
                     }
@@ -825,7 +899,7 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
                         const uint32_t gl = __funnelshift_r(gw[s], gw[s + 1], 16);
                         const uint32_t ul = __funnelshift_r(uw[s], uw[s + 1], 16);
                         const uint32_t gh = gw[9 + s], uh = uw[9 + s];
-                        const uint2 xl = xb(s), xh = xb(8 + s);
+                        const uint2 xl = xb(s, tq), xh = xb(8 + s, tq);
                         mma16816(c4[0], q80_pair_f16(gl, Dg0), q80_pair_f16(ul, Du0), q80_pair_f16(gl >> 16, Dg0),
                                  q80_pair_f16(ul >> 16, Du0), xl.x, xl.y);
                         mma16816(c4[1], q80_pair_f16(gh, Dg1), q80_pair_f16(uh, Du1), q80_pair_f16(gh >> 16, Dg1),
@@ -869,7 +943,7 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
             }
             // ---- down rows of unit u - 1 (the 8 rows are the MMA K), for this warp's block
             if (u > 0 && prev_live)
-                down(prev, wring_p + (uint32_t)((3 * u - 1) % S) * kSlotBytes, s_wa + (buf ^ 1) * kDecTok * kUnitRows);
+                down(prev, wring_p + (uint32_t)((3 * u - 1) % S) * SLOT, s_wa + (buf ^ 1) * kDecTok * kUnitRows);
             // the slots of stages 3u - 1, 3u and 3u + 1 are read: refill them
             __syncwarp();
             issue();                                     // stages 3u - 1 + S .. 3u + 1 + S
@@ -883,12 +957,13 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
             __syncwarp();
             asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");   // the last activations
             if (prev_live)
-                down(prev, wring_p + (uint32_t)((3 * n_unit - 1) % S) * kSlotBytes,
+                down(prev, wring_p + (uint32_t)((3 * n_unit - 1) % S) * SLOT,
                      s_wa + ((n_unit - 1) & 1) * kDecTok * kUnitRows);
         }
         // ---- this CTA's share of y, for the window tokens its units served
         {
-            const int hl = 256 * warp + 64 * (g >> 1) + 16 * (g & 1);
+            const int hl = HALF ? 256 * cb + 64 * (2 * hh + (g >> 2)) + 8 * (g & 3)
+                                : 256 * cb + 64 * (g >> 1) + 16 * (g & 1);
 #pragma unroll
             for (int half = 0; half < 2; ++half)
 #pragma unroll
@@ -897,7 +972,7 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
                     if ((touched >> n) & 1u) {
                         float *dst = a.yacc + (int64_t)n * H + hl + 32 * half;
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
+                        for (int v = 0; v < NT / 4; ++v)
                             red_add_v4(dst + 4 * v, D[4 * v][2 * half + tk], D[4 * v + 1][2 * half + tk],
                                        D[4 * v + 2][2 * half + tk], D[4 * v + 3][2 * half + tk]);
                     }
@@ -915,15 +990,29 @@ __global__ void __maxnreg__(128) k_dec_layer(DecArgs a)
     __syncthreads();
     if (*s_is_last) {
         __threadfence();
+        // y = bf16(yacc): the loads of a batch are issued before its stores
         const int n4 = T * H / 4;
-        for (int i = threadIdx.x; i < n4; i += nthr) {
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.yacc) + i);
-            const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x)) |
-                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y)) << 16);
-            const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z)) |
-                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w)) << 16);
-            reinterpret_cast<uint2 *>(a.y)[i] = make_uint2(lo, hi);
-            if (a.y_f32) reinterpret_cast<float4 *>(a.y_f32)[i] = v;
+        const float4 *__restrict__ acc = reinterpret_cast<const float4 *>(a.yacc);
+        uint2 *__restrict__ yb = reinterpret_cast<uint2 *>(a.y);
+        float4 *__restrict__ yf = reinterpret_cast<float4 *>(a.y_f32);
+        constexpr int kBatch = 8;
+        for (int i0 = threadIdx.x; i0 < n4; i0 += kBatch * nthr) {
+            float4 v[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (i0 + j * nthr < n4) v[j] = __ldcg(acc + i0 + j * nthr);
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int i = i0 + j * nthr;
+                if (i < n4) {
+                    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].x)) |
+                                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].y)) << 16);
+                    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].z)) |
+                                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].w)) << 16);
+                    yb[i] = make_uint2(lo, hi);
+                    if (yf) yf[i] = v[j];
+                }
+            }
         }
         if (threadIdx.x == 0) a.header[kHdrTicketDown] = 0u;
     }
@@ -947,12 +1036,16 @@ int dec_route_parts(int H)
     return 0;   // unsupported
 }
 
-int dec_consumers(int H) { return H / 256; }
+// Half-block warps (128 columns each) for layers without a shared expert whose
+// 128-column blocks fit kMaxConsHalf warps; 256-column warps otherwise.
+bool dec_half(const moe_config &c) { return c.shared_ff == 0 && c.hidden / 128 <= kMaxConsHalf; }
+
+int dec_consumers(const moe_config &c) { return dec_half(c) ? c.hidden / 128 : c.hidden / 256; }
 
 // The staging rings take all the shared memory the rest of the kernel leaves.
 static int64_t dec_base_ring(const moe_config &c, int32_t T)
 {
-    const LayerSmem base = layer_smem(c.n_experts, T, c.hidden, dec_consumers(c.hidden), 0);
+    const LayerSmem base = layer_smem(c.n_experts, T, c.hidden, dec_consumers(c), 0);
     return ((int64_t)kDecSmemBudget - (int64_t)base.total) & ~(int64_t)127;
 }
 
@@ -960,14 +1053,31 @@ uint32_t dec_ring_bytes(const moe_config &c, int32_t T) { return (uint32_t)dec_b
 
 // Stages of each consumer warp's ring: the largest of the compiled counts that
 // fits (0: none does, or the routing scratch does not fit the ring).
-static const int kStageCounts[] = {16, 12, 10, 8, 6};
+static const int kStageCounts[] = {16, 14, 12, 10, 8, 7, 6};
+
+using LayerFn = void (*)(DecArgs);
+
+template <bool HALF>
+static LayerFn layer_fn(int S)
+{
+    switch (S) {
+    case 16: return k_dec_layer<16, HALF>;
+    case 14: return k_dec_layer<14, HALF>;
+    case 12: return k_dec_layer<12, HALF>;
+    case 10: return k_dec_layer<10, HALF>;
+    case 8: return k_dec_layer<8, HALF>;
+    case 7: return k_dec_layer<7, HALF>;
+    case 6: return k_dec_layer<6, HALF>;
+    }
+    return nullptr;
+}
 
 int dec_stages(const moe_config &c, int32_t T)
 {
     const int64_t ring = dec_base_ring(c, T);
-    const int nc = dec_consumers(c.hidden);
+    const int nc = dec_consumers(c);
     if (nc <= 0 || ring < (int64_t)T * c.n_experts * 12 + 16) return 0;
-    const int64_t per = ring / ((int64_t)nc * kSlotBytes);
+    const int64_t per = ring / ((int64_t)nc * (dec_half(c) ? kSlotHalf : kSlotBytes));
     for (int s : kStageCounts)
         if (per >= s) return s;
     return 0;
@@ -975,7 +1085,7 @@ int dec_stages(const moe_config &c, int32_t T)
 
 bool dec_supported(const moe_config &c, int32_t T)
 {
-    return T >= 0 && T <= kDecTok && dec_route_parts(c.hidden) != 0 && c.hidden / 256 <= kMaxCons &&
+    return T >= 0 && T <= kDecTok && dec_route_parts(c.hidden) != 0 && (dec_half(c) || c.hidden / 256 <= kMaxCons) &&
            c.ff % kUnitRows == 0 && c.shared_ff % kSharedRows == 0 && dec_stages(c, T) > 0;
 }
 
@@ -1010,11 +1120,10 @@ static cudaError_t dec_set_attributes()
     if (done[dev]) return cudaSuccess;
     e = cudaFuncSetAttribute(k_dec_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kDecTok * 8192 * (int)sizeof(uint16_t));
-    const void *layers[] = {(const void *)k_dec_layer<16>, (const void *)k_dec_layer<12>,
-                            (const void *)k_dec_layer<10>, (const void *)k_dec_layer<8>,
-                            (const void *)k_dec_layer<6>};
-    for (const void *f : layers)
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBudget);
+    for (int S : kStageCounts)
+        for (LayerFn f : {layer_fn<false>(S), layer_fn<true>(S)})
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBudget);
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
@@ -1034,14 +1143,8 @@ cudaError_t launch_decode(const DecArgs &a0, cudaStream_t s)
     const LayerSmem L = layer_smem(a.E, a.T, a.H, a.nc, a.ring_bytes);
     const dim3 grid(dec_sms()), block(32 * std::max(a.nc, kDecTok));   // at least one warp per token
     prof_begin(kPhDecLayer, s);
-    switch (a.stages) {
-    case 16: e = launch_pdl(k_dec_layer<16>, grid, block, L.total, s, true, a); break;
-    case 12: e = launch_pdl(k_dec_layer<12>, grid, block, L.total, s, true, a); break;
-    case 10: e = launch_pdl(k_dec_layer<10>, grid, block, L.total, s, true, a); break;
-    case 8: e = launch_pdl(k_dec_layer<8>, grid, block, L.total, s, true, a); break;
-    case 6: e = launch_pdl(k_dec_layer<6>, grid, block, L.total, s, true, a); break;
-    default: e = cudaErrorInvalidValue;
-    }
+    const LayerFn fn = a.half ? layer_fn<true>(a.stages) : layer_fn<false>(a.stages);
+    e = fn ? launch_pdl(fn, grid, block, L.total, s, true, a) : cudaErrorInvalidValue;
     prof_end(kPhDecLayer, s);
     return e;
 }

@@ -134,6 +134,7 @@ struct DecArgs {
     int H, E, FF, k, T, SFF, score_fn;
     int route_parts;             // router row split per CTA (1, 2, 4 or 8)
     int nc;                      // consumer warps of the layer kernel
+    int half;                    // they own 128 columns each (else 256)
     uint32_t ring_bytes;         // their staging rings
     int stages;                  // stages of each consumer warp's ring
     int overlap_prev;            // weights may be read before the previous kernel ends
@@ -154,7 +155,8 @@ struct DecArgs {
     uint32_t *header;
 };
 int dec_route_parts(int H);
-int dec_consumers(int H);
+bool dec_half(const moe_config &c);
+int dec_consumers(const moe_config &c);
 uint32_t dec_ring_bytes(const moe_config &c, int32_t T);
 int dec_stages(const moe_config &c, int32_t T);
 bool dec_supported(const moe_config &c, int32_t T);
