@@ -312,13 +312,15 @@ MOE_API int32_t moe_profile_read(moe_profile_entry *out, int32_t max_entries);
  *   MOE_DEBUG_WAIT_CYCLES  value > 0: every bounded wait of the kernels
  *                          launched afterwards gives up after `value` clock
  *                          cycles (0 restores the default, ~2 s).
- *   MOE_DEBUG_SKIP_COPY    value >= 0: in the next decode-path call, CTA
- *                          `value` of the layer kernel never issues the bulk
- *                          copy of the window's x fragments and logits, so its
- *                          wait for them runs out: the call then ends with
- *                          MOE_ERR_TIMEOUT in its status word (the context
- *                          stays usable; a value past the grid does nothing).
- *                          -1 clears it.
+ *   MOE_DEBUG_SKIP_COPY    value >= 0: in the next call, CTA `value` of its
+ *                          main kernel never issues one bulk copy that it
+ *                          waits for -- on the decode path the layer kernel's
+ *                          copy of the window's x fragments and logits, on the
+ *                          tensor-core path the routed gate/up kernel's first
+ *                          token-row copy -- so that wait runs out: the call
+ *                          then ends with MOE_ERR_TIMEOUT in its status word
+ *                          (the context stays usable; a value past the grid
+ *                          does nothing).  -1 clears it.
  * Errors: MOE_ERR_INVALID_ARG for an unknown `what` or a value out of range.
  */
 enum { MOE_DEBUG_WAIT_CYCLES = 1, MOE_DEBUG_SKIP_COPY = 2 };

@@ -352,6 +352,8 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
     a.y = y;
     a.y_f32 = y_f32;
     a.header = r.header;
+    a.wait_cycles = debug_wait_cycles();
+    a.skip_cta = debug_take_skip_copy();
     {
         GemmWs gw{};
         gw.xg = (__half *)(base + L.xg);

@@ -83,6 +83,8 @@ struct GemmArgs {
     uint32_t *split_cnt;     // split-K arrival counters, one per (expert, m, n) group
     uint32_t *status;
     CUtensorMap *tmaps;      // [grid][2] per-CTA tensor maps of the current expert's blob
+    long long wait_cycles;   // limit of the bounded waits
+    int skip_cta;            // test hook: this CTA never issues its first token-row copy (-1: none)
 };
 
 struct TileInfo {
@@ -122,14 +124,15 @@ __device__ __forceinline__ __half act_to_f16(float a, uint32_t *status)
 // Waiting warps sleep in the try_wait (hardware suspend, up to ~20 us per
 // try) rather than spin, so they do not take issue slots from the working
 // warps.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort, uint32_t *status)
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort, uint32_t *status,
+                                         long long limit)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             set_status(status, MOE_ERR_TIMEOUT);
             return false;
@@ -308,9 +311,10 @@ struct GemmCfg {
 
 // Bounded wait of a whole warp: every lane polls, and the lanes agree on the
 // outcome (false if any lane saw an abort or a timeout).
-__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, volatile int *abort, uint32_t *status)
+__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, volatile int *abort, uint32_t *status,
+                                              long long limit)
 {
-    const bool ok = wait_bar(bar, parity, abort, status);
+    const bool ok = wait_bar(bar, parity, abort, status, limit);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -386,7 +390,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
         const int ei = eg * 128 + et;        // 0 .. kEpi-1
         auto epi_sync = [&]() -> bool {      // the epilogue warps only, bounded
             mbar_arrive(epi_bar);
-            return wait_bar(epi_bar, (epi_it++) & 1, abort_flag, g.status);
+            return wait_bar(epi_bar, (epi_it++) & 1, abort_flag, g.status, g.wait_cycles);
         };
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
                 }
                 if (!(ok = epi_sync())) break;
             }
-            if (!(ok = wait_bar(acc_full(acc), (t_it >> 1) & 1, abort_flag, g.status))) break;
+            if (!(ok = wait_bar(acc_full(acc), (t_it >> 1) & 1, abort_flag, g.status, g.wait_cycles))) break;
             tc_fence_after();
             const int ffop = FMT == kWQ4K ? g.FF : g.SFF;
             for (int cc = eg; cc < ti.nmma / 16; cc += kEG) {
@@ -523,14 +527,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
             const TileInfo ti = tile_info<OP, FMT>(g, tile);
             if (!ti.blob) continue;
             const int acc = t_it & 1;
-            if (!(ok = warp_wait_bar(acc_empty(acc), ((t_it >> 1) & 1) ^ 1, abort_flag, g.status))) break;
+            if (!(ok = warp_wait_bar(acc_empty(acc), ((t_it >> 1) & 1) ^ 1, abort_flag, g.status, g.wait_cycles))) break;
             tc_fence_after();
             const uint32_t idesc = idesc_f16_f32(128, ti.nmma) | (OP == kOpDown ? kIdescAMnMajor : 0u);
             const uint32_t d_tmem = tmem_base + acc * NMAX;
             const int nst = (ti.ksteps + KS - 1) / KS;
             for (int st = 0; st < nst; ++st, ++st_it) {
                 const int slot = st_it % S;
-                if (!(ok = warp_wait_bar(full(slot), (st_it / S) & 1, abort_flag, g.status))) break;
+                if (!(ok = warp_wait_bar(full(slot), (st_it / S) & 1, abort_flag, g.status, g.wait_cycles))) break;
                 tc_fence_after();
                 // straight-line issue: no branch between the MMAs of a stage (the
                 // issue rate halves otherwise); gate/up stages always hold 8 K16 steps
@@ -615,7 +619,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
             const int nrs = ((ti.ksteps + KS - 1) / KS + SPR - 1) / SPR;
             for (int rsi = 0; rsi < nrs; ++rsi, ++rs_it) {
                 const int slot = rs_it % RS;
-                if (!(ok = warp_wait_bar(empty_raw(slot), ((rs_it / RS) & 1) ^ 1, abort_flag, g.status))) break;
+                if (!(ok = warp_wait_bar(empty_raw(slot), ((rs_it / RS) & 1) ^ 1, abort_flag, g.status, g.wait_cycles))) break;
                 if (lane == 0) {
                     const uint32_t dst0 = smem_addr(raw_base + slot * C::kRawStage);
                     mbar_arrive_expect_tx(full_raw(slot), C::kRawStage);
@@ -662,11 +666,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
                 const int nst = (ti.ksteps + KS - 1) / KS;
                 for (int st = 0; st < nst; ++st, ++st_it) {
                     const int slot = st_it % S;
-                    if (!(ok = warp_wait_bar(empty(slot), ((st_it / S) & 1) ^ 1, abort_flag, g.status))) break;
+                    if (!(ok = warp_wait_bar(empty(slot), ((st_it / S) & 1) ^ 1, abort_flag, g.status, g.wait_cycles))) break;
                     if (lane == 0) {
                         const bool has = st * KS + sub < ti.ksteps;
                         mbar_arrive_expect_tx(full(slot), has ? (uint32_t)C::kBSub : 0u);
-                        if (has)
+                        // test hook: the first copy of this CTA is armed but never issued,
+                        // so the waits for its stage run out
+                        const bool skip = (int)blockIdx.x == g.skip_cta && st_it == 0 && sub == 0;
+                        if (has && !skip)
                             tma_load_2d(sB + slot * C::kBStage + sub * C::kBSub, &tmap_b,
                                         (ti.k0 + st * KS + sub) * 64, row0, full(slot));
                     }
@@ -700,9 +707,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
                 const int kst = ti.k0 / KS + st;                  // global stage index along K
                 const bool first = SPR == 1 || (kst & 1) == 0, last = SPR == 1 || (kst & 1) == 1;
                 const int rslot = rs_it % RS;
-                if (first && !(ok = warp_wait_bar(full_raw(rslot), (rs_it / RS) & 1, abort_flag, g.status))) break;
+                if (first && !(ok = warp_wait_bar(full_raw(rslot), (rs_it / RS) & 1, abort_flag, g.status, g.wait_cycles))) break;
                 const int slot = st_it % S;
-                if (!(ok = warp_wait_bar(empty(slot), ((st_it / S) & 1) ^ 1, abort_flag, g.status))) break;
+                if (!(ok = warp_wait_bar(empty(slot), ((st_it / S) & 1) ^ 1, abort_flag, g.status, g.wait_cycles))) break;
                 const uint8_t *raw = raw_base + rslot * C::kRawStage;
                 if (OP == kOpGateUp) {
                     tc_fence_after();
@@ -1105,6 +1112,8 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     g.sh_out = a.sh_out;
     g.status = a.header + kHdrStatus;
     g.tmaps = reinterpret_cast<CUtensorMap *>(w.tmaps);
+    g.wait_cycles = a.wait_cycles;
+    g.skip_cta = a.skip_cta;                 // the routed gate/up launch only
     const int grid = num_sms();
     cudaError_t e;
 
@@ -1115,6 +1124,7 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     g.gu = w.gu;
     g.split_cnt = w.split_cnt;
     e = launch_gemm_cfg<kOpGateUp, kWQ4K>(g, grid, small, false, s);
+    g.skip_cta = -1;
     if (e == cudaSuccess && a.shared_blob) {
         g.tiles = w.tiles_gus;
         g.n_tiles = a.header + kHdrTilesGUS;

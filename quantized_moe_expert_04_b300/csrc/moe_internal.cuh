@@ -119,6 +119,8 @@ struct ExpertArgs {
     uint16_t *y;                        // bf16 [T][H]
     float *y_f32;                       // optional
     uint32_t *header;
+    long long wait_cycles;              // limit of every bounded wait
+    int skip_cta;                       // test hook: the routed gate/up kernel's CTA that never issues its first copy
 };
 
 // ---- decode path (T <= kDecTok): router logits, then one persistent kernel

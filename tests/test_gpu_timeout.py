@@ -52,3 +52,34 @@ def test_debug_hook_rejects_bad_values():
         moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, -5)
     with pytest.raises(moe.MoeError):
         moe.moe_debug_set(moe.MOE_DEBUG_SKIP_COPY, -2)
+
+
+@pytest.mark.parametrize("cta", [0, 3])
+def test_gemm_wait_timeout_is_reported_and_the_context_survives(cta):
+    """The tensor-core path: one CTA of the routed gate/up GEMM arms a token-row
+    copy it never issues; its MMA warp's wait runs out, every role of the CTA
+    leaves its loop on the abort flag, in-flight copies and MMAs drain, and the
+    tensor memory is freed.  The call reports MOE_ERR_TIMEOUT; the next one is
+    right."""
+    wl = synth.small_variant(synth.WORKLOADS["qwen_decode"], name="qwen_e64", n_experts=64)
+    T = 40
+    pl = pack_layer(wl, gen_device="cpu")
+    cfg = moe.config_for(wl, moe.MOE_FLAG_FORCE_GEMM)
+    ws = workspace(cfg, T)
+    x = synth.hidden_states(wl, T).cuda()
+    try:
+        moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, 1 << 22)      # ~2 ms
+        moe.moe_debug_set(moe.MOE_DEBUG_SKIP_COPY, cta)
+        forward(pl, x, ws, cfg=cfg)
+        assert moe.moe_last_device_status(ws) == moe.MOE_ERR_TIMEOUT
+    finally:
+        moe.moe_debug_set(moe.MOE_DEBUG_SKIP_COPY, -1)
+        moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, 0)
+    y32 = torch.empty(T, wl.hidden, dtype=torch.float32, device="cuda")
+    forward(pl, x, ws, y_f32=y32, cfg=cfg)
+    assert moe.moe_last_device_status(ws) == moe.MOE_OK
+    xb, wr, b = oracle_inputs(wl, T, x=x.cpu())
+    import oracle
+    ids, _, _, _ = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
+    blobs, sblob = oracle_blobs(wl, ids.reshape(-1))
+    check_close(y32.cpu().numpy(), oracle_forward(wl, xb, wr, b, blobs, sblob))
