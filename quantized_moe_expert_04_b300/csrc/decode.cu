@@ -488,24 +488,6 @@ __device__ __forceinline__ void copy_block(uint32_t dst, const uint8_t *src, int
     }
 }
 
-// A half-block warp's copy of a Q4_K slab: of each of the 8 rows, the 16-byte
-// header (piece 0) and the 64 quant bytes of its half hh (pieces 1..4), packed
-// as [8][64] quant bytes then [8][16] headers (a 64-byte row stride keeps the
-// gate/up reads of two rows on disjoint banks).
-__device__ __forceinline__ void copy_half(uint32_t dst, const uint8_t *src, int rowb, int hh, int lane)
-{
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int i = lane + 32 * k;
-        if (i < kUnitRows * 5) {
-            const int r = i / 5, p = i - r * 5;
-            const uint32_t d = p == 0 ? 512u + 16u * r : (uint32_t)(64 * r + 16 * (p - 1));
-            const int o = p == 0 ? 0 : 16 + 64 * hh + 16 * (p - 1);
-            cp16(dst + d, src + r * rowb + o);
-        }
-    }
-}
-
 // The layer kernel, S stages per consumer warp.  HALF: each consumer warp owns
 // 128 columns (half a Q4_K super-block) instead of 256, for twice the warps;
 // only for layers without a shared expert.  128 registers a thread at 256
@@ -722,12 +704,29 @@ __global__ void __maxnreg__(HALF ? 96 : 128) k_dec_layer(DecArgs a)
         const UnitInfo ui0 = unit_info(a, un, s_pe, s_tab, (int)u_begin);
         UnitCursor ic{ui0, (int)u_begin};
         int js = 0, im = 0;
+        // HALF: this lane's pieces of every slab, fixed for the whole stream: piece i
+        // (lane, and lane + 32 for lanes < 8) = (offset in the slab << 10) | offset in
+        // the slot (the slab offset is < 8 rows x 1440 bytes, the slot offset < 640)
+        uint32_t hp0 = 0, hp1 = 0;
+        if (HALF) {
+            auto piece = [&](int i) {
+                const int r = i / 5, p = i - r * 5;
+                const uint32_t d = p == 0 ? 512u + 16u * r : (uint32_t)(64 * r + 16 * (p - 1));
+                const uint32_t o = (uint32_t)(r * un.rb + (p == 0 ? 0 : 16 + 64 * hh + 16 * (p - 1)));
+                return (o << 10) | d;
+            };
+            hp0 = piece(lane);
+            hp1 = lane < kUnitRows * 5 - 32 ? piece(lane + 32) : 0u;
+        }
         auto issue = [&]() {
             if (js < n_stage && ic.ui.blob) {
                 const uint8_t *src = ic.ui.blob + ((int64_t)im * ic.ui.ffm + ic.ui.f0) * ic.ui.rowb;
                 const uint32_t dst = wring + (uint32_t)(js % S) * SLOT;
-                if (HALF) copy_half(dst, src + cb * kPieceQ4K, ic.ui.rowb, hh, lane);   // routed units only
-                else if (ic.ui.fmt == 0) copy_block<kPieceQ4K / 16, kUnitRows>(dst, src + cb * kPieceQ4K, ic.ui.rowb, lane);
+                if (HALF) {                              // routed units only
+                    const uint8_t *sb = src + cb * kPieceQ4K;
+                    cp16(dst + (hp0 & 1023u), sb + (hp0 >> 10));
+                    if (lane < kUnitRows * 5 - 32) cp16(dst + (hp1 & 1023u), sb + (hp1 >> 10));
+                } else if (ic.ui.fmt == 0) copy_block<kPieceQ4K / 16, kUnitRows>(dst, src + cb * kPieceQ4K, ic.ui.rowb, lane);
                 else copy_block<kPieceQ80 / 16, kSharedRows>(dst, src + cb * kPieceQ80, ic.ui.rowb, lane);
             }
             cp_commit();                                 // one group a stage, empty or not
@@ -924,22 +923,53 @@ __global__ void __maxnreg__(HALF ? 96 : 128) k_dec_layer(DecArgs a)
             __syncwarp();
             asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
             // B operand of the down projection of unit u: w_{n,e} * SiLU(g) * u in fp16, [token n][ff row f]
-            for (int ct = warp * 32 + lane; ct < kUnitRows * kDecTok; ct += NC * 32) {
+            // (half-block warps: 8 threads an activation, each adding every 8th warp's partial
+            // sums, then the 8 added across lanes in a fixed order; otherwise one thread an
+            // activation: the other warps go on to their down rows meanwhile)
+            {
                 const float2 *red = s_red + (size_t)buf * NC * kDecTok * kUnitRows;
-                const int f = ct & 7, n = ct >> 3;
-                float v = 0.0f;
-                if (((tmask >> n) & 1u) && f < ui.rows) {
-                    float gs = 0.0f, us = 0.0f;
-                    for (int w2 = 0; w2 < NC; ++w2) {
-                        const float2 pv = red[(w2 * kDecTok + n) * kUnitRows + f];
-                        gs += pv.x;
-                        us += pv.y;
+                auto finish = [&](int n, int f, bool act, float gs, float us) {
+                    float v = 0.0f;
+                    if (act) {
+                        const float wt = ui.u >= 0 ? s_w[s_ptok[ui.u][n]] : 1.0f;
+                        v = silu_mul(gs, us) * wt;
+                        if (!(fabsf(v) <= 65504.0f)) set_status(status, MOE_ERR_DEVICE_FAULT);
                     }
-                    const float wt = ui.u >= 0 ? s_w[s_ptok[ui.u][n]] : 1.0f;
-                    v = silu_mul(gs, us) * wt;
-                    if (!(fabsf(v) <= 65504.0f)) set_status(status, MOE_ERR_DEVICE_FAULT);
+                    s_wa[buf * kDecTok * kUnitRows + n * kUnitRows + f] = __float2half_rn(v);
+                };
+                if (HALF && NC >= 16) {
+                    const int ct = warp * 32 + lane;
+                    if (ct < 8 * kUnitRows * kDecTok) {             // warps 0 .. 15, whole warps
+                        const int item = ct >> 3, sl = ct & 7, f = item & 7, n = item >> 3;
+                        const bool act = ((tmask >> n) & 1u) && f < ui.rows;
+                        float gs = 0.0f, us = 0.0f;
+                        if (act)
+                            for (int w2 = sl; w2 < NC; w2 += 8) {
+                                const float2 pv = red[(w2 * kDecTok + n) * kUnitRows + f];
+                                gs += pv.x;
+                                us += pv.y;
+                            }
+#pragma unroll
+                        for (int off = 1; off < 8; off <<= 1) {
+                            gs += __shfl_xor_sync(0xffffffffu, gs, off);
+                            us += __shfl_xor_sync(0xffffffffu, us, off);
+                        }
+                        if (sl == 0) finish(n, f, act, gs, us);
+                    }
+                } else {
+                    for (int ct = warp * 32 + lane; ct < kUnitRows * kDecTok; ct += NC * 32) {
+                        const int f = ct & 7, n = ct >> 3;
+                        const bool act = ((tmask >> n) & 1u) && f < ui.rows;
+                        float gs = 0.0f, us = 0.0f;
+                        if (act)
+                            for (int w2 = 0; w2 < NC; ++w2) {
+                                const float2 pv = red[(w2 * kDecTok + n) * kUnitRows + f];
+                                gs += pv.x;
+                                us += pv.y;
+                            }
+                        finish(n, f, act, gs, us);
+                    }
                 }
-                s_wa[buf * kDecTok * kUnitRows + n * kUnitRows + f] = __float2half_rn(v);
             }
             // ---- down rows of unit u - 1 (the 8 rows are the MMA K), for this warp's block
             if (u > 0 && prev_live)
