@@ -34,6 +34,7 @@
 //
 // Operand precision: fp16 A and B (sub-block scale and min rounded to fp16,
 // one fused multiply-add per weight), fp32 accumulation.
+#include <mutex>
 #include <algorithm>
 #include <cmath>
 
@@ -983,12 +984,21 @@ template <int OP, int FMT, int NMAX, int S, int RAW, int EW>
 static cudaError_t launch_gemm(const GemmArgs &g, int grid, cudaStream_t s)
 {
     using C = GemmCfg<OP, FMT, NMAX, S, RAW>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<OP, FMT, NMAX, S, RAW, EW>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
+    {
+        // function attributes are per device: set once for each device this process uses
+        static std::mutex mu;
+        static bool done[64] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
-        attr = true;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            e = cudaFuncSetAttribute(k_moe_gemm<OP, FMT, NMAX, S, RAW, EW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::kBytes);
+            if (e != cudaSuccess) return e;
+            done[dev] = true;
+        }
     }
     CUtensorMap tmap_b, tmap_w;
     if (!make_tmap_b<OP, FMT, NMAX>(&tmap_b, g) || !make_tmap_w<FMT>(&tmap_w, g)) return cudaErrorInvalidValue;

@@ -15,6 +15,7 @@
 //   k_topk           one warp per token, E/32 logits per lane in registers,
 //                    k rounds of a warp arg-max (equal keys: lower id).
 //   k_bucket_*       stable counting sort of the T*k assignments over the grid.
+#include <mutex>
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -467,14 +468,29 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
         cudaMemsetAsync(a.header + kHdrNActive, 0, sizeof(uint32_t), s);
         return cudaGetLastError();
     }
-    // opt-in shared memory limits, set once per process (the kernels run on one device per process)
-    static bool attrs_set = false;
-    if (!attrs_set) {
-        cudaFuncSetAttribute(k_router_logits, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(kRouterTokens * 8192 * sizeof(uint16_t)));
-        cudaFuncSetAttribute(k_bucket_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(32 * 1024 * sizeof(int32_t)));
-        attrs_set = true;
+    // opt-in shared memory limits: function attributes are per device, set once for
+    // each device this process launches on
+    {
+        static std::mutex mu;
+        static bool done[64] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            e = cudaFuncSetAttribute(k_router_logits, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kRouterTokens * 8192 * sizeof(uint16_t)));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k_bucket_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(32 * 1024 * sizeof(int32_t)));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k_router_mma<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k_router_mma<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
+            if (e != cudaSuccess) return e;
+            done[dev] = true;
+        }
     }
     const size_t xs_bytes = (size_t)kRouterTokens * a.H * sizeof(uint16_t);
     const int experts_per_cta = a.T > kRouterTokens ? 16 * kRouterWarps : kRouterWarps;
@@ -484,12 +500,6 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
         // tensor-core logits: 128-token x 64-expert tiles
         const bool wide = false;
         const size_t smem = (size_t)(2 * kRmM * kRmLd + 2 * 3 * (wide ? 128 : 64) * kRmLd) * sizeof(uint16_t);
-        static bool mattr = false;
-        if (!mattr) {
-            cudaFuncSetAttribute(k_router_mma<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-            cudaFuncSetAttribute(k_router_mma<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-            mattr = true;
-        }
         const dim3 g2((a.T + kRmM - 1) / kRmM, (a.E + (wide ? 127 : 63)) / (wide ? 128 : 64));
         if (wide) k_router_mma<128><<<g2, 256, smem, s>>>(a.x, a.wr, a.T, a.H, a.E, a.logits);
         else k_router_mma<64><<<g2, 256, smem, s>>>(a.x, a.wr, a.T, a.H, a.E, a.logits);
