@@ -38,7 +38,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from quantized_moe_expert_04_b300 import moe, synth  # noqa: E402
-from quantized_moe_expert_04_b300.layer import pack_layer, routing_views, workspace  # noqa: E402
+from quantized_moe_expert_04_b300.layer import TieredLayer, pack_layer, routing_views, workspace  # noqa: E402
 
 DEFAULT_TOKENS = {"tiny": 4, "qwen_decode": 3, "deepseek_decode": 4, "qwen_prefill": 4096,
                   "deepseek_prefill_skewed": 4096}
@@ -484,6 +484,49 @@ def measure(args, wl, T, nL, world, rank, local, K=None, soak_s=0.0, target_s=0.
     return out
 
 
+def measure_tiered(wl, T, nL, n_slots, windows):
+    """Host tier of the experts: every expert of nL layers in pinned host memory,
+    a device cache of n_slots per layer.  Each decode step runs the nL layer
+    calls eagerly (route -> ids to the host -> cache plan -> fills of the missed
+    experts on a copy stream, waited for by the compute stream -> pointer table
+    to the device -> moe_forward), windows steps in a row with fresh inputs (the
+    synthetic routing has no locality, so the hit rate stays near the cache's
+    share of the experts).  Reports tokens/s per layer, the hit rate, the rate at
+    which missed experts' bytes cross from host memory and the fill rate."""
+    cfg = moe.config_for(wl)
+    layers = [TieredLayer(pack_layer(wl, 0, l, gen_device="cuda"), n_slots) for l in range(nL)]
+    ws = workspace(cfg, T)
+    xs = [[synth.hidden_states(wl, T, 1 + w, l, device="cuda") for l in range(nL)] for w in range(windows)]
+    for l in range(nL):                      # one untimed step
+        layers[l].forward(xs[0][l], ws)
+    torch.cuda.synchronize()
+    base = [tl.stats() for tl in layers]
+    t0 = time.time()
+    for w in range(windows):
+        for l in range(nL):
+            layers[l].forward(xs[w][l], ws)
+    torch.cuda.synchronize()
+    dt = time.time() - t0
+    st = [tl.stats() for tl in layers]
+    hits = sum(a["hits"] - b["hits"] for a, b in zip(st, base))
+    misses = sum(a["misses"] - b["misses"] for a, b in zip(st, base))
+    filled = sum(a["bytes"] - b["bytes"] for a, b in zip(st, base))
+    status = moe.moe_last_device_status(ws)
+    out = {"workload": wl.name, "tokens_per_window": T, "distinct_layers": nL, "slots_per_layer": n_slots,
+           "experts_per_layer": wl.n_experts, "windows": windows, "status": status,
+           "value": round(T * nL * windows / dt, 1), "unit": UNIT, "us_per_layer": round(dt * 1e6 / (nL * windows), 1),
+           "hit_rate": round(hits / max(1, hits + misses), 4),
+           "missed_bytes_gbs": round(misses * wl.blob_bytes / dt / 1e9, 2),
+           "fill_gbs": round(filled / dt / 1e9, 2),
+           "path": "eager per layer: route, ids to host, plan, fills (copy stream), table to device, forward"}
+    for tl in layers:
+        tl.cache.close()
+    del layers, ws, xs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     wl = synth.WORKLOADS[args.workload or "qwen_decode"]
@@ -520,6 +563,8 @@ def run_ours(args, world, rank, local):
                                             "steps", "ms_per_step", "us_per_layer", "hbm", "tflops", "roofline",
                                             "kernel_share", "clocks", "cpu_baseline", "parity") if k in r})
         out["configs"] = confs
+        # host tier of the experts (decode windows): 4 layers, a quarter of each layer's experts cached
+        out["tiered"] = measure_tiered(synth.WORKLOADS["qwen_decode"], 3, 4, 128, 20)
     if rank == 0:
         print(json.dumps(out), flush=True)
 

@@ -216,13 +216,16 @@ MOE_API moe_status moe_route(const moe_config *cfg, const uint16_t *x, const flo
  * The routing of the call stays readable in the workspace
  * (moe_workspace_routing) until the next call.
  * Path: T <= 8 (or MOE_FLAG_FORCE_GEMV) runs the decode path: each selected
- * expert's bytes are streamed once per window; gate/up multiply fp16
- * dequantised weights by the fp16 hidden states with fp32 accumulation (warp
- * MMAs), the down projection runs in fp32.  Larger T runs the tensor-core
- * grouped GEMM with fp16 operands and fp32 accumulation.  Both paths need
- * |x| < 65504 (fp16 range; larger values set MOE_ERR_DEVICE_FAULT), and the
- * tensor-core path also needs |SiLU(g)*u| <= 65504 (its down projection
- * multiplies fp16 activations; a larger one sets MOE_ERR_DEVICE_FAULT).
+ * expert's bytes are streamed once per window; both projections multiply
+ * fp16 dequantised weights by fp16 operands (x; the weighted activations
+ * w * SiLU(g) * u) with fp32 accumulation (warp MMAs).  Larger T runs the
+ * tensor-core grouped GEMM with fp16 operands and fp32 accumulation.  Both
+ * paths need |x| < 65504 (fp16 range; larger values set MOE_ERR_DEVICE_FAULT)
+ * and an fp16-representable activation (a larger one sets
+ * MOE_ERR_DEVICE_FAULT).  On the decode path an expert blob may live in
+ * pinned, mapped host memory (its device-usable address in the table): the
+ * kernels then read it from there (see the expert cache below); the
+ * tensor-core path needs every blob in device memory.
  */
 MOE_API moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *router_w,
                        const float *router_bias, const uint8_t *const *expert_blobs,
@@ -244,6 +247,61 @@ MOE_API moe_status moe_workspace_routing(const moe_config *cfg, int32_t T, const
  * (MOE_OK if none) and clears it.
  */
 MOE_API moe_status moe_last_device_status(void *ws, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- host tier of the experts */
+
+/*
+ * A device cache of expert blobs over pinned host memory: every expert has a
+ * copy in pinned, mapped host memory, a part of them also in device slots.
+ * Host-side bookkeeping only; the copies are cudaMemcpyAsync on a stream the
+ * caller names.  One cache serves one table of n_experts entries (a layer, or
+ * the experts of several layers numbered as the caller likes).  Not
+ * thread-safe.
+ *
+ * moe_cache_create: host_blobs is a HOST array of n_experts device-usable
+ * addresses (cudaHostAlloc(..., cudaHostAllocMapped) + cudaHostGetDevicePointer),
+ * each 16-byte aligned and blob_bytes long; slot_memory is DEVICE memory of
+ * n_slots * blob_bytes bytes (16-byte aligned; n_slots may be 0).  The caller
+ * owns both and keeps them alive until moe_cache_destroy.
+ * Errors: MOE_ERR_INVALID_ARG (null or non-positive arguments),
+ * MOE_ERR_MISALIGNED.
+ */
+typedef struct moe_cache moe_cache;
+MOE_API moe_status moe_cache_create(int32_t n_experts, int64_t blob_bytes, const uint8_t *const *host_blobs,
+                                    uint8_t *slot_memory, int32_t n_slots, moe_cache **out);
+/* Frees the bookkeeping (not the memory the caller owns).  NULL is a no-op. */
+MOE_API void moe_cache_destroy(moe_cache *cache);
+/*
+ * Host only, no CUDA call.  ids: HOST array of the window's selected expert
+ * ids (any order, repeats allowed).  Marks them used and gives each missed
+ * expert a slot -- a free one, or the least recently used slot whose expert
+ * this window does not select -- with a fill planned for moe_cache_issue.
+ * Writes the HOST array table[n_experts] (to be copied to the device table
+ * moe_forward reads): the slot address of every expert that has a slot
+ * (resident, or filled by this window's moe_cache_issue), else its host
+ * address (a missed expert that found no slot is read from host memory by
+ * the decode kernels).  *n_fills (may be NULL) = fills planned.
+ * Errors: MOE_ERR_INVALID_ARG (null pointers, an id out of range).
+ */
+MOE_API moe_status moe_cache_plan(moe_cache *cache, const int32_t *ids, int32_t n_ids, const uint8_t **table,
+                                  int32_t *n_fills);
+/*
+ * Queues the planned fills on copy_stream (one cudaMemcpyAsync per expert
+ * blob) behind the work queued so far on compute_stream -- a refilled slot may
+ * still be read by a queued kernel -- and makes compute_stream wait for them:
+ * call it after moe_cache_plan and before queueing the window's moe_forward
+ * on compute_stream.  Errors: MOE_ERR_CUDA (the window's fills are then
+ * dropped: do not run the window with that plan's table).
+ */
+MOE_API moe_status moe_cache_issue(moe_cache *cache, moe_stream_t compute_stream, moe_stream_t copy_stream);
+/* Kept for callers that poll: every fill is ordered by moe_cache_issue, so
+ * there is nothing to collect (MOE_OK). */
+MOE_API moe_status moe_cache_poll(moe_cache *cache);
+/* out[4] = {hits, misses, fills issued, bytes filled} since creation. */
+MOE_API moe_status moe_cache_stats(const moe_cache *cache, int64_t *out);
+/* The device-usable address of pinned, mapped host memory (a CUDA call).
+ * Errors: MOE_ERR_INVALID_ARG when host_ptr is not such memory. */
+MOE_API moe_status moe_host_address(const void *host_ptr, const uint8_t **device_ptr);
 
 /* ---------------------------------------------------------------- no-allocation variant */
 

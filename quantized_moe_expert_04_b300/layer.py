@@ -92,3 +92,45 @@ def routing_views(cfg: moe.moe_config, T: int, ws: torch.Tensor):
     offsets = view(addrs[2], E + 1, torch.int32)
     assign = view(addrs[3], T * k, torch.int32)
     return ids, w, offsets, assign
+
+
+class TieredLayer:
+    """A packed layer whose experts live in pinned host memory, n_slots of them
+    also in a device cache (moe_cache_*): per window the router's selection
+    decides the pointer table; missed experts are copied into slots by the copy
+    engine before the window's forward (the least recently used slots make
+    room), and a missed expert that finds no slot is read by the kernels from
+    host memory."""
+
+    def __init__(self, pl: PackedLayer, n_slots: int):
+        self.pl = pl
+        E, bb = pl.wl.n_experts, pl.wl.blob_bytes
+        self.host = pl.blobs.cpu().pin_memory()
+        addrs = [moe.moe_host_address(self.host[e]) for e in range(E)]
+        self.slots = torch.empty(max(1, n_slots) * bb, dtype=torch.uint8, device="cuda")
+        self.cache = moe.ExpertCache(E, bb, addrs, self.slots, n_slots)
+        self.table = torch.empty(E, dtype=torch.int64, device="cuda")
+        self.copy_stream = torch.cuda.Stream()
+
+    def forward(self, x: torch.Tensor, ws: torch.Tensor, y: Optional[torch.Tensor] = None,
+                y_f32: Optional[torch.Tensor] = None, cfg: Optional[moe.moe_config] = None):
+        pl, T = self.pl, x.shape[0]
+        cfg = cfg or pl.cfg
+        if T > 8 and not (cfg.flags & moe.MOE_FLAG_FORCE_GEMV):
+            raise ValueError("host-resident experts are read by the decode path only (T <= 8)")
+        k = pl.wl.top_k
+        ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+        w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+        off = torch.empty(pl.wl.n_experts + 1, dtype=torch.int32, device="cuda")
+        asg = torch.empty(T * k, dtype=torch.int32, device="cuda")
+        moe.moe_route(cfg, x, pl.router_w, pl.router_bias, T, ids, w, off, asg, ws)
+        table, fills = self.cache.plan(ids.cpu().reshape(-1).tolist())
+        self.cache.issue(torch.cuda.current_stream(), self.copy_stream)   # the forward waits for the fills
+        self.table.copy_(torch.tensor(table, dtype=torch.int64))
+        if y is None:
+            y = torch.empty(T, pl.wl.hidden, dtype=torch.bfloat16, device="cuda")
+        moe.moe_forward(cfg, x, pl.router_w, pl.router_bias, self.table, pl.shared, T, y, y_f32, ws)
+        return y, fills
+
+    def stats(self):
+        return self.cache.stats()

@@ -39,6 +39,8 @@ EXPORTS = (
     "moe_workspace_routing", "moe_last_device_status", "moe_status_string",
     "moe_profile_enable", "moe_profile_read", "moe_forward_static_ws",
     "moe_dequant_q4k_f16", "moe_dequant_q8_0_f16", "moe_debug_set",
+    "moe_cache_create", "moe_cache_destroy", "moe_cache_plan", "moe_cache_issue", "moe_cache_poll",
+    "moe_cache_stats", "moe_host_address",
 )
 
 MOE_DEBUG_WAIT_CYCLES = 1
@@ -112,6 +114,13 @@ def lib() -> ctypes.CDLL:
             "moe_debug_set": (ctypes.c_int, [_I32, _I64]),
             "moe_forward_static_ws": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P]),
             "moe_profile_read": (_I32, [ctypes.POINTER(moe_profile_entry), _I32]),
+            "moe_cache_create": (ctypes.c_int, [_I32, _I64, _P, _P, _I32, ctypes.POINTER(_P)]),
+            "moe_cache_destroy": (None, [_P]),
+            "moe_cache_plan": (ctypes.c_int, [_P, _P, _I32, _P, ctypes.POINTER(_I32)]),
+            "moe_cache_issue": (ctypes.c_int, [_P, _P, _P]),
+            "moe_cache_poll": (ctypes.c_int, [_P]),
+            "moe_cache_stats": (ctypes.c_int, [_P, _P]),
+            "moe_host_address": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -289,3 +298,61 @@ def moe_profile_read():
     buf = (moe_profile_entry * 64)()
     n = lib().moe_profile_read(buf, 64)
     return {buf[i].name.decode(): (buf[i].launches, buf[i].timed, buf[i].total_ms) for i in range(n)}
+
+
+# ---------------------------------------------------------------- host tier of the experts
+
+def moe_host_address(host: torch.Tensor) -> int:
+    """Device-usable address (int) of a pinned, mapped host tensor's first byte."""
+    d = ctypes.c_void_p()
+    _check(lib().moe_host_address(ctypes.c_void_p(host.data_ptr()), ctypes.byref(d)), "moe_host_address")
+    return d.value
+
+
+class ExpertCache:
+    """The C library's device cache of expert blobs over pinned host memory
+    (moe_cache_* in include/moe.h): marshalling only.
+
+    host_blobs: device-usable addresses (ints) of the pinned, mapped host copies;
+    slot_memory: a device tensor of n_slots * blob_bytes bytes (kept alive here)."""
+
+    def __init__(self, n_experts: int, blob_bytes: int, host_blobs, slot_memory, n_slots: int):
+        self.n_experts = int(n_experts)
+        self._host = (ctypes.c_void_p * self.n_experts)(*[int(p) for p in host_blobs])
+        self._slots = slot_memory
+        self._table = (ctypes.c_void_p * self.n_experts)()
+        h = ctypes.c_void_p()
+        _check(lib().moe_cache_create(self.n_experts, int(blob_bytes), ctypes.cast(self._host, _P),
+                                      _ptr(slot_memory) if n_slots else None, int(n_slots), ctypes.byref(h)),
+               "moe_cache_create")
+        self._h = h
+
+    def plan(self, ids):
+        """Host array of the window's expert ids -> (table as a list of ints, fills planned)."""
+        arr = (ctypes.c_int32 * len(ids))(*[int(i) for i in ids])
+        n = ctypes.c_int32()
+        _check(lib().moe_cache_plan(self._h, ctypes.cast(arr, _P), len(ids), ctypes.cast(self._table, _P),
+                                    ctypes.byref(n)), "moe_cache_plan")
+        return [self._table[i] or 0 for i in range(self.n_experts)], n.value
+
+    def issue(self, compute_stream=None, copy_stream=None):
+        _check(lib().moe_cache_issue(self._h, _stream(compute_stream), _stream(copy_stream)), "moe_cache_issue")
+
+    def poll(self):
+        _check(lib().moe_cache_poll(self._h), "moe_cache_poll")
+
+    def stats(self):
+        out = (ctypes.c_int64 * 4)()
+        _check(lib().moe_cache_stats(self._h, ctypes.cast(out, _P)), "moe_cache_stats")
+        return {"hits": out[0], "misses": out[1], "fills": out[2], "bytes": out[3]}
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().moe_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
