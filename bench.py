@@ -215,6 +215,42 @@ def oracle_sample(wl, T, layers, x_layers, gpu_ids=None, gpu_y32=None, time_budg
     return done_tok / spent, threads, desc, parity
 
 
+def cpu_kernel_sample(wl, T, layers, time_budget_s=8.0):
+    """Time the AVX2 multi-token CPU expert kernel (cpu_baseline/) on the host
+    cores: the experts' FFN and combine of one window per layer (the oracle's
+    routing and Q4_K blobs, both untimed set-up), the first layers of the
+    workload within the budget.  Returns tokens/s per layer, the selected
+    experts' bytes per second, the threads and a description."""
+    import cpu_baseline
+    import oracle
+    threads = os.cpu_count() or 1
+    done_tok, spent, moved, used = 0, 0.0, 0, 0
+    for l in range(layers):
+        xb = synth.bf16_bits(synth.hidden_states(wl, T, 0, l))
+        wr = synth.router_weight(wl, 0, l, device="cuda").cpu().numpy()
+        b = synth.router_bias(wl, 0, l, device="cuda")
+        b = None if b is None else b.cpu().numpy()
+        ids, w, _, _ = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
+        sel = sorted(set(ids.reshape(-1).tolist()))
+        U = len(sel)
+        blobs = [None] * wl.n_experts
+        for e in sel:
+            blobs[e] = oracle.pack_expert_q4k(synth.expert_weight(wl, e, 0, l, device="cuda").cpu().numpy())
+        cpu_baseline.moe_window(wl.hidden, wl.n_experts, wl.ff, wl.top_k, xb, ids, w, blobs, threads=threads)
+        t0 = time.time()
+        cpu_baseline.moe_window(wl.hidden, wl.n_experts, wl.ff, wl.top_k, xb, ids, w, blobs, threads=threads)
+        spent += time.time() - t0
+        done_tok += T
+        moved += U * wl.blob_bytes
+        used += 1
+        if spent > time_budget_s:
+            break
+    return {"value": round(done_tok / spent, 2), "unit": UNIT, "gbs": round(moved / spent / 1e9, 2),
+            "cores": threads, "kind": "avx2 multi-token expert kernel",
+            "sample": "%d layer(s) x %d token(s) of %s (expert FFN + combine; routing and packing untimed)"
+                      % (used, T, wl.name)}
+
+
 # ------------------------------------------------------------------ algorithmic work
 
 def algorithmic(wl, T, ids_per_layer):
@@ -553,6 +589,11 @@ def run_ours(args, world, rank, local):
     if "cpu_baseline" in head:
         out["cpu_baseline"] = head["cpu_baseline"]
         out["parity"] = head["parity"]
+        if not wl.has_shared and T <= 64 and rank == 0:
+            try:
+                out["cpu_kernel"] = cpu_kernel_sample(wl, T, 8)
+            except Exception as exc:          # no AVX2/FMA on this host, or no compiler
+                out["cpu_kernel"] = {"unavailable": str(exc).splitlines()[0][:200]}
     if args.workload is None and not args.no_configs:
         confs = []
         for name, Tc in CONFIG_SET:
