@@ -19,6 +19,9 @@ from . import build as _build
 
 QK_K = 256
 Q4K_BYTES = 144
+Q5K_BYTES = 176
+CODEC_Q4K = 0
+CODEC_Q5K = 1
 QK8 = 32
 Q8_BYTES = 34
 SCORE_SOFTMAX = 0
@@ -60,6 +63,15 @@ def lib() -> ctypes.CDLL:
         L.orc_moe_forward.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                       _p, _p, _p, _p, _p, _i64, _p, _p]
         L.orc_moe_forward.restype = _i32
+        for name in ("orc_q5k_quantize",):
+            getattr(L, name).argtypes = [_p, _i64, _i64, _p]
+            getattr(L, name).restype = _i32
+        for name in ("orc_q5k_dequantize", "orc_q5k_dequantize_f16"):
+            getattr(L, name).argtypes = [_p, _i64, _i64, _p]
+            getattr(L, name).restype = None
+        L.orc_moe_forward_codec.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                            _p, _p, _p, _p, _p, _i64, _p, _i32, _p]
+        L.orc_moe_forward_codec.restype = _i32
         L.orc_set_threads.argtypes = [_i32]
         L.orc_set_threads.restype = _i32
         _lib = L
@@ -131,6 +143,33 @@ def q8_0_dequantize_f16(blob: np.ndarray, rows: int, cols: int) -> np.ndarray:
     return out
 
 
+def q5k_quantize(w: np.ndarray) -> np.ndarray:
+    """[rows, cols] fp32 -> [rows, cols/256*176] uint8 Q5_K blocks (R10, R11)."""
+    w = _c(w, np.float32)
+    rows, cols = w.shape
+    out = np.zeros((rows, cols // QK_K * Q5K_BYTES), np.uint8)
+    if lib().orc_q5k_quantize(_ptr(w), rows, cols, _ptr(out)) != 0:
+        raise ValueError("q5k_quantize: bad shape or non-finite / out-of-range input")
+    return out
+
+
+def q5k_dequantize(blob: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    blob = _c(blob, np.uint8)
+    assert blob.size == rows * (cols // QK_K) * Q5K_BYTES
+    out = np.empty((rows, cols), np.float32)
+    lib().orc_q5k_dequantize(_ptr(blob), rows, cols, _ptr(out))
+    return out
+
+
+def q5k_dequantize_f16(blob: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """The fp16 operand rounding (R9) of the Q5_K weights: uint16 bit patterns [rows, cols]."""
+    blob = _c(blob, np.uint8)
+    assert blob.size == rows * (cols // QK_K) * Q5K_BYTES
+    out = np.empty((rows, cols), np.uint16)
+    lib().orc_q5k_dequantize_f16(_ptr(blob), rows, cols, _ptr(out))
+    return out
+
+
 def q8_0_quantize(w: np.ndarray) -> np.ndarray:
     w = _c(w, np.float32)
     rows, cols = w.shape
@@ -151,6 +190,15 @@ def q8_0_dequantize(blob: np.ndarray, rows: int, cols: int) -> np.ndarray:
 def pack_expert_q4k(w3: np.ndarray) -> np.ndarray:
     """[3, FF, H] fp32 (gate, up, down stored [FF][H]) -> flat expert blob."""
     return np.concatenate([q4k_quantize(w3[m]).reshape(-1) for m in range(3)])
+
+
+def pack_expert_q5k(w3: np.ndarray) -> np.ndarray:
+    """[3, FF, H] fp32 -> flat Q5_K expert blob (same matrix order as Q4_K)."""
+    return np.concatenate([q5k_quantize(w3[m]).reshape(-1) for m in range(3)])
+
+
+def pack_expert(w3: np.ndarray, codec: int = CODEC_Q4K) -> np.ndarray:
+    return pack_expert_q5k(w3) if codec == CODEC_Q5K else pack_expert_q4k(w3)
 
 
 def pack_shared_q8_0(w3: np.ndarray) -> np.ndarray:
@@ -198,8 +246,9 @@ def moe_forward(hidden: int, n_experts: int, ff: int, top_k: int, score_fn: int,
                 x_bf16: np.ndarray, wr: np.ndarray, bias: Optional[np.ndarray],
                 blobs: Sequence[Optional[np.ndarray]], shared_ff: int = 0,
                 shared_blob: Optional[np.ndarray] = None,
-                forced_ids: Optional[np.ndarray] = None) -> np.ndarray:
-    """The whole layer in fp64.  ``blobs[e]`` is expert e's blob (or None if unused)."""
+                forced_ids: Optional[np.ndarray] = None, codec: int = CODEC_Q4K) -> np.ndarray:
+    """The whole layer in fp64.  ``blobs[e]`` is expert e's blob (or None if unused),
+    Q4_K or (codec = CODEC_Q5K) Q5_K."""
     L = lib()
     x = _c(x_bf16, np.uint16)
     wr = _c(wr, np.float32)
@@ -211,9 +260,9 @@ def moe_forward(hidden: int, n_experts: int, ff: int, top_k: int, score_fn: int,
     sb = None if shared_blob is None else _c(shared_blob, np.uint8)
     f = None if forced_ids is None else _c(forced_ids, np.int32)
     y = np.zeros((T, hidden), np.float64)
-    rc = L.orc_moe_forward(hidden, n_experts, ff, top_k, score_fn, int(sb is not None), shared_ff,
-                           _ptr(x), _ptr(wr), _ptr(b), ctypes.cast(table, ctypes.c_void_p),
-                           _ptr(sb), T, _ptr(f), _ptr(y))
+    rc = L.orc_moe_forward_codec(hidden, n_experts, ff, top_k, score_fn, int(sb is not None), shared_ff,
+                                 _ptr(x), _ptr(wr), _ptr(b), ctypes.cast(table, ctypes.c_void_p),
+                                 _ptr(sb), T, _ptr(f), int(codec), _ptr(y))
     if rc != 0:
         raise ValueError("moe_forward failed (%d)" % rc)
     return y

@@ -80,6 +80,16 @@
  *              in fp32, rounded once to fp16), w = fp16(q*S_j + NZ_j) with the
  *              sum taken exactly and rounded once;
  *        Q8_0: w = fp16(d*q) (exact product, rounded once).
+ *  R10 Q5_K super-block, 176 bytes for 256 weights (the pages' deployments mix
+ *      Q4_K and Q5_K experts): bytes 0-1 d (fp16), 2-3 dmin (fp16), 4-15
+ *      scales[12] packed as in R1, 16-47 qh[32], 48-175 qs[128].  Quant of
+ *      element 64c + 32h + l (c in 0..3, h in 0..1, l in 0..31): its low four
+ *      bits are the low (h = 0) or high (h = 1) nibble of qs[32c + l], its
+ *      fifth bit is bit 2c + h of qh[l]; q in 0..31.  Value as R1:
+ *      y = fp32(fp32(d)*sc_j) * q - fp32(fp32(dmin)*m_j), j = 2c + h.
+ *  R11 Q5_K quantiser: R2 with 31 levels -- scale_j = (mx - mn) / 31,
+ *      q = s > 0 ? clamp(rint((x + z) / s), 0, 31) : 0; the rest as R2.
+ *      Operand rounding of the tensor-core paths as R9 (q up to 31 is exact).
  *
  * Precision: quantise/dequantise in fp32 exactly as R1-R3 state; router,
  * scores, weights and every FFN product and sum in fp64.
@@ -97,6 +107,7 @@
 
 #define ORC_QK_K 256            /* weights per Q4_K super-block            */
 #define ORC_Q4K_BYTES 144       /* 2 + 2 + 12 + 128                        */
+#define ORC_Q5K_BYTES 176       /* 2 + 2 + 12 + 32 + 128                   */
 #define ORC_QK8 32              /* weights per Q8_0 block                  */
 #define ORC_Q8_BYTES 34         /* 2 + 32                                  */
 
@@ -288,6 +299,123 @@ void orc_q4k_dequantize(const uint8_t *blob, int64_t rows, int64_t cols, float *
 }
 
 /* ------------------------------------------------------------------ */
+/* Q5_K (R10, R11)                                                     */
+/* ------------------------------------------------------------------ */
+
+/* Quantise 256 fp32 weights into one 176-byte block.  0 / -1 as Q4_K. */
+int orc_q5k_quantize_block(const float *x, uint8_t *blk)
+{
+    float scale[8], nmin[8];
+    for (int j = 0; j < 8; ++j) {
+        const float *s = x + 32 * j;
+        float mn = s[0], mx = s[0];
+        for (int i = 0; i < 32; ++i) {
+            if (!isfinite(s[i])) return -1;
+            if (s[i] < mn) mn = s[i];
+            if (s[i] > mx) mx = s[i];
+        }
+        if (mn > 0.0f) mn = 0.0f;
+        scale[j] = (mx - mn) / 31.0f;
+        nmin[j] = -mn;
+    }
+    float max_scale = 0.0f, max_nmin = 0.0f;
+    for (int j = 0; j < 8; ++j) {
+        if (scale[j] > max_scale) max_scale = scale[j];
+        if (nmin[j] > max_nmin) max_nmin = nmin[j];
+    }
+    uint16_t d_h = orc_f32_to_f16(max_scale / 63.0f);
+    uint16_t dmin_h = orc_f32_to_f16(max_nmin / 63.0f);
+    float d = orc_f16_to_f32(d_h), dmin = orc_f16_to_f32(dmin_h);
+    if (!isfinite(d) || !isfinite(dmin)) return -1;
+
+    int sc[8], m[8];
+    for (int j = 0; j < 8; ++j) {
+        sc[j] = d > 0.0f ? (int)fminf(63.0f, rintf(scale[j] / d)) : 0;
+        m[j] = dmin > 0.0f ? (int)fminf(63.0f, rintf(nmin[j] / dmin)) : 0;
+    }
+
+    memset(blk, 0, ORC_Q5K_BYTES);
+    blk[0] = (uint8_t)(d_h & 0xff);
+    blk[1] = (uint8_t)(d_h >> 8);
+    blk[2] = (uint8_t)(dmin_h & 0xff);
+    blk[3] = (uint8_t)(dmin_h >> 8);
+    uint8_t *scales = blk + 4;
+    for (int j = 0; j < 4; ++j) {
+        scales[j] = (uint8_t)(sc[j] | ((sc[j + 4] >> 4) << 6));
+        scales[j + 4] = (uint8_t)(m[j] | ((m[j + 4] >> 4) << 6));
+        scales[j + 8] = (uint8_t)((sc[j + 4] & 15) | ((m[j + 4] & 15) << 4));
+    }
+
+    uint8_t q[ORC_QK_K];
+    for (int j = 0; j < 8; ++j) {
+        float s = d * (float)sc[j];
+        float z = dmin * (float)m[j];
+        for (int i = 0; i < 32; ++i) {
+            int qi = 0;
+            if (s > 0.0f) {
+                float v = rintf((x[32 * j + i] + z) / s);
+                qi = v < 0.0f ? 0 : (v > 31.0f ? 31 : (int)v);
+            }
+            q[32 * j + i] = (uint8_t)qi;
+        }
+    }
+    uint8_t *qh = blk + 16, *qs = blk + 48;
+    for (int c = 0; c < 4; ++c)
+        for (int h = 0; h < 2; ++h)
+            for (int l = 0; l < 32; ++l) {
+                const int v = q[64 * c + 32 * h + l];
+                qs[32 * c + l] |= (uint8_t)((v & 15) << (4 * h));
+                qh[l] |= (uint8_t)(((v >> 4) & 1) << (2 * c + h));
+            }
+    return 0;
+}
+
+/* The quant of element 64c + 32h + l of a Q5_K block (R10). */
+static int q5k_quant(const uint8_t *blk, int c, int h, int l)
+{
+    const uint8_t *qh = blk + 16, *qs = blk + 48;
+    const int lo = h ? (qs[32 * c + l] >> 4) : (qs[32 * c + l] & 15);
+    return lo | (((qh[l] >> (2 * c + h)) & 1) << 4);
+}
+
+/* Dequantise one 176-byte block into 256 fp32 weights (R10). */
+void orc_q5k_dequantize_block(const uint8_t *blk, float *y)
+{
+    float d = orc_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+    float dmin = orc_f16_to_f32((uint16_t)(blk[2] | (blk[3] << 8)));
+    for (int c = 0; c < 4; ++c)
+        for (int h = 0; h < 2; ++h) {
+            int sc, m;
+            q4k_get_scale_min(blk + 4, 2 * c + h, &sc, &m);
+            float s = d * (float)sc;
+            float z = dmin * (float)m;
+            for (int l = 0; l < 32; ++l) {
+                float t = s * (float)q5k_quant(blk, c, h, l);
+                y[64 * c + 32 * h + l] = t - z;
+            }
+        }
+}
+
+int orc_q5k_quantize(const float *w, int64_t rows, int64_t cols, uint8_t *out)
+{
+    if (rows < 0 || cols <= 0 || cols % ORC_QK_K) return -1;
+    int64_t nb = rows * (cols / ORC_QK_K);
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t b = 0; b < nb; ++b)
+        bad |= orc_q5k_quantize_block(w + b * ORC_QK_K, out + b * ORC_Q5K_BYTES) != 0;
+    return bad ? -1 : 0;
+}
+
+void orc_q5k_dequantize(const uint8_t *blob, int64_t rows, int64_t cols, float *out)
+{
+    int64_t nb = rows * (cols / ORC_QK_K);
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nb; ++b)
+        orc_q5k_dequantize_block(blob + b * ORC_Q5K_BYTES, out + b * ORC_QK_K);
+}
+
+/* ------------------------------------------------------------------ */
 /* Q8_0 (R3)                                                           */
 /* ------------------------------------------------------------------ */
 
@@ -375,6 +503,30 @@ void orc_q4k_dequantize_f16(const uint8_t *blob, int64_t rows, int64_t cols, uin
 }
 
 /* One Q8_0 block -> 32 binary16 patterns fp16(d*q) (d*q exact in fp32). */
+/* R9 applied to a Q5_K block (R10): S, NZ as for Q4_K, w = fp16(q*S + NZ). */
+void orc_q5k_dequantize_f16_block(const uint8_t *blk, uint16_t *y)
+{
+    float d = orc_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+    float dmin = orc_f16_to_f32((uint16_t)(blk[2] | (blk[3] << 8)));
+    for (int c = 0; c < 4; ++c)
+        for (int h = 0; h < 2; ++h) {
+            int sc, m;
+            q4k_get_scale_min(blk + 4, 2 * c + h, &sc, &m);
+            const double S = (double)orc_f16_to_f32(orc_f64_to_f16((double)d * (double)sc));
+            const double NZ = (double)orc_f16_to_f32(orc_f64_to_f16(-((double)dmin * (double)m)));
+            for (int l = 0; l < 32; ++l)
+                y[64 * c + 32 * h + l] = orc_f64_to_f16((double)q5k_quant(blk, c, h, l) * S + NZ);
+        }
+}
+
+void orc_q5k_dequantize_f16(const uint8_t *blob, int64_t rows, int64_t cols, uint16_t *out)
+{
+    int64_t nb = rows * (cols / ORC_QK_K);
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nb; ++b)
+        orc_q5k_dequantize_f16_block(blob + b * ORC_Q5K_BYTES, out + b * ORC_QK_K);
+}
+
 void orc_q8_0_dequantize_f16(const uint8_t *blob, int64_t rows, int64_t cols, uint16_t *out)
 {
     int64_t nb = rows * (cols / ORC_QK8);
@@ -557,11 +709,12 @@ static void expert_ffn(const float *Wg, const float *Wu, const float *Wd, int FF
  *   y        [T][H] fp64 output
  * Returns 0, -1 (bad arguments) or -2 (a selected expert has no blob).
  */
-int orc_moe_forward(int H, int E, int FF, int k, int score_fn, int has_shared, int shared_ff,
-                    const uint16_t *x, const float *wr, const float *bias,
-                    const uint8_t *const *blobs, const uint8_t *shared, int64_t T,
-                    const int32_t *forced, double *y)
+int orc_moe_forward_codec(int H, int E, int FF, int k, int score_fn, int has_shared, int shared_ff,
+                          const uint16_t *x, const float *wr, const float *bias,
+                          const uint8_t *const *blobs, const uint8_t *shared, int64_t T,
+                          const int32_t *forced, int codec, double *y)
 {
+    if (codec != 0 && codec != 1) return -1;
     if (H <= 0 || H % ORC_QK_K || FF <= 0 || T < 0) return -1;
     if (has_shared && (!shared || shared_ff <= 0)) return -1;
     int64_t TK = T * k;
@@ -583,7 +736,7 @@ int orc_moe_forward(int H, int E, int FF, int k, int score_fn, int has_shared, i
     for (int64_t i = 0; i < T * H; ++i) xd[i] = (double)orc_bf16_to_f32(x[i]);
 
     int64_t mat = (int64_t)FF * H;
-    int64_t mat_bytes = (int64_t)FF * (H / ORC_QK_K) * ORC_Q4K_BYTES;
+    int64_t mat_bytes = (int64_t)FF * (H / ORC_QK_K) * (codec ? ORC_Q5K_BYTES : ORC_Q4K_BYTES);
     float *W = malloc(sizeof(float) * (size_t)(3 * mat));
     double *slot = calloc((size_t)(TK > 0 ? TK : 1) * (size_t)H, sizeof(double));
     int64_t maxc = 0;
@@ -596,8 +749,10 @@ int orc_moe_forward(int H, int E, int FF, int k, int score_fn, int has_shared, i
     for (int e = 0; e < E; ++e) {
         int64_t n = counts[e];
         if (n == 0) continue;
-        for (int m = 0; m < 3; ++m)
-            orc_q4k_dequantize(blobs[e] + m * mat_bytes, FF, H, W + m * mat);
+        for (int m = 0; m < 3; ++m) {
+            if (codec) orc_q5k_dequantize(blobs[e] + m * mat_bytes, FF, H, W + m * mat);
+            else orc_q4k_dequantize(blobs[e] + m * mat_bytes, FF, H, W + m * mat);
+        }
         for (int64_t b = 0; b < n; ++b) {
             int64_t t = assign[offsets[e] + b] / k;
             memcpy(xs + b * H, xd + t * H, sizeof(double) * (size_t)H);
@@ -630,6 +785,16 @@ int orc_moe_forward(int H, int E, int FF, int k, int score_fn, int has_shared, i
     free(ids); free(w); free(counts); free(offsets); free(assign);
     free(xd); free(W); free(slot); free(xs); free(act); free(ob);
     return 0;
+}
+
+/* The layer with Q4_K experts (the codec-0 case above). */
+int orc_moe_forward(int H, int E, int FF, int k, int score_fn, int has_shared, int shared_ff,
+                    const uint16_t *x, const float *wr, const float *bias,
+                    const uint8_t *const *blobs, const uint8_t *shared, int64_t T,
+                    const int32_t *forced, double *y)
+{
+    return orc_moe_forward_codec(H, E, FF, k, score_fn, has_shared, shared_ff, x, wr, bias, blobs, shared, T,
+                                 forced, 0, y);
 }
 
 /* Threads the OpenMP regions above use (0 or less: leave the default). */
