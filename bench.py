@@ -41,7 +41,7 @@ from quantized_moe_expert_04_b300 import moe, synth  # noqa: E402
 from quantized_moe_expert_04_b300.layer import TieredLayer, pack_layer, routing_views, workspace  # noqa: E402
 
 DEFAULT_TOKENS = {"tiny": 4, "qwen_decode": 3, "deepseek_decode": 4, "qwen_prefill": 4096,
-                  "deepseek_prefill_skewed": 4096}
+                  "deepseek_prefill_skewed": 4096, "qwen_decode_q5k": 3, "deepseek_decode_q5k": 8}
 METRIC = "MoE-layer tokens/s"
 UNIT = "tokens/s"
 
@@ -186,13 +186,13 @@ def oracle_sample(wl, T, layers, x_layers, gpu_ids=None, gpu_y32=None, time_budg
         used = set(oids.reshape(-1).tolist()) | (set(forced.reshape(-1).tolist()) if forced is not None else set())
         blobs = [None] * wl.n_experts
         for e in sorted(used):
-            blobs[e] = oracle.pack_expert_q4k(synth.expert_weight(wl, e, 0, l, device=gen_device).cpu().numpy())
+            blobs[e] = oracle.pack_expert(synth.expert_weight(wl, e, 0, l, device=gen_device).cpu().numpy(), wl.codec)
         sblob = None
         if wl.has_shared:
             sblob = oracle.pack_shared_q8_0(synth.shared_weight(wl, 0, l, device=gen_device).cpu().numpy())
         t0 = time.perf_counter()
         ref = oracle.moe_forward(wl.hidden, wl.n_experts, wl.ff, wl.top_k, wl.score_fn, xb, wr, b, blobs,
-                                 wl.shared_ff, sblob, forced_ids=forced)
+                                 wl.shared_ff, sblob, forced_ids=forced, codec=wl.codec)
         spent += time.perf_counter() - t0
         if gpu_y32 is not None and l in gpu_y32:
             got = gpu_y32[l][:Ts].astype(np.float64)
@@ -340,7 +340,7 @@ def profiled_traffic(kernel, workload, T):
 # the same process after the headline.
 CONFIG_SET = [("qwen_decode", 1), ("qwen_decode", 3), ("qwen_decode", 5), ("deepseek_decode", 1),
               ("deepseek_decode", 4), ("deepseek_decode", 8), ("qwen_prefill", 4096),
-              ("deepseek_prefill_skewed", 4096)]
+              ("deepseek_prefill_skewed", 4096), ("qwen_decode_q5k", 3), ("deepseek_decode_q5k", 8)]
 
 
 def measure(args, wl, T, nL, world, rank, local, K=None, soak_s=0.0, target_s=0.3, e2e=False,
@@ -575,7 +575,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": head["steps"],
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
-        "data": "synthetic (seeded; x~N(0,1) bf16, router W~N(0,1/H), experts N(0,0.02^2) packed to Q4_K)",
+        "data": "synthetic (seeded; x~N(0,1) bf16, router W~N(0,1/H), experts N(0,0.02^2) packed to %s)" % ("Q5_K" if wl.codec else "Q4_K"),
         "config": {"workload": wl.name, "tokens_per_window": T, "hidden": wl.hidden, "experts": wl.n_experts,
                    "top_k": wl.top_k, "ff": wl.ff, "shared_ff": wl.shared_ff, "distinct_layers": nL,
                    "resident_expert_gb": round(nL * (wl.n_experts * wl.blob_bytes + wl.shared_blob_bytes) / 1e9, 2),
@@ -589,7 +589,7 @@ def run_ours(args, world, rank, local):
     if "cpu_baseline" in head:
         out["cpu_baseline"] = head["cpu_baseline"]
         out["parity"] = head["parity"]
-        if not wl.has_shared and T <= 64 and rank == 0:
+        if not wl.has_shared and wl.codec == 0 and T <= 64 and rank == 0:
             try:
                 out["cpu_kernel"] = cpu_kernel_sample(wl, T, 8)
             except Exception as exc:          # no AVX2/FMA on this host, or no compiler
@@ -631,7 +631,7 @@ def run_reference(args, world, rank):
         ids, _, _, _ = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
         blobs = [None] * wl.n_experts
         for e in sorted(set(ids.reshape(-1).tolist())):
-            blobs[e] = oracle.pack_expert_q4k(synth.expert_weight(wl, e, 0, l, device=gen).cpu().numpy())
+            blobs[e] = oracle.pack_expert(synth.expert_weight(wl, e, 0, l, device=gen).cpu().numpy(), wl.codec)
         sblob = oracle.pack_shared_q8_0(synth.shared_weight(wl, 0, l, device=gen).cpu().numpy()) \
             if wl.has_shared else None
         prepared.append((xb, wr, b, blobs, sblob))
@@ -639,7 +639,7 @@ def run_reference(args, world, rank):
     def step(i):
         xb, wr, b, blobs, sblob = prepared[i % nL]
         oracle.moe_forward(wl.hidden, wl.n_experts, wl.ff, wl.top_k, wl.score_fn, xb, wr, b, blobs,
-                           wl.shared_ff, sblob)
+                           wl.shared_ff, sblob, codec=wl.codec)
 
     for i in range(args.warmup):
         step(i)

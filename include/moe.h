@@ -102,6 +102,14 @@ enum {
                                         inputs are read only after it has finished)     */
 };
 
+/* Block format of the routed experts (the shared expert is always Q8_0).
+ * Q5_K experts run on the decode path only (T <= 8): a call that would take
+ * the tensor-core path returns MOE_ERR_UNSUPPORTED_SHAPE. */
+typedef enum {
+    MOE_CODEC_Q4K = 0,               /* 144 bytes per 256 weights (4-bit)                */
+    MOE_CODEC_Q5K = 1                /* 176 bytes per 256 weights (5-bit, fifth bits in qh) */
+} moe_codec;
+
 /*
  * Layer shape.  Limits: hidden % 256 == 0 and 256 <= hidden <= 8192;
  * 1 <= n_experts <= 1024; ff % 64 == 0 and 64 <= ff <= 8192;
@@ -116,7 +124,7 @@ typedef struct {
     int32_t score_fn;    /* moe_score_fn                        */
     int32_t shared_ff;   /* shared expert width, 0 = none       */
     int32_t flags;       /* MOE_FLAG_*                          */
-    int32_t reserved;    /* must be 0                           */
+    int32_t codec;       /* routed experts' blocks: moe_codec   */
 } moe_config;
 
 /* ---------------------------------------------------------------- sizes */
@@ -124,9 +132,12 @@ typedef struct {
 /* Bytes of a [rows][cols] matrix in Q4_K (cols % 256 == 0): rows*cols/256*144.
  * Returns 0 for an invalid shape. */
 MOE_API size_t moe_q4k_bytes(int64_t rows, int64_t cols);
+/* Bytes of a [rows][cols] matrix in Q5_K (cols % 256 == 0): rows*cols/256*176. */
+MOE_API size_t moe_q5k_bytes(int64_t rows, int64_t cols);
 /* Bytes of a [rows][cols] matrix in Q8_0 (cols % 32 == 0): rows*cols/32*34. */
 MOE_API size_t moe_q8_0_bytes(int64_t rows, int64_t cols);
-/* Bytes of one routed-expert blob, 3*moe_q4k_bytes(ff, hidden); 0 if cfg invalid. */
+/* Bytes of one routed-expert blob, 3*moe_q4k_bytes(ff, hidden) (Q5_K:
+ * 3*moe_q5k_bytes); 0 if cfg invalid. */
 MOE_API size_t moe_expert_bytes(const moe_config *cfg);
 /* Bytes of the shared-expert blob, 3*moe_q8_0_bytes(shared_ff, hidden); 0 if none. */
 MOE_API size_t moe_shared_bytes(const moe_config *cfg);
@@ -152,6 +163,18 @@ MOE_API moe_status moe_pack_q4k(const float *w, int64_t rows, int64_t cols, uint
                         uint32_t *dev_status, moe_stream_t stream);
 
 /*
+ * Quantise w[rows][cols] (device fp32) to Q5_K blocks (GGUF layout: fp16 d,
+ * fp16 dmin, scales[12] packed as Q4_K's, qh[32], qs[128]; the quant of
+ * element 64c + 32h + l keeps its low four bits in the low (h = 0) or high
+ * (h = 1) nibble of qs[32c + l] and its fifth bit in bit 2c + h of qh[l]).
+ * The quantiser is moe_pack_q4k's with 31 levels: scale_j = (mx - mn)/31 and
+ * q clamped to 0..31.  out gets moe_q5k_bytes(rows, cols) bytes; errors as
+ * moe_pack_q4k.
+ */
+MOE_API moe_status moe_pack_q5k(const float *w, int64_t rows, int64_t cols, uint8_t *out,
+                        uint32_t *dev_status, moe_stream_t stream);
+
+/*
  * Quantise w[rows][cols] (device fp32) to Q8_0: d = fp16(max|x|/127),
  * q = d > 0 ? clamp(rint(x/d), -127, 127) : 0.  cols % 32 == 0; out gets
  * moe_q8_0_bytes(rows, cols) bytes.  cols*34/32 must be a multiple of 16 for
@@ -161,10 +184,12 @@ MOE_API moe_status moe_pack_q4k(const float *w, int64_t rows, int64_t cols, uint
 MOE_API moe_status moe_pack_q8_0(const float *w, int64_t rows, int64_t cols, uint8_t *out,
                          uint32_t *dev_status, moe_stream_t stream);
 
-/* Test hooks: dequantise a Q4_K / Q8_0 matrix to fp32 out[rows][cols]
- * (device).  Bit-exact with the format definition (each product and the
- * difference rounded to fp32 separately). */
+/* Test hooks: dequantise a Q4_K / Q5_K / Q8_0 matrix to fp32
+ * out[rows][cols] (device).  Bit-exact with the format definition (each
+ * product and the difference rounded to fp32 separately). */
 MOE_API moe_status moe_dequant_q4k(const uint8_t *blocks, int64_t rows, int64_t cols, float *out,
+                           moe_stream_t stream);
+MOE_API moe_status moe_dequant_q5k(const uint8_t *blocks, int64_t rows, int64_t cols, float *out,
                            moe_stream_t stream);
 MOE_API moe_status moe_dequant_q8_0(const uint8_t *blocks, int64_t rows, int64_t cols, float *out,
                             moe_stream_t stream);
@@ -176,6 +201,8 @@ MOE_API moe_status moe_dequant_q8_0(const uint8_t *blocks, int64_t rows, int64_t
  * w = fp16(q*S_j + NZ_j) rounded once; Q8_0: w = fp16(d*q).  The pages fix no
  * precision; this rounding is the library's (see moe_forward).  Errors as
  * moe_dequant_q4k (Q8_0: out 4-byte aligned). */
+MOE_API moe_status moe_dequant_q5k_f16(const uint8_t *blocks, int64_t rows, int64_t cols, uint16_t *out,
+                               moe_stream_t stream);   /* Q5_K: as Q4_K, q in 0..31 */
 MOE_API moe_status moe_dequant_q4k_f16(const uint8_t *blocks, int64_t rows, int64_t cols, uint16_t *out,
                                moe_stream_t stream);
 MOE_API moe_status moe_dequant_q8_0_f16(const uint8_t *blocks, int64_t rows, int64_t cols, uint16_t *out,

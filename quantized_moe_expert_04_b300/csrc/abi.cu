@@ -20,7 +20,7 @@ static bool cfg_valid(const moe_config *c)
     if (c->top_k < 1 || c->top_k > 32 || c->top_k > c->n_experts) return false;
     if (c->score_fn != MOE_SCORE_SOFTMAX && c->score_fn != MOE_SCORE_SIGMOID_BIAS) return false;
     if (c->shared_ff != 0 && (c->shared_ff < 64 || c->shared_ff > 8192 || c->shared_ff % 64)) return false;
-    if (c->reserved != 0) return false;
+    if (c->codec != MOE_CODEC_Q4K && c->codec != MOE_CODEC_Q5K) return false;
     return true;
 }
 
@@ -99,7 +99,9 @@ static moe_status check_call(const moe_config *cfg, const uint16_t *x, const flo
         if (!cfg) return MOE_ERR_INVALID_ARG;
         if (cfg->score_fn != MOE_SCORE_SOFTMAX && cfg->score_fn != MOE_SCORE_SIGMOID_BIAS)
             return MOE_ERR_INVALID_ARG;
-        if (cfg->reserved != 0 || cfg->top_k < 1 || cfg->top_k > cfg->n_experts) return MOE_ERR_INVALID_ARG;
+        if ((cfg->codec != MOE_CODEC_Q4K && cfg->codec != MOE_CODEC_Q5K) || cfg->top_k < 1 ||
+            cfg->top_k > cfg->n_experts)
+            return MOE_ERR_INVALID_ARG;
         return MOE_ERR_UNSUPPORTED_SHAPE;
     }
     if (T < 0) return MOE_ERR_INVALID_ARG;
@@ -125,6 +127,8 @@ moe_status forward_checks(const moe_config *cfg, const uint16_t *x, const float 
     if ((y && !aligned16(y)) || (y_f32 && !aligned16(y_f32)) || (shared_blob && !aligned16(shared_blob)))
         return MOE_ERR_MISALIGNED;
     if (T > 0 && (cfg->flags & MOE_FLAG_FORCE_GEMV) && !use_gemv(*cfg, T)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    // Q5_K experts: the decode path only
+    if (T > 0 && cfg->codec == MOE_CODEC_Q5K && !use_gemv(*cfg, T)) return MOE_ERR_UNSUPPORTED_SHAPE;
     return MOE_OK;
 }
 }  // namespace moe
@@ -139,6 +143,12 @@ size_t moe_q4k_bytes(int64_t rows, int64_t cols)
     return (size_t)rows * (size_t)(cols / kQK) * kQ4KBytes;
 }
 
+size_t moe_q5k_bytes(int64_t rows, int64_t cols)
+{
+    if (rows < 0 || cols <= 0 || cols % kQK) return 0;
+    return (size_t)rows * (size_t)(cols / kQK) * kQ5KBytes;
+}
+
 size_t moe_q8_0_bytes(int64_t rows, int64_t cols)
 {
     if (rows < 0 || cols <= 0 || cols % kQK8) return 0;
@@ -148,7 +158,7 @@ size_t moe_q8_0_bytes(int64_t rows, int64_t cols)
 size_t moe_expert_bytes(const moe_config *cfg)
 {
     if (!cfg_valid(cfg)) return 0;
-    return 3 * moe_q4k_bytes(cfg->ff, cfg->hidden);
+    return 3 * (cfg->codec == MOE_CODEC_Q5K ? moe_q5k_bytes(cfg->ff, cfg->hidden) : moe_q4k_bytes(cfg->ff, cfg->hidden));
 }
 
 size_t moe_shared_bytes(const moe_config *cfg)
@@ -166,6 +176,17 @@ moe_status moe_pack_q4k(const float *w, int64_t rows, int64_t cols, uint8_t *out
     if (!w || !out) return MOE_ERR_INVALID_ARG;
     if (!aligned16(w) || !aligned16(out)) return MOE_ERR_MISALIGNED;
     return cuda_status(launch_pack_q4k(w, rows * (cols / kQK), out, dev_status, (cudaStream_t)stream));
+}
+
+moe_status moe_pack_q5k(const float *w, int64_t rows, int64_t cols, uint8_t *out, uint32_t *dev_status,
+                        moe_stream_t stream)
+{
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % kQK) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!w || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(out)) return MOE_ERR_MISALIGNED;
+    return cuda_status(launch_pack_q5k(w, rows * (cols / kQK), out, dev_status, (cudaStream_t)stream));
 }
 
 moe_status moe_pack_q8_0(const float *w, int64_t rows, int64_t cols, uint8_t *out, uint32_t *dev_status,
@@ -187,6 +208,26 @@ moe_status moe_dequant_q4k(const uint8_t *blocks, int64_t rows, int64_t cols, fl
     if (!blocks || !out) return MOE_ERR_INVALID_ARG;
     if (!aligned16(blocks) || !aligned16(out)) return MOE_ERR_MISALIGNED;
     return cuda_status(launch_dequant_q4k(blocks, rows * (cols / kQK), out, (cudaStream_t)stream));
+}
+
+moe_status moe_dequant_q5k(const uint8_t *blocks, int64_t rows, int64_t cols, float *out, moe_stream_t stream)
+{
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % kQK) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(blocks) || !aligned16(out)) return MOE_ERR_MISALIGNED;
+    return cuda_status(launch_dequant_q5k(blocks, rows * (cols / kQK), out, (cudaStream_t)stream));
+}
+
+moe_status moe_dequant_q5k_f16(const uint8_t *blocks, int64_t rows, int64_t cols, uint16_t *out, moe_stream_t stream)
+{
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % kQK) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(blocks) || !aligned16(out)) return MOE_ERR_MISALIGNED;
+    return cuda_status(launch_dequant_q5k_f16(blocks, rows * (cols / kQK), out, (cudaStream_t)stream));
 }
 
 moe_status moe_dequant_q8_0(const uint8_t *blocks, int64_t rows, int64_t cols, float *out, moe_stream_t stream)
@@ -306,6 +347,7 @@ moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *ro
         d.route_parts = dec_route_parts(cfg->hidden);
         d.nc = dec_consumers(*cfg);
         d.half = dec_half(*cfg) ? 1 : 0;
+        d.codec = cfg->codec;
         d.ring_bytes = dec_ring_bytes(*cfg, T);
         d.stages = dec_stages(*cfg, T);
         d.overlap_prev = (cfg->flags & MOE_FLAG_STATIC_WEIGHTS) != 0;

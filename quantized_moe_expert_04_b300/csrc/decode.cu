@@ -327,9 +327,11 @@ __global__ void __maxnreg__(88) k_dec_route(DecArgs a)
 constexpr int kUnitRows = 8;            // ff rows of a routed unit (the 8 MMA rows of each of gate, up)
 constexpr int kSharedRows = 4;          // ff rows of a shared-expert unit
 constexpr int kPieceQ4K = 144;          // bytes of one row's 256-column block: one Q4_K super-block
+constexpr int kPieceQ5K = 176;          // ... in Q5_K
 constexpr int kPieceQ80 = 272;          // the same block in Q8_0: eight 34-byte blocks
 constexpr uint32_t kSlotBytes = 1152;   // one stage of one warp: 8 x 144 (>= 4 x 272)
 constexpr uint32_t kSlotHalf = 640;     // ... of a half-block warp: 8 x 64 quant bytes, then 8 x 16 header bytes
+constexpr uint32_t kSlotQ5K = 1408;     // ... of a Q5_K warp: 8 x 176
 constexpr int kMaxCons = 16;            // consumer warps of 256 columns
 constexpr int kMaxConsHalf = 20;        // consumer warps of 128 columns (96 registers a thread)
 
@@ -369,7 +371,7 @@ __host__ __device__ inline LayerSmem layer_smem(int E, int T, int H, int nc, uin
 struct Units {
     int64_t nr, ns;          // unit counts
     int64_t br, bs;          // bytes of one unit (3 slabs)
-    int rb, rbs;             // row bytes: Q4_K routed, Q8_0 shared
+    int rb, rbs;             // row bytes: routed (Q4_K or Q5_K), Q8_0 shared
 };
 
 __device__ __forceinline__ int64_t first_unit(const Units &u, int64_t byte)
@@ -381,7 +383,7 @@ __device__ __forceinline__ int64_t first_unit(const Units &u, int64_t byte)
 
 struct UnitInfo {
     const uint8_t *blob;
-    int fmt;                 // 0: Q4_K routed, 1: Q8_0 shared
+    int fmt;                 // 0: routed (the kernel's codec), 1: Q8_0 shared
     int u;                   // active-expert index (routed), -1 shared
     int f0;                  // first ff row
     int ffm;                 // rows of one matrix in the blob (FF or SFF)
@@ -457,6 +459,18 @@ __device__ __forceinline__ void nib_pair(uint32_t w0, uint32_t w1, int b, __half
     q_hi = __hfma2(dq_u2h2((p & 0x00F000F0u) | 0x64006400u), __float2half2_rn(0.0625f), __float2half2_rn(-64.0f));
 }
 
+// Q5_K: as nib_pair, with the fifth bits in bit 0 (low nibble's element) and
+// bit 1 (high nibble's) of byte b of h0 (row r0) and h1 (row r1).
+__device__ __forceinline__ void nib5_pair(uint32_t w0, uint32_t w1, uint32_t h0, uint32_t h1, int b, __half2 &q_lo,
+                                          __half2 &q_hi)
+{
+    const uint32_t sel = (uint32_t)b | ((uint32_t)(4 + b) << 8);
+    const uint32_t p = __byte_perm(w0, w1, sel), f = __byte_perm(h0, h1, sel);
+    q_lo = __hsub2(dq_u2h2((p & 0x000F000Fu) | ((f << 4) & 0x00100010u) | 0x64006400u), __float2half2_rn(1024.0f));
+    q_hi = __hfma2(dq_u2h2((p & 0x00F000F0u) | ((f << 7) & 0x01000100u) | 0x64006400u), __float2half2_rn(0.0625f),
+                   __float2half2_rn(-64.0f));
+}
+
 // int8 pair (row r0, row r1) at byte b of words w0 and w1 -> exact fp16 pair.
 __device__ __forceinline__ __half2 i8_pair(uint32_t w0, uint32_t w1, int b)
 {
@@ -488,15 +502,23 @@ __device__ __forceinline__ void copy_block(uint32_t dst, const uint8_t *src, int
     }
 }
 
+// Variants of the layer kernel: Q4_K routed rows with 256-column warps, with
+// 128-column warps, or Q5_K routed rows with 256-column warps.
+constexpr int kVarQ4K = 0, kVarHalf = 1, kVarQ5K = 2;
+
 // The layer kernel, S stages per consumer warp.  HALF: each consumer warp owns
 // 128 columns (half a Q4_K super-block) instead of 256, for twice the warps;
 // only for layers without a shared expert.  128 registers a thread at 256
 // columns (16 warps, 4 on each SM sub-partition, fit one SM), 96 at 128
-// columns (20 warps).
-template <int S, bool HALF>
-__global__ void __maxnreg__(HALF ? 96 : 128) k_dec_layer(DecArgs a)
+// columns (20 warps).  Q5: the routed rows are Q5_K blocks (the layout of
+// Q4_K's plus 32 bytes of fifth bits, qh, before the nibbles).
+template <int S, int V>
+__global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_layer(DecArgs a)
 {
     static_assert(S >= 4, "the lagging down projection keeps 3 stages busy");
+    constexpr bool HALF = V == kVarHalf, Q5 = V == kVarQ5K;
+    constexpr int PIECE = Q5 ? kPieceQ5K : kPieceQ4K;   // bytes of a routed row's 256-column block
+    constexpr int QS = Q5 ? 48 : 16;                     // offset of its nibbles
     extern __shared__ __align__(128) uint8_t smem[];
     const int T = a.T, H = a.H, E = a.E, k = a.k, nb = H / 256, NC = a.nc;
     const LayerSmem L = layer_smem(E, T, H, NC, a.ring_bytes);
@@ -670,7 +692,7 @@ __global__ void __maxnreg__(HALF ? 96 : 128) k_dec_layer(DecArgs a)
 
     // ---- this CTA's share of the window's units
     Units un;
-    un.rb = nb * kPieceQ4K;
+    un.rb = nb * PIECE;
     un.rbs = nb * kPieceQ80;
     un.nr = (int64_t)U * (a.FF / kUnitRows);
     un.ns = a.shared_blob ? a.SFF / kSharedRows : 0;
@@ -693,7 +715,7 @@ __global__ void __maxnreg__(HALF ? 96 : 128) k_dec_layer(DecArgs a)
         // both the partial sums (gate/up) and the activations (down).
         // (HALF: warp w owns the 128-column half w % 2 of block w / 2, and stages the
         // row headers and its half of the quant bytes.)
-        constexpr uint32_t SLOT = HALF ? kSlotHalf : kSlotBytes;
+        constexpr uint32_t SLOT = HALF ? kSlotHalf : Q5 ? kSlotQ5K : kSlotBytes;
         constexpr int NT = HALF ? 8 : 16;                // down tiles of 16 columns (x 2) per warp
         const int g = lane >> 2, tq = lane & 3;
         const int cb = HALF ? warp >> 1 : warp, hh = HALF ? warp & 1 : 0;
@@ -726,7 +748,7 @@ __global__ void __maxnreg__(HALF ? 96 : 128) k_dec_layer(DecArgs a)
                     const uint8_t *sb = src + cb * kPieceQ4K;
                     cp16(dst + (hp0 & 1023u), sb + (hp0 >> 10));
                     if (lane < kUnitRows * 5 - 32) cp16(dst + (hp1 & 1023u), sb + (hp1 >> 10));
-                } else if (ic.ui.fmt == 0) copy_block<kPieceQ4K / 16, kUnitRows>(dst, src + cb * kPieceQ4K, ic.ui.rowb, lane);
+                } else if (ic.ui.fmt == 0) copy_block<PIECE / 16, kUnitRows>(dst, src + cb * PIECE, ic.ui.rowb, lane);
                 else copy_block<kPieceQ80 / 16, kSharedRows>(dst, src + cb * kPieceQ80, ic.ui.rowb, lane);
             }
             cp_commit();                                 // one group a stage, empty or not
@@ -774,8 +796,8 @@ __global__ void __maxnreg__(HALF ? 96 : 128) k_dec_layer(DecArgs a)
                     mma16808(D[t8], dq_h22u(__hfma2(ql, Slo, Nlo)), dq_h22u(__hfma2(qh, Shi, Nhi)), bfr);
                 }
             } else if (ui.fmt == 0) {
-                const uint8_t *r0 = dn + (2 * tq) * kPieceQ4K, *r1 = r0 + kPieceQ4K;
-                // Q4_K: lane g takes quant bytes 16 g .. 16 g + 15 of the block: chunk c = g / 2
+                const uint8_t *r0 = dn + (2 * tq) * PIECE, *r1 = r0 + PIECE;
+                // lane g takes quant bytes 16 g .. 16 g + 15 of the block: chunk c = g / 2
                 // (sub-blocks 2c low nibbles, 2c + 1 high), columns hl(g, i)
                 const int c = g >> 1;
                 __half2 S0, N0, S1, N1;
@@ -783,13 +805,25 @@ __global__ void __maxnreg__(HALF ? 96 : 128) k_dec_layer(DecArgs a)
                 q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(r1), c, S1, N1);
                 const __half2 Slo = __lows2half2(S0, S1), Shi = __highs2half2(S0, S1);
                 const __half2 Nlo = __lows2half2(N0, N1), Nhi = __highs2half2(N0, N1);
-                const uint4 q0 = *reinterpret_cast<const uint4 *>(r0 + 16 + 16 * g);
-                const uint4 q1 = *reinterpret_cast<const uint4 *>(r1 + 16 + 16 * g);
+                const uint4 q0 = *reinterpret_cast<const uint4 *>(r0 + QS + 16 * g);
+                const uint4 q1 = *reinterpret_cast<const uint4 *>(r1 + QS + 16 * g);
                 const uint32_t w0[4] = {q0.x, q0.y, q0.z, q0.w}, w1[4] = {q1.x, q1.y, q1.z, q1.w};
+                uint32_t f0[4] = {0u, 0u, 0u, 0u}, f1[4] = {0u, 0u, 0u, 0u};
+                if (Q5) {
+                    // the fifth bits of the same 16 elements: qh bytes 16 (g % 2) .. + 15, bits
+                    // 2c (low sub-block) and 2c + 1 (high) moved to bits 0 and 1
+                    const uint4 h0 = *reinterpret_cast<const uint4 *>(r0 + 16 + 16 * (g & 1));
+                    const uint4 h1 = *reinterpret_cast<const uint4 *>(r1 + 16 + 16 * (g & 1));
+                    const int sh = 2 * c;
+                    f0[0] = h0.x >> sh; f0[1] = h0.y >> sh; f0[2] = h0.z >> sh; f0[3] = h0.w >> sh;
+                    f1[0] = h1.x >> sh; f1[1] = h1.y >> sh; f1[2] = h1.z >> sh; f1[3] = h1.w >> sh;
+                }
 #pragma unroll
                 for (int t16 = 0; t16 < NT; ++t16) {
                     __half2 ql, qh;
-                    nib_pair(w0[(t16 >> 2) & 3], w1[(t16 >> 2) & 3], t16 & 3, ql, qh);
+                    if (Q5) nib5_pair(w0[(t16 >> 2) & 3], w1[(t16 >> 2) & 3], f0[(t16 >> 2) & 3], f1[(t16 >> 2) & 3],
+                                      t16 & 3, ql, qh);
+                    else nib_pair(w0[(t16 >> 2) & 3], w1[(t16 >> 2) & 3], t16 & 3, ql, qh);
                     mma16808(D[t16], dq_h22u(__hfma2(ql, Slo, Nlo)), dq_h22u(__hfma2(qh, Shi, Nhi)), bfr);
                 }
             } else {
@@ -863,21 +897,32 @@ __global__ void __maxnreg__(HALF ? 96 : 128) k_dec_layer(DecArgs a)
                         mma16816(c4[1], og[2], ou[2], og[3], ou[3], xh.x, xh.y);
                     }
                 } else if (ui.fmt == 0) {
-                    const uint8_t *gr = gst + g * kPieceQ4K, *ur = ust + g * kPieceQ4K;
+                    const uint8_t *gr = gst + g * PIECE, *ur = ust + g * PIECE;
                     __half2 Sg, NZg, Su, NZu;
                     q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(gr), tq, Sg, NZg);
                     q4k_pair_scales_h(*reinterpret_cast<const uint4 *>(ur), tq, Su, NZu);
-                    const uint4 ga = *reinterpret_cast<const uint4 *>(gr + 16 + 32 * tq);
-                    const uint4 gb = *reinterpret_cast<const uint4 *>(gr + 32 + 32 * tq);
-                    const uint4 ua = *reinterpret_cast<const uint4 *>(ur + 16 + 32 * tq);
-                    const uint4 ub = *reinterpret_cast<const uint4 *>(ur + 32 + 32 * tq);
+                    const uint4 ga = *reinterpret_cast<const uint4 *>(gr + QS + 32 * tq);
+                    const uint4 gb = *reinterpret_cast<const uint4 *>(gr + QS + 16 + 32 * tq);
+                    const uint4 ua = *reinterpret_cast<const uint4 *>(ur + QS + 32 * tq);
+                    const uint4 ub = *reinterpret_cast<const uint4 *>(ur + QS + 16 + 32 * tq);
                     const uint32_t gq[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
                     const uint32_t uq[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+                    // Q5_K: the fifth bits of quant byte l of chunk tq are bits 2 tq, 2 tq + 1
+                    // of qh[l]; word s of qh covers the bytes of word s of the chunk
+                    const uint32_t *gqh = reinterpret_cast<const uint32_t *>(gr + 16);
+                    const uint32_t *uqh = reinterpret_cast<const uint32_t *>(ur + 16);
 #pragma unroll
                     for (int s = 0; s < 8; ++s) {
                         uint32_t og[4], ou[4];
-                        q4k_word_f16(gq[s], __low2half2(Sg), __low2half2(NZg), __high2half2(Sg), __high2half2(NZg), og);
-                        q4k_word_f16(uq[s], __low2half2(Su), __low2half2(NZu), __high2half2(Su), __high2half2(NZu), ou);
+                        if (Q5) {
+                            q5k_word_f16(gq[s], gqh[s] >> (2 * tq), __low2half2(Sg), __low2half2(NZg), __high2half2(Sg),
+                                         __high2half2(NZg), og);
+                            q5k_word_f16(uq[s], uqh[s] >> (2 * tq), __low2half2(Su), __low2half2(NZu), __high2half2(Su),
+                                         __high2half2(NZu), ou);
+                        } else {
+                            q4k_word_f16(gq[s], __low2half2(Sg), __low2half2(NZg), __high2half2(Sg), __high2half2(NZg), og);
+                            q4k_word_f16(uq[s], __low2half2(Su), __low2half2(NZu), __high2half2(Su), __high2half2(NZu), ou);
+                        }
                         const uint2 xl = xb(s, tq), xh = xb(8 + s, tq);
                         mma16816(c4[0], og[0], ou[0], og[1], ou[1], xl.x, xl.y);
                         mma16816(c4[1], og[2], ou[2], og[3], ou[3], xh.x, xh.y);
@@ -1066,9 +1111,17 @@ int dec_route_parts(int H)
     return 0;   // unsupported
 }
 
-// Half-block warps (128 columns each) for layers without a shared expert whose
-// 128-column blocks fit kMaxConsHalf warps; 256-column warps otherwise.
-bool dec_half(const moe_config &c) { return c.shared_ff == 0 && c.hidden / 128 <= kMaxConsHalf; }
+// Half-block warps (128 columns each) for Q4_K layers without a shared expert
+// whose 128-column blocks fit kMaxConsHalf warps; 256-column warps otherwise.
+bool dec_half(const moe_config &c)
+{
+    return c.codec == MOE_CODEC_Q4K && c.shared_ff == 0 && c.hidden / 128 <= kMaxConsHalf;
+}
+
+static uint32_t dec_slot(const moe_config &c)
+{
+    return dec_half(c) ? kSlotHalf : c.codec == MOE_CODEC_Q5K ? kSlotQ5K : kSlotBytes;
+}
 
 int dec_consumers(const moe_config &c) { return dec_half(c) ? c.hidden / 128 : c.hidden / 256; }
 
@@ -1087,17 +1140,17 @@ static const int kStageCounts[] = {16, 14, 12, 10, 8, 7, 6};
 
 using LayerFn = void (*)(DecArgs);
 
-template <bool HALF>
+template <int V>
 static LayerFn layer_fn(int S)
 {
     switch (S) {
-    case 16: return k_dec_layer<16, HALF>;
-    case 14: return k_dec_layer<14, HALF>;
-    case 12: return k_dec_layer<12, HALF>;
-    case 10: return k_dec_layer<10, HALF>;
-    case 8: return k_dec_layer<8, HALF>;
-    case 7: return k_dec_layer<7, HALF>;
-    case 6: return k_dec_layer<6, HALF>;
+    case 16: return k_dec_layer<16, V>;
+    case 14: return k_dec_layer<14, V>;
+    case 12: return k_dec_layer<12, V>;
+    case 10: return k_dec_layer<10, V>;
+    case 8: return k_dec_layer<8, V>;
+    case 7: return k_dec_layer<7, V>;
+    case 6: return k_dec_layer<6, V>;
     }
     return nullptr;
 }
@@ -1107,7 +1160,7 @@ int dec_stages(const moe_config &c, int32_t T)
     const int64_t ring = dec_base_ring(c, T);
     const int nc = dec_consumers(c);
     if (nc <= 0 || ring < (int64_t)T * c.n_experts * 12 + 16) return 0;
-    const int64_t per = ring / ((int64_t)nc * (dec_half(c) ? kSlotHalf : kSlotBytes));
+    const int64_t per = ring / ((int64_t)nc * dec_slot(c));
     for (int s : kStageCounts)
         if (per >= s) return s;
     return 0;
@@ -1151,7 +1204,7 @@ static cudaError_t dec_set_attributes()
     e = cudaFuncSetAttribute(k_dec_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kDecTok * 8192 * (int)sizeof(uint16_t));
     for (int S : kStageCounts)
-        for (LayerFn f : {layer_fn<false>(S), layer_fn<true>(S)})
+        for (LayerFn f : {layer_fn<kVarQ4K>(S), layer_fn<kVarHalf>(S), layer_fn<kVarQ5K>(S)})
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBudget);
     if (e == cudaSuccess) done[dev] = true;
@@ -1173,7 +1226,8 @@ cudaError_t launch_decode(const DecArgs &a0, cudaStream_t s)
     const LayerSmem L = layer_smem(a.E, a.T, a.H, a.nc, a.ring_bytes);
     const dim3 grid(dec_sms()), block(32 * std::max(a.nc, kDecTok));   // at least one warp per token
     prof_begin(kPhDecLayer, s);
-    const LayerFn fn = a.half ? layer_fn<true>(a.stages) : layer_fn<false>(a.stages);
+    const LayerFn fn = a.half ? layer_fn<kVarHalf>(a.stages)
+                       : a.codec == MOE_CODEC_Q5K ? layer_fn<kVarQ5K>(a.stages) : layer_fn<kVarQ4K>(a.stages);
     e = fn ? launch_pdl(fn, grid, block, L.total, s, true, a) : cudaErrorInvalidValue;
     prof_end(kPhDecLayer, s);
     return e;

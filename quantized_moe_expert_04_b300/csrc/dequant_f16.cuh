@@ -10,6 +10,7 @@
 //   Q4_K  S_j = fp16(d * sc_j), NZ_j = fp16(-(dmin * m_j)) (exact products,
 //         one rounding each), then w = fp16(q * S_j + NZ_j) with one rounding
 //         (a fused fp16 multiply-add on the exact integer q);
+//   Q5_K  as Q4_K, q the 5-bit quant (0..31): exact in fp16 too;
 //   Q8_0  w = fp16(d * q) (exact product, one rounding).
 #pragma once
 
@@ -74,6 +75,39 @@ __device__ __forceinline__ void q4k_word_f16(uint32_t w, __half2 S_lo, __half2 N
 {
     __half2 l01, l23, h01, h23;
     nibbles_to_q(w, l01, l23, h01, h23);
+    out[0] = dq_h22u(__hfma2(l01, S_lo, NZ_lo));
+    out[1] = dq_h22u(__hfma2(l23, S_lo, NZ_lo));
+    out[2] = dq_h22u(__hfma2(h01, S_hi, NZ_hi));
+    out[3] = dq_h22u(__hfma2(h23, S_hi, NZ_hi));
+}
+
+// Q5_K: 4-bit parts w as nibbles_to_q, and hb the fifth bits of the same 4
+// elements: bit 0 of byte i for the low sub-block's element, bit 1 for the
+// high one's.  The fifth bit enters the fp16 mantissa next to the nibble: at
+// bit 4 of 1024 + q (low), at bit 8 of 1024 + 16 q (high); both stay exact
+// integers below 2048.
+__device__ __forceinline__ void nibbles5_to_q(uint32_t w, uint32_t hb, __half2 &lo01, __half2 &lo23, __half2 &hi01,
+                                              __half2 &hi23)
+{
+    const uint32_t p01 = __byte_perm(w, 0, 0x4140), p23 = __byte_perm(w, 0, 0x4342);
+    const uint32_t h01 = __byte_perm(hb, 0, 0x4140), h23 = __byte_perm(hb, 0, 0x4342);
+    const __half2 k1024 = __float2half2_rn(1024.0f);
+    const __half2 k16th = __float2half2_rn(0.0625f);
+    const __half2 km64 = __float2half2_rn(-64.0f);
+    lo01 = __hsub2(dq_u2h2((p01 & 0x000F000Fu) | ((h01 << 4) & 0x00100010u) | 0x64006400u), k1024);
+    lo23 = __hsub2(dq_u2h2((p23 & 0x000F000Fu) | ((h23 << 4) & 0x00100010u) | 0x64006400u), k1024);
+    hi01 = __hfma2(dq_u2h2((p01 & 0x00F000F0u) | ((h01 << 7) & 0x01000100u) | 0x64006400u), k16th, km64);
+    hi23 = __hfma2(dq_u2h2((p23 & 0x00F000F0u) | ((h23 << 7) & 0x01000100u) | 0x64006400u), k16th, km64);
+}
+
+// One word of Q5_K quants (4-bit parts w, fifth bits hb as nibbles5_to_q) of
+// the sub-block pair -> 8 fp16 weights, laid out as q4k_word_f16's.  The
+// header (d, dmin, scales) is Q4_K's: q4k_pair_scales_h gives S and NZ.
+__device__ __forceinline__ void q5k_word_f16(uint32_t w, uint32_t hb, __half2 S_lo, __half2 NZ_lo, __half2 S_hi,
+                                             __half2 NZ_hi, uint32_t (&out)[4])
+{
+    __half2 l01, l23, h01, h23;
+    nibbles5_to_q(w, hb, l01, l23, h01, h23);
     out[0] = dq_h22u(__hfma2(l01, S_lo, NZ_lo));
     out[1] = dq_h22u(__hfma2(l23, S_lo, NZ_lo));
     out[2] = dq_h22u(__hfma2(h01, S_hi, NZ_hi));

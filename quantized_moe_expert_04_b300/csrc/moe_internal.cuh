@@ -16,6 +16,7 @@ namespace moe {
 // ---- tensors in the DeepSeek-V4-Flash GGUF anatomy table, section 二)
 constexpr int kQK = 256;          // weights per Q4_K super-block
 constexpr int kQ4KBytes = 144;    // fp16 d, fp16 dmin, scales[12], qs[128]
+constexpr int kQ5KBytes = 176;    // fp16 d, fp16 dmin, scales[12], qh[32], qs[128]
 constexpr int kQK8 = 32;          // weights per Q8_0 block
 constexpr int kQ8Bytes = 34;      // fp16 d, int8 qs[32]
 
@@ -84,6 +85,7 @@ bool use_gemv(const moe_config &c, int32_t T);
 WsLayout ws_layout(const moe_config &c, int32_t T);
 
 // ---- launchers (each returns cudaGetLastError() of its launches) ----------
+cudaError_t launch_pack_q5k(const float *w, int64_t nblocks, uint8_t *out, uint32_t *status, cudaStream_t s);
 cudaError_t launch_pack_q4k(const float *w, int64_t nblocks, uint8_t *out, uint32_t *status,
                             cudaStream_t s);
 cudaError_t launch_pack_q8_0(const float *w, int64_t nblocks, uint8_t *out, uint32_t *status,
@@ -91,6 +93,8 @@ cudaError_t launch_pack_q8_0(const float *w, int64_t nblocks, uint8_t *out, uint
 cudaError_t launch_dequant_q4k(const uint8_t *blk, int64_t nblocks, float *out, cudaStream_t s);
 cudaError_t launch_dequant_q8_0(const uint8_t *blk, int64_t nblocks, float *out, cudaStream_t s);
 cudaError_t launch_dequant_q4k_f16(const uint8_t *blk, int64_t nblocks, uint16_t *out, cudaStream_t s);
+cudaError_t launch_dequant_q5k(const uint8_t *blk, int64_t nblocks, float *out, cudaStream_t s);
+cudaError_t launch_dequant_q5k_f16(const uint8_t *blk, int64_t nblocks, uint16_t *out, cudaStream_t s);
 cudaError_t launch_dequant_q8_0_f16(const uint8_t *blk, int64_t nblocks, uint16_t *out, cudaStream_t s);
 
 struct RouteArgs {
@@ -137,6 +141,7 @@ struct DecArgs {
     int route_parts;             // router row split per CTA (1, 2, 4 or 8)
     int nc;                      // consumer warps of the layer kernel
     int half;                    // they own 128 columns each (else 256)
+    int codec;                   // routed experts' blocks (moe_codec); Q5_K: 256-column warps
     uint32_t ring_bytes;         // their staging rings
     int stages;                  // stages of each consumer warp's ring
     int overlap_prev;            // weights may be read before the previous kernel ends

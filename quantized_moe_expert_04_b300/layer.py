@@ -1,8 +1,8 @@
 """Device-resident layer state for the C ABI: packed experts, router, workspace.
 
 Plumbing around the binding: the fp32 expert weights come from the seeded
-generators in ``synth`` and are packed on the GPU by ``moe_pack_q4k`` /
-``moe_pack_q8_0``; the pointer table, the router tensors and the workspace are
+generators in ``synth`` and are packed on the GPU by ``moe_pack_q4k`` (or
+``moe_pack_q5k``) / ``moe_pack_q8_0``; the pointer table, the router tensors and the workspace are
 plain torch allocations.  No arithmetic of the layer happens here.
 """
 from dataclasses import dataclass
@@ -40,9 +40,10 @@ def pack_layer(wl: synth.Workload, seed: int = 0, layer: int = 0, gen_device: st
     assert nbytes == wl.blob_bytes
     blobs = torch.zeros(wl.n_experts, nbytes, dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pack = moe.moe_pack_q5k if wl.codec == moe.MOE_CODEC_Q5K else moe.moe_pack_q4k
     for e in (range(wl.n_experts) if experts is None else experts):
         w = synth.expert_weight(wl, e, seed, layer, device=gen_device).to(dev)
-        moe.moe_pack_q4k(w.reshape(3 * wl.ff, wl.hidden), blobs[e], status)
+        pack(w.reshape(3 * wl.ff, wl.hidden), blobs[e], status)
     shared = None
     if wl.has_shared:
         sw = synth.shared_weight(wl, seed, layer, device=gen_device).to(dev)

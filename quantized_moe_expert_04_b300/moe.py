@@ -27,18 +27,22 @@ MOE_ERR_DEVICE_FAULT = 7
 MOE_SCORE_SOFTMAX = 0
 MOE_SCORE_SIGMOID_BIAS = 1
 
+MOE_CODEC_Q4K = 0
+MOE_CODEC_Q5K = 1
+
 MOE_FLAG_DETERMINISTIC = 1
 MOE_FLAG_FORCE_GEMV = 2
 MOE_FLAG_FORCE_GEMM = 4
 MOE_FLAG_STATIC_WEIGHTS = 8
 
 EXPORTS = (
-    "moe_q4k_bytes", "moe_q8_0_bytes", "moe_expert_bytes", "moe_shared_bytes",
-    "moe_pack_q4k", "moe_pack_q8_0", "moe_dequant_q4k", "moe_dequant_q8_0",
+    "moe_q4k_bytes", "moe_q5k_bytes", "moe_q8_0_bytes", "moe_expert_bytes", "moe_shared_bytes",
+    "moe_pack_q4k", "moe_pack_q5k", "moe_pack_q8_0", "moe_dequant_q4k", "moe_dequant_q8_0",
     "moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_forward",
     "moe_workspace_routing", "moe_last_device_status", "moe_status_string",
     "moe_profile_enable", "moe_profile_read", "moe_forward_static_ws",
     "moe_dequant_q4k_f16", "moe_dequant_q8_0_f16", "moe_debug_set",
+    "moe_dequant_q5k", "moe_dequant_q5k_f16",
     "moe_cache_create", "moe_cache_destroy", "moe_cache_plan", "moe_cache_issue", "moe_cache_poll",
     "moe_cache_stats", "moe_host_address",
 )
@@ -63,16 +67,17 @@ class MoeError(RuntimeError):
 class moe_config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32), ("ff", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("score_fn", ctypes.c_int32), ("shared_ff", ctypes.c_int32),
-                ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32), ("codec", ctypes.c_int32)]
 
 
-def make_config(hidden, n_experts, ff, top_k, score_fn=MOE_SCORE_SOFTMAX, shared_ff=0, flags=0) -> moe_config:
-    return moe_config(hidden, n_experts, ff, top_k, score_fn, shared_ff, flags, 0)
+def make_config(hidden, n_experts, ff, top_k, score_fn=MOE_SCORE_SOFTMAX, shared_ff=0, flags=0,
+                codec=MOE_CODEC_Q4K) -> moe_config:
+    return moe_config(hidden, n_experts, ff, top_k, score_fn, shared_ff, flags, codec)
 
 
 def config_for(wl, flags: int = 0) -> moe_config:
     """moe_config of a synthetic workload (quantized_moe_expert_04_b300.synth.Workload)."""
-    return make_config(wl.hidden, wl.n_experts, wl.ff, wl.top_k, wl.score_fn, wl.shared_ff, flags)
+    return make_config(wl.hidden, wl.n_experts, wl.ff, wl.top_k, wl.score_fn, wl.shared_ff, flags, wl.codec)
 
 
 _lib = None
@@ -93,14 +98,18 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         sig = {
             "moe_q4k_bytes": (_SZ, [_I64, _I64]),
+            "moe_q5k_bytes": (_SZ, [_I64, _I64]),
             "moe_q8_0_bytes": (_SZ, [_I64, _I64]),
             "moe_expert_bytes": (_SZ, [_CFG]),
             "moe_shared_bytes": (_SZ, [_CFG]),
             "moe_pack_q4k": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
+            "moe_pack_q5k": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
             "moe_pack_q8_0": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
             "moe_dequant_q4k": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
             "moe_dequant_q8_0": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
             "moe_dequant_q4k_f16": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
+            "moe_dequant_q5k": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
+            "moe_dequant_q5k_f16": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
             "moe_dequant_q8_0_f16": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
             "moe_workspace_bytes": (_SZ, [_CFG, _I32]),
             "moe_workspace_init": (ctypes.c_int, [_P, _SZ, _P]),
@@ -171,6 +180,10 @@ def moe_q4k_bytes(rows: int, cols: int) -> int:
     return int(lib().moe_q4k_bytes(rows, cols))
 
 
+def moe_q5k_bytes(rows: int, cols: int) -> int:
+    return int(lib().moe_q5k_bytes(rows, cols))
+
+
 def moe_q8_0_bytes(rows: int, cols: int) -> int:
     return int(lib().moe_q8_0_bytes(rows, cols))
 
@@ -197,6 +210,14 @@ def moe_pack_q4k(w: torch.Tensor, out: torch.Tensor, dev_status: Optional[torch.
     return out
 
 
+def moe_pack_q5k(w: torch.Tensor, out: torch.Tensor, dev_status: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    assert w.dtype == torch.float32 and w.dim() == 2 and out.dtype == torch.uint8
+    _check(lib().moe_pack_q5k(_ptr(w), w.shape[0], w.shape[1], _ptr(out), _ptr(dev_status), _stream(stream)),
+           "moe_pack_q5k")
+    return out
+
+
 def moe_pack_q8_0(w: torch.Tensor, out: torch.Tensor, dev_status: Optional[torch.Tensor] = None,
                   stream=None) -> torch.Tensor:
     assert w.dtype == torch.float32 and w.dim() == 2 and out.dtype == torch.uint8
@@ -208,6 +229,19 @@ def moe_pack_q8_0(w: torch.Tensor, out: torch.Tensor, dev_status: Optional[torch
 def moe_dequant_q4k(blocks: torch.Tensor, rows: int, cols: int, out: torch.Tensor, stream=None) -> torch.Tensor:
     assert out.dtype == torch.float32 and out.numel() == rows * cols
     _check(lib().moe_dequant_q4k(_ptr(blocks), rows, cols, _ptr(out), _stream(stream)), "moe_dequant_q4k")
+    return out
+
+
+def moe_dequant_q5k(blocks: torch.Tensor, rows: int, cols: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    assert out.dtype == torch.float32 and out.numel() == rows * cols
+    _check(lib().moe_dequant_q5k(_ptr(blocks), rows, cols, _ptr(out), _stream(stream)), "moe_dequant_q5k")
+    return out
+
+
+def moe_dequant_q5k_f16(blocks: torch.Tensor, rows: int, cols: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """fp16 operand weights (bit patterns in an int16/uint16 tensor) of a Q5_K matrix."""
+    assert out.element_size() == 2 and out.numel() == rows * cols
+    _check(lib().moe_dequant_q5k_f16(_ptr(blocks), rows, cols, _ptr(out), _stream(stream)), "moe_dequant_q5k_f16")
     return out
 
 

@@ -54,6 +54,7 @@ class Workload:
     bias: str               # "none" | "normal" | "zipf"
     layers: int             # distinct layers the benchmark rotates through
     tokens: Tuple[int, ...] = field(default=(1,))
+    codec: int = 0          # routed experts' blocks: 0 Q4_K, 1 Q5_K
 
     @property
     def has_shared(self) -> bool:
@@ -61,8 +62,9 @@ class Workload:
 
     @property
     def blob_bytes(self) -> int:
-        """Bytes of one routed expert: 3 Q4_K matrices [FF][H] (144 B / 256 weights)."""
-        return 3 * self.ff * (self.hidden // 256) * 144
+        """Bytes of one routed expert: 3 Q4_K matrices [FF][H] (144 B / 256 weights;
+        Q5_K 176 B)."""
+        return 3 * self.ff * (self.hidden // 256) * (176 if self.codec == 1 else 144)
 
     @property
     def shared_blob_bytes(self) -> int:
@@ -78,6 +80,10 @@ WORKLOADS = {
     "qwen_prefill": Workload("qwen_prefill", 2560, 512, 320, 10, SOFTMAX, 0, "none", 4, (4096,)),
     "deepseek_prefill_skewed": Workload("deepseek_prefill_skewed", 4096, 256, 2048, 6,
                                         SIGMOID_BIAS, 2048, "zipf", 2, (4096,)),
+    # the decode shapes with Q5_K routed experts (a codec of the same GGUF family)
+    "qwen_decode_q5k": Workload("qwen_decode_q5k", 2560, 512, 320, 10, SOFTMAX, 0, "none", 48, (3,), 1),
+    "deepseek_decode_q5k": Workload("deepseek_decode_q5k", 4096, 256, 2048, 6, SIGMOID_BIAS, 2048,
+                                    "normal", 8, (8,), 1),
 }
 
 

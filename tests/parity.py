@@ -83,11 +83,12 @@ def oracle_inputs(wl, T, seed=0, layer=0, gen_device="cpu", experts=None, x=None
 
 
 def oracle_blobs(wl, expert_ids, seed=0, layer=0, gen_device="cpu"):
-    """The oracle's own Q4_K blobs (its quantiser) for the listed experts; None elsewhere."""
+    """The oracle's own blobs (its quantiser, the workload's codec) for the listed
+    experts; None elsewhere."""
     blobs = [None] * wl.n_experts
     for e in sorted(set(int(i) for i in expert_ids)):
         w = synth.expert_weight(wl, e, seed, layer, device=gen_device).cpu().numpy()
-        blobs[e] = oracle.pack_expert_q4k(w)
+        blobs[e] = oracle.pack_expert(w, wl.codec)
     sblob = None
     if wl.has_shared:
         sblob = oracle.pack_shared_q8_0(synth.shared_weight(wl, seed, layer, device=gen_device).cpu().numpy())
@@ -96,4 +97,4 @@ def oracle_blobs(wl, expert_ids, seed=0, layer=0, gen_device="cpu"):
 
 def oracle_forward(wl, xb, wr, b, blobs, sblob, forced=None):
     return oracle.moe_forward(wl.hidden, wl.n_experts, wl.ff, wl.top_k, wl.score_fn, xb, wr, b, blobs,
-                              wl.shared_ff, sblob, forced_ids=forced)
+                              wl.shared_ff, sblob, forced_ids=forced, codec=wl.codec)

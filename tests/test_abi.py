@@ -45,6 +45,13 @@ def test_sizes():
     assert moe.moe_workspace_bytes(moe.make_config(2500, 512, 320, 10), 5) == 0     # H % 256
     assert moe.moe_workspace_bytes(moe.make_config(2560, 512, 300, 10), 5) == 0     # FF % 64
     assert moe.moe_workspace_bytes(moe.make_config(256, 4, 64, 5), 5) == 0          # k > E
+    # Q5_K experts: 176 bytes a 256-weight block
+    assert moe.moe_q5k_bytes(320, 2560) == 320 * 10 * 176
+    assert moe.moe_q5k_bytes(1, 255) == 0
+    qwen5 = moe.make_config(2560, 512, 320, 10, codec=moe.MOE_CODEC_Q5K)
+    assert moe.moe_expert_bytes(qwen5) == 3 * 320 * 10 * 176
+    assert moe.moe_expert_bytes(moe.make_config(2560, 512, 320, 10, codec=2)) == 0    # unknown codec
+    assert moe.moe_workspace_bytes(moe.make_config(2560, 512, 320, 10, codec=-1), 5) == 0
 
 
 def test_host_checks_reject_before_launch():
@@ -73,6 +80,20 @@ def test_host_checks_reject_before_launch():
     need_ds = moe.moe_workspace_bytes(ds, 4)
     assert L.moe_forward(ctypes.byref(ds), p, p, None, p, None, 4, p, None, p, need_ds,
                          None) == moe.MOE_ERR_INVALID_ARG     # shared expert without its blob
+    # unknown codec; Q5_K experts off the decode path (a window above 8 tokens, or
+    # the tensor-core path forced)
+    bad_codec = moe.make_config(256, 16, 128, 2, codec=3)
+    assert L.moe_forward(ctypes.byref(bad_codec), p, p, None, p, None, 4, p, None, p, need,
+                         None) == moe.MOE_ERR_INVALID_ARG
+    q5 = moe.make_config(256, 16, 128, 2, codec=moe.MOE_CODEC_Q5K)
+    need40 = moe.moe_workspace_bytes(q5, 40)
+    assert L.moe_forward(ctypes.byref(q5), p, p, None, p, None, 40, p, None, p, need40,
+                         None) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    q5g = moe.make_config(256, 16, 128, 2, flags=moe.MOE_FLAG_FORCE_GEMM, codec=moe.MOE_CODEC_Q5K)
+    assert L.moe_forward(ctypes.byref(q5g), p, p, None, p, None, 4, p, None, p, moe.moe_workspace_bytes(q5g, 4),
+                         None) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_pack_q5k(p, 4, 100, p, None, None) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_pack_q5k(ctypes.c_void_p(4100), 4, 256, p, None, None) == moe.MOE_ERR_MISALIGNED
     # T = 0 is a no-op success
     assert L.moe_forward(ctypes.byref(cfg), None, None, None, None, None, 0, None, None, p, need, None) == 0
 

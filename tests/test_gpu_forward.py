@@ -32,6 +32,14 @@ SMALL = [
     (sv(W["deepseek_decode"], name="ds_small", hidden=1024, n_experts=32, ff=512, shared_ff=512), 8),
     (sv(W["deepseek_prefill_skewed"], name="ds_skew_small", hidden=1024, n_experts=32, ff=256, shared_ff=256), 77),
     (sv(W["qwen_prefill"], name="qwen_e64_prefill", n_experts=64), 200),
+    # Q5_K routed experts (the decode path)
+    (sv(W["qwen_decode"], name="qwen_e64_q5k", n_experts=64, codec=1), 1),
+    (sv(W["qwen_decode"], name="qwen_e64_q5k", n_experts=64, codec=1), 3),
+    (sv(W["qwen_decode"], name="qwen_e64_q5k", n_experts=64, codec=1), 8),
+    (sv(W["qwen_decode"], name="qwen_e8_k4_q5k", n_experts=8, top_k=4, codec=1), 8),
+    (sv(W["deepseek_decode"], name="ds_small_q5k", hidden=1024, n_experts=32, ff=512, shared_ff=512, codec=1), 1),
+    (sv(W["deepseek_decode"], name="ds_small_q5k", hidden=1024, n_experts=32, ff=512, shared_ff=512, codec=1), 4),
+    (sv(W["deepseek_decode"], name="ds_small_q5k", hidden=1024, n_experts=32, ff=512, shared_ff=512, codec=1), 8),
 ]
 
 
@@ -171,6 +179,8 @@ FULL = [
     (W["deepseek_decode"], 1, None), (W["deepseek_decode"], 4, None), (W["deepseek_decode"], 8, None),
     (W["qwen_prefill"], 4096, None),                    # every token (the oracle takes ~15 s)
     (W["deepseek_prefill_skewed"], 4096, "tiles"),      # every GEMM tile position
+    (sv(W["qwen_decode"], name="qwen_decode_q5k", codec=1), 3, None),
+    (sv(W["deepseek_decode"], name="deepseek_decode_q5k", codec=1), 8, None),
 ]
 
 

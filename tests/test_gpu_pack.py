@@ -71,6 +71,53 @@ def test_pack_q4k_handmade_block():
     assert torch.equal(deq.cpu().view(-1), x)
 
 
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("rows,cols", [(1, 256), (37, 2560), (130, 4096)])
+def test_pack_q5k_bit_exact(kind, rows, cols):
+    """Q5_K: the device quantiser's bytes equal the oracle's; the fp32 and the
+    fp16 operand dequantisation (the decode kernel's device functions) equal
+    the oracle's bit for bit."""
+    w = _inputs(kind, rows, cols, seed=7 * rows + cols)
+    ref = oracle.q5k_quantize(w.numpy())
+    out = torch.zeros(moe.moe_q5k_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_pack_q5k(w.cuda(), out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = out.cpu().numpy().reshape(ref.shape)
+    assert np.array_equal(got, ref), "first differing byte at %s" % (np.argwhere(got != ref)[:3],)
+    deq = torch.empty(rows, cols, dtype=torch.float32, device="cuda")
+    moe.moe_dequant_q5k(out, rows, cols, deq)
+    refd = oracle.q5k_dequantize(ref, rows, cols)
+    assert np.array_equal(deq.cpu().numpy().view(np.uint32), refd.view(np.uint32))
+    h = torch.empty(rows, cols, dtype=torch.int16, device="cuda")
+    moe.moe_dequant_q5k_f16(out, rows, cols, h)
+    bad = np.argwhere(h.cpu().numpy().view(np.uint16) != oracle.q5k_dequantize_f16(ref, rows, cols))
+    assert bad.size == 0, "first differing fp16 weights at %s" % (bad[:3],)
+
+
+def test_pack_q5k_uses_the_fifth_bit():
+    """A ramp over 0..31 steps per sub-block: the quants span all 32 levels, so
+    every qh bit position is exercised both ways."""
+    j = np.arange(256)
+    x = ((j % 32) * (1 + j // 32) / 64.0 - 0.25).astype(np.float32).reshape(1, 256)
+    ref = oracle.q5k_quantize(x)
+    assert ref[0, 16:48].min() == 0 and ref[0, 16:48].max() == 255
+    out = torch.zeros(176, dtype=torch.uint8, device="cuda")
+    moe.moe_pack_q5k(torch.from_numpy(x).cuda(), out)
+    assert np.array_equal(out.cpu().numpy(), ref.reshape(-1))
+
+
+@pytest.mark.parametrize("bad", [float("nan"), float("inf")])
+def test_pack_q5k_flags_bad_input(bad):
+    w = torch.zeros(2, 512, dtype=torch.float32)
+    w[1, 300] = bad
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.zeros(moe.moe_q5k_bytes(2, 512), dtype=torch.uint8, device="cuda")
+    moe.moe_pack_q5k(w.cuda(), out, st)
+    assert int(st.item()) == moe.MOE_ERR_DEVICE_FAULT
+
+
 @pytest.mark.parametrize("kind", ["normal", "wide", "sparse", "ties"])
 def test_pack_q8_0_bit_exact(kind):
     rows, cols = 33, 4096

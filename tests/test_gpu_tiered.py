@@ -25,8 +25,12 @@ def _oracle_y(wl, T, x):
     return oracle_forward(wl, xb, wr, b, blobs, sblob)
 
 
-@pytest.mark.parametrize("wl,T,n_slots", [(QWEN_E64, 3, 40), (QWEN_E64, 5, 0), (DS_SMALL, 4, 10)],
-                         ids=["qwen_e64-slots40", "qwen_e64-host-only", "ds_small-slots10"])
+QWEN_E64_Q5K = synth.small_variant(QWEN_E64, name="qwen_e64_q5k", codec=1)
+
+
+@pytest.mark.parametrize("wl,T,n_slots", [(QWEN_E64, 3, 40), (QWEN_E64, 5, 0), (DS_SMALL, 4, 10),
+                                          (QWEN_E64_Q5K, 3, 30)],
+                         ids=["qwen_e64-slots40", "qwen_e64-host-only", "ds_small-slots10", "qwen_e64_q5k-slots30"])
 def test_tiered_layer_matches_the_oracle_and_fills_its_cache(wl, T, n_slots):
     pl = pack_layer(wl, gen_device="cpu")
     tl = TieredLayer(pl, n_slots)
