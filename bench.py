@@ -38,7 +38,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from quantized_moe_expert_04_b300 import moe, synth  # noqa: E402
-from quantized_moe_expert_04_b300.layer import TieredLayer, pack_layer, routing_views, workspace  # noqa: E402
+from quantized_moe_expert_04_b300.layer import (LayerStack, TieredLayer, pack_layer, routing_views,  # noqa: E402
+                                                workspace)
 
 DEFAULT_TOKENS = {"tiny": 4, "qwen_decode": 3, "deepseek_decode": 4, "qwen_prefill": 4096,
                   "deepseek_prefill_skewed": 4096, "qwen_decode_q5k": 3, "deepseek_decode_q5k": 8}
@@ -338,6 +339,7 @@ def profiled_traffic(kernel, workload, T):
 # The five workloads: the headline (the Qwen-shaped MTP window of 3 tokens)
 # plus every other window size and the two prefill batches, each measured in
 # the same process after the headline.
+STACK_SET = [("qwen_decode", 3), ("qwen_decode", 1), ("deepseek_decode", 8)]
 CONFIG_SET = [("qwen_decode", 1), ("qwen_decode", 3), ("qwen_decode", 5), ("deepseek_decode", 1),
               ("deepseek_decode", 4), ("deepseek_decode", 8), ("qwen_prefill", 4096),
               ("deepseek_prefill_skewed", 4096), ("qwen_decode_q5k", 3), ("deepseek_decode_q5k", 8)]
@@ -520,6 +522,103 @@ def measure(args, wl, T, nL, world, rank, local, K=None, soak_s=0.0, target_s=0.
     return out
 
 
+def measure_stack(args, wl, T, nL, world, rank, local, target_s=1.0, cpu_budget=None, parity_layers=2,
+                  layers=None):
+    """The window through all nL layers in one launch (moe_forward_stack), every
+    layer reading its own seeded input (the inputs of measure(): the two lines
+    are the same work), layer l + 1 after layer l has finished.  (The residual
+    stream of moe_forward_stack has no normalisation between layers: on the
+    DeepSeek shapes it leaves the fp16 range within a few layers, so it is
+    tested, not benchmarked.)  A step is one call: an 8-byte memset of the grid
+    barrier words and the cooperative kernel.  Timing, clocks and roofline as
+    measure(); the routing of every layer, for the byte counts, comes from
+    moe_route on the same inputs."""
+    dev = torch.device("cuda", local)
+    t_setup = time.time()
+    if layers is None:
+        layers = [pack_layer(wl, 0, l, gen_device="cuda") for l in range(nL)]
+    st = LayerStack(layers)
+    cfg = moe.config_for(wl)
+    ws = workspace(cfg, T)
+    x = torch.stack([synth.hidden_states(wl, T, 0, l, device="cuda") for l in range(nL)]).contiguous()
+    y = torch.empty(nL, T, wl.hidden, dtype=torch.bfloat16, device=dev)
+    y32 = torch.empty(nL, T, wl.hidden, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    setup_s = time.time() - t_setup
+
+    def step(yf=None):
+        moe.moe_forward_stack(cfg, nL, x, st.router_w, st.router_bias, st.blobs, st.shared, T, y, yf, ws, stream)
+
+    with torch.cuda.stream(stream):
+        step(y32)
+    status = moe.moe_last_device_status(ws, stream)
+    if status != moe.MOE_OK:
+        raise moe.MoeError(status, "device status of the layer stack (%s T=%d)" % (wl.name, T))
+    # every layer's routing on the kernel's own inputs (the library's router, one call a layer)
+    rcfg = moe.config_for(wl, moe.MOE_FLAG_FORCE_GEMM)
+    rws = workspace(rcfg, T)
+    ids_per_layer = []
+    rid = torch.empty(T, wl.top_k, dtype=torch.int32, device=dev)
+    rw = torch.empty(T, wl.top_k, dtype=torch.float32, device=dev)
+    roff = torch.empty(wl.n_experts + 1, dtype=torch.int32, device=dev)
+    ras = torch.empty(T * wl.top_k, dtype=torch.int32, device=dev)
+    for l in range(nL):
+        moe.moe_route(rcfg, x[l], layers[l].router_w, layers[l].router_bias, T, rid, rw, roff, ras, rws)
+        ids_per_layer.append(rid.cpu().numpy().copy())
+    gpu_y32 = {l: y32[l].cpu().numpy() for l in range(min(parity_layers, nL))}
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    per = (time.perf_counter() - t0) / 3
+    K = int(max(10, min(20000, target_s / max(per, 1e-7))))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(K):
+                step()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = all_max(ev0.elapsed_time(ev1), world)
+    step_ms = ms / K
+    pk = peaks()
+    step_bytes, _, _, _ = algorithmic(wl, T, ids_per_layer)
+    launch_bytes = step_bytes * nL
+    achieved = launch_bytes / (step_ms / 1e3) / 1e9
+    out = {"workload": wl.name, "tokens_per_window": T, "distinct_layers": nL,
+           "value": round(T * nL * K * world / (ms / 1e3), 2), "unit": UNIT, "steps": K,
+           "ms_per_step": round(step_ms, 5), "us_per_layer": round(step_ms * 1e3 / nL, 3),
+           "setup_s": round(setup_s, 1), "clocks": clk.summary(), "timed_region_s": round(ms / 1e3, 3),
+           "hbm": {"algorithmic_bytes_per_call": int(step_bytes),
+                   "gbs": round(achieved, 1), "frac": round(achieved / pk["hbm_gbs"], 4)},
+           "roofline": {"bound": "hbm", "kernel": "dec_stack", "achieved": round(achieved, 1),
+                        "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                        "traffic": profiled_traffic("dec_stack", wl.name, T),
+                        "peak_source": pk["source"] + " (burst copy)",
+                        "avg_launch_us": round(step_ms * 1e3, 3), "algorithmic_bytes_per_launch": int(launch_bytes)},
+           "gpu_launches": K, "inputs": "each layer's own seeded x (the per-layer calls' inputs)"}
+    if rank == 0 and cpu_budget is not None:
+        xs = [x[l] for l in range(nL)]
+        v, threads, desc, parity = oracle_sample(wl, T, list(range(min(parity_layers, nL))), xs,
+                                                 gpu_ids=ids_per_layer, gpu_y32=gpu_y32,
+                                                 time_budget_s=cpu_budget, wall_budget_s=4 * cpu_budget + 10)
+        out["cpu_baseline"] = {"value": round(v, 3), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+        out["parity"] = parity
+    del layers, st, ws, rws, x, y, y32
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_tiered(wl, T, nL, n_slots, windows):
     """Host tier of the experts: every expert of nL layers in pinned host memory,
     a device cache of n_slots per layer.  Each decode step runs the nL layer
@@ -565,6 +664,14 @@ def measure_tiered(wl, T, nL, n_slots, windows):
 
 def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
+    if args.stack_only:
+        wl = synth.WORKLOADS[args.workload or "qwen_decode"]
+        T = args.tokens or DEFAULT_TOKENS[wl.name]
+        r = measure_stack(args, wl, T, wl.layers if args.layers is None else args.layers, world, rank, local,
+                          cpu_budget=None if args.no_cpu_baseline else min(args.cpu_budget, 4.0))
+        if rank == 0:
+            print(json.dumps({"stack": r}), flush=True)
+        return
     wl = synth.WORKLOADS[args.workload or "qwen_decode"]
     T = args.tokens or DEFAULT_TOKENS[wl.name]
     nL = wl.layers if args.layers is None else args.layers
@@ -606,6 +713,19 @@ def run_ours(args, world, rank, local):
         out["configs"] = confs
         # host tier of the experts (decode windows): 4 layers, a quarter of each layer's experts cached
         out["tiered"] = measure_tiered(synth.WORKLOADS["qwen_decode"], 3, 4, 128, 20)
+        # the window through each decode workload's whole layer stack in one launch
+        packed = {}
+        out["stack"] = []
+        for name, Tc in STACK_SET:
+            wls = synth.WORKLOADS[name]
+            if name not in packed:
+                packed.clear()
+                torch.cuda.empty_cache()
+                packed[name] = [pack_layer(wls, 0, l, gen_device="cuda") for l in range(wls.layers)]
+            out["stack"].append(measure_stack(args, wls, Tc, wls.layers, world, rank, local,
+                                              cpu_budget=None if cpu is None else min(cpu, 4.0),
+                                              layers=packed[name]))
+        packed.clear()
     if rank == 0:
         print(json.dumps(out), flush=True)
 
@@ -670,6 +790,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default=None,
                     help="one workload only (default: the qwen_decode T=3 headline, then every config)")
     ap.add_argument("--tokens", type=int, default=None)
+    ap.add_argument("--stack-only", action="store_true",
+                    help="only the one-launch layer stack of --workload (default qwen_decode) at --tokens")
     ap.add_argument("--layers", type=int, default=None)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--cpu-tokens", type=int, default=16)

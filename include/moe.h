@@ -93,13 +93,15 @@ enum {
                                         order on every path (bit-identical reruns)        */
     MOE_FLAG_FORCE_GEMV = 2,         /* use the decode (grouped GEMV) path; T <= 8 only  */
     MOE_FLAG_FORCE_GEMM = 4,         /* use the prefill (tensor-core GEMM) path at any T */
-    MOE_FLAG_STATIC_WEIGHTS = 8      /* the caller guarantees that router_w, router_bias,
+    MOE_FLAG_STATIC_WEIGHTS = 8,     /* the caller guarantees that router_w, router_bias,
                                         the expert table and the expert blobs are not
                                         written by the work enqueued just before this call
                                         on the stream: a decode call may then start
                                         reading the router rows and the expert table
                                         while that work is still running (its other
                                         inputs are read only after it has finished)     */
+    MOE_FLAG_RESIDUAL = 16           /* moe_forward_stack: the layers' inputs form a
+                                        residual stream (see there)                      */
 };
 
 /* Block format of the routed experts (the shared expert is always Q8_0).
@@ -371,6 +373,52 @@ MOE_API moe_status moe_forward_static_ws(const moe_config *cfg, const uint16_t *
                                          const uint8_t *shared_blob, int32_t T, uint16_t *y, float *y_f32,
                                          uint32_t *dev_status, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- layer stack */
+
+/*
+ * One decode window through a stack of n_layers MoE layers in one launch:
+ * every layer computes what moe_forward computes on the decode path, with
+ * its own router, experts and shared expert, and the layers run in order --
+ * layer l + 1 reads its input only once y of layer l is complete.  One
+ * persistent CTA per SM (a cooperative launch: the call fails with
+ * MOE_ERR_CUDA if the GPU cannot hold them all at once) takes the layers one
+ * after the other with two grid-wide barriers each, instead of two kernels
+ * per layer.  The barriers' waits are bounded (MOE_ERR_TIMEOUT, see
+ * moe_debug_set).  This follows the verify-window forward of the teardown page
+ * ("Strata 引擎深度拆解", lcz.me/topic/2098/5, section 二 item 1: the 3-5
+ * drafted tokens verified in one forward; item 2: a window crosses the layer
+ * stack with one hand-off between the halves of the stack).
+ *
+ *   x      device bf16 [n_layers][T][hidden].  Without MOE_FLAG_RESIDUAL
+ *          every x[l] is an input.  With it only x[0] is read, and the call
+ *          writes the residual stream x[l + 1] = bf16(x[l] + y[l]) (the fp32
+ *          sum of the two bf16 values, rounded to nearest even once) for
+ *          l + 1 < n_layers.
+ *   router_w      device array of n_layers device pointers, each to a
+ *                 16-byte aligned [E][H] fp32 matrix.
+ *   router_bias   device array of n_layers pointers ([E] fp32), or NULL; read
+ *                 for MOE_SCORE_SIGMOID_BIAS only.
+ *   expert_blobs  device array [n_layers][n_experts] of blob pointers (as
+ *                 moe_forward's, layer after layer; blobs in device memory).
+ *   shared_blobs  device array of n_layers 16-byte aligned shared-expert
+ *                 blobs when cfg->shared_ff > 0, else ignored.
+ *   The pointer arrays themselves must be 8-byte aligned (else
+ *   MOE_ERR_MISALIGNED); the pointers in them are not read on the host.
+ *   y      device bf16 [n_layers][T][hidden]; y_f32 optional fp32, same shape.
+ *   ws     as moe_forward's (moe_workspace_bytes(cfg, T)); its routing views
+ *          hold the last layer's routing afterwards.
+ * T in 1..8 with a configuration the decode path runs (not
+ * MOE_FLAG_DETERMINISTIC or MOE_FLAG_FORCE_GEMM), and each CTA must hold
+ * ceil(n_experts / SMs) <= 8 router rows beside its staging ring; otherwise
+ * MOE_ERR_UNSUPPORTED_SHAPE.  n_layers == 0 or T == 0 is a no-op.  Host
+ * checks as moe_forward; nothing is enqueued when one fails.
+ */
+MOE_API moe_status moe_forward_stack(const moe_config *cfg, int32_t n_layers, uint16_t *x,
+                                     const float *const *router_w, const float *const *router_bias,
+                                     const uint8_t *const *expert_blobs, const uint8_t *const *shared_blobs,
+                                     int32_t T, uint16_t *y, float *y_f32, void *ws, size_t ws_bytes,
+                                     moe_stream_t stream);
+
 /* ---------------------------------------------------------------- diagnostics */
 
 /*
@@ -402,7 +450,8 @@ MOE_API int32_t moe_profile_read(moe_profile_entry *out, int32_t max_entries);
  *                          waits for -- on the decode path the layer kernel's
  *                          copy of the window's x fragments and logits, on the
  *                          tensor-core path the routed gate/up kernel's first
- *                          token-row copy -- so that wait runs out: the call
+ *                          token-row copy; in moe_forward_stack that CTA never
+ *                          arrives at the first grid-wide barrier -- so that wait runs out: the call
  *                          then ends with MOE_ERR_TIMEOUT in its status word
  *                          (the context stays usable; a value past the grid
  *                          does nothing).  -1 clears it.

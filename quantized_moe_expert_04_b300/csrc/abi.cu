@@ -63,7 +63,7 @@ WsLayout ws_layout(const moe_config &c, int32_t T)
     L.bhist = take((TK + kBucketItems - 1) / kBucketItems * E * 4);
     const bool gemv = use_gemv(c, T), det = (c.flags & MOE_FLAG_DETERMINISTIC) != 0;
     L.slots = take(det ? TK * H * 4 : 0);
-    L.yacc = take((size_t)T * H * 4);
+    L.yacc = take((size_t)T * H * 4 * (gemv ? 2 : 1));   // decode: two (the layer stack alternates them)
     L.xfrag = take(gemv ? (size_t)T * H * 2 : 0);
     L.xg = take(gemv ? 0 : TK * H * 2);
     L.x16 = take(gemv || !c.shared_ff ? 0 : (size_t)T * H * 2);
@@ -322,6 +322,65 @@ moe_status moe_route(const moe_config *cfg, const uint16_t *x, const float *rout
     return cuda_status(e);
 }
 
+
+moe_status moe_forward_stack(const moe_config *cfg, int32_t n_layers, uint16_t *x, const float *const *router_w,
+                             const float *const *router_bias, const uint8_t *const *expert_blobs,
+                             const uint8_t *const *shared_blobs, int32_t T, uint16_t *y, float *y_f32, void *ws,
+                             size_t ws_bytes, moe_stream_t stream)
+{
+    if (n_layers < 0 || T < 0) return MOE_ERR_INVALID_ARG;
+    // configuration, workspace and x as for one layer call (the router matrices come from a table here)
+    moe_status st = check_call(cfg, x, nullptr, nullptr, 0, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (n_layers == 0 || T == 0) return MOE_OK;
+    if (!x || !router_w || !y || !expert_blobs || (cfg->shared_ff > 0 && !shared_blobs)) return MOE_ERR_INVALID_ARG;
+    auto al8 = [](const void *p) { return ((uintptr_t)p & 7u) == 0; };
+    if (!aligned16(y) || (y_f32 && !aligned16(y_f32)) || !al8(router_w) || !al8(expert_blobs) ||
+        (router_bias && !al8(router_bias)) || (shared_blobs && !al8(shared_blobs)))
+        return MOE_ERR_MISALIGNED;
+    if (!use_gemv(*cfg, T) || !stack_supported(*cfg, T)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (ws_bytes < ws_layout(*cfg, T).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    const WsLayout L = ws_layout(*cfg, T);
+    char *base = (char *)ws;
+    RouteArgs r = route_args(cfg, x, nullptr, nullptr, T, ws);
+    StackArgs a{};
+    DecArgs &d = a.d;
+    d.H = cfg->hidden;
+    d.E = cfg->n_experts;
+    d.FF = cfg->ff;
+    d.k = cfg->top_k;
+    d.T = T;
+    d.SFF = cfg->shared_ff;
+    d.score_fn = cfg->score_fn;
+    d.route_parts = dec_route_parts(cfg->hidden);
+    d.nc = dec_consumers(*cfg);
+    d.half = dec_half(*cfg) ? 1 : 0;
+    d.codec = cfg->codec;
+    d.ring_bytes = dec_ring_bytes(*cfg, T);
+    d.stages = dec_stages(*cfg, T);
+    d.wait_cycles = debug_wait_cycles();
+    d.skip_cta = debug_take_skip_copy();
+    d.logits = r.logits;
+    d.ids = r.ids;
+    d.w = r.w;
+    d.counts = r.counts;
+    d.offsets = r.offsets;
+    d.assign = r.assign;
+    d.active = r.active;
+    d.header = r.header;
+    a.L = n_layers;
+    a.residual = (cfg->flags & MOE_FLAG_RESIDUAL) != 0;
+    a.rows = (cfg->n_experts + stack_grid() - 1) / stack_grid();
+    a.wr = router_w;
+    a.bias = cfg->score_fn == MOE_SCORE_SIGMOID_BIAS ? router_bias : nullptr;
+    a.blobs = expert_blobs;
+    a.shared = cfg->shared_ff > 0 ? shared_blobs : nullptr;
+    a.x = x;
+    a.y = y;
+    a.y_f32 = y_f32;
+    a.yacc = (float *)(base + L.yacc);
+    return cuda_status(launch_stack(a, (cudaStream_t)stream));
+}
 
 moe_status moe_forward(const moe_config *cfg, const uint16_t *x, const float *router_w,
                        const float *router_bias, const uint8_t *const *expert_blobs,

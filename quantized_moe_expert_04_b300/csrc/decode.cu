@@ -372,6 +372,7 @@ struct Units {
     int64_t nr, ns;          // unit counts
     int64_t br, bs;          // bytes of one unit (3 slabs)
     int rb, rbs;             // row bytes: routed (Q4_K or Q5_K), Q8_0 shared
+    const uint8_t *shared;   // the shared expert's blob, or null
 };
 
 __device__ __forceinline__ int64_t first_unit(const Units &u, int64_t byte)
@@ -409,7 +410,7 @@ __device__ __forceinline__ UnitInfo unit_info(const DecArgs &a, const Units &un,
         ui.u = -1;
         ui.rows = kSharedRows;
         ui.f0 = (i - (int)un.nr) * kSharedRows;
-        ui.blob = a.shared_blob;
+        ui.blob = un.shared;
         ui.fmt = 1;
         ui.ffm = a.SFF;
         ui.rowb = un.rbs;
@@ -506,20 +507,25 @@ __device__ __forceinline__ void copy_block(uint32_t dst, const uint8_t *src, int
 // 128-column warps, or Q5_K routed rows with 256-column warps.
 constexpr int kVarQ4K = 0, kVarHalf = 1, kVarQ5K = 2;
 
-// The layer kernel, S stages per consumer warp.  HALF: each consumer warp owns
-// 128 columns (half a Q4_K super-block) instead of 256, for twice the warps;
-// only for layers without a shared expert.  128 registers a thread at 256
-// columns (16 warps, 4 on each SM sub-partition, fit one SM), 96 at 128
-// columns (20 warps).  Q5: the routed rows are Q5_K blocks (the layout of
-// Q4_K's plus 32 bytes of fifth bits, qh, before the nibbles).
+// One layer of a window, in every CTA (the body of the layer kernel and of
+// the stack kernel): the routing of the window from the logits in shared
+// memory (the ring's first 4 T E bytes), then this CTA's share of the units,
+// whose down projections are added into yacc; CTA 0 publishes the routing to
+// the workspace when `publish` is set.  On entry the expert table
+// and the x fragments are in shared memory, the abort flag is settled, and
+// every thread that reads the logits has seen them land.  S stages per
+// consumer warp.  HALF: each consumer warp owns 128 columns (half a Q4_K
+// super-block) instead of 256, for twice the warps; only for layers without a
+// shared expert.  Q5: the routed rows are Q5_K blocks (the layout of Q4_K's
+// plus 32 bytes of fifth bits, qh, before the nibbles).
 template <int S, int V>
-__global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_layer(DecArgs a)
+__device__ __forceinline__ void dec_window(const DecArgs &a, uint8_t *smem, const float *bias,
+                                           const uint8_t *shared_blob, float *yacc, bool publish)
 {
     static_assert(S >= 4, "the lagging down projection keeps 3 stages busy");
     constexpr bool HALF = V == kVarHalf, Q5 = V == kVarQ5K;
     constexpr int PIECE = Q5 ? kPieceQ5K : kPieceQ4K;   // bytes of a routed row's 256-column block
     constexpr int QS = Q5 ? 48 : 16;                     // offset of its nibbles
-    extern __shared__ __align__(128) uint8_t smem[];
     const int T = a.T, H = a.H, E = a.E, k = a.k, nb = H / 256, NC = a.nc;
     const LayerSmem L = layer_smem(E, T, H, NC, a.ring_bytes);
     const uint8_t **s_tab = reinterpret_cast<const uint8_t **>(smem + L.tab);
@@ -533,60 +539,22 @@ __global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_layer(DecArgs a)
     int32_t *s_pre = reinterpret_cast<int32_t *>(smem + L.pre);
     float2 *s_red = reinterpret_cast<float2 *>(smem + L.red);     // [2][NC][window token][8]
     __half *s_wa = reinterpret_cast<__half *>(smem + L.sa);       // [2][kDecTok][8]
-    const uint32_t bx = sm_addr(smem + L.bar);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc);
     int *s_nact = reinterpret_cast<int *>(smem + L.misc + 4);
-    int *s_is_last = reinterpret_cast<int *>(smem + L.misc + 8);
     uint8_t *ring = smem + L.ring;
     uint32_t *status = a.header + kHdrStatus;
-    const long long limit = a.wait_cycles;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x;
 
-    if (threadIdx.x == 0) {
-        mbar_init(bx, 1);
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    // no thread may touch the barrier (or the abort flag) before they are initialised:
-    // warps start independently, and a wait on an uninitialised barrier is undefined
-    __syncthreads();
-    // the expert table: before the dependency wait when the weights are static
-    if (a.overlap_prev)
-        for (int e = threadIdx.x; e < E; e += nthr) s_tab[e] = a.blobs[e];
-    // the next call's router kernel may launch now and load its (static) rows
-    // while this window streams
-    griddep_launch();
-    griddep_wait();
-    if (!a.overlap_prev)
-        for (int e = threadIdx.x; e < E; e += nthr) s_tab[e] = a.blobs[e];
-
-    // ---- the window's x fragments (built by the router kernel) and logits: one bulk
-    //      copy each (every CTA reads the same bytes: whole copies keep that cheap).
-    //      The selection keys follow in the ring, which is not in use yet.
-    float *s_lg = reinterpret_cast<float *>(ring);
+    // selection keys and values beside the logits (the ring is not in use yet)
+    const float *s_lg = reinterpret_cast<const float *>(ring);
     uint32_t *s_key = reinterpret_cast<uint32_t *>(ring + 4 * T * E);
     float *s_val = reinterpret_cast<float *>(ring + 8 * T * E);
     {
-        const uint32_t xbytes = 2u * T * H, lbytes = (4u * T * E + 15u) & ~15u;
-        if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(bx, xbytes + lbytes);
-            if ((int)blockIdx.x != a.skip_cta) {      // test hook: never issued, so the wait runs out
-                bulk_g2s(sm_addr(s_xf), a.xfrag, xbytes, bx);
-                bulk_g2s(sm_addr(s_lg), a.logits, lbytes, bx);
-            }
-        }
         const bool sig = a.score_fn != MOE_SCORE_SOFTMAX;
-        if (!wait_phase(bx, 0u, abort_flag, status, limit) && threadIdx.x == 0) {
-            *abort_flag = 1;
-            // copies in flight must land before the CTA ends (bounded)
-            const long long t0 = clock64();
-            while ((int)blockIdx.x != a.skip_cta && !mbar_poll(bx, 0u) && clock64() - t0 < limit) {
-            }
-        }
         for (int i = threadIdx.x; i < T * E; i += nthr) {
             const float l = s_lg[i];
             const float sv = sig ? 1.0f / (1.0f + expf(-l)) : l;
-            const float b = (sig && a.bias) ? __ldg(a.bias + i % E) : 0.0f;
+            const float b = (sig && bias) ? __ldg(bias + i % E) : 0.0f;
             s_val[i] = sv;
             s_key[i] = key_bits(sig ? sv + b : sv);
         }
@@ -642,7 +610,7 @@ __global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_layer(DecArgs a)
         atomicOr(&s_tmask[u], 1u << t);
     }
     __syncthreads();
-    if (blockIdx.x == 0) {
+    if (publish && blockIdx.x == 0) {
         // publish the routing: ids, w, counts, offsets, assign, active list
         for (int i = threadIdx.x; i < TK; i += nthr) {
             a.ids[i] = s_ids[i];
@@ -695,7 +663,8 @@ __global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_layer(DecArgs a)
     un.rb = nb * PIECE;
     un.rbs = nb * kPieceQ80;
     un.nr = (int64_t)U * (a.FF / kUnitRows);
-    un.ns = a.shared_blob ? a.SFF / kSharedRows : 0;
+    un.shared = shared_blob;
+    un.ns = shared_blob ? a.SFF / kSharedRows : 0;
     un.br = 3ll * kUnitRows * un.rb;
     un.bs = 3ll * kSharedRows * un.rbs;
     const int64_t total = un.nr * un.br + un.ns * un.bs;
@@ -1045,7 +1014,7 @@ __global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_layer(DecArgs a)
                 for (int tk = 0; tk < 2; ++tk) {
                     const int n = 2 * tq + tk;
                     if ((touched >> n) & 1u) {
-                        float *dst = a.yacc + (int64_t)n * H + hl + 32 * half;
+                        float *dst = yacc + (int64_t)n * H + hl + 32 * half;
 #pragma unroll
                         for (int v = 0; v < NT / 4; ++v)
                             red_add_v4(dst + 4 * v, D[4 * v][2 * half + tk], D[4 * v + 1][2 * half + tk],
@@ -1054,6 +1023,93 @@ __global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_layer(DecArgs a)
                 }
         }
     }
+}
+
+// y = bf16(acc) (and y_f32 = acc when given) over float4 items i0, i0 + step, ...
+// below n4; the loads of a batch are issued before its stores.
+__device__ __forceinline__ void y_from_acc(const float *acc_, uint16_t *y_, float *y_f32_, int i0, int n4, int step)
+{
+    const float4 *__restrict__ acc = reinterpret_cast<const float4 *>(acc_);
+    uint2 *__restrict__ yb = reinterpret_cast<uint2 *>(y_);
+    float4 *__restrict__ yf = reinterpret_cast<float4 *>(y_f32_);
+    constexpr int kBatch = 8;
+    for (; i0 < n4; i0 += kBatch * step) {
+        float4 v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            if (i0 + j * step < n4) v[j] = __ldcg(acc + i0 + j * step);
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = i0 + j * step;
+            if (i < n4) {
+                const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].x)) |
+                                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].y)) << 16);
+                const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].z)) |
+                                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].w)) << 16);
+                yb[i] = make_uint2(lo, hi);
+                if (yf) yf[i] = v[j];
+            }
+        }
+    }
+}
+
+// The layer kernel of one window: one persistent CTA per SM, S stages per
+// consumer warp.  128 registers a thread at 256 columns (16 warps, 4 on each
+// SM sub-partition, fit one SM), 96 for half-block warps (20 warps).
+template <int S, int V>
+__global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_layer(const __grid_constant__ DecArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int T = a.T, H = a.H, E = a.E;
+    const LayerSmem L = layer_smem(E, T, H, a.nc, a.ring_bytes);
+    const uint8_t **s_tab = reinterpret_cast<const uint8_t **>(smem + L.tab);
+    uint2 *s_xf = reinterpret_cast<uint2 *>(smem + L.xf);
+    const uint32_t bx = sm_addr(smem + L.bar);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc);
+    int *s_is_last = reinterpret_cast<int *>(smem + L.misc + 8);
+    uint8_t *ring = smem + L.ring;
+    uint32_t *status = a.header + kHdrStatus;
+    const long long limit = a.wait_cycles;
+    const int nthr = blockDim.x;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bx, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // no thread may touch the barrier (or the abort flag) before they are initialised:
+    // warps start independently, and a wait on an uninitialised barrier is undefined
+    __syncthreads();
+    // the expert table: before the dependency wait when the weights are static
+    if (a.overlap_prev)
+        for (int e = threadIdx.x; e < E; e += nthr) s_tab[e] = a.blobs[e];
+    // the next call's router kernel may launch now and load its (static) rows
+    // while this window streams
+    griddep_launch();
+    griddep_wait();
+    if (!a.overlap_prev)
+        for (int e = threadIdx.x; e < E; e += nthr) s_tab[e] = a.blobs[e];
+
+    // ---- the window's x fragments (built by the router kernel) and logits: one bulk
+    //      copy each (every CTA reads the same bytes: whole copies keep that cheap)
+    {
+        const uint32_t xbytes = 2u * T * H, lbytes = (4u * T * E + 15u) & ~15u;
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(bx, xbytes + lbytes);
+            if ((int)blockIdx.x != a.skip_cta) {      // test hook: never issued, so the wait runs out
+                bulk_g2s(sm_addr(s_xf), a.xfrag, xbytes, bx);
+                bulk_g2s(sm_addr(ring), a.logits, lbytes, bx);
+            }
+        }
+        if (!wait_phase(bx, 0u, abort_flag, status, limit) && threadIdx.x == 0) {
+            *abort_flag = 1;
+            // copies in flight must land before the CTA ends (bounded)
+            const long long t0 = clock64();
+            while ((int)blockIdx.x != a.skip_cta && !mbar_poll(bx, 0u) && clock64() - t0 < limit) {
+            }
+        }
+    }
+    dec_window<S, V>(a, smem, a.bias, a.shared_blob, a.yacc, true);
 
     // ---- the last CTA to finish writes y
     __threadfence();
@@ -1065,32 +1121,242 @@ __global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_layer(DecArgs a)
     __syncthreads();
     if (*s_is_last) {
         __threadfence();
-        // y = bf16(yacc): the loads of a batch are issued before its stores
-        const int n4 = T * H / 4;
-        const float4 *__restrict__ acc = reinterpret_cast<const float4 *>(a.yacc);
-        uint2 *__restrict__ yb = reinterpret_cast<uint2 *>(a.y);
-        float4 *__restrict__ yf = reinterpret_cast<float4 *>(a.y_f32);
-        constexpr int kBatch = 8;
-        for (int i0 = threadIdx.x; i0 < n4; i0 += kBatch * nthr) {
-            float4 v[kBatch];
+        y_from_acc(a.yacc, a.y, a.y_f32, threadIdx.x, T * H / 4, nthr);
+        if (threadIdx.x == 0) a.header[kHdrTicketDown] = 0u;
+    }
+}
+
+// ---------------------------------------------------------------- the layer stack
+
+constexpr int kStackMaxRows = 8;        // router rows a CTA of the stack kernel holds
+
+// Bounded grid-wide barrier n (0, 1, ...) of a cooperative launch: thread 0 of
+// every CTA adds one to *count with release semantics (publishing the CTA's
+// writes), then polls it with acquire loads until all CTAs have arrived at
+// barrier n.  A wait that runs out records
+// MOE_ERR_TIMEOUT and raises the grid's abort word, which ends every other
+// CTA's wait as well.  arrive == false is the test hook of a CTA that never
+// arrives.
+__device__ __forceinline__ bool grid_barrier(uint32_t *count, uint32_t *gabort, uint32_t n, bool arrive,
+                                             long long limit, uint32_t *status, volatile int *abort)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // release: the CTA's writes (ordered before this thread by the CTA barrier) before the arrival
+        if (arrive) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
+        const uint32_t target = (n + 1u) * gridDim.x;
+        const long long t0 = clock64();
+        while (true) {
+            uint32_t c;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(c) : "l"(count) : "memory");
+            if (c >= target) break;
+            if (*reinterpret_cast<volatile uint32_t *>(gabort)) {
+                *abort = 1;
+                break;
+            }
+            if (clock64() - t0 > limit) {
+                set_status(status, MOE_ERR_TIMEOUT);
+                atomicExch(gabort, 1u);
+                *abort = 1;
+                break;
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    return !*abort;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
+{
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
+// The input of layer l, in every CTA: x of the window as fp16 MMA fragments
+// (s_xf, the layout k_dec_route writes), and the logits of this CTA's router
+// rows (r0 .. r0 + nr - 1, held in shared memory at s_wr) written to the
+// workspace.  From layer 1 on it first finishes layer l - 1: y = bf16 of its
+// accumulator, written by this CTA for the float4 items [q0, q1).  With the
+// residual stream the input is bf16(x[l - 1] + y[l - 1]) (an fp32 sum of the
+// two bf16 values, rounded once), also written for [q0, q1); otherwise it is
+// x[l].  Every CTA reads the accumulator whole in the residual case, so no
+// barrier separates y from the next layer's logits.  x is staged in bf16 at
+// s_x (the ring's head) with its loads in flight together; each router row's
+// T logits are one warp's dot products over it.
+__device__ __noinline__ void stack_input(const StackArgs &sa, int l, uint8_t *smem, const LayerSmem &L, const float *s_wr,
+                            int r0, int nr, int q0, int q1)
+{
+    const DecArgs &d = sa.d;
+    const int T = d.T, H = d.H, E = d.E, H4 = H / 4, n4 = T * H4, nthr = blockDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = nthr >> 5;
+    uint2 *s_xf = reinterpret_cast<uint2 *>(smem + L.xf);
+    uint2 *s_x = reinterpret_cast<uint2 *>(smem + L.ring);           // bf16 [T][H], 4 a uint2
+    const size_t TH = (size_t)T * H;
+    const bool res = sa.residual && l > 0;
+    const float4 *yprev = reinterpret_cast<const float4 *>(sa.yacc + (size_t)((l + 1) & 1) * TH);  // layer l - 1's
+    uint2 *yout = reinterpret_cast<uint2 *>(sa.y + (size_t)(l > 0 ? l - 1 : 0) * TH);
+    float4 *yfout = sa.y_f32 ? reinterpret_cast<float4 *>(sa.y_f32 + (size_t)(l > 0 ? l - 1 : 0) * TH) : nullptr;
+    if (!res) {
+        // x[l] as it is: one cp.async group; y of layer l - 1 for this CTA's items meanwhile
+        const uint16_t *xin = sa.x + (size_t)l * TH;
+        const uint32_t dst = sm_addr(s_x);
+        for (int i = threadIdx.x; i < n4 / 2; i += nthr) cp16(dst + 16u * i, xin + 8 * i);
+        cp_commit();
+        if (l > 0)
+            for (int q = q0 + threadIdx.x; q < q1; q += nthr) {
+                const float4 v = __ldcg(yprev + q);
+                yout[q] = make_uint2(bf16x2_rn(v.x, v.y), bf16x2_rn(v.z, v.w));
+                if (yfout) yfout[q] = v;
+            }
+        cp_wait<0>();
+    } else {
+        // x[l] = bf16(x[l - 1] + bf16(acc)), one item at a time (deeper batches here cost the
+        // streaming loop registers)
+        const uint2 *xin = reinterpret_cast<const uint2 *>(sa.x + (size_t)(l - 1) * TH);
+        uint2 *xout = reinterpret_cast<uint2 *>(sa.x + (size_t)l * TH);
+        constexpr int kB = 1;
+        for (int i0 = threadIdx.x; i0 < n4; i0 += kB * nthr) {
+            float4 yv[kB];
+            uint2 xv[kB];
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j)
-                if (i0 + j * nthr < n4) v[j] = __ldcg(acc + i0 + j * nthr);
+            for (int j = 0; j < kB; ++j)
+                if (i0 + j * nthr < n4) {
+                    yv[j] = __ldcg(yprev + i0 + j * nthr);
+                    xv[j] = __ldcg(xin + i0 + j * nthr);
+                }
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const int i = i0 + j * nthr;
-                if (i < n4) {
-                    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].x)) |
-                                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].y)) << 16);
-                    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].z)) |
-                                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j].w)) << 16);
-                    yb[i] = make_uint2(lo, hi);
-                    if (yf) yf[i] = v[j];
+            for (int j = 0; j < kB; ++j) {
+                const int q = i0 + j * nthr;
+                if (q < n4) {
+                    const uint32_t ylo = bf16x2_rn(yv[j].x, yv[j].y), yhi = bf16x2_rn(yv[j].z, yv[j].w);
+                    uint2 xb = xv[j];
+                    xb.x = bf16x2_rn(__fadd_rn(bf16_bits_to_f32(xb.x & 0xffff), bf16_bits_to_f32(ylo & 0xffff)),
+                                     __fadd_rn(bf16_bits_to_f32(xb.x >> 16), bf16_bits_to_f32(ylo >> 16)));
+                    xb.y = bf16x2_rn(__fadd_rn(bf16_bits_to_f32(xb.y & 0xffff), bf16_bits_to_f32(yhi & 0xffff)),
+                                     __fadd_rn(bf16_bits_to_f32(xb.y >> 16), bf16_bits_to_f32(yhi >> 16)));
+                    s_x[q] = xb;
+                    if (q >= q0 && q < q1) {
+                        yout[q] = make_uint2(ylo, yhi);
+                        if (yfout) yfout[q] = yv[j];
+                        xout[q] = xb;
+                    }
                 }
             }
         }
-        if (threadIdx.x == 0) a.header[kHdrTicketDown] = 0u;
     }
+    __syncthreads();
+    // fp16 MMA fragments: item q = (token g, elements e .. e + 3), e = 4 (q % H4), to slot
+    // ((cb * 16 + s) * 4 + tq) * T + g with e = 256 cb + 64 tq + (s < 8 ? 4 s : 32 + 4 (s - 8))
+    bool bad = false;
+    for (int q = threadIdx.x; q < n4; q += nthr) {
+        const int g = q / H4, e = 4 * (q - g * H4);
+        const uint2 xb = s_x[q];
+        const float x0 = bf16_bits_to_f32(xb.x & 0xffff), x1 = bf16_bits_to_f32(xb.x >> 16);
+        const float x2 = bf16_bits_to_f32(xb.y & 0xffff), x3 = bf16_bits_to_f32(xb.y >> 16);
+        const float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+        bad |= !(m < 65504.0f);      // beyond the fp16 range, or NaN
+        const int cb = e >> 8, rem = e & 255, tq = rem >> 6, r2 = rem & 63;
+        const int sx = r2 < 32 ? r2 >> 2 : 8 + ((r2 - 32) >> 2);
+        s_xf[((cb * 16 + sx) * 4 + tq) * T + g] =
+            make_uint2(dq_h22u(__floats2half2_rn(x0, x1)), dq_h22u(__floats2half2_rn(x2, x3)));
+    }
+    if (bad) set_status(d.header + kHdrStatus, MOE_ERR_DEVICE_FAULT);
+    // logits: warp p takes (row r, token g) pairs, lanes along H in float4 steps
+    for (int p = warp; p < nr * T; p += nwarp) {
+        const int r = p / T, g = p - r * T;
+        const float4 *w4 = reinterpret_cast<const float4 *>(s_wr + (size_t)r * H);
+        const uint2 *x4 = s_x + (size_t)g * H4;
+        float acc = 0.0f;
+        for (int j = lane; j < H4; j += 32) {
+            const float4 w = w4[j];
+            const uint2 xb = x4[j];
+            acc = fmaf(w.x, bf16_bits_to_f32(xb.x & 0xffff), acc);
+            acc = fmaf(w.y, bf16_bits_to_f32(xb.x >> 16), acc);
+            acc = fmaf(w.z, bf16_bits_to_f32(xb.y & 0xffff), acc);
+            acc = fmaf(w.w, bf16_bits_to_f32(xb.y >> 16), acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) d.logits[(size_t)g * E + r0 + r] = acc;
+    }
+}
+
+// A decode window through a stack of L layers in one launch: one persistent
+// CTA per SM (a cooperative launch), the layers in order, each between two
+// grid-wide barriers -- after its router logits (each CTA computes those of
+// its share of the router rows, kept in shared memory), and after its experts
+// (every contribution to its accumulator added).  The two accumulators
+// alternate: layer l + 1's is zeroed while layer l streams, and layer l's is
+// read whole by every CTA to build layer l + 1's input.  A CTA that has
+// finished its units loads the next layer's router rows into the tail of its
+// ring while it waits for the rest of the grid.
+template <int S, int V>
+__global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_stack(const __grid_constant__ StackArgs sa)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const DecArgs &d = sa.d;
+    const int T = d.T, H = d.H, E = d.E, G = gridDim.x, b = blockIdx.x, nthr = blockDim.x;
+    const LayerSmem L = layer_smem(E, T, H, d.nc, d.ring_bytes);
+    const uint8_t **s_tab = reinterpret_cast<const uint8_t **>(smem + L.tab);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc);
+    float *s_lg = reinterpret_cast<float *>(smem + L.ring);
+    const float *s_wr = reinterpret_cast<const float *>(smem + L.ring + L.ring_bytes - (uint32_t)sa.rows * H * 4);
+    uint32_t *status = d.header + kHdrStatus;
+    uint32_t *gbar = d.header + kHdrGridBar, *gabort = d.header + kHdrGridAbort;
+    const int r0 = (int)((int64_t)E * b / G), nr = (int)((int64_t)E * (b + 1) / G) - r0;
+    const int n4 = T * H / 4;
+    const int q0 = (int)((int64_t)n4 * b / G), q1 = (int)((int64_t)n4 * (b + 1) / G);
+    const size_t TH = (size_t)T * H;
+
+    if (threadIdx.x == 0) *abort_flag = 0;
+    // this CTA's router rows of layer l -> the ring's tail (one cp.async group)
+    auto load_rows = [&](int l) {
+        const float *wr = sa.wr[l] + (size_t)r0 * H;
+        const uint32_t dst = sm_addr(s_wr);
+        for (int i = threadIdx.x; i < nr * H / 4; i += nthr) cp16(dst + 16u * i, wr + 4 * i);
+        cp_commit();
+    };
+    load_rows(0);
+    for (int i = q0 + threadIdx.x; i < q1; i += nthr) reinterpret_cast<float4 *>(sa.yacc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    uint32_t nbar = 0;
+    bool ok = true;
+    for (int l = 0; l < sa.L && ok; ++l) {
+        cp_wait<0>();
+        __syncthreads();
+        stack_input(sa, l, smem, L, s_wr, r0, nr, q0, q1);
+        // ---- every CTA's logits of layer l are in place
+        ok = grid_barrier(gbar, gabort, nbar++, !(l == 0 && b == d.skip_cta), d.wait_cycles, status, abort_flag);
+        if (!ok) break;
+        const uint8_t *const *blobs = sa.blobs + (size_t)l * E;
+        for (int e = threadIdx.x; e < E; e += nthr) s_tab[e] = blobs[e];
+        for (int i = threadIdx.x; i < T * E; i += nthr) s_lg[i] = __ldcg(d.logits + i);
+        // nobody reads the other accumulator past that barrier: this CTA's share of it, zeroed for layer l + 1
+        if (l + 1 < sa.L) {
+            float4 *nxt = reinterpret_cast<float4 *>(sa.yacc + (size_t)((l + 1) & 1) * TH);
+            for (int i = q0 + threadIdx.x; i < q1; i += nthr) nxt[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncthreads();
+        dec_window<S, V>(d, smem, sa.bias ? sa.bias[l] : nullptr, sa.shared ? sa.shared[l] : nullptr,
+                         sa.yacc + (size_t)(l & 1) * TH, l == sa.L - 1);
+        // ---- the ring is free: the next layer's router rows
+        __syncthreads();
+        if (l + 1 < sa.L) load_rows(l + 1);
+        ok = grid_barrier(gbar, gabort, nbar++, true, d.wait_cycles, status, abort_flag);
+    }
+    // y of the last layer (the earlier layers' were written while building the next input)
+    if (ok) {
+        const size_t lo = (size_t)(sa.L - 1) * TH;
+        const float4 *acc = reinterpret_cast<const float4 *>(sa.yacc + (size_t)((sa.L - 1) & 1) * TH);
+        uint2 *yo = reinterpret_cast<uint2 *>(sa.y + lo);
+        float4 *yf = sa.y_f32 ? reinterpret_cast<float4 *>(sa.y_f32 + lo) : nullptr;
+        for (int q = q0 + threadIdx.x; q < q1; q += nthr) {
+            const float4 v = __ldcg(acc + q);
+            yo[q] = make_uint2(bf16x2_rn(v.x, v.y), bf16x2_rn(v.z, v.w));
+            if (yf) yf[q] = v;
+        }
+    }
+    cp_wait<0>();           // no copy outlives the CTA (an aborted stack may leave the next rows in flight)
 }
 
 // ---------------------------------------------------------------- launch
@@ -1139,6 +1405,7 @@ uint32_t dec_ring_bytes(const moe_config &c, int32_t T) { return (uint32_t)dec_b
 static const int kStageCounts[] = {16, 14, 12, 10, 8, 7, 6};
 
 using LayerFn = void (*)(DecArgs);
+using StackFn = void (*)(StackArgs);
 
 template <int V>
 static LayerFn layer_fn(int S)
@@ -1151,6 +1418,21 @@ static LayerFn layer_fn(int S)
     case 8: return k_dec_layer<8, V>;
     case 7: return k_dec_layer<7, V>;
     case 6: return k_dec_layer<6, V>;
+    }
+    return nullptr;
+}
+
+template <int V>
+static StackFn stack_fn(int S)
+{
+    switch (S) {
+    case 16: return k_dec_stack<16, V>;
+    case 14: return k_dec_stack<14, V>;
+    case 12: return k_dec_stack<12, V>;
+    case 10: return k_dec_stack<10, V>;
+    case 8: return k_dec_stack<8, V>;
+    case 7: return k_dec_stack<7, V>;
+    case 6: return k_dec_stack<6, V>;
     }
     return nullptr;
 }
@@ -1207,6 +1489,10 @@ static cudaError_t dec_set_attributes()
         for (LayerFn f : {layer_fn<kVarQ4K>(S), layer_fn<kVarHalf>(S), layer_fn<kVarQ5K>(S)})
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBudget);
+    for (int S : kStageCounts)
+        for (StackFn f : {stack_fn<kVarQ4K>(S), stack_fn<kVarHalf>(S), stack_fn<kVarQ5K>(S)})
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBudget);
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
@@ -1230,6 +1516,49 @@ cudaError_t launch_decode(const DecArgs &a0, cudaStream_t s)
                        : a.codec == MOE_CODEC_Q5K ? layer_fn<kVarQ5K>(a.stages) : layer_fn<kVarQ4K>(a.stages);
     e = fn ? launch_pdl(fn, grid, block, L.total, s, true, a) : cudaErrorInvalidValue;
     prof_end(kPhDecLayer, s);
+    return e;
+}
+
+// The stack kernel needs the decode path's layer kernel configuration, and
+// room in the ring for a CTA's router rows (tail) beside the staged x (head);
+// both are live only between a layer's experts.
+int stack_grid() { return dec_sms(); }
+
+bool stack_supported(const moe_config &c, int32_t T)
+{
+    if (T < 1 || !dec_supported(c, T)) return false;
+    const int G = dec_sms();
+    const int rows = (c.n_experts + G - 1) / G;
+    if (rows > kStackMaxRows) return false;
+    // x staged in bf16 at the ring's head, the router rows at its tail
+    return 2ll * T * c.hidden + (int64_t)rows * c.hidden * 4 <= (int64_t)dec_ring_bytes(c, T);
+}
+
+cudaError_t launch_stack(const StackArgs &a, cudaStream_t s)
+{
+    if (a.d.T <= 0 || a.L <= 0) return cudaSuccess;
+    cudaError_t e = dec_set_attributes();
+    if (e != cudaSuccess) return e;
+    // the grid barriers count from zero in every launch
+    e = cudaMemsetAsync(a.d.header + kHdrGridBar, 0, 2 * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    const LayerSmem L = layer_smem(a.d.E, a.d.T, a.d.H, a.d.nc, a.d.ring_bytes);
+    const StackFn fn = a.d.half ? stack_fn<kVarHalf>(a.d.stages)
+                       : a.d.codec == MOE_CODEC_Q5K ? stack_fn<kVarQ5K>(a.d.stages) : stack_fn<kVarQ4K>(a.d.stages);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(dec_sms());
+    cfg.blockDim = dim3(32 * std::max(a.d.nc, kDecTok));
+    cfg.dynamicSmemBytes = L.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;     // every CTA resident at once: the grid barriers need it
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    prof_begin(kPhDecStack, s);
+    e = cudaLaunchKernelEx(&cfg, fn, a);
+    prof_end(kPhDecStack, s);
     return e;
 }
 

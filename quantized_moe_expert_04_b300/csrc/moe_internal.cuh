@@ -34,6 +34,8 @@ enum HeaderWord : int {
     kHdrTicketRoute = 6,  // decode path: CTAs done with the router logits (last one routes)
     kHdrTicketDown = 7,   // decode path: CTAs done with the down projection (last one writes y)
     kHdrCounter0 = 8,     // completion counters, reset by their last user
+    kHdrGridBar = 56,     // layer stack: arrivals at its grid-wide barriers (zeroed before each launch)
+    kHdrGridAbort = 57,   //              raised by a CTA whose barrier wait ran out
 };
 
 __device__ __forceinline__ void set_status(uint32_t *status, uint32_t code)
@@ -63,7 +65,7 @@ __device__ __forceinline__ void q4k_scale_min(const uint8_t *scales, int j, int 
 // Kernels counted / timed by the diagnostics API (moe_profile_*).
 enum Phase : int {
     kPhRouterLogits = 0, kPhTopk, kPhBucket, kPhGemmPrep, kPhGemmGateUp, kPhGemmDown, kPhGemmFinish,
-    kPhDecRoute, kPhDecLayer, kNumPhases
+    kPhDecRoute, kPhDecLayer, kPhDecStack, kNumPhases
 };
 void prof_begin(int phase, cudaStream_t s);   // no-ops unless profiling is enabled
 void prof_end(int phase, cudaStream_t s);
@@ -168,6 +170,25 @@ uint32_t dec_ring_bytes(const moe_config &c, int32_t T);
 int dec_stages(const moe_config &c, int32_t T);
 bool dec_supported(const moe_config &c, int32_t T);
 cudaError_t launch_decode(const DecArgs &a, cudaStream_t s);
+
+// A window through a stack of layers in one cooperative launch (moe_forward_stack).
+struct StackArgs {
+    DecArgs d;                          // shapes, ring, hooks, workspace views (logits, routing, header)
+    int L;                              // layers
+    int residual;                       // x[l + 1] = bf16(x[l] + y[l]) written by the kernel
+    int rows;                           // router rows a CTA holds: ceil(E / CTAs)
+    const float *const *wr;             // device [L] router matrices
+    const float *const *bias;           // device [L] or null
+    const uint8_t *const *blobs;        // device [L][E] expert blobs
+    const uint8_t *const *shared;       // device [L] or null
+    uint16_t *x;                        // bf16 [L][T][H]
+    uint16_t *y;                        // bf16 [L][T][H]
+    float *y_f32;                       // [L][T][H] or null
+    float *yacc;                        // [2][T][H] fp32 accumulators (alternating layers)
+};
+bool stack_supported(const moe_config &c, int32_t T);
+int stack_grid();                       // CTAs of the stack kernel: one per SM
+cudaError_t launch_stack(const StackArgs &a, cudaStream_t s);
 
 // Test hooks (moe_debug_set): limit of the bounded device waits, and a CTA of
 // the next call's main kernel that never issues its first bulk copy.

@@ -10,7 +10,7 @@ namespace moe {
 
 static const char *kPhaseNames[kNumPhases] = {
     "router_logits", "topk", "bucket", "gemm_prep", "gemm_gateup", "gemm_down", "gemm_finish",
-    "dec_route", "dec_layer",
+    "dec_route", "dec_layer", "dec_stack",
 };
 
 namespace {

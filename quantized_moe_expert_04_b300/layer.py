@@ -58,6 +58,31 @@ def pack_layer(wl: synth.Workload, seed: int = 0, layer: int = 0, gen_device: st
     return PackedLayer(wl, rw, rb, blobs, table, shared)
 
 
+class LayerStack:
+    """Pointer tables of a list of packed layers for moe_forward_stack."""
+
+    def __init__(self, layers: List[PackedLayer]):
+        dev = torch.device("cuda")
+        wl = layers[0].wl
+        self.layers, self.wl = layers, wl
+        ptrs = lambda ts: torch.tensor([t.data_ptr() for t in ts], dtype=torch.int64, device=dev)
+        self.router_w = ptrs([pl.router_w for pl in layers])
+        self.router_bias = ptrs([pl.router_bias for pl in layers]) if layers[0].router_bias is not None else None
+        self.blobs = torch.cat([pl.table for pl in layers]).contiguous()
+        self.shared = ptrs([pl.shared for pl in layers]) if wl.has_shared else None
+
+    def forward(self, x: torch.Tensor, ws: torch.Tensor, y: Optional[torch.Tensor] = None,
+                y_f32: Optional[torch.Tensor] = None, residual: bool = True, flags: int = 0, stream=None):
+        """x: bf16 [L][T][H] (residual: x[0] is read, x[1:] written); returns y [L][T][H]."""
+        L, T = len(self.layers), x.shape[1]
+        if y is None:
+            y = torch.empty(L, T, self.wl.hidden, dtype=torch.bfloat16, device="cuda")
+        cfg = moe.config_for(self.wl, flags | (moe.MOE_FLAG_RESIDUAL if residual else 0))
+        moe.moe_forward_stack(cfg, L, x, self.router_w, self.router_bias, self.blobs, self.shared, T, y, y_f32,
+                              ws, stream)
+        return y
+
+
 def workspace(cfg: moe.moe_config, max_tokens: int) -> torch.Tensor:
     """A zero-initialised workspace for calls of up to max_tokens tokens."""
     nbytes = moe.moe_workspace_bytes(cfg, max_tokens)

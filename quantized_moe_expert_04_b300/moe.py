@@ -34,6 +34,7 @@ MOE_FLAG_DETERMINISTIC = 1
 MOE_FLAG_FORCE_GEMV = 2
 MOE_FLAG_FORCE_GEMM = 4
 MOE_FLAG_STATIC_WEIGHTS = 8
+MOE_FLAG_RESIDUAL = 16
 
 EXPORTS = (
     "moe_q4k_bytes", "moe_q5k_bytes", "moe_q8_0_bytes", "moe_expert_bytes", "moe_shared_bytes",
@@ -42,7 +43,7 @@ EXPORTS = (
     "moe_workspace_routing", "moe_last_device_status", "moe_status_string",
     "moe_profile_enable", "moe_profile_read", "moe_forward_static_ws",
     "moe_dequant_q4k_f16", "moe_dequant_q8_0_f16", "moe_debug_set",
-    "moe_dequant_q5k", "moe_dequant_q5k_f16",
+    "moe_dequant_q5k", "moe_dequant_q5k_f16", "moe_forward_stack",
     "moe_cache_create", "moe_cache_destroy", "moe_cache_plan", "moe_cache_issue", "moe_cache_poll",
     "moe_cache_stats", "moe_host_address",
 )
@@ -109,6 +110,7 @@ def lib() -> ctypes.CDLL:
             "moe_dequant_q8_0": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
             "moe_dequant_q4k_f16": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
             "moe_dequant_q5k": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
+            "moe_forward_stack": (ctypes.c_int, [_CFG, _I32, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
             "moe_dequant_q5k_f16": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
             "moe_dequant_q8_0_f16": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
             "moe_workspace_bytes": (_SZ, [_CFG, _I32]),
@@ -288,6 +290,20 @@ def moe_forward(cfg: moe_config, x: torch.Tensor, router_w: torch.Tensor, router
     _check(lib().moe_forward(ctypes.byref(cfg), _ptr(x), _ptr(router_w), _ptr(router_bias), _ptr(expert_blobs),
                              _ptr(shared_blob), T, _ptr(y), _ptr(y_f32), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(stream)), "moe_forward")
+
+
+def moe_forward_stack(cfg: moe_config, n_layers: int, x: torch.Tensor, router_w: torch.Tensor,
+                      router_bias: Optional[torch.Tensor], expert_blobs: torch.Tensor,
+                      shared_blobs: Optional[torch.Tensor], T: int, y: torch.Tensor, y_f32: Optional[torch.Tensor],
+                      ws: torch.Tensor, stream=None):
+    """A window through n_layers layers in one launch.  x, y: bf16 [L][T][H]
+    (with MOE_FLAG_RESIDUAL x[1:] is written); router_w, router_bias,
+    shared_blobs: int64 CUDA tensors [L] of device pointers; expert_blobs:
+    int64 CUDA tensor [L * E] of blob pointers."""
+    x = _bf16_bits(x)
+    _check(lib().moe_forward_stack(ctypes.byref(cfg), n_layers, _ptr(x), _ptr(router_w), _ptr(router_bias),
+                                   _ptr(expert_blobs), _ptr(shared_blobs), T, _ptr(y), _ptr(y_f32), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _stream(stream)), "moe_forward_stack")
 
 
 def moe_forward_static_ws(cfg: moe_config, x: torch.Tensor, router_w: torch.Tensor,

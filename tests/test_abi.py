@@ -121,3 +121,30 @@ def test_static_ws_checks_arguments_before_any_cuda_call():
     assert L.moe_forward_static_ws(*args(cfg=gemv, T=9)) == moe.MOE_ERR_UNSUPPORTED_SHAPE
     big = moe.make_config(2560, 512, 320, 10)
     assert L.moe_forward_static_ws(*args(cfg=big, T=4096)) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_stack_checks_arguments_before_any_cuda_call():
+    """moe_forward_stack rejects bad arguments and unsupported shapes on the
+    host (no GPU in this process)."""
+    L = moe.lib()
+    p = ctypes.c_void_p(4096)
+    cfg = moe.make_config(256, 16, 128, 2)
+    need = moe.moe_workspace_bytes(cfg, 4)
+
+    def call(c=cfg, n=2, x=p, wr=p, blobs=p, shared=None, T=4, y=p, y32=None, ws=p, nbytes=need):
+        return L.moe_forward_stack(ctypes.byref(c), n, x, wr, None, blobs, shared, T, y, y32, ws, nbytes, None)
+
+    assert call(n=0) == moe.MOE_OK and call(T=0) == moe.MOE_OK            # no-ops
+    assert call(n=-1) == moe.MOE_ERR_INVALID_ARG
+    assert call(T=-1) == moe.MOE_ERR_INVALID_ARG
+    assert call(y=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(wr=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(x=ctypes.c_void_p(4098)) == moe.MOE_ERR_MISALIGNED
+    assert call(wr=ctypes.c_void_p(4100)) == moe.MOE_ERR_MISALIGNED
+    assert call(nbytes=need - 1) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert call(T=9, nbytes=moe.moe_workspace_bytes(cfg, 9)) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    for fl in (moe.MOE_FLAG_FORCE_GEMM, moe.MOE_FLAG_DETERMINISTIC):
+        c = moe.make_config(256, 16, 128, 2, flags=fl)
+        assert call(c=c, nbytes=moe.moe_workspace_bytes(c, 4)) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    ds = moe.make_config(256, 16, 128, 2, moe.MOE_SCORE_SIGMOID_BIAS, 64)
+    assert call(c=ds, nbytes=moe.moe_workspace_bytes(ds, 4)) == moe.MOE_ERR_INVALID_ARG   # no shared table
