@@ -3,35 +3,35 @@
 // The teardown page ("Strata 引擎深度拆解", lcz.me/topic/2098/5, section 一,
 // CPU ledger) computes each selected expert once for all tokens of a 3-token
 // verify window, and the decode critical path there is the expert arithmetic
-// (section 二 item 5).  A window is two kernels here, chained with
+// (section 二 item 5).  One layer call is two kernels here, chained with
 // programmatic dependent launch:
 //
 //   k_dec_route  router logits over the grid (each router row read once per
 //                window, held in registers: with static weights the rows are
-//                loaded before the previous call has finished); zeroes the
-//                fp32 accumulator of y.
+//                loaded before the previous call has finished); the window's
+//                x as fp16 MMA fragments; zeroes the fp32 accumulator of y.
 //   k_dec_layer  one persistent CTA per SM.  Every CTA routes the window
 //                itself (one warp per token: top-k by warp arg-max rounds;
 //                bitmap bucketing of the selected experts), then takes an
-//                equal share, by bytes, of the window's work: "units" of 8
-//                consecutive ff rows of one selected expert -- its 8 gate
-//                rows, 8 up rows and 8 down rows (the down matrix is stored
-//                [FF][H], so down row f needs only a[f]) -- followed by the
-//                shared expert's units.  A producer warp streams each unit's
-//                three 8-row slabs (contiguous in the blob) with 1-D bulk
-//                copies into a byte ring in shared memory, tracked by
-//                mbarriers; consumer warp w owns the 256-column block w of
-//                H: gate/up as fp16 warp MMAs (8 gate + 8 up rows = the 16
-//                MMA rows, the window's tokens = the 8 MMA columns) over its
-//                block, partial sums reduced across the warps in shared
-//                memory, a = SiLU(g) * u, then the down rows of the same
-//                unit for its block in fp32, accumulated in registers while
-//                consecutive units belong to one expert and added into the
-//                fp32 y accumulator with vector reductions when the expert
-//                changes.  The last CTA to finish writes y in bf16.
+//                equal share of the window's "units": 8 consecutive ff rows
+//                of one selected expert -- its 8 gate, 8 up and 8 down rows
+//                (the down matrix is stored [FF][H], so down row f needs only
+//                a[f]) -- followed by the shared expert's 4-row units.
+//                Consumer warp w owns a column block of H (256 columns, or
+//                128 for layers without a shared expert) and stages only its
+//                block of every slab into a private ring with 16-byte
+//                cp.async.  Gate/up are fp16 warp MMAs (8 gate + 8 up rows =
+//                the 16 MMA rows, the window's tokens = the 8 MMA columns);
+//                the warps' partial sums meet in shared memory; a = w SiLU(g)
+//                u in fp16 is the B operand of the down MMAs (the unit's 8
+//                rows = K), which run one unit late so that one barrier per
+//                unit orders both.  Down results stay in registers across all
+//                the CTA's units and are added into the fp32 accumulator
+//                once; the last CTA to finish writes y in bf16.
 //
-// Every selected expert's bytes (and the shared expert's) are read once per
-// window; there is no grid-wide wait between gate/up and down.
+// k_dec_stack runs the same layer body for a window through a whole stack of
+// layers in one cooperative launch (see there).  Every selected expert's
+// bytes (and the shared expert's) are read once per window.
 #include <algorithm>
 #include <mutex>
 
@@ -367,20 +367,17 @@ __host__ __device__ inline LayerSmem layer_smem(int E, int T, int H, int nc, uin
 }
 
 // Unit geometry of a window: Nr routed units (8 ff rows of one active expert)
-// then Ns shared-expert units (4 rows), split over the CTAs by bytes.
+// then Ns shared-expert units (4 rows), split over the CTAs in equal counts.
+// A unit's time is set by its instructions, not its bytes: a 4-row Q8_0 unit
+// of the shared expert (52 KB at H = 4096) took as long as an 8-row Q4_K
+// unit (55 KB) -- the same MMA and dequantisation steps a warp, half of the
+// shared unit's MMA rows idle -- so a split by bytes left the CTAs holding
+// shared units about 7% behind the rest.
 struct Units {
     int64_t nr, ns;          // unit counts
-    int64_t br, bs;          // bytes of one unit (3 slabs)
     int rb, rbs;             // row bytes: routed (Q4_K or Q5_K), Q8_0 shared
     const uint8_t *shared;   // the shared expert's blob, or null
 };
-
-__device__ __forceinline__ int64_t first_unit(const Units &u, int64_t byte)
-{
-    const int64_t rbytes = u.nr * u.br;
-    if (byte <= rbytes) return (byte + u.br - 1) / u.br;
-    return u.nr + (byte - rbytes + u.bs - 1) / u.bs;
-}
 
 struct UnitInfo {
     const uint8_t *blob;
@@ -560,6 +557,7 @@ __device__ __forceinline__ void dec_window(const DecArgs &a, uint8_t *smem, cons
         }
     }
     if (threadIdx.x < 32) s_bits[threadIdx.x] = 0u;
+    for (int i = threadIdx.x; i < 2 * kDecTok * kUnitRows; i += nthr) s_wa[i] = __float2half_rn(0.0f);
     __syncthreads();
     if (warp < T) {
         int id;
@@ -665,11 +663,9 @@ __device__ __forceinline__ void dec_window(const DecArgs &a, uint8_t *smem, cons
     un.nr = (int64_t)U * (a.FF / kUnitRows);
     un.shared = shared_blob;
     un.ns = shared_blob ? a.SFF / kSharedRows : 0;
-    un.br = 3ll * kUnitRows * un.rb;
-    un.bs = 3ll * kSharedRows * un.rbs;
-    const int64_t total = un.nr * un.br + un.ns * un.bs;
-    const int64_t u_begin = first_unit(un, total * blockIdx.x / gridDim.x);
-    const int64_t u_end = first_unit(un, total * (blockIdx.x + 1) / gridDim.x);
+    const int64_t total = un.nr + un.ns;
+    const int64_t u_begin = total * blockIdx.x / gridDim.x;
+    const int64_t u_end = total * (blockIdx.x + 1) / gridDim.x;
     __syncthreads();   // the routing scratch in the ring is free from here on; the abort flag is settled
 
     if (warp < NC && !*abort_flag) {
@@ -936,7 +932,8 @@ __device__ __forceinline__ void dec_window(const DecArgs &a, uint8_t *smem, cons
             // complete past this barrier
             __syncwarp();
             asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
-            // B operand of the down projection of unit u: w_{n,e} * SiLU(g) * u in fp16, [token n][ff row f]
+            // B operand of the down projection of unit u: w_{n,e} * SiLU(g) * u in fp16, [token n][ff row f],
+            // for the window's tokens (the MMA columns of absent tokens hold zeros)
             // (half-block warps: 8 threads an activation, each adding every 8th warp's partial
             // sums, then the 8 added across lanes in a fixed order; otherwise one thread an
             // activation: the other warps go on to their down rows meanwhile)
@@ -953,7 +950,7 @@ __device__ __forceinline__ void dec_window(const DecArgs &a, uint8_t *smem, cons
                 };
                 if (HALF && NC >= 16) {
                     const int ct = warp * 32 + lane;
-                    if (ct < 8 * kUnitRows * kDecTok) {             // warps 0 .. 15, whole warps
+                    if (ct < 8 * kUnitRows * T) {                   // whole warps (T of them)
                         const int item = ct >> 3, sl = ct & 7, f = item & 7, n = item >> 3;
                         const bool act = ((tmask >> n) & 1u) && f < ui.rows;
                         float gs = 0.0f, us = 0.0f;
@@ -971,7 +968,7 @@ __device__ __forceinline__ void dec_window(const DecArgs &a, uint8_t *smem, cons
                         if (sl == 0) finish(n, f, act, gs, us);
                     }
                 } else {
-                    for (int ct = warp * 32 + lane; ct < kUnitRows * kDecTok; ct += NC * 32) {
+                    for (int ct = warp * 32 + lane; ct < kUnitRows * T; ct += NC * 32) {
                         const int f = ct & 7, n = ct >> 3;
                         const bool act = ((tmask >> n) & 1u) && f < ui.rows;
                         float gs = 0.0f, us = 0.0f;
