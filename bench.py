@@ -576,7 +576,7 @@ def measure_stack(args, wl, T, nL, world, rank, local, target_s=1.0, cpu_budget=
         step()
     torch.cuda.synchronize()
     per = (time.perf_counter() - t0) / 3
-    K = int(max(10, min(20000, target_s / max(per, 1e-7))))
+    K = args.steps if args.stack_only and args.steps else int(max(10, min(20000, target_s / max(per, 1e-7))))
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
