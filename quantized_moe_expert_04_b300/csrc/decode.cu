@@ -480,6 +480,10 @@ __device__ __forceinline__ void cp16(uint32_t dst, const void *src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp8(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N> __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
@@ -1307,11 +1311,14 @@ __global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_stack(const __grid_c
     const size_t TH = (size_t)T * H;
 
     if (threadIdx.x == 0) *abort_flag = 0;
-    // this CTA's router rows of layer l -> the ring's tail (one cp.async group)
+    // one cp.async group: this CTA's router rows of layer l -> the ring's tail, and the
+    // layer's expert table -> s_tab (both free once the previous layer's units are done)
     auto load_rows = [&](int l) {
         const float *wr = sa.wr[l] + (size_t)r0 * H;
         const uint32_t dst = sm_addr(s_wr);
         for (int i = threadIdx.x; i < nr * H / 4; i += nthr) cp16(dst + 16u * i, wr + 4 * i);
+        const uint8_t *const *blobs = sa.blobs + (size_t)l * E;
+        for (int e = threadIdx.x; e < E; e += nthr) cp8(sm_addr(s_tab + e), blobs + e);
         cp_commit();
     };
     load_rows(0);
@@ -1325,8 +1332,6 @@ __global__ void __maxnreg__(V == kVarHalf ? 96 : 128) k_dec_stack(const __grid_c
         // ---- every CTA's logits of layer l are in place
         ok = grid_barrier(gbar, gabort, nbar++, !(l == 0 && b == d.skip_cta), d.wait_cycles, status, abort_flag);
         if (!ok) break;
-        const uint8_t *const *blobs = sa.blobs + (size_t)l * E;
-        for (int e = threadIdx.x; e < E; e += nthr) s_tab[e] = blobs[e];
         for (int i = threadIdx.x; i < T * E; i += nthr) s_lg[i] = __ldcg(d.logits + i);
         // nobody reads the other accumulator past that barrier: this CTA's share of it, zeroed for layer l + 1
         if (l + 1 < sa.L) {
