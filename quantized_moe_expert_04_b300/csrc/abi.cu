@@ -61,6 +61,7 @@ WsLayout ws_layout(const moe_config &c, int32_t T)
     L.assign = take(TK * 4);
     L.active = take((E + 1) * 4);
     L.bhist = take((TK + kBucketItems - 1) / kBucketItems * E * 4);
+    L.wsplit = take(router_split_bytes(c.n_experts, c.hidden, T));
     const bool gemv = use_gemv(c, T), det = (c.flags & MOE_FLAG_DETERMINISTIC) != 0;
     L.slots = take(det ? TK * H * 4 : 0);
     L.yacc = take((size_t)T * H * 4 * (gemv ? 2 : 1));   // decode: two (the layer stack alternates them)
@@ -295,6 +296,7 @@ static RouteArgs route_args(const moe_config *cfg, const uint16_t *x, const floa
     r.assign = (int32_t *)(base + L.assign);
     r.active = (int32_t *)(base + L.active);
     r.bhist = (int32_t *)(base + L.bhist);
+    r.wsplit = (uint16_t *)(base + L.wsplit);
     r.header = (uint32_t *)(base + L.header);
     return r;
 }

@@ -905,6 +905,173 @@ __global__ void __launch_bounds__(256) k_gemm_finish(const float *__restrict__ y
     }
 }
 
+// ---------------------------------------------------------------- router logits on tcgen05
+
+// logits[T][E] = x[T][H] * Wr[E][H]^T for the tensor-core routing path.  The
+// fp32 router matrix arrives split into three bf16 planes (w = w1 + w2 + w3
+// exactly: each bf16 x bf16 product is exact), stacked as [3E][H].  CTA tile:
+// 128 tokens (MMA M) x N experts; K stages of 64 (one 128-byte swizzle row of
+// bf16), kRtStages in flight.  The 24 MMAs of every two stages (128 of K x
+// 3 planes) sum into a fresh accumulator in tensor memory (two, used in turn),
+// and the epilogue warps add those partial sums into fp32 registers: no long
+// chain runs inside the tensor-memory accumulator (one chain over all of K
+// drifted by ~2e-6 on logits of ~2.5, beyond the 1e-6 near-tie band of the
+// selection).
+// Warp 0 issues the 2-D tensor copies, warp 1 owns the tensor memory and
+// issues the MMAs, warps 2-5 add and store (one lane quadrant each).
+constexpr int kRtM = 128, kRtK = 64, kRtStages = 3, kRtThreads = 192, kRtEpi = 4;
+constexpr int kRtKpb = 2;               // K stages summed in one tensor-memory accumulator
+
+template <int N>
+struct RtSmem {
+    static constexpr uint32_t kX = kRtM * kRtK * 2;       // x rows of a stage
+    static constexpr uint32_t kW = N * kRtK * 2;          // one plane's rows of a stage
+    static constexpr uint32_t kStage = kX + 3 * kW;
+    static constexpr uint32_t kBytes = kRtStages * kStage + 1024 /* alignment */ + 256 /* barriers, slots */;
+};
+
+template <int N>
+__global__ void __launch_bounds__(kRtThreads, 1) k_router_tc(const __grid_constant__ CUtensorMap tmap_x,
+                                                            const __grid_constant__ CUtensorMap tmap_w, int T, int H,
+                                                            int E, float *__restrict__ logits, uint32_t *status,
+                                                            long long limit)
+{
+    using C = RtSmem<N>;
+    extern __shared__ uint8_t rt_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(rt_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sX = smem_addr(smem), sW = sX + kRtStages * C::kX;   // x stages, then [stage][plane] rows
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRtStages * C::kStage);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kRtStages + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * kRtM, e0 = blockIdx.y * N, nk = H / kRtK;
+    auto full = [&](int s) { return smem_addr(bars + s); };
+    auto empty = [&](int s) { return smem_addr(bars + kRtStages + s); };
+    auto acc_full = [&](int b) { return smem_addr(bars + 2 * kRtStages + b); };
+    auto acc_empty = [&](int b) { return smem_addr(bars + 2 * kRtStages + 2 + b); };
+    const uint32_t done = smem_addr(bars + 2 * kRtStages + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRtStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full(b), 1);
+            mbar_init(acc_empty(b), kRtEpi);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), 2 * N);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % kRtStages;
+                if (kb >= kRtStages && !wait_bar(empty(s), ((kb / kRtStages) - 1) & 1, abort_flag, status, limit))
+                    break;
+                mbar_arrive_expect_tx(full(s), C::kStage);
+                tma_load_2d(sX + s * C::kX, &tmap_x, kb * kRtK, t0, full(s));
+#pragma unroll
+                for (int sp = 0; sp < 3; ++sp)
+                    tma_load_2d(sW + (s * 3 + sp) * C::kW, &tmap_w, kb * kRtK, sp * E + e0, full(s));
+                ++issued;
+            }
+            // copies in flight must land before the CTA ends (only left after an abort)
+            for (int kb = issued > kRtStages ? issued - kRtStages : 0; kb < issued; ++kb) {
+                const long long c0 = clock64();
+                while (!mbar_try_wait(full(kb % kRtStages), (kb / kRtStages) & 1) && clock64() - c0 < limit) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kRtM, N);
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % kRtStages, pb = kb / kRtKpb, b = pb & 1;
+                const bool first = kb % kRtKpb == 0, last = kb % kRtKpb == kRtKpb - 1 || kb == nk - 1;
+                if (!wait_bar(full(s), (kb / kRtStages) & 1, abort_flag, status, limit)) break;
+                if (first && pb >= 2 && !wait_bar(acc_empty(b), ((pb >> 1) - 1) & 1, abort_flag, status, limit))
+                    break;
+                tc_fence_after();
+                const uint64_t a0 = sdesc_kmajor_sw128(sX + s * C::kX);
+#pragma unroll
+                for (int kk = 0; kk < kRtK / 16; ++kk)
+#pragma unroll
+                    for (int sp = 0; sp < 3; ++sp)
+                        mma_f16(tmem + b * N, a0 + (uint64_t)((32 * kk) >> 4),
+                                sdesc_kmajor_sw128(sW + (s * 3 + sp) * C::kW) + (uint64_t)((32 * kk) >> 4), idesc,
+                                !first || (kk | sp) != 0);
+                mma_commit(empty(s));
+                if (last) mma_commit(acc_full(b));
+            }
+            mma_commit(done);           // every MMA issued (all of them, or those before an abort)
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;         // the lane quadrant this warp may read
+        float acc[N];
+#pragma unroll
+        for (int c = 0; c < N; ++c) acc[c] = 0.0f;
+        bool ok = true;
+        const int np = (nk + kRtKpb - 1) / kRtKpb;
+        for (int pb = 0; pb < np && ok; ++pb) {
+            const int b = pb & 1;
+            if (lane == 0) ok = wait_bar(acc_full(b), (pb >> 1) & 1, abort_flag, status, limit);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            // 64 columns a round: four loads in flight, then the adds
+#pragma unroll
+            for (int c = 0; c < N; c += 64) {
+                uint32_t v[4][16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (c + 16 * i < N) tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + b * N + c + 16 * i, v[i]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (c + 16 * i < N) acc[c + 16 * i + j] += __uint_as_float(v[i][j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(b));
+        }
+        const int t = t0 + 32 * q + lane;
+        if (ok && t < T) {
+            float *row = logits + (int64_t)t * E + e0;
+#pragma unroll
+            for (int c = 0; c < N; ++c)
+                if (e0 + c < E) row[c] = acc[c];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        // every issued MMA has completed before the tensor memory is freed
+        if (lane == 0) {
+            const long long c0 = clock64();
+            while (!mbar_try_wait(done, 0) && clock64() - c0 < limit) {
+            }
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 2 * N);
+    }
+}
+
 // ---------------------------------------------------------------- launch
 
 // cuTensorMapEncodeTiled, fetched from the driver through the runtime (no
@@ -1168,6 +1335,59 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
         w.yacc, det ? a.slots : nullptr, det ? a.sh_out : nullptr, a.T, a.H, a.k, a.y, a.y_f32);
     prof_end(kPhGemmFinish, s);
     return cudaGetLastError();
+}
+
+// Tensor map of a bf16 matrix [rows][cols] (row-major, base 16-byte aligned,
+// cols % 8 == 0): boxes of 64 columns x box_rows rows, 128-byte swizzle, zero
+// fill past the edges.
+static bool make_tmap_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn || rows <= 0 || cols <= 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int N>
+static cudaError_t launch_router_tc_n(const uint16_t *x, const uint16_t *planes, int T, int H, int E, float *logits,
+                                      uint32_t *status, long long limit, cudaStream_t s)
+{
+    static std::mutex mu;
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            e = cudaFuncSetAttribute(k_router_tc<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)RtSmem<N>::kBytes);
+            if (e != cudaSuccess) return e;
+            done[dev] = true;
+        }
+    }
+    CUtensorMap tx, tw;
+    if (!make_tmap_bf16(&tx, x, T, H, kRtM) || !make_tmap_bf16(&tw, planes, 3 * (int64_t)E, H, N))
+        return cudaErrorInvalidValue;
+    const dim3 grid((T + kRtM - 1) / kRtM, (E + N - 1) / N);
+    k_router_tc<N><<<grid, kRtThreads, RtSmem<N>::kBytes, s>>>(tx, tw, T, H, E, logits, status, limit);
+    return cudaGetLastError();
+}
+
+// 128-expert tiles when they fill most SMs, else 64
+cudaError_t launch_router_tc(const uint16_t *x, const uint16_t *planes, int T, int H, int E, float *logits,
+                             uint32_t *status, long long limit, cudaStream_t s)
+{
+    const int64_t tiles128 = (int64_t)((T + kRtM - 1) / kRtM) * ((E + 127) / 128);
+    if (E % 128 == 0 && tiles128 >= 120)
+        return launch_router_tc_n<128>(x, planes, T, H, E, logits, status, limit, s);
+    return launch_router_tc_n<64>(x, planes, T, H, E, logits, status, limit, s);
 }
 
 }  // namespace moe

@@ -73,7 +73,7 @@ void prof_end(int phase, cudaStream_t s);
 // Workspace regions (byte offsets from the workspace base) for one call shape.
 struct WsLayout {
     size_t header, logits, ids, w, counts, offsets, assign, active;
-    size_t slots, yacc, xg, x16, sh_out, bhist, xfrag;
+    size_t slots, yacc, xg, x16, sh_out, bhist, xfrag, wsplit;
     size_t act16, sh_act16, tiles_gu, tiles_dn, tiles_gus, tiles_dns, tmaps, gu, sh_gu, split_cnt;
     size_t total;
 };
@@ -108,8 +108,13 @@ struct RouteArgs {
     float *w;
     int32_t *counts, *offsets, *assign, *active;
     int32_t *bhist;                      // bucketing: [ceil(T*k / kBucketItems)][E] per-CTA counts
+    uint16_t *wsplit;                    // [3][E][H] bf16 parts of the router matrix (tensor-core logits)
     uint32_t *header;
 };
+size_t router_split_bytes(int E, int H, int T);
+// Router logits on tcgen05 from the split planes (gemm_tc.cu).
+cudaError_t launch_router_tc(const uint16_t *x, const uint16_t *planes, int T, int H, int E, float *logits,
+                             uint32_t *status, long long limit, cudaStream_t s);
 constexpr int kBucketItems = 1024;       // assignments per CTA of the parallel bucketing
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s);
 

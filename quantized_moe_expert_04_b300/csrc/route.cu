@@ -15,6 +15,7 @@
 //   k_topk           one warp per token, E/32 logits per lane in registers,
 //                    k rounds of a warp arg-max (equal keys: lower id).
 //   k_bucket_*       stable counting sort of the T*k assignments over the grid.
+#include <algorithm>
 #include <mutex>
 #include "moe_internal.cuh"
 
@@ -69,39 +70,13 @@ k_router_logits(const uint16_t *__restrict__ x, const float *__restrict__ wr, in
     }
 }
 
-// Router logits for larger T on the warp-level tensor cores: C[T][E] =
-// X[T][H] * Wr[E][H]^T.  Each fp32 router weight is split exactly into three
-// bf16 parts (w = w1 + w2 + w3: 8 significant bits each), so with bf16 x the
-// three bf16 x bf16 products are exact and the MMAs accumulate them in fp32 --
-// the logits of an fp32 dot product, in another summation order.  Each
-// 32-wide K stage is summed by the MMAs into a fresh accumulator and the
-// stage sums are added with fp32 adds, so no long chain runs inside the MMA
-// accumulator.
-// CTA tile 128 tokens x RN experts, K stages of 32, double-buffered in
-// padded shared memory (rows of 40 bf16: ldmatrix without bank conflicts);
-// 8 warps as 4 (tokens) x 2 (experts), each 32 x RN/2.
-constexpr int kRmM = 128, kRmK = 32, kRmLd = 40;
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                 "{%0,%1,%2,%3};"
-                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, bool valid)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
-}
+// Router logits for larger T on the tensor cores (k_router_tc, gemm_tc.cu):
+// each fp32 router weight is split exactly into three bf16 parts (w = w1 + w2
+// + w3: 8 significant bits each), so with bf16 x the three bf16 x bf16
+// products are exact and the MMAs accumulate them in fp32 -- the logits of an
+// fp32 dot product, in another summation order.  The split is done once per
+// call, into the workspace.
+constexpr int kRmK = 64;                // the tensor-core kernel's K stage: H % kRmK == 0
 
 // w -> (w1, w2, w3) bf16 with w1 + w2 + w3 == w
 __device__ __forceinline__ void split3(float w, uint16_t &a, uint16_t &b, uint16_t &c)
@@ -116,136 +91,24 @@ __device__ __forceinline__ void split3(float w, uint16_t &a, uint16_t &b, uint16
     c = __bfloat16_as_ushort(h3);
 }
 
-template <int RN>
-__global__ void __launch_bounds__(256) k_router_mma(const uint16_t *__restrict__ x, const float *__restrict__ wr,
-                                                    int T, int H, int E, float *__restrict__ logits)
+// The router matrix split once per call for the tensor-core logits:
+// planes[sp][e][h] (sp = 0, 1, 2) with planes[0] + planes[1] + planes[2] == wr
+// exactly (split3).
+__global__ void __launch_bounds__(256) k_router_split(const float *__restrict__ wr, int64_t n,
+                                                      uint16_t *__restrict__ planes)
 {
-    constexpr int NT = RN / 16;                       // n8 tiles per warp (warp covers RN/2 experts)
-    extern __shared__ __align__(16) uint16_t rsm[];
-    uint16_t *sX = rsm;                               // [2][128][40]
-    uint16_t *sW = rsm + 2 * kRmM * kRmLd;            // [2][3][RN][40]
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wm = warp & 3, wn = warp >> 2;
-    const int t0 = blockIdx.x * kRmM, e0 = blockIdx.y * RN;
-    const int nstage = H / kRmK;
-
-    float acc[2][NT][4], sacc[2][NT][4];
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n / 4; i += (int64_t)gridDim.x * 256) {
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(wr) + i);
+        uint16_t h[3][4];
+        split3(w.x, h[0][0], h[1][0], h[2][0]);
+        split3(w.y, h[0][1], h[1][1], h[2][1]);
+        split3(w.z, h[0][2], h[1][2], h[2][2]);
+        split3(w.w, h[0][3], h[1][3], h[2][3]);
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.0f;
-
-    // X: 128 rows x 4 pieces of 16 bytes; Wr: RN rows x 8 float4
-    auto load_x = [&](int st, int buf) {
-        for (int p = tid; p < kRmM * 4; p += 256) {
-            const int r = p >> 2, pc = p & 3;
-            const int t = t0 + r;
-            const uint16_t *src = x + (int64_t)min(t, T - 1) * H + st * kRmK + pc * 8;
-            cp_async16_zfill((uint32_t)__cvta_generic_to_shared(sX + (buf * kRmM + r) * kRmLd + pc * 8), src, t < T);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    constexpr int WV = RN * 8 / 256;                  // float4 of Wr per thread per stage
-    float4 wreg[WV];
-    auto load_w = [&](int st) {
-#pragma unroll
-        for (int i = 0; i < WV; ++i) {
-            const int p = tid + i * 256, r = p >> 3, c4 = p & 7;
-            const int e = min(e0 + r, E - 1);
-            wreg[i] = __ldg(reinterpret_cast<const float4 *>(wr + (int64_t)e * H + st * kRmK) + c4);
-        }
-    };
-    auto store_w = [&](int buf) {
-#pragma unroll
-        for (int i = 0; i < WV; ++i) {
-            const int p = tid + i * 256, r = p >> 3, c4 = p & 7;
-            uint16_t h[3][4];
-            split3(wreg[i].x, h[0][0], h[1][0], h[2][0]);
-            split3(wreg[i].y, h[0][1], h[1][1], h[2][1]);
-            split3(wreg[i].z, h[0][2], h[1][2], h[2][2]);
-            split3(wreg[i].w, h[0][3], h[1][3], h[2][3]);
-#pragma unroll
-            for (int sp = 0; sp < 3; ++sp) {
-                uint2 v;
-                v.x = (uint32_t)h[sp][0] | ((uint32_t)h[sp][1] << 16);
-                v.y = (uint32_t)h[sp][2] | ((uint32_t)h[sp][3] << 16);
-                *reinterpret_cast<uint2 *>(sW + ((buf * 3 + sp) * RN + r) * kRmLd + c4 * 4) = v;
-            }
-        }
-    };
-
-    load_x(0, 0);
-    load_w(0);
-    store_w(0);
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
-    for (int st = 0; st < nstage; ++st) {
-        const int buf = st & 1;
-        if (st + 1 < nstage) {
-            load_x(st + 1, buf ^ 1);
-            load_w(st + 1);
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) sacc[i][j][q] = 0.0f;
-#pragma unroll
-        for (int kk = 0; kk < kRmK; kk += 16) {
-            uint32_t af[2][4];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int r = wm * 32 + i * 16 + (lane & 15);
-                const int c = kk + (lane >> 4) * 8;
-                ldsm_x4((uint32_t)__cvta_generic_to_shared(sX + (buf * kRmM + r) * kRmLd + c), af[i][0], af[i][1],
-                        af[i][2], af[i][3]);
-            }
-#pragma unroll
-            for (int sp = 0; sp < 3; ++sp) {
-#pragma unroll
-                for (int j = 0; j < NT; j += 2) {
-                    // two n8 tiles: lanes 0-7 / 8-15 rows of tile j at k, k+8; 16-23 / 24-31 tile j+1
-                    const int n = wn * (RN / 2) + (j + (lane >> 4)) * 8 + (lane & 7);
-                    const int c = kk + ((lane >> 3) & 1) * 8;
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4((uint32_t)__cvta_generic_to_shared(sW + ((buf * 3 + sp) * RN + n) * kRmLd + c), b0, b1,
-                            b2, b3);
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        mma_bf16(sacc[i][j], af[i][0], af[i][1], af[i][2], af[i][3], b0, b1);
-                        mma_bf16(sacc[i][j + 1], af[i][0], af[i][1], af[i][2], af[i][3], b2, b3);
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[i][j][q] += sacc[i][j][q];
-        if (st + 1 < nstage) store_w(buf ^ 1);
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncthreads();
+        for (int sp = 0; sp < 3; ++sp)
+            reinterpret_cast<uint2 *>(planes + sp * n)[i] =
+                make_uint2((uint32_t)h[sp][0] | ((uint32_t)h[sp][1] << 16), (uint32_t)h[sp][2] | ((uint32_t)h[sp][3] << 16));
     }
-    // C fragment: c0,c1 = (row g, cols 2t, 2t+1), c2,c3 = (row g+8, ...)
-    const int g = lane >> 2, tq = lane & 3;
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int t = t0 + wm * 32 + i * 16 + g + 8 * hh;
-                const int e = e0 + wn * (RN / 2) + j * 8 + 2 * tq;
-                if (t < T) {
-                    if (e < E) logits[(int64_t)t * E + e] = acc[i][j][2 * hh];
-                    if (e + 1 < E) logits[(int64_t)t * E + e + 1] = acc[i][j][2 * hh + 1];
-                }
-            }
 }
 
 // One warp per token.  Keys: the logit (softmax: the order of p equals the
@@ -484,10 +347,6 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(k_bucket_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(32 * 1024 * sizeof(int32_t)));
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(k_router_mma<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(k_router_mma<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
             if (e != cudaSuccess) return e;
             done[dev] = true;
         }
@@ -496,13 +355,16 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
     const int experts_per_cta = a.T > kRouterTokens ? 16 * kRouterWarps : kRouterWarps;
     dim3 grid((a.E + experts_per_cta - 1) / experts_per_cta, (a.T + kRouterTokens - 1) / kRouterTokens);
     prof_begin(kPhRouterLogits, s);
-    if (a.T > kRouterTokens && a.H % kRmK == 0) {
-        // tensor-core logits: 128-token x 64-expert tiles
-        const bool wide = false;
-        const size_t smem = (size_t)(2 * kRmM * kRmLd + 2 * 3 * (wide ? 128 : 64) * kRmLd) * sizeof(uint16_t);
-        const dim3 g2((a.T + kRmM - 1) / kRmM, (a.E + (wide ? 127 : 63)) / (wide ? 128 : 64));
-        if (wide) k_router_mma<128><<<g2, 256, smem, s>>>(a.x, a.wr, a.T, a.H, a.E, a.logits);
-        else k_router_mma<64><<<g2, 256, smem, s>>>(a.x, a.wr, a.T, a.H, a.E, a.logits);
+    if (router_split_bytes(a.E, a.H, a.T) > 0) {
+        // tensor-core logits: the split planes, then tcgen05 tiles
+        const int64_t n = (int64_t)a.E * a.H;
+        k_router_split<<<(unsigned)std::min<int64_t>((n / 4 + 255) / 256, 148 * 16), 256, 0, s>>>(a.wr, n, a.wsplit);
+        const cudaError_t e2 = launch_router_tc(a.x, a.wsplit, a.T, a.H, a.E, a.logits, a.header + kHdrStatus,
+                                                debug_wait_cycles(), s);
+        if (e2 != cudaSuccess) {
+            prof_end(kPhRouterLogits, s);
+            return e2;
+        }
     } else {
         k_router_logits<<<grid, kRouterWarps * 32, xs_bytes, s>>>(a.x, a.wr, a.T, a.H, a.E, experts_per_cta,
                                                                   a.logits);
@@ -525,6 +387,13 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
     k_bucket_scatter<<<nblk, kBucketItems, 32 * a.E * sizeof(int32_t), s>>>(a.ids, TK, a.E, a.bhist, a.assign);
     prof_end(kPhBucket, s);
     return cudaGetLastError();
+}
+
+// Bytes of the split router planes the tensor-core logits read (0: the call
+// takes the scalar logits kernel).
+size_t router_split_bytes(int E, int H, int T)
+{
+    return T > kRouterTokens && H % kRmK == 0 ? (size_t)3 * E * H * sizeof(uint16_t) : 0;
 }
 
 }  // namespace moe

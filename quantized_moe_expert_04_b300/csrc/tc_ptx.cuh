@@ -230,6 +230,15 @@ __host__ __device__ __forceinline__ uint32_t idesc_f16_f32(int M, int N)
            | ((uint32_t)(M >> 4) << 24);      // M >> 4
 }
 
+// Instruction descriptor, kind::f16 with bf16 A and B (both K-major), fp32 D, M x N.
+__host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N)
+{
+    return (1u << 4)                          // D format: f32
+           | (1u << 7) | (1u << 10)           // A, B format: bf16
+           | ((uint32_t)(N >> 3) << 17)
+           | ((uint32_t)(M >> 4) << 24);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
