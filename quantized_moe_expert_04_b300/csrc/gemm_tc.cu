@@ -745,53 +745,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
 
 // ---------------------------------------------------------------- helpers
 
-// fp16 operand copies of x: xg, the rows in bucket order (row p holds token
-// assign[p] / k), and x16 in token order when a shared expert needs it; zero
-// the fp32 output accumulator, the split-K partial sums and their counters.
-// Eight elements per item (16-byte loads and stores).
-__global__ void __launch_bounds__(256) k_gemm_prep(const uint16_t *__restrict__ x, const int32_t *__restrict__ assign,
-                                                   int k, int T, int H, __half *__restrict__ xg,
-                                                   __half *__restrict__ x16, float *__restrict__ yacc,
-                                                   float *__restrict__ gu, int64_t n_gu, uint32_t *__restrict__ cnt,
-                                                   int64_t n_cnt, uint32_t *status)
-{
-    bool bad = false;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int cpr = H / 8;                               // 8-element chunks per row
-    auto convert = [&](const uint16_t *src, __half *dst) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float lo = bf16_bits_to_f32(w[i] & 0xffffu), hi = bf16_bits_to_f32(w[i] >> 16);
-            const __half2 h = __floats2half2_rn(lo, hi);
-            bad |= (isfinite(lo) && !isfinite(__low2float(h))) || (isfinite(hi) && !isfinite(__high2float(h)));
-            memcpy(&o[i], &h, 4);
-        }
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
-    };
-    // one warp per row: lanes take consecutive 16-byte chunks
-    const int lane = threadIdx.x & 31;
-    const int64_t gwarp = tid >> 5, nwarps = stride >> 5;
-    for (int64_t p = gwarp; p < (int64_t)T * k; p += nwarps) {
-        const int t = assign[p] / k;
-        const uint16_t *src = x + (int64_t)t * H;
-        __half *dst = xg + p * H;
-        for (int c = lane; c < cpr; c += 32) convert(src + 8 * c, dst + 8 * c);
-    }
-    const int64_t n_x = (int64_t)T * cpr;
-    if (x16)
-        for (int64_t i = tid; i < n_x; i += stride) convert(x + 8 * i, x16 + 8 * i);
-    if (yacc)
-        for (int64_t i = tid; i < 2 * n_x; i += stride)
-            reinterpret_cast<float4 *>(yacc)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int64_t i = tid; i < n_gu; i += stride) gu[i] = 0.0f;
-    for (int64_t i = tid; i < n_cnt; i += stride) cnt[i] = 0u;
-    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, MOE_ERR_DEVICE_FAULT);
-}
-
 struct PlanArgs {
     int H, FF, SFF, T, split_gu, split_dn, split_gus, split_dns;
     const int32_t *offsets, *active;
@@ -807,11 +760,12 @@ __device__ __forceinline__ void split_tokens(int n_e, int &tn, int &nt)
 }
 
 // Work tiles of the routed experts (both projections) and of the shared
-// expert; one CTA, one thread per active expert, block-wide prefix sums.
+// expert, by one CTA of 1024 threads (block 0 of k_gemm_prep, beside the
+// permutation): one thread per active expert, block-wide prefix sums.
 // Tile (e, m | ks << 16, n0, n): expert e (-1 = shared), weight tile m, K
 // split ks, tokens n0 .. n0+n-1 of the expert's bucket.  The splits of one
 // (e, m, n0) group are consecutive.
-__global__ void __launch_bounds__(1024) k_gemm_plan(PlanArgs p)
+__device__ __forceinline__ void plan_tiles(const PlanArgs &p)
 {
     __shared__ int scan_gu[1024], scan_dn[1024];
     __shared__ int s_e[1024], s_n[1024], s_tn[1024];
@@ -882,6 +836,66 @@ __global__ void __launch_bounds__(1024) k_gemm_plan(PlanArgs p)
         p.header[kHdrTilesGUS] = 0;
         p.header[kHdrTilesDNS] = 0;
     }
+}
+
+// fp16 operand copies of x: xg, the rows in bucket order (row p holds token
+// assign[p] / k), and x16 in token order when a shared expert needs it; zero
+// the fp32 output accumulator, the split-K partial sums and their counters.
+// Eight elements per item (16-byte loads and stores).  Block 0 plans the
+// GEMMs' work tiles meanwhile (plan_tiles); the other blocks do the rest.
+__global__ void __launch_bounds__(1024) k_gemm_prep(const uint16_t *__restrict__ x, const int32_t *__restrict__ assign,
+                                                    int k, int T, int H, __half *__restrict__ xg,
+                                                    __half *__restrict__ x16, float *__restrict__ yacc,
+                                                    float *__restrict__ gu, int64_t n_gu, uint32_t *__restrict__ cnt,
+                                                    int64_t n_cnt, uint32_t *status, const __grid_constant__ PlanArgs plan)
+{
+    if (blockIdx.x == 0) {
+        plan_tiles(plan);
+        return;
+    }
+    bool bad = false;
+    const int64_t stride = (int64_t)(gridDim.x - 1) * blockDim.x;
+    const int64_t tid = (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+    const int cpr = H / 8;                               // 8-element chunks per row
+    auto convert_v = [&](const uint4 v, __half *dst) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float lo = bf16_bits_to_f32(w[i] & 0xffffu), hi = bf16_bits_to_f32(w[i] >> 16);
+            const __half2 h = __floats2half2_rn(lo, hi);
+            bad |= (isfinite(lo) && !isfinite(__low2float(h))) || (isfinite(hi) && !isfinite(__high2float(h)));
+            memcpy(&o[i], &h, 4);
+        }
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    auto convert = [&](const uint16_t *src, __half *dst) { convert_v(__ldg(reinterpret_cast<const uint4 *>(src)), dst); };
+    // one warp per row: lanes take consecutive 16-byte chunks, four loads in flight
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarp = tid >> 5, nwarps = stride >> 5;
+    for (int64_t p = gwarp; p < (int64_t)T * k; p += nwarps) {
+        const int t = assign[p] / k;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)t * H);
+        __half *dst = xg + p * H;
+        for (int c0 = lane; c0 < cpr; c0 += 4 * 32) {
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (c0 + 32 * j < cpr) v[j] = __ldg(src + c0 + 32 * j);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (c0 + 32 * j < cpr) convert_v(v[j], dst + 8 * (c0 + 32 * j));
+        }
+    }
+    const int64_t n_x = (int64_t)T * cpr;
+    if (x16)
+        for (int64_t i = tid; i < n_x; i += stride) convert(x + 8 * i, x16 + 8 * i);
+    if (yacc)
+        for (int64_t i = tid; i < 2 * n_x; i += stride)
+            reinterpret_cast<float4 *>(yacc)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int64_t i = tid; i < n_gu; i += stride) gu[i] = 0.0f;
+    for (int64_t i = tid; i < n_cnt; i += stride) cnt[i] = 0u;
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, MOE_ERR_DEVICE_FAULT);
 }
 
 // y = bf16(accumulated y) (atomic path) or the fixed-order sum of the slots.
@@ -1260,12 +1274,11 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     const GemmSplits sp = w.splits;
     prof_begin(kPhGemmPrep, s);
     const int64_t items = std::max<int64_t>((int64_t)a.T * a.k * (a.H / 8), w.n_gu);
-    k_gemm_prep<<<(unsigned)std::min<int64_t>((items + 255) / 256, 148 * 8), 256, 0, s>>>(
-        a.x, a.assign, a.k, a.T, a.H, w.xg, a.shared_blob ? w.x16 : nullptr, det ? nullptr : w.yacc, w.gu, w.n_gu,
-        w.split_cnt, w.n_cnt, a.header + kHdrStatus);
     PlanArgs p{a.H, a.FF, a.SFF, a.T, sp.gu, sp.dn, sp.gus, sp.dns, a.offsets, a.active, a.header,
                w.tiles_gu, w.tiles_dn, w.tiles_gus, w.tiles_dns};
-    k_gemm_plan<<<1, 1024, 0, s>>>(p);
+    k_gemm_prep<<<1 + (unsigned)std::min<int64_t>((items + 1023) / 1024, 148 * 2), 1024, 0, s>>>(
+        a.x, a.assign, a.k, a.T, a.H, w.xg, a.shared_blob ? w.x16 : nullptr, det ? nullptr : w.yacc, w.gu, w.n_gu,
+        w.split_cnt, w.n_cnt, a.header + kHdrStatus, p);
     prof_end(kPhGemmPrep, s);
 
     GemmArgs g{};
