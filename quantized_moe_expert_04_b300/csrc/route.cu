@@ -126,8 +126,10 @@ __device__ __forceinline__ uint32_t topk_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// (Four CTAs an SM up to 512 experts: every token's warp resident in one wave
+// at T = 4096.)
 template <int NPER>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, NPER <= 16 ? 4 : 2)
 k_topk(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k,
        int score_fn, int32_t *__restrict__ ids, float *__restrict__ wout, uint32_t *status)
 {
@@ -137,13 +139,17 @@ k_topk(const float *__restrict__ logits, const float *__restrict__ bias, int T, 
     const float *lrow = logits + (int64_t)t * E;
     uint32_t key[NPER];
     float val[NPER];
+    // all of the lane's loads in flight first
+    float lg[NPER];
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) lg[i] = __ldg(lrow + min(lane + 32 * i, E - 1));
 #pragma unroll
     for (int i = 0; i < NPER; ++i) {
         const int e = lane + 32 * i;
         key[i] = 0u;
         val[i] = 0.0f;
         if (e < E) {
-            const float l = __ldg(lrow + e);
+            const float l = lg[i];
             if (score_fn == MOE_SCORE_SOFTMAX) {
                 val[i] = l;
                 key[i] = topk_key(l);
