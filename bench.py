@@ -280,7 +280,7 @@ def algorithmic(wl, T, ids_per_layer):
 # The sources a kernel's code comes from: its own file and the shared headers.
 KERNEL_SOURCES = {
     "dec": ["decode.cu", "moe_internal.cuh", "dequant_f16.cuh"],
-    "gemm": ["gemm_tc.cu", "moe_internal.cuh", "tc_ptx.cuh", "dequant_f16.cuh"],
+    "gemm": ["gemm_tc.cu", "moe_internal.cuh", "tc_ptx.cuh", "dequant_f16.cuh", "debug_hooks.cuh"],
 }
 
 

@@ -455,9 +455,18 @@ MOE_API int32_t moe_profile_read(moe_profile_entry *out, int32_t max_entries);
  *                          then ends with MOE_ERR_TIMEOUT in its status word
  *                          (the context stays usable; a value past the grid
  *                          does nothing).  -1 clears it.
+ *   MOE_DEBUG_SKIP_ROUTER  value >= 0: in the next call whose router logits
+ *                          run on the tensor cores (more than 8 tokens,
+ *                          hidden a multiple of 64), router tile `value`
+ *                          (tiles of 128 tokens; index = token tile + expert
+ *                          tile * token tiles) never issues the copies of its
+ *                          first stage, so its MMA warp's wait runs out and
+ *                          the call ends with MOE_ERR_TIMEOUT; the logits of
+ *                          that tile are left unwritten.  A value past the
+ *                          grid does nothing; -1 clears it.
  * Errors: MOE_ERR_INVALID_ARG for an unknown `what` or a value out of range.
  */
-enum { MOE_DEBUG_WAIT_CYCLES = 1, MOE_DEBUG_SKIP_COPY = 2 };
+enum { MOE_DEBUG_WAIT_CYCLES = 1, MOE_DEBUG_SKIP_COPY = 2, MOE_DEBUG_SKIP_ROUTER = 3 };
 MOE_API moe_status moe_debug_set(int32_t what, int64_t value);
 
 /* Static string for a status code. */

@@ -6,6 +6,7 @@
 #include <atomic>
 
 #include "moe_internal.cuh"
+#include "debug_hooks.cuh"
 
 namespace moe {
 
@@ -39,8 +40,10 @@ bool use_gemv(const moe_config &c, int32_t T)
 // ---- test hooks of the bounded device waits (moe_debug_set)
 static std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
 static std::atomic<int> g_skip_copy{-1};
+static std::atomic<int> g_skip_router{-1};
 long long debug_wait_cycles() { return g_wait_cycles.load(); }
 int debug_take_skip_copy() { return g_skip_copy.exchange(-1); }
+int debug_take_skip_router() { return g_skip_router.exchange(-1); }
 
 WsLayout ws_layout(const moe_config &c, int32_t T)
 {
@@ -525,6 +528,10 @@ moe_status moe_debug_set(int32_t what, int64_t value)
     case MOE_DEBUG_SKIP_COPY:
         if (value < -1 || value > (1 << 20)) return MOE_ERR_INVALID_ARG;
         g_skip_copy.store((int)value);
+        return MOE_OK;
+    case MOE_DEBUG_SKIP_ROUTER:
+        if (value < -1 || value > (1 << 20)) return MOE_ERR_INVALID_ARG;
+        g_skip_router.store((int)value);
         return MOE_OK;
     }
     return MOE_ERR_INVALID_ARG;

@@ -34,6 +34,7 @@
 //
 // Operand precision: fp16 A and B (sub-block scale and min rounded to fp16,
 // one fused multiply-add per weight), fp32 accumulation.
+#include <atomic>
 #include <mutex>
 #include <algorithm>
 #include <cmath>
@@ -41,6 +42,7 @@
 #include <cuda.h>
 
 #include "moe_internal.cuh"
+#include "debug_hooks.cuh"
 #include "tc_ptx.cuh"
 #include "dequant_f16.cuh"
 
@@ -857,14 +859,18 @@ __global__ void __launch_bounds__(1024) k_gemm_prep(const uint16_t *__restrict__
     const int64_t stride = (int64_t)(gridDim.x - 1) * blockDim.x;
     const int64_t tid = (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
     const int cpr = H / 8;                               // 8-element chunks per row
+    // bf16 pairs -> fp16 pairs (each rounded once); |x| >= 65504 -- for a bf16
+    // value, magnitude bits >= 0x4780 (2^16; the bf16 below it, 65280, is an
+    // fp16 number), infinities and NaN included -- flags the call
     auto convert_v = [&](const uint4 v, __half *dst) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[4];
+        const uint32_t mag = __vmaxu2(__vmaxu2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu),
+                                      __vmaxu2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu));
+        bad |= __vcmpgeu2(mag, 0x47804780u) != 0u;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float lo = bf16_bits_to_f32(w[i] & 0xffffu), hi = bf16_bits_to_f32(w[i] >> 16);
-            const __half2 h = __floats2half2_rn(lo, hi);
-            bad |= (isfinite(lo) && !isfinite(__low2float(h))) || (isfinite(hi) && !isfinite(__high2float(h)));
+            const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
             memcpy(&o[i], &h, 4);
         }
         *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -948,7 +954,7 @@ template <int N>
 __global__ void __launch_bounds__(kRtThreads, 1) k_router_tc(const __grid_constant__ CUtensorMap tmap_x,
                                                             const __grid_constant__ CUtensorMap tmap_w, int T, int H,
                                                             int E, float *__restrict__ logits, uint32_t *status,
-                                                            long long limit)
+                                                            long long limit, int skip_cta)
 {
     using C = RtSmem<N>;
     extern __shared__ uint8_t rt_raw[];
@@ -989,11 +995,17 @@ __global__ void __launch_bounds__(kRtThreads, 1) k_router_tc(const __grid_consta
 
     if (warp == 0) {
         if (lane == 0) {
+            // test hook: this tile never issues (nor arms) its first stage
+            const bool skip0 = skip_cta == (int)(blockIdx.y * gridDim.x + blockIdx.x);
             int issued = 0;
             for (int kb = 0; kb < nk; ++kb) {
                 const int s = kb % kRtStages;
                 if (kb >= kRtStages && !wait_bar(empty(s), ((kb / kRtStages) - 1) & 1, abort_flag, status, limit))
                     break;
+                if (kb == 0 && skip0) {
+                    ++issued;
+                    continue;
+                }
                 mbar_arrive_expect_tx(full(s), C::kStage);
                 tma_load_2d(sX + s * C::kX, &tmap_x, kb * kRtK, t0, full(s));
 #pragma unroll
@@ -1003,6 +1015,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) k_router_tc(const __grid_consta
             }
             // copies in flight must land before the CTA ends (only left after an abort)
             for (int kb = issued > kRtStages ? issued - kRtStages : 0; kb < issued; ++kb) {
+                if (kb == 0 && skip0) continue;
                 const long long c0 = clock64();
                 while (!mbar_try_wait(full(kb % kRtStages), (kb / kRtStages) & 1) && clock64() - c0 < limit) {
                 }
@@ -1276,7 +1289,15 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     const int64_t items = std::max<int64_t>((int64_t)a.T * a.k * (a.H / 8), w.n_gu);
     PlanArgs p{a.H, a.FF, a.SFF, a.T, sp.gu, sp.dn, sp.gus, sp.dns, a.offsets, a.active, a.header,
                w.tiles_gu, w.tiles_dn, w.tiles_gus, w.tiles_dns};
-    k_gemm_prep<<<1 + (unsigned)std::min<int64_t>((items + 1023) / 1024, 148 * 2), 1024, 0, s>>>(
+    // one wave: the planning CTA and as many grid-stride CTAs as stay resident beside it
+    static std::atomic<int> prep_per_sm{0};
+    if (prep_per_sm.load() == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_gemm_prep, 1024, 0) != cudaSuccess || n < 1) n = 1;
+        prep_per_sm.store(n);
+    }
+    const int64_t prep_workers = std::max<int64_t>(1, (int64_t)prep_per_sm.load() * num_sms() - 1);
+    k_gemm_prep<<<1 + (unsigned)std::min<int64_t>((items + 1023) / 1024, prep_workers), 1024, 0, s>>>(
         a.x, a.assign, a.k, a.T, a.H, w.xg, a.shared_blob ? w.x16 : nullptr, det ? nullptr : w.yacc, w.gu, w.n_gu,
         w.split_cnt, w.n_cnt, a.header + kHdrStatus, p);
     prof_end(kPhGemmPrep, s);
@@ -1368,7 +1389,7 @@ static bool make_tmap_bf16(CUtensorMap *m, const void *base, int64_t rows, int64
 
 template <int N>
 static cudaError_t launch_router_tc_n(const uint16_t *x, const uint16_t *planes, int T, int H, int E, float *logits,
-                                      uint32_t *status, long long limit, cudaStream_t s)
+                                      uint32_t *status, long long limit, int skip_cta, cudaStream_t s)
 {
     static std::mutex mu;
     static bool done[64] = {};
@@ -1389,7 +1410,7 @@ static cudaError_t launch_router_tc_n(const uint16_t *x, const uint16_t *planes,
     if (!make_tmap_bf16(&tx, x, T, H, kRtM) || !make_tmap_bf16(&tw, planes, 3 * (int64_t)E, H, N))
         return cudaErrorInvalidValue;
     const dim3 grid((T + kRtM - 1) / kRtM, (E + N - 1) / N);
-    k_router_tc<N><<<grid, kRtThreads, RtSmem<N>::kBytes, s>>>(tx, tw, T, H, E, logits, status, limit);
+    k_router_tc<N><<<grid, kRtThreads, RtSmem<N>::kBytes, s>>>(tx, tw, T, H, E, logits, status, limit, skip_cta);
     return cudaGetLastError();
 }
 
@@ -1398,9 +1419,10 @@ cudaError_t launch_router_tc(const uint16_t *x, const uint16_t *planes, int T, i
                              uint32_t *status, long long limit, cudaStream_t s)
 {
     const int64_t tiles128 = (int64_t)((T + kRtM - 1) / kRtM) * ((E + 127) / 128);
+    const int skip = debug_take_skip_router();
     if (E % 128 == 0 && tiles128 >= 120)
-        return launch_router_tc_n<128>(x, planes, T, H, E, logits, status, limit, s);
-    return launch_router_tc_n<64>(x, planes, T, H, E, logits, status, limit, s);
+        return launch_router_tc_n<128>(x, planes, T, H, E, logits, status, limit, skip, s);
+    return launch_router_tc_n<64>(x, planes, T, H, E, logits, status, limit, skip, s);
 }
 
 }  // namespace moe

@@ -228,10 +228,11 @@ k_topk(const float *__restrict__ logits, const float *__restrict__ bias, int T, 
 // b owns the kBucketItems assignments [b*kBucketItems, (b+1)*kBucketItems).
 //   1. k_bucket_hist: each CTA's per-expert counts (shared-memory atomics);
 //   2. k_bucket_scan (one CTA): per expert, the CTAs' counts prefix-summed in
-//      CTA order and the expert totals scanned -> counts, offsets, the
-//      ascending list of experts that received tokens; base[b][e] = where
-//      CTA b's first assignment to e goes;
-//   3. k_bucket_scatter: within a CTA, lanes with the same expert are ranked
+//      CTA order (in place: bhist[b][e] = how many assignments to e the CTAs
+//      before b hold) and the expert totals scanned -> counts, offsets, the
+//      ascending list of experts that received tokens;
+//   3. k_bucket_scatter: CTA b's first assignment to e goes to offsets[e] +
+//      bhist[b][e]; within a CTA, lanes with the same expert are ranked
 //      by lane (__match_any_sync) and warps by a per-expert prefix over the
 //      warps, so equal keys keep the input order -- the sort is stable.
 __global__ void __launch_bounds__(kBucketItems)
@@ -256,52 +257,72 @@ __global__ void __launch_bounds__(1024)
 k_bucket_scan(int nblk, int E, int32_t *__restrict__ bhist, int32_t *__restrict__ counts,
               int32_t *__restrict__ offsets, int32_t *__restrict__ active, uint32_t *header)
 {
-    __shared__ int32_t scan[1024];
-    const int e = threadIdx.x;                   // one thread per expert (E <= 1024)
+    __shared__ int32_t w_tot[32], w_act[32];
+    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;   // one thread per expert (E <= 1024)
     int tot = 0;
     if (e < E) {
-#pragma unroll 8
-        for (int b = 0; b < nblk; ++b) {
-            const int c = bhist[(int64_t)b * E + e];
-            bhist[(int64_t)b * E + e] = tot;
-            tot += c;
+        // the expert's column over the CTAs: 16 loads in flight, then their
+        // exclusive prefix written back in their place
+        for (int b0 = 0; b0 < nblk; b0 += 16) {
+            int c[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) c[j] = b0 + j < nblk ? bhist[(int64_t)(b0 + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (b0 + j < nblk) {
+                    bhist[(int64_t)(b0 + j) * E + e] = tot;
+                    tot += c[j];
+                }
         }
         counts[e] = tot;
     }
-    // exclusive scans over the experts: of the totals, and of (total > 0)
-    scan[e] = tot;
-    __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {
-        const int v = e >= off ? scan[e - off] : 0;
-        __syncthreads();
-        scan[e] += v;
-        __syncthreads();
+    // inclusive scans over the experts of the totals and of (total > 0):
+    // within each warp, then over the 32 warps' sums
+    int sum = tot, act = tot > 0 ? 1 : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, sum, off), b = __shfl_up_sync(0xffffffffu, act, off);
+        if (lane >= off) {
+            sum += a;
+            act += b;
+        }
     }
-    const int base = scan[e] - tot, total = scan[1023];
+    if (lane == 31) {
+        w_tot[warp] = sum;
+        w_act[warp] = act;
+    }
     __syncthreads();
-    scan[e] = tot > 0 ? 1 : 0;
+    if (warp == 0) {
+        int ws = w_tot[lane], wa = w_act[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, ws, off), b = __shfl_up_sync(0xffffffffu, wa, off);
+            if (lane >= off) {
+                ws += a;
+                wa += b;
+            }
+        }
+        w_tot[lane] = ws;
+        w_act[lane] = wa;
+    }
     __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {
-        const int v = e >= off ? scan[e - off] : 0;
-        __syncthreads();
-        scan[e] += v;
-        __syncthreads();
+    if (warp > 0) {
+        sum += w_tot[warp - 1];
+        act += w_act[warp - 1];
     }
     if (e < E) {
-        offsets[e] = base;
-        if (tot > 0) active[scan[e] - 1] = e;
-#pragma unroll 8
-        for (int b = 0; b < nblk; ++b) bhist[(int64_t)b * E + e] += base;
+        offsets[e] = sum - tot;
+        if (tot > 0) active[act - 1] = e;
     }
     if (e == 1023) {
-        offsets[E] = total;                      // = number of valid assignments
-        header[kHdrNActive] = (uint32_t)scan[1023];
+        offsets[E] = sum;                        // = number of valid assignments
+        header[kHdrNActive] = (uint32_t)act;
     }
 }
 
 __global__ void __launch_bounds__(kBucketItems)
 k_bucket_scatter(const int32_t *__restrict__ ids, int TK, int E, const int32_t *__restrict__ bhist,
-                 int32_t *__restrict__ assign)
+                 const int32_t *__restrict__ offsets, int32_t *__restrict__ assign)
 {
     extern __shared__ int32_t wh[];              // [32 warps][E]
     for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wh[i] = 0;
@@ -325,7 +346,7 @@ k_bucket_scatter(const int32_t *__restrict__ ids, int TK, int E, const int32_t *
         }
     }
     __syncthreads();
-    if (valid) assign[bhist[(int64_t)blockIdx.x * E + e] + wh[warp * E + e] + rank] = a;
+    if (valid) assign[__ldg(offsets + e) + bhist[(int64_t)blockIdx.x * E + e] + wh[warp * E + e] + rank] = a;
 }
 
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
@@ -390,7 +411,8 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
     prof_begin(kPhBucket, s);
     k_bucket_hist<<<nblk, kBucketItems, a.E * sizeof(int32_t), s>>>(a.ids, TK, a.E, a.bhist, a.header);
     k_bucket_scan<<<1, 1024, 0, s>>>(nblk, a.E, a.bhist, a.counts, a.offsets, a.active, a.header);
-    k_bucket_scatter<<<nblk, kBucketItems, 32 * a.E * sizeof(int32_t), s>>>(a.ids, TK, a.E, a.bhist, a.assign);
+    k_bucket_scatter<<<nblk, kBucketItems, 32 * a.E * sizeof(int32_t), s>>>(a.ids, TK, a.E, a.bhist, a.offsets,
+                                                                            a.assign);
     prof_end(kPhBucket, s);
     return cudaGetLastError();
 }

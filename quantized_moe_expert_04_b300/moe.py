@@ -50,6 +50,7 @@ EXPORTS = (
 
 MOE_DEBUG_WAIT_CYCLES = 1
 MOE_DEBUG_SKIP_COPY = 2
+MOE_DEBUG_SKIP_ROUTER = 3
 
 MOE_STATIC_WS_BYTES = 4 << 20
 

@@ -148,3 +148,19 @@ def test_stack_checks_arguments_before_any_cuda_call():
         assert call(c=c, nbytes=moe.moe_workspace_bytes(c, 4)) == moe.MOE_ERR_UNSUPPORTED_SHAPE
     ds = moe.make_config(256, 16, 128, 2, moe.MOE_SCORE_SIGMOID_BIAS, 64)
     assert call(c=ds, nbytes=moe.moe_workspace_bytes(ds, 4)) == moe.MOE_ERR_INVALID_ARG   # no shared table
+
+
+def test_debug_hooks_check_their_values_on_the_host():
+    """moe_debug_set touches host state only: each skip hook takes -1 .. 2^20
+    and rejects the rest; the wait limit takes any value >= 0."""
+    for what in (moe.MOE_DEBUG_SKIP_COPY, moe.MOE_DEBUG_SKIP_ROUTER):
+        for bad in (-2, (1 << 20) + 1):
+            with pytest.raises(moe.MoeError):
+                moe.moe_debug_set(what, bad)
+        moe.moe_debug_set(what, 7)
+        moe.moe_debug_set(what, -1)
+    with pytest.raises(moe.MoeError):
+        moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, -1)
+    moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, 0)
+    with pytest.raises(moe.MoeError):
+        moe.moe_debug_set(4, 0)

@@ -279,3 +279,32 @@ def test_prefill_activation_beyond_fp16_is_reported():
     pl2 = pack_layer(wl, gen_device="cpu")
     forward(pl2, synth.hidden_states(wl, T).cuda(), ws, cfg=cfg)
     assert moe.moe_last_device_status(ws) == moe.MOE_OK
+
+
+@pytest.mark.parametrize("flags,T", [(moe.MOE_FLAG_FORCE_GEMM, 40), (moe.MOE_FLAG_FORCE_GEMV, 3)], ids=["gemm", "decode"])
+def test_input_beyond_fp16_is_reported_on_both_paths(flags, T):
+    """Both paths multiply fp16 copies of x: an element whose magnitude is not
+    below 65504 -- for a bf16 value, 65536 and up (the bf16 number below it,
+    65280, is an fp16 number), infinities and NaN too -- raises
+    MOE_ERR_DEVICE_FAULT; 65280 itself passes.  The experts are scaled down
+    (x 1e-3) so that the large element leaves the activations inside the fp16
+    range."""
+    wl = sv(W["qwen_decode"], name="qwen_e16", n_experts=16)
+    pl = pack_layer(wl, gen_device="cpu", experts=[])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for e in range(wl.n_experts):
+        w = synth.expert_weight(wl, e) * 1e-3
+        moe.moe_pack_q4k(w.reshape(3 * wl.ff, wl.hidden).cuda(), pl.blobs[e], st)
+    assert int(st.item()) == 0
+    cfg = moe.config_for(wl, flags)
+    ws = workspace(cfg, T)
+    x0 = synth.hidden_states(wl, T)
+    for v, ok in [(65280.0, True), (-65280.0, True), (65536.0, False), (-65536.0, False),
+                  (float("inf"), False), (float("nan"), False)]:
+        x = x0.clone()
+        x[T - 1, 7] = v
+        y = forward(pl, x.cuda(), ws, cfg=cfg)
+        status = moe.moe_last_device_status(ws)
+        assert status == (moe.MOE_OK if ok else moe.MOE_ERR_DEVICE_FAULT), (v, status)
+        if ok:
+            assert bool(torch.isfinite(y.float()).all())

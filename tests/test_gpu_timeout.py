@@ -83,3 +83,36 @@ def test_gemm_wait_timeout_is_reported_and_the_context_survives(cta):
     ids, _, _, _ = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
     blobs, sblob = oracle_blobs(wl, ids.reshape(-1))
     check_close(y32.cpu().numpy(), oracle_forward(wl, xb, wr, b, blobs, sblob))
+
+
+@pytest.mark.parametrize("E,tile,times_out", [(64, 0, True), (64, 2, True), (128, 4, True), (128, 1000, False)])
+def test_router_wait_timeout_is_reported_and_the_context_survives(E, tile, times_out):
+    """The tensor-core router (T = 300: three 128-token tiles, the last one
+    ragged; E = 128 adds a second expert tile): one tile never issues its first
+    stage's copies, its MMA warp's wait runs out, the epilogue leaves on the
+    abort flag without writing that tile's logits, and the call reports
+    MOE_ERR_TIMEOUT (the routing that follows reads whatever the logits buffer
+    held: ids stay in range whatever it holds).  A tile past the grid skips
+    nothing.  Either way the hook is spent and the next call is right."""
+    wl = synth.small_variant(synth.WORKLOADS["qwen_decode"], name="qwen_e%d" % E, n_experts=E)
+    T = 300
+    pl = pack_layer(wl, gen_device="cpu")
+    cfg = moe.config_for(wl)
+    ws = workspace(cfg, T)
+    x = synth.hidden_states(wl, T).cuda()
+    try:
+        moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, 1 << 22)      # ~2 ms
+        moe.moe_debug_set(moe.MOE_DEBUG_SKIP_ROUTER, tile)
+        forward(pl, x, ws, cfg=cfg)
+        assert moe.moe_last_device_status(ws) == (moe.MOE_ERR_TIMEOUT if times_out else moe.MOE_OK)
+    finally:
+        moe.moe_debug_set(moe.MOE_DEBUG_SKIP_ROUTER, -1)
+        moe.moe_debug_set(moe.MOE_DEBUG_WAIT_CYCLES, 0)
+    y32 = torch.empty(T, wl.hidden, dtype=torch.float32, device="cuda")
+    forward(pl, x, ws, y_f32=y32, cfg=cfg)
+    assert moe.moe_last_device_status(ws) == moe.MOE_OK
+    xb, wr, b = oracle_inputs(wl, T, x=x.cpu())
+    import oracle
+    ids, _, _, _ = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
+    blobs, sblob = oracle_blobs(wl, ids.reshape(-1))
+    check_close(y32.cpu().numpy(), oracle_forward(wl, xb, wr, b, blobs, sblob))
