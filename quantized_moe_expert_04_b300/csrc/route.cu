@@ -13,11 +13,13 @@
 //                    8 tokens whose bf16 rows sit in shared memory, so each
 //                    router row is read once per 8 tokens.
 //   k_topk           one warp per token, E/32 logits per lane in registers,
-//                    k rounds of a warp arg-max (equal keys: lower id).
+//                    sorted per lane, k rounds of a warp arg-max (equal
+//                    keys: lower id).
 //   k_bucket_*       stable counting sort of the T*k assignments over the grid.
 #include <algorithm>
 #include <mutex>
 #include "moe_internal.cuh"
+#include "topk_warp.cuh"
 
 namespace moe {
 
@@ -113,15 +115,10 @@ __global__ void __launch_bounds__(256) k_router_split(const float *__restrict__ 
 
 // One warp per token.  Keys: the logit (softmax: the order of p equals the
 // order of the logits) or s_e + b_e (sigmoid), as order-preserving integers
-// (NaN -> 0, never selected).  Lane l holds experts l, l + 32, ... (NPER) as
-// 64-bit words key << 32 | (0xffff - e), so that a larger word is the larger
-// key and, among equal keys, the lower id; it sorts them once, in
-// registers, with Batcher's odd-even merge network (uniform code, every lane
-// busy).  Each round takes the warp maximum of the lanes' first words (the
-// key, then the lowest id among equal keys: two reductions) and the lane that
-// held it shifts its words by one.  Weights: softmax over the k selected
-// logits (= the full softmax renormalised over the k), or s_e / sum of the
-// selected s.
+// (NaN -> 0, never selected); lane l holds experts l, l + 32, ... (NPER) and
+// warp_select (topk_warp.cuh) takes the k largest, ties to the lower id.
+// Weights: softmax over the k selected logits (= the full softmax
+// renormalised over the k), or s_e / sum of the selected s.
 __device__ __forceinline__ uint32_t topk_key(float f)
 {
     if (isnan(f)) return 0u;
@@ -133,39 +130,6 @@ __device__ __forceinline__ uint32_t topk_key(float f)
 __device__ __forceinline__ float topk_key_value(uint32_t key)
 {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
-}
-
-// Batcher's odd-even merge sort of N words into descending order (N a power
-// of two): for p = 1, 2, 4, ... < N: for k = p, p/2, ..., 1: compare-exchange
-// elements i + j and i + j + k (j from k mod p in steps of 2k, i < k) when
-// both lie in the same block of 2p.  19 / 63 / 191 comparators for 8 / 16 /
-// 32.  One pass (p, k) per instantiation, so that every loop bound is a
-// constant and the words stay in registers.
-template <int N, int P, int K>
-struct OddEvenPass {
-    static __device__ __forceinline__ void run(uint64_t (&v)[N])
-    {
-#pragma unroll
-        for (int j = K % P; j + K < N; j += 2 * K)
-#pragma unroll
-            for (int i = 0; i < K; ++i) {
-                const int lo = i + j, hi = i + j + K;
-                if (hi < N && lo / (2 * P) == hi / (2 * P)) {
-                    const uint64_t x = v[lo], y = v[hi];
-                    const bool sw = y > x;
-                    v[lo] = sw ? y : x;
-                    v[hi] = sw ? x : y;
-                }
-            }
-        if constexpr (K > 1) OddEvenPass<N, P, K / 2>::run(v);
-        else if constexpr (2 * P < N) OddEvenPass<N, 2 * P, 2 * P>::run(v);
-    }
-};
-
-template <int N>
-__device__ __forceinline__ void sort_desc(uint64_t (&v)[N])
-{
-    OddEvenPass<N, 1, 1>::run(v);
 }
 
 // (Four CTAs an SM up to 512 experts: every token's warp resident in one wave
@@ -183,40 +147,24 @@ k_topk(const float *__restrict__ logits, const float *__restrict__ bias, int T, 
     float lg[NPER];
 #pragma unroll
     for (int i = 0; i < NPER; ++i) lg[i] = __ldg(lrow + min(lane + 32 * i, E - 1));
-    uint64_t v[NPER];
+    uint32_t key[NPER];
 #pragma unroll
     for (int i = 0; i < NPER; ++i) {
         const int e = lane + 32 * i;
-        uint32_t key = 0u;
+        key[i] = 0u;
         if (e < E) {
             if (score_fn == MOE_SCORE_SOFTMAX) {
-                key = topk_key(lg[i]);
+                key[i] = topk_key(lg[i]);
             } else {
                 const float sg = 1.0f / (1.0f + expf(-lg[i]));
-                key = topk_key(sg + (bias ? __ldg(bias + e) : 0.0f));
+                key[i] = topk_key(sg + (bias ? __ldg(bias + e) : 0.0f));
             }
         }
-        v[i] = ((uint64_t)key << 32) | (uint32_t)(0xffff - e);
     }
-    sort_desc<NPER>(v);
-    int my_id = 0;
-    uint32_t my_key = 0u;
-    bool fault = false;
-    for (int r = 0; r < k; ++r) {
-        const uint32_t hk = (uint32_t)(v[0] >> 32);
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, hk);
-        const uint32_t ml = __reduce_max_sync(0xffffffffu, hk == mk ? (uint32_t)v[0] : 0u);
-        const int e = 0xffff - (int)ml;                  // the lowest id among the equal keys
-        if (mk == 0u) fault = true;                      // nothing selectable (non-finite scores)
-        if (lane == r) {
-            my_id = mk == 0u ? r : e;
-            my_key = mk;
-        }
-        const bool pop = mk != 0u && lane == (e & 31);
-#pragma unroll
-        for (int i = 0; i + 1 < NPER; ++i) v[i] = pop ? v[i + 1] : v[i];
-        v[NPER - 1] = pop ? 0ull : v[NPER - 1];
-    }
+    int my_id;
+    uint32_t my_key;
+    bool fault;
+    warp_select<NPER>(key, k, lane, my_id, my_key, fault);
     // weights over the k selected (lane r holds selection r): the selected
     // logit (softmax; recovered from its key) or s = sigmoid(logit), as above
     float my_val = 0.0f;
