@@ -80,7 +80,7 @@ struct GemmArgs {
     __half *sh_act16;        // [T][SFF]
     float *yacc;             // [T][H]
     float *slots, *sh_out;   // deterministic combine
-    const int4 *tiles;       // {expert (-1 shared), m tile | k split << 16, n0, n}
+    const int4 *tiles;       // {expert (-1 shared), m tile | k split << 16 | no blob << 30, first row, n}
     const uint32_t *n_tiles; // device count
     float *gu;               // split-K gate/up partial sums [rows][2 FF] (splits > 1)
     uint32_t *split_cnt;     // split-K arrival counters, one per (expert, m, n) group
@@ -90,27 +90,39 @@ struct GemmArgs {
     int skip_cta;            // test hook: this CTA never issues its first token-row copy (-1: none)
 };
 
+// A work tile.  The record holds everything the roles need but the blob's
+// address (read by the raw-weight copier alone): row0 is the first row of the
+// tile's tokens in the operand (the expert's bucket offset + the tile's
+// position in it, or the token index for the shared expert), live is false
+// when the expert's blob pointer is null.
 struct TileInfo {
-    int e, m, ks, n0, n, nmma, bb, ksteps, k0;   // k0: first K-step of this split
-    const uint8_t *blob;
+    int e, m, ks, row0, n, nmma, ksteps, k0;   // k0: first K-step of this split
+    bool live;
 };
 
+constexpr int kTileNoBlob = 1 << 30;         // record flag: the expert's blob pointer is null
+
 template <int OP, int FMT>
-__device__ __forceinline__ TileInfo tile_info(const GemmArgs &g, int idx)
+__device__ __forceinline__ TileInfo tile_decode(const GemmArgs &g, int4 t)
 {
-    const int4 t = g.tiles[idx];
     TileInfo ti;
     ti.e = t.x;
     ti.m = t.y & 0xffff;
-    ti.ks = t.y >> 16;
-    ti.n0 = t.z;
+    ti.ks = (t.y >> 16) & 0x3fff;
+    ti.live = !(t.y & kTileNoBlob);
+    ti.row0 = t.z;
     ti.n = t.w;
     ti.nmma = (t.w + 15) & ~15;
-    ti.bb = t.x >= 0 ? g.offsets[t.x] : 0;
-    ti.blob = t.x >= 0 ? g.blobs[t.x] : g.shared_blob;
     ti.ksteps = (OP == kOpGateUp ? g.H : (FMT == kWQ4K ? g.FF : g.SFF)) / 64 / g.splits;
     ti.k0 = ti.ks * ti.ksteps;
     return ti;
+}
+
+// Record of tile idx (zeros past the list): each role reads the next tile's
+// record one tile ahead, so the load is in flight while the current tile runs.
+__device__ __forceinline__ int4 tile_fetch(const GemmArgs &g, int idx, int n_tiles)
+{
+    return idx < n_tiles ? __ldg(g.tiles + idx) : make_int4(0, 0, 0, 0);
 }
 
 // a = SiLU(g) * u as the fp16 operand of the down projection.  A value
@@ -396,34 +408,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
             return wait_bar(epi_bar, (epi_it++) & 1, abort_flag, g.status, g.wait_cycles);
         };
         bool ok = true;
+        // routed down: each thread owns column ei of every tile (kEpi >= NMAX); its
+        // slot and routing weight are loaded a tile ahead (the slot once the next
+        // tile's record is in, the weight after this tile's sums)
+        static_assert(kEpi >= NMAX, "one column of metadata per epilogue thread");
+        constexpr bool kMeta = OP == kOpDown && FMT == kWQ4K;
+        int4 tnext = tile_fetch(g, blockIdx.x, n_tiles);
+        int pslot = 0;
+        float pw = 0.0f;
+        if (kMeta && (int)blockIdx.x < n_tiles && ei < tnext.w && !(tnext.y & kTileNoBlob)) {
+            pslot = __ldg(g.assign + tnext.z + ei);
+            pw = __ldg(g.w + pslot);
+        }
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-            const TileInfo ti = tile_info<OP, FMT>(g, tile);
-            if (!ti.blob) {
+            const TileInfo ti = tile_decode<OP, FMT>(g, tnext);
+            tnext = tile_fetch(g, tile + (int)gridDim.x, n_tiles);
+            const int cslot = pslot;
+            const float cw = pw;
+            const bool nmeta = kMeta && tile + (int)gridDim.x < n_tiles;   // the next tile's column, if any
+            if (!ti.live) {
                 if (ei == 0) set_status(g.status, MOE_ERR_DEVICE_FAULT);
+                if (nmeta && ei < tnext.w && !(tnext.y & kTileNoBlob)) {
+                    pslot = __ldg(g.assign + tnext.z + ei);
+                    pw = __ldg(g.w + pslot);
+                }
                 continue;
             }
             const int acc = t_it & 1;
             if (OP == kOpDown) {
                 // column metadata: token, routing weight and slot of each column
-                for (int j = ei; j < ti.n; j += kEpi) {
+                if (ei < ti.n) {
                     int tok, slot;
                     float wt;
                     if (FMT == kWQ4K) {
-                        slot = g.assign[ti.bb + ti.n0 + j];
+                        slot = cslot;
                         tok = slot / g.k;
-                        wt = g.w[slot];
+                        wt = cw;
                     } else {
-                        tok = slot = ti.n0 + j;
+                        tok = slot = ti.row0 + ei;
                         wt = 1.0f;
                     }
-                    meta_tok[acc * NMAX + j] = tok;
-                    meta_w[acc * NMAX + j] = wt;
-                    meta_slot[acc * NMAX + j] = slot;
+                    meta_tok[acc * NMAX + ei] = tok;
+                    meta_w[acc * NMAX + ei] = wt;
+                    meta_slot[acc * NMAX + ei] = slot;
                 }
                 if (!(ok = epi_sync())) break;
             }
             if (!(ok = wait_bar(acc_full(acc), (t_it >> 1) & 1, abort_flag, g.status, g.wait_cycles))) break;
             tc_fence_after();
+            int nslot = 0;
+            const bool nload = nmeta && ei < tnext.w && !(tnext.y & kTileNoBlob);
+            if (nload) nslot = __ldg(g.assign + tnext.z + ei);
             const int ffop = FMT == kWQ4K ? g.FF : g.SFF;
             for (int cc = eg; cc < ti.nmma / 16; cc += kEG) {
                 uint32_t v[16];
@@ -444,8 +479,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
                             const int j = cc * 16 + 2 * pp + par;
                             if (j < ti.n) {
                                 const float a = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
-                                __half *dst = FMT == kWQ4K ? g.act16 + (int64_t)(ti.bb + ti.n0 + j) * ffop + f
-                                                           : g.sh_act16 + (int64_t)(ti.n0 + j) * ffop + f;
+                                __half *dst = FMT == kWQ4K ? g.act16 + (int64_t)(ti.row0 + j) * ffop + f
+                                                           : g.sh_act16 + (int64_t)(ti.row0 + j) * ffop + f;
                                 *dst = act_to_f16(a, g.status);
                             }
                         }
@@ -455,7 +490,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const int j = cc * 16 + i;
-                            const int rowi = FMT == kWQ4K ? ti.bb + ti.n0 + j : ti.n0 + j;
+                            const int rowi = ti.row0 + j;
                             if (j < ti.n) red_add_f32(g.gu + (int64_t)rowi * 2 * ffop + col, __uint_as_float(v[i]));
                         }
                     }
@@ -490,6 +525,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
                     }
                 }
             }
+            if (nload) {
+                pslot = nslot;
+                pw = __ldg(g.w + nslot);
+            }
             tc_fence_before();
             mbar_arrive(acc_empty(acc));
             ++t_it;
@@ -507,7 +546,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
                     const int f = ti.m * 64 + (et >> 1);
                     if (!(et & 1)) {
                         for (int j = 0; j < ti.n; ++j) {
-                            const int rowi = FMT == kWQ4K ? ti.bb + ti.n0 + j : ti.n0 + j;
+                            const int rowi = ti.row0 + j;
                             const float gg = ld_cg_f32(g.gu + (int64_t)rowi * 2 * ffop + f);
                             const float uu = ld_cg_f32(g.gu + (int64_t)rowi * 2 * ffop + ffop + f);
                             __half *dst = FMT == kWQ4K ? g.act16 + (int64_t)rowi * ffop + f
@@ -526,9 +565,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
         // every MMA and every commit (a commit tracks the issuing thread's MMAs)
         uint32_t st_it = 0, t_it = 0;
         bool ok = true;
+        int4 tnext = tile_fetch(g, blockIdx.x, n_tiles);
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-            const TileInfo ti = tile_info<OP, FMT>(g, tile);
-            if (!ti.blob) continue;
+            const TileInfo ti = tile_decode<OP, FMT>(g, tnext);
+            tnext = tile_fetch(g, tile + (int)gridDim.x, n_tiles);
+            if (!ti.live) continue;
             const int acc = t_it & 1;
             if (!(ok = warp_wait_bar(acc_empty(acc), ((t_it >> 1) & 1) ^ 1, abort_flag, g.status, g.wait_cycles))) break;
             tc_fence_after();
@@ -594,9 +635,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
             __syncwarp();
         }
         bool ok = true;
+        // the next tile's record and (once that is in) its blob address, a tile ahead
+        int4 tnext = tile_fetch(g, blockIdx.x, n_tiles);
+        const uint8_t *bnext = FMT == kWQ4K && (int)blockIdx.x < n_tiles && tnext.x >= 0 ? g.blobs[tnext.x]
+                                                                                       : nullptr;
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-            const TileInfo ti = tile_info<OP, FMT>(g, tile);
-            if (!ti.blob) continue;
+            const TileInfo ti = tile_decode<OP, FMT>(g, tnext);
+            const uint8_t *blob = bnext;
+            tnext = tile_fetch(g, tile + (int)gridDim.x, n_tiles);
+            if (!ti.live) {
+                if (FMT == kWQ4K)
+                    bnext = tnext.x >= 0 && tile + (int)gridDim.x < n_tiles ? g.blobs[tnext.x] : nullptr;
+                continue;
+            }
             if (FMT == kWQ4K && ti.e != cur_e) {
                 const int ms = nmaps & 1;
                 // the copies that last named this slot must have landed (a raw slot is
@@ -610,7 +661,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
                 }
                 __syncwarp();
                 CUtensorMap *gslot = g.tmaps + 2 * blockIdx.x + ms;
-                if (lane == 0) tmap_set_addr_smem(s_tmap, ti.blob);
+                if (lane == 0) tmap_set_addr_smem(s_tmap, blob);
                 __syncwarp();
                 tmap_copy_release(gslot, s_tmap);
                 if (lane == 0) tmap_acquire(gslot);
@@ -642,6 +693,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
             if (FMT == kWQ4K) {
                 if ((nmaps - 1) & 1) last_rs1 = rs_it;
                 else last_rs0 = rs_it;
+                bnext = tnext.x >= 0 && tile + (int)gridDim.x < n_tiles ? g.blobs[tnext.x] : nullptr;
             }
         }
         // copies still in flight (an early exit) must land before the CTA ends
@@ -662,10 +714,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
         uint32_t st_it = 0;
         bool ok = true;
         if (sub < KS) {
+            int4 tnext = tile_fetch(g, blockIdx.x, n_tiles);
             for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-                const TileInfo ti = tile_info<OP, FMT>(g, tile);
-                if (!ti.blob) continue;
-                const int row0 = FMT == kWQ4K ? ti.bb + ti.n0 : ti.n0;
+                const TileInfo ti = tile_decode<OP, FMT>(g, tnext);
+                tnext = tile_fetch(g, tile + (int)gridDim.x, n_tiles);
+                if (!ti.live) continue;
+                const int row0 = ti.row0;
                 const int nst = (ti.ksteps + KS - 1) / KS;
                 for (int st = 0; st < nst; ++st, ++st_it) {
                     const int slot = st_it % S;
@@ -701,9 +755,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
         const int q_lane = 32 * (warp & 3), row = q_lane + lane, hh = (warp - 8) >> 2;
         uint32_t st_it = 0, rs_it = 0;
         bool ok = true;
+        int4 tnext = tile_fetch(g, blockIdx.x, n_tiles);
         for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-            const TileInfo ti = tile_info<OP, FMT>(g, tile);
-            if (!ti.blob) continue;
+            const TileInfo ti = tile_decode<OP, FMT>(g, tnext);
+            tnext = tile_fetch(g, tile + (int)gridDim.x, n_tiles);
+            if (!ti.live) continue;
             const int nst = (ti.ksteps + KS - 1) / KS;
             for (int st = 0; st < nst; ++st, ++st_it) {
                 // warp-wide waits: the tensor-memory stores below are warp-collective
@@ -750,6 +806,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_moe_gemm(GemmArgs g, const 
 struct PlanArgs {
     int H, FF, SFF, T, split_gu, split_dn, split_gus, split_dns;
     const int32_t *offsets, *active;
+    const uint8_t *const *blobs;   // routed experts' blobs (a null one is flagged in its tiles)
     uint32_t *header;
     int4 *gu, *dn, *gus, *dns;
 };
@@ -764,25 +821,30 @@ __device__ __forceinline__ void split_tokens(int n_e, int &tn, int &nt)
 // Work tiles of the routed experts (both projections) and of the shared
 // expert, by one CTA of 1024 threads (block 0 of k_gemm_prep, beside the
 // permutation): one thread per active expert, block-wide prefix sums.
-// Tile (e, m | ks << 16, n0, n): expert e (-1 = shared), weight tile m, K
-// split ks, tokens n0 .. n0+n-1 of the expert's bucket.  The splits of one
-// (e, m, n0) group are consecutive.
+// Tile (e, m | ks << 16 | no blob << 30, row0, n): expert e (-1 = shared),
+// weight tile m, K split ks, tokens n0 .. n0+n-1 of the expert's bucket, whose
+// rows start at row0 = the bucket's offset + n0 (the shared expert: row0 =
+// n0, a token index).  The splits of one (e, m, n0) group are consecutive.
 __device__ __forceinline__ void plan_tiles(const PlanArgs &p)
 {
     __shared__ int scan_gu[1024], scan_dn[1024];
-    __shared__ int s_e[1024], s_n[1024], s_tn[1024];
+    __shared__ int s_e[1024], s_n[1024], s_tn[1024], s_bb[1024], s_flag[1024];
     const int u = threadIdx.x;
     const int n_active = (int)p.header[kHdrNActive];
     const int mt_gu = p.FF / 64, mt_dn = p.H / 128;
-    int e = -1, n_e = 0, tn = 0, nt = 0;
+    int e = -1, n_e = 0, tn = 0, nt = 0, bb = 0, flag = 0;
     if (u < n_active) {
         e = p.active[u];
-        n_e = p.offsets[e + 1] - p.offsets[e];
+        bb = p.offsets[e];
+        n_e = p.offsets[e + 1] - bb;
         split_tokens(n_e, tn, nt);
+        flag = p.blobs[e] ? 0 : kTileNoBlob;
     }
     s_e[u] = e;
     s_n[u] = n_e;
     s_tn[u] = tn;
+    s_bb[u] = bb;
+    s_flag[u] = flag;
     scan_gu[u] = nt * mt_gu * p.split_gu;
     scan_dn[u] = nt * mt_dn * p.split_dn;
     __syncthreads();
@@ -808,7 +870,7 @@ __device__ __forceinline__ void plan_tiles(const PlanArgs &p)
             const int l = i - (lo ? scan[lo - 1] : 0);
             const int ks = l % split, m = (l / split) % mt, j = l / (split * mt);
             const int n0 = j * s_tn[lo];
-            out[i] = make_int4(s_e[lo], m | (ks << 16), n0, min(s_tn[lo], s_n[lo] - n0));
+            out[i] = make_int4(s_e[lo], m | (ks << 16) | s_flag[lo], s_bb[lo] + n0, min(s_tn[lo], s_n[lo] - n0));
         }
     };
     fill(scan_gu, mt_gu, p.split_gu, p.gu);
@@ -1287,7 +1349,7 @@ cudaError_t launch_experts_gemm(const ExpertArgs &a, const GemmWs &w, cudaStream
     const GemmSplits sp = w.splits;
     prof_begin(kPhGemmPrep, s);
     const int64_t items = std::max<int64_t>((int64_t)a.T * a.k * (a.H / 8), w.n_gu);
-    PlanArgs p{a.H, a.FF, a.SFF, a.T, sp.gu, sp.dn, sp.gus, sp.dns, a.offsets, a.active, a.header,
+    PlanArgs p{a.H, a.FF, a.SFF, a.T, sp.gu, sp.dn, sp.gus, sp.dns, a.offsets, a.active, a.blobs, a.header,
                w.tiles_gu, w.tiles_dn, w.tiles_gus, w.tiles_dns};
     // one wave: the planning CTA and as many grid-stride CTAs as stay resident beside it
     static std::atomic<int> prep_per_sm{0};

@@ -222,6 +222,34 @@ def test_device_faults_are_reported():
     assert moe.moe_last_device_status(ws) == moe.MOE_ERR_DEVICE_FAULT
 
 
+def test_missing_expert_blob_on_tensor_cores_is_reported():
+    """The tensor-core path: the work tiles of a selected expert whose blob
+    pointer is null are flagged when the tiles are planned, every role of both
+    GEMMs skips them, and the call reports MOE_ERR_DEVICE_FAULT; the next call
+    with the full table is right."""
+    wl = sv(W["qwen_decode"], name="qwen_e16", n_experts=16)
+    T = 40
+    pl = pack_layer(wl, gen_device="cpu")
+    cfg = moe.config_for(wl, moe.MOE_FLAG_FORCE_GEMM)
+    ws = workspace(cfg, T)
+    x = synth.hidden_states(wl, T).cuda()
+    forward(pl, x, ws, cfg=cfg)
+    assert moe.moe_last_device_status(ws) == moe.MOE_OK
+    ids, _, _, _ = routing_views(cfg, T, ws)
+    table = pl.table.clone()
+    table[int(ids[0, 0].item())] = 0
+    y = torch.empty(T, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(cfg, x, pl.router_w, pl.router_bias, table, pl.shared, T, y, None, ws)
+    assert moe.moe_last_device_status(ws) == moe.MOE_ERR_DEVICE_FAULT
+    y32 = torch.empty(T, wl.hidden, dtype=torch.float32, device="cuda")
+    forward(pl, x, ws, y_f32=y32, cfg=cfg)
+    assert moe.moe_last_device_status(ws) == moe.MOE_OK
+    xb, wr, b = oracle_inputs(wl, T, x=x.cpu())
+    oids, _, _, _ = oracle.route(xb, wr, b, wl.top_k, wl.score_fn)
+    blobs, sblob = oracle_blobs(wl, oids.reshape(-1))
+    check_close(y32.cpu().numpy(), oracle_forward(wl, xb, wr, b, blobs, sblob))
+
+
 GEMM_SMALL = [
     (W["tiny"], 4),
     (W["tiny"], 1),
