@@ -1,8 +1,10 @@
 """The DRAM-traffic figures bench.py reports are keyed to a hash of the CUDA
 sources a kernel is built from (bench.KERNEL_SOURCES); a figure whose hash no
 longer matches is reported as null.  That only holds if the hash covers every
-local header the kernel's file includes, directly or through another header:
-checked here, on the sources, without a GPU."""
+header of the kernels' directory that the kernel's file includes, directly or
+through another header: checked here, on the sources, without a GPU.  (The
+public header include/moe.h, reached from moe_internal.cuh, holds the API's
+declarations and constants, no kernel code, and is left out of the hash.)"""
 import importlib.util
 import os
 import re
