@@ -479,19 +479,23 @@ def measure(args, wl, T, nL, world, rank, local, K=None, soak_s=0.0, target_s=0.
     out["dtype"] = "f16xf16->f32 (tensor-core MMAs), f32 combine"
 
     if e2e:
-        # end to end through the C ABI with host buffers
-        xh = [x.cpu().pin_memory() for x in xs]
-        yh = [torch.empty(T, wl.hidden, dtype=torch.bfloat16).pin_memory() for _ in range(nL)]
-        xd = [torch.empty_like(x) for x in xs]
+        # end to end through the C ABI with host buffers: every step copies its
+        # inputs (the nL layers' x, one pinned host -> device copy), makes the
+        # step's nL layer calls, and reads its results (the nL layers' y) back
+        # into pinned host memory with one copy
+        xh = torch.stack([x.cpu() for x in xs]).pin_memory()                   # [nL][T][H]
+        yh = torch.empty(nL, T, wl.hidden, dtype=torch.bfloat16).pin_memory()
+        xd = torch.empty(xh.shape, dtype=xh.dtype, device=dev)
+        yd = torch.empty(yh.shape, dtype=yh.dtype, device=dev)
         Ke = max(3, min(K, 50))
 
         def e2e_step():
+            xd.copy_(xh, non_blocking=True)
             for l in range(nL):
                 pl = layers[l]
-                xd[l].copy_(xh[l], non_blocking=True)
-                moe.moe_forward(cfg, xd[l], pl.router_w, pl.router_bias, pl.table, pl.shared, T, ys[l], None, ws,
+                moe.moe_forward(cfg, xd[l], pl.router_w, pl.router_bias, pl.table, pl.shared, T, yd[l], None, ws,
                                 stream)
-                yh[l].copy_(ys[l], non_blocking=True)
+            yh.copy_(yd, non_blocking=True)
 
         with torch.cuda.stream(stream):
             for _ in range(2):
@@ -508,7 +512,8 @@ def measure(args, wl, T, nL, world, rank, local, K=None, soak_s=0.0, target_s=0.
         out["e2e"] = {"value": round(T * nL * Ke * world / (e2e_ms / 1e3), 2), "unit": UNIT,
                       "h2d_bytes_per_step": int(nL * T * wl.hidden * 2),
                       "d2h_bytes_per_step": int(nL * T * wl.hidden * 2),
-                      "path": "pinned H2D x -> moe_forward -> D2H y, per layer, eager"}
+                      "path": "per step: one pinned H2D copy of the nL layers' x -> nL moe_forward calls -> "
+                              "one D2H copy of their y, eager"}
 
     if rank == 0 and cpu_budget is not None:
         v, threads, desc, parity = oracle_sample(wl, T, list(range(nL)), xs, gpu_ids=ids_per_layer, gpu_y32=y32,
