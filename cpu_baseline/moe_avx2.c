@@ -100,26 +100,6 @@ static inline void q32_to_f32_affine(__m256i q8, __m256 S, __m256 Z, __m256 out[
     out[3] = _mm256_fmsub_ps(_mm256_cvtepi32_ps(_mm256_cvtepu8_epi32(_mm_srli_si128(hi, 8))), S, Z);
 }
 
-/* One Q4_K super-block (256 weights) -> w[256] fp32. */
-static inline void q4k_block(const uint8_t *blk, float *w)
-{
-    const float d = f16_to_f32(blk), dmin = f16_to_f32(blk + 2);
-    const uint8_t *s = blk + 4, *qs = blk + 16;
-    const __m256i m4 = _mm256_set1_epi8(0x0f);
-    for (int c = 0; c < 4; ++c) {
-        const __m256i v = _mm256_loadu_si256((const __m256i *)(qs + 32 * c));
-        const __m256i lo = _mm256_and_si256(v, m4), hi = _mm256_and_si256(_mm256_srli_epi16(v, 4), m4);
-        int sc, m;
-        __m256 o[4];
-        q4k_scale_min(s, 2 * c, &sc, &m);
-        q32_to_f32_affine(lo, _mm256_set1_ps(d * (float)sc), _mm256_set1_ps(dmin * (float)m), o);
-        for (int i = 0; i < 4; ++i) _mm256_storeu_ps(w + 64 * c + 8 * i, o[i]);
-        q4k_scale_min(s, 2 * c + 1, &sc, &m);
-        q32_to_f32_affine(hi, _mm256_set1_ps(d * (float)sc), _mm256_set1_ps(dmin * (float)m), o);
-        for (int i = 0; i < 4; ++i) _mm256_storeu_ps(w + 64 * c + 32 + 8 * i, o[i]);
-    }
-}
-
 static inline float hsum(__m256 v)
 {
     __m128 s = _mm_add_ps(_mm256_castps256_ps128(v), _mm256_extractf128_ps(v, 1));
@@ -268,7 +248,6 @@ static void *down_worker(void *arg)
     const Job *j = arg;
     const int H = j->H, nb = j->nb, FF = j->FF;
     const int64_t mat = (int64_t)FF * nb * Q4K_BYTES;
-    float *wd = aligned_alloc(32, sizeof(float) * QK);
     for (int b = j->id; b < nb; b += j->nthr) {
         for (int s = 0; s < j->n_sel; ++s) {
             const int a0 = j->tok_off[s], n = j->tok_off[s + 1] - a0;
@@ -279,11 +258,24 @@ static void *down_worker(void *arg)
                 for (int t = 0; t < nt; ++t)
                     for (int i = 0; i < QK / 8; ++i) acc[t][i] = _mm256_setzero_ps();
                 for (int f = 0; f < FF; ++f) {
-                    q4k_block(rd + (int64_t)f * nb * Q4K_BYTES, wd);
-                    for (int t = 0; t < nt; ++t) {
-                        const __m256 av = _mm256_set1_ps(j->act[(int64_t)(a0 + t0 + t) * FF + f]);
-                        for (int i = 0; i < QK / 8; ++i)
-                            acc[t][i] = _mm256_fmadd_ps(_mm256_load_ps(wd + 8 * i), av, acc[t][i]);
+                    /* the row block's weights, unpacked 32 at a time straight into the sums */
+                    const uint8_t *blk = rd + (int64_t)f * nb * Q4K_BYTES;
+                    const float d = f16_to_f32(blk), dmin = f16_to_f32(blk + 2);
+                    __m256 av[4];
+                    for (int t = 0; t < nt; ++t) av[t] = _mm256_set1_ps(j->act[(int64_t)(a0 + t0 + t) * FF + f]);
+                    for (int c = 0; c < 4; ++c) {
+                        const __m256i v = _mm256_loadu_si256((const __m256i *)(blk + 16 + 32 * c));
+                        for (int half = 0; half < 2; ++half) {
+                            const int sb = 2 * c + half;
+                            int sc, m;
+                            q4k_scale_min(blk + 4, sb, &sc, &m);
+                            __m256 w[4];
+                            q32_to_f32_affine(q4k_sub(v, half), _mm256_set1_ps(d * (float)sc),
+                                              _mm256_set1_ps(dmin * (float)m), w);
+                            for (int t = 0; t < nt; ++t)
+                                for (int i = 0; i < 4; ++i)
+                                    acc[t][4 * sb + i] = _mm256_fmadd_ps(w[i], av[t], acc[t][4 * sb + i]);
+                        }
                     }
                 }
                 for (int t = 0; t < nt; ++t) {
@@ -294,7 +286,7 @@ static void *down_worker(void *arg)
             }
         }
     }
-    free(wd);
+
     return NULL;
 }
 
